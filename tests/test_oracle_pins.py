@@ -1,0 +1,428 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+format definitions checked against a library cast, hand-derived layout numbers,
+byte counts printed by the pages, exact rational arithmetic and invariants."""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from conftest import GOLDEN
+
+# ---------------------------------------------------------------------------
+# E4M3 decode / encode
+# ---------------------------------------------------------------------------
+
+
+def test_e4m3_table_matches_torch_cast_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = O.E4M3_TABLE
+    nan_ref, nan_ours = np.isnan(ref), np.isnan(ours)
+    assert np.array_equal(nan_ref, nan_ours)
+    assert np.array_equal(ref[~nan_ref], ours[~nan_ours])
+    assert np.array_equal(np.signbit(ref[~nan_ref]), np.signbit(ours[~nan_ours]))
+
+
+def test_e4m3_closed_forms():
+    assert O.E4M3_TABLE[0x7E] == 448.0
+    assert O.E4M3_TABLE[0x01] == 2.0 ** -9
+    assert O.E4M3_TABLE[0x07] == 7 * 2.0 ** -9
+    assert O.E4M3_TABLE[0x08] == 2.0 ** -6
+    assert O.E4M3_TABLE[0x38] == 1.0
+    assert O.E4M3_TABLE[0xB8] == -1.0
+    assert math.isnan(O.E4M3_TABLE[0x7F]) and math.isnan(O.E4M3_TABLE[0xFF])
+    assert O.E4M3_TABLE[0x80] == 0.0 and np.signbit(O.E4M3_TABLE[0x80])
+    # 126 distinct positive finite values, strictly increasing with the code
+    pos = O.E4M3_TABLE[1:0x7F]
+    assert np.all(np.diff(pos) > 0)
+
+
+def test_e4m3_encode_round_trip_all_finite_codes():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(O.e4m3_encode_rne(O.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_encode_midpoints_go_to_even_code():
+    pos = O.E4M3_TABLE[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2.0
+    got = O.e4m3_encode_rne(mids)
+    lo = np.arange(0, 0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(got, want.astype(np.uint8))
+    assert np.array_equal(O.e4m3_encode_rne(-mids), (want | 0x80).astype(np.uint8))
+
+
+def test_e4m3_encode_matches_torch_cast_random():
+    rng = np.random.default_rng(123)
+    mag = 2.0 ** rng.uniform(-14, np.log2(448.0), size=200_000)
+    v = mag * rng.choice([-1.0, 1.0], size=mag.size)
+    v = v.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode_rne(v), ref)
+
+
+def test_e4m3_encode_saturates():
+    assert O.e4m3_encode_rne(np.array([1e6, -1e6, 448.0, 465.0]))[:].tolist() == [0x7E, 0xFE, 0x7E, 0x7E]
+
+
+# ---------------------------------------------------------------------------
+# flat layout
+# ---------------------------------------------------------------------------
+
+
+def _read_offsets_golden():
+    rows = {}
+    with open(os.path.join(GOLDEN, "layout_offsets.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, ents, total, chunk = [p.strip() for p in line.split("|")]
+            name, n = head.split()
+            offs = dict((kv.split("=")[0], int(kv.split("=")[1])) for kv in ents.split())
+            rows[name] = (int(n), offs, int(total), int(chunk))
+    return rows
+
+
+def _plan_for(w: WL.Workload, n=None):
+    return O.plan_layout([(0, e.rows, e.cols, 1) for e in w.entries], n or w.n_shards)
+
+
+@pytest.mark.parametrize("wname", ["tiny_flat_layer", "shared_expert_layer", "attn_kda_layer", "prefill_kda_8"])
+def test_layout_matches_hand_derived_offsets(wname):
+    gold = _read_offsets_golden()[wname]
+    w = [x for x in WL.WORKLOADS.values() if x.name == wname][0]
+    n, offs, total, chunk = gold
+    assert n == w.n_shards
+    p = _plan_for(w)
+    ly = p.layers[0]
+    for j, e in enumerate(w.entries):
+        assert ly.offsets[j] == offs[e.name]
+    assert ly.total == total and ly.chunk == chunk
+
+
+def test_shared_expert_sizes_match_printed_byte_counts():
+    vals = {}
+    with open(os.path.join(GOLDEN, "pages_byte_counts.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                name, v, unit, dec = line.split()
+                vals[name] = (float(v), unit, int(dec))
+    p = _plan_for(WL.SHARED_EXPERT)
+    ly = p.layers[0]
+
+    def fmt(nbytes, unit, dec):
+        div = 1e6 if unit == "MB" else 2.0 ** 30
+        return round(nbytes / div, dec)
+
+    assert fmt(ly.sizes[0], "MB", 1) == vals["shared_gate_up"][0]
+    assert fmt(ly.sizes[1], "MB", 1) == vals["shared_down"][0]
+    assert fmt(ly.total, "MB", 1) == vals["shared_layer"][0]
+    assert fmt(92 * ly.total, "GiB", 1) == vals["shared_92_layers"][0]
+
+
+def test_worked_example_rank1_holds_tail_of_a_and_head_of_b():
+    p = _plan_for(WL.TINY)
+    ly = p.layers[0]
+    c = ly.chunk
+    want = []
+    with open(os.path.join(GOLDEN, "flat_layout_example.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                r, name, a, b = line.split()
+                want.append((int(r), name, int(a), int(b)))
+    names = [e.name for e in WL.TINY.entries]
+    rank = 1
+    got = []
+    for j in ly.entries:
+        lo, hi = ly.offsets[j], ly.offsets[j] + ly.sizes[j]
+        a, b = max(lo, rank * c), min(hi, (rank + 1) * c)
+        if a < b:
+            rowb = p.cols[j]
+            got.append((rank, names[j], (a - lo) // rowb, (b - lo) // rowb - 1))
+    assert got == want
+
+
+def _rand_shapes(rng, n_entries, n):
+    ents = []
+    for _ in range(n_entries):
+        rows = int(rng.integers(1, 9)) * n if rng.random() < 0.8 else int(rng.integers(1, 40))
+        cols = int(rng.integers(1, 70))
+        ents.append((0, rows, cols, int(rng.choice([1, 1, 2, 4]))))
+    return ents
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 8, 16])
+def test_layout_invariants_random_shapes(n):
+    rng = np.random.default_rng(n)
+    for trial in range(20):
+        ents = _rand_shapes(rng, int(rng.integers(1, 7)), n)
+        p = O.plan_layout(ents, n)
+        ly = p.layers[0]
+        assert ly.total % (16 * n) == 0 and ly.chunk * n == ly.total
+        data = {j: rng.integers(0, 256, size=ly.sizes[j], dtype=np.uint8) for j in ly.entries}
+        t = O.pack(p, 0, data)
+        for j in ly.entries:
+            assert ly.offsets[j] % 16 == 0
+            assert np.array_equal(O.view(p, 0, t, j).reshape(-1), data[j])
+        # bytes outside every entry are zero
+        covered = np.zeros(ly.total, bool)
+        for j in ly.entries:
+            covered[ly.offsets[j]:ly.offsets[j] + ly.sizes[j]] = True
+        assert not t[~covered].any()
+        ch = O.split_chunks(p, 0, t)
+        assert len(ch) == n and all(x.size == ly.chunk for x in ch)
+        assert np.array_equal(O.gather(ch), t)
+        # replicated entries are exactly those whose rows do not divide by N
+        for j, (_, rows, _, _) in enumerate(ents):
+            assert (j in ly.entries) == (rows % n == 0)
+
+
+def test_chunk_size_depends_only_on_total_and_n():
+    # Two layouts with different weight boundaries but the same |T|.
+    a = O.plan_layout([(0, 16, 64, 1), (0, 16, 192, 1)], 4)
+    b = O.plan_layout([(0, 16, 128, 1), (0, 16, 128, 1)], 4)
+    assert a.layers[0].total == b.layers[0].total
+    assert a.layers[0].chunk == b.layers[0].chunk
+    assert a.layers[0].offsets[1] != b.layers[0].offsets[1]
+
+
+def test_chunks_straddle_weights_in_kda_layer():
+    p = _plan_for(WL.ATTN_KDA)
+    ly = p.layers[0]
+    c = ly.chunk
+    straddling = []
+    for i in range(p.n_shards):
+        inside = [j for j in ly.entries if ly.offsets[j] < (i + 1) * c and ly.offsets[j] + ly.sizes[j] > i * c]
+        if len(inside) > 1:
+            straddling.append(i)
+    assert 5 in straddling  # f_b's tail and o's head share chunk 5
+    # boundaries 4, 8 and 12 fall exactly on entry starts
+    starts = set(ly.offsets.values())
+    assert {4 * c, 8 * c, 12 * c} <= starts
+
+
+# ---------------------------------------------------------------------------
+# relayout: per-weight row shards -> flat chunks
+# ---------------------------------------------------------------------------
+
+
+def _relayout_by_byte_formula(p, shards, n):
+    """Independent formulation: chunk byte b of rank i is T byte g = i*C + b; in
+    entry j at local byte u = g - o_j it comes from row shard u // (s_j/N) at
+    offset u % (s_j/N); every other byte is zero."""
+    ly = p.layers[0]
+    c = ly.chunk
+    out = [np.zeros(c, np.uint8) for _ in range(n)]
+    for i in range(n):
+        for b in range(c):
+            g = i * c + b
+            for j in ly.entries:
+                u = g - ly.offsets[j]
+                if 0 <= u < ly.sizes[j]:
+                    per = ly.sizes[j] // n
+                    out[i][b] = shards[j][u // per].reshape(-1)[u % per]
+    return out
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 7])
+def test_relayout_matches_byte_formula(n):
+    rng = np.random.default_rng(100 + n)
+    for trial in range(4):
+        ents = [(0, int(rng.integers(1, 5)) * n, int(rng.integers(1, 40)), 1) for _ in range(int(rng.integers(1, 5)))]
+        p = O.plan_layout(ents, n)
+        ly = p.layers[0]
+        full = {j: rng.integers(0, 256, size=(ents[j][1], ents[j][2]), dtype=np.uint8) for j in ly.entries}
+        shards = {j: WL.row_shards(full[j], n) for j in ly.entries}
+        got = O.relayout(p, 0, shards)
+        want = _relayout_by_byte_formula(p, shards, n)
+        for a, b in zip(got, want):
+            assert np.array_equal(a, b)
+        # and it agrees with packing the full weights and slicing T
+        t = O.pack(p, 0, full)
+        for a, b in zip(got, O.split_chunks(p, 0, t)):
+            assert np.array_equal(a, b)
+
+
+def test_relayout_n1_is_identity_of_pack():
+    ents = [(0, 3, 5, 1), (0, 2, 16, 1)]
+    p = O.plan_layout(ents, 1)
+    rng = np.random.default_rng(7)
+    full = {j: rng.integers(0, 256, size=(r, c), dtype=np.uint8) for j, (_, r, c, _) in enumerate(ents)}
+    ch = O.relayout(p, 0, {j: [full[j]] for j in full})
+    assert len(ch) == 1 and np.array_equal(ch[0], O.pack(p, 0, full))
+
+
+# ---------------------------------------------------------------------------
+# cost model
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("wname", ["tiny_flat_layer", "shared_expert_layer", "attn_kda_layer"])
+def test_per_rank_traffic_is_n_minus_1_over_n_of_s(wname):
+    w = [x for x in WL.WORKLOADS.values() if x.name == wname][0]
+    p = _plan_for(w)
+    s = p.layers[0].total
+    n = p.n_shards
+    for rank in range(n):
+        got = O.gather_bytes_received(p, 0, rank)
+        assert Fraction(got) == Fraction(n - 1, n) * s
+
+
+def test_resident_memory_formula_92_layer_stack():
+    w = WL.STACK92
+    ents = [(layer, e.rows, e.cols, 1) for layer in range(w.n_layers) for e in w.entries]
+    p = O.plan_layout(ents, w.n_shards)
+    r = sum(ly.total for ly in p.layers.values())
+    assert r == 24_310_185_984
+    assert Fraction(O.resident_bytes_per_rank(p)) == Fraction(r, w.n_shards) + 2 * p.slot_bytes
+    assert p.slot_bytes == 264_241_152
+
+
+# ---------------------------------------------------------------------------
+# linear
+# ---------------------------------------------------------------------------
+
+
+def _bf16_values(rng, shape):
+    x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+    return WL.bf16_to_f64(WL.bf16_bits(x))
+
+
+def test_linear_matches_exact_rational_dot_products():
+    rng = np.random.default_rng(5)
+    for (m, out, inn) in [(1, 3, 5), (2, 130, 7), (4, 5, 200), (3, 2, 256)]:
+        q = rng.integers(0, 256, size=(out, inn), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0x11  # no NaN codes
+        s = (2.0 ** rng.uniform(-8, -4, size=(-(-out // 128), -(-inn // 128)))).astype(np.float32)
+        x = _bf16_values(rng, (m, inn))
+        y = O.linear(x, q, s)
+        for a in range(m):
+            for o in range(out):
+                exact = sum(Fraction(float(x[a, i])) * Fraction(float(O.E4M3_TABLE[q[o, i]]))
+                            * Fraction(float(s[o // 128, i // 128])) for i in range(inn))
+                assert abs(Fraction(float(y[a, o])) - exact) <= Fraction(1, 10**12) * (1 + abs(exact))
+
+
+def test_linear_one_hot_selects_dequantized_column():
+    rng = np.random.default_rng(9)
+    q = rng.integers(0, 0x7E, size=(200, 300), dtype=np.uint8)
+    s = (2.0 ** rng.uniform(-8, -4, size=(2, 3))).astype(np.float32)
+    for i in [0, 127, 128, 299]:
+        x = np.zeros((1, 300))
+        x[0, i] = 1.0
+        y = O.linear(x, q, s)[0]
+        col = np.array([O.E4M3_TABLE[q[o, i]] * float(s[o // 128, i // 128]) for o in range(200)])
+        assert np.array_equal(y, col)
+
+
+def test_linear_zero_scales_give_zero():
+    rng = np.random.default_rng(10)
+    q = rng.integers(0, 0x7E, size=(64, 256), dtype=np.uint8)
+    x = _bf16_values(rng, (3, 256))
+    assert not O.linear(x, q, np.zeros((1, 2), np.float32)).any()
+
+
+def test_linear_transposition_and_block_index_are_pinned():
+    # A scale that differs between the two 128-blocks of a row catches a swapped
+    # block index; a non-square weight catches a transposed operand.
+    q = np.full((130, 256), 0x38, np.uint8)  # all ones
+    s = np.array([[1.0, 2.0], [4.0, 8.0]], np.float32)
+    x = np.ones((1, 256))
+    y = O.linear(x, q, s)[0]
+    assert y[0] == 128 * 1.0 + 128 * 2.0 and y[129] == 128 * 4.0 + 128 * 8.0
+
+
+# ---------------------------------------------------------------------------
+# prefill activation quantiser
+# ---------------------------------------------------------------------------
+
+
+def _k_exact(amax: float) -> int:
+    """Smallest integer k with amax <= 448 * 2^k, by exact rational search."""
+    if amax == 0:
+        return 0
+    a = Fraction(amax)
+    k = 0
+    while a > 448 * Fraction(2) ** k:
+        k += 1
+    while a <= 448 * Fraction(2) ** (k - 1):
+        k -= 1
+    return k
+
+
+def test_quantizer_scale_exponent_matches_rational_search():
+    rng = np.random.default_rng(11)
+    x = _bf16_values(rng, (64, 300)) * (2.0 ** rng.integers(-20, 20, size=(64, 1)))
+    x[3] = 0.0
+    x[4, :5] = 448.0
+    x[4, 5:] = 0.0
+    x[5] = 0.0
+    x[5, 0] = 450.0  # next bf16 above 448
+    xq, e = O.quantize_x(x)
+    for m in range(x.shape[0]):
+        for g in range(e.shape[1]):
+            amax = float(np.max(np.abs(x[m, g * 128:(g + 1) * 128])))
+            assert e[m, g] == 2.0 ** _k_exact(amax)
+    assert e[3, 0] == 1.0 and e[4, 0] == 1.0 and e[5, 0] == 2.0
+
+
+def test_quantizer_codes_match_library_cast():
+    rng = np.random.default_rng(12)
+    x = _bf16_values(rng, (32, 512)) * 3.0
+    xq, e = O.quantize_x(x)
+    e_full = np.repeat(e.astype(np.float64), 128, axis=1)[:, :512]
+    ref = torch.from_numpy((x / e_full).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(xq, ref)
+    assert np.all(np.abs(x / e_full) <= 448.0)
+
+
+def test_quantizer_is_invariant_under_doubling():
+    rng = np.random.default_rng(13)
+    x = _bf16_values(rng, (8, 384))
+    xq1, e1 = O.quantize_x(x)
+    xq2, e2 = O.quantize_x(2.0 * x)
+    assert np.array_equal(xq1, xq2) and np.array_equal(2 * e1, e2)
+
+
+def test_quantizer_ragged_group_and_error_bound():
+    rng = np.random.default_rng(14)
+    x = _bf16_values(rng, (4, 200))
+    xq, e = O.quantize_x(x)
+    assert e.shape == (4, 2)
+    xd = O.dequant_x(xq, e)
+    # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 for normal codes, and
+    # absolute error <= half the subnormal step 2^-10 * e below them.
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, np.repeat(e.astype(np.float64), 128, axis=1)[:, :200] * 2.0 ** -10)
+    assert np.all(np.abs(xd - x) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# schedule model
+# ---------------------------------------------------------------------------
+
+
+def test_schedule_slots_alternate_and_first_layer_predispatched():
+    ops = O.schedule(3, 8)
+    gathers = [op for op in ops if op.kind == "gather"]
+    assert [g.layer for g in gathers] == list(range(3, 9))
+    assert [g.slot for g in gathers] == [0, 1, 0, 1, 0, 1]
+    assert ops[1].kind == "gather" and ops[1].layer == 3  # before any compute
+    waits = [op for op in ops if op.kind == "wait_ready"]
+    assert [w.layer for w in waits] == list(range(3, 9))  # once per layer
+
+
+def test_schedule_gates_each_gather_on_the_slot_previous_user():
+    ops = O.schedule(0, 9)
+    for i, op in enumerate(ops):
+        if op.kind == "gather" and op.layer >= 2:
+            prev = ops[i - 1]
+            assert prev.kind == "wait_done" and prev.layer == op.layer - 2 and prev.slot == op.slot
+    assert O.max_live_layers(0, 9) == 2
+    assert O.max_live_layers(5, 5) == 1
+    assert O.schedule(4, 3) == []
