@@ -1,0 +1,228 @@
+/*
+ * sws.h - C ABI of the sharded weight storage library ("store sharded,
+ * compute full"), for NVIDIA GB300 (sm_103a).
+ *
+ * The method (weight-sharding blog, zdszero.github.io/weight_sharding.html):
+ * every layer's replicated weights are packed into one flat byte stream T
+ * (section "一层一次 AllGather：flat layout"); T is cut into N equal chunks, one
+ * per rank; before a layer runs, one gather restores T into one of two
+ * ping-pong slots (section "提前一层：lookahead 与 ping-pong slot") and the
+ * layer's linears read zero-copy views of the slot. Here the N ranks are N
+ * device buffers on one GPU and the AllGather is an on-GPU copy kernel.
+ *
+ * Conventions for every call:
+ *   - Return value: SWS_OK (0), a positive warning, or a negative error code.
+ *     The message of the last error on the calling thread is available from
+ *     sws_last_error(). No C++ exception crosses this boundary and no kernel
+ *     traps; faults of queued GPU work surface as SWS_E_CUDA on a later call.
+ *   - Memory: the caller allocates and owns every device buffer (chunks, row
+ *     shards, slots, scales, activations, outputs, workspace) and keeps it
+ *     alive until the work queued on it has finished. The library allocates
+ *     host objects and CUDA events only; it never calls cudaMalloc.
+ *   - Alignment: every device pointer passed in must be 16-byte aligned
+ *     (SWS_E_ALIGN otherwise).
+ *   - Streams: sws_stream_t is a cudaStream_t; NULL is the legacy default
+ *     stream. All device work is asynchronous with respect to the host.
+ *   - Element types: SWS_E4M3 is OCP FP8 E4M3FN (1 byte), SWS_BF16 2 bytes,
+ *     SWS_F32 4 bytes, SWS_U8 1 byte.
+ */
+#ifndef SWS_H_
+#define SWS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define SWS_OK 0
+/* Some entry has rows % N != 0 and stays replicated, outside T (the blog's
+ * section "只 shard 真正 replicated 的权重": such weights are skipped with a
+ * warning). The plan is still created. */
+#define SWS_W_SKIPPED 1
+#define SWS_E_INVALID (-1)     /* bad argument: N, shape, index, size, layout */
+#define SWS_E_ALIGN (-2)       /* a device pointer is not 16-byte aligned */
+#define SWS_E_STATE (-3)       /* slot holds another layer, or calls out of order */
+#define SWS_E_CUDA (-4)        /* a CUDA runtime call failed (message has the name) */
+#define SWS_E_TIMEOUT (-5)     /* a device-side wait gave up (see sws_ctx_status) */
+#define SWS_E_UNSUPPORTED (-6) /* device is not sm_103, or shape outside a kernel's range */
+#define SWS_E_WORKSPACE (-7)   /* workspace smaller than sws_workspace_bytes() */
+
+/* ---- element types ----------------------------------------------------- */
+#define SWS_E4M3 0
+#define SWS_BF16 1
+#define SWS_F32 2
+#define SWS_U8 3
+
+/* ---- linear weight sources --------------------------------------------- */
+#define SWS_SRC_SLOT0 0 /* view of slot 0 (must hold the entry's layer) */
+#define SWS_SRC_SLOT1 1 /* view of slot 1 (must hold the entry's layer) */
+#define SWS_SRC_FUSED 2 /* read the layer's chunks directly through the chunk map */
+
+/* ---- run_layers flags -------------------------------------------------- */
+#define SWS_RUN_FUSED 1u  /* no gather: every linear reads the chunks directly */
+#define SWS_RUN_TIMING 2u /* record per-layer CUDA events (see sws_run_timing) */
+
+typedef struct CUstream_st* sws_stream_t;
+typedef struct sws_plan sws_plan;
+typedef struct sws_ctx sws_ctx;
+
+/* One weight declared to the planner. rows = out_features (dimension 0, the
+ * one row shards split), cols = in_features; row-major [rows, cols]. */
+typedef struct sws_entry {
+  int32_t layer; /* layer id, 0 <= layer < 2^20 */
+  int32_t dtype; /* SWS_E4M3, SWS_BF16, SWS_F32 or SWS_U8 */
+  int64_t rows;
+  int64_t cols;
+} sws_entry;
+
+/* Activations and outputs of one layer for sws_run_layers: x[k] / y[k] belong
+ * to the k-th entry of that layer in declaration order (replicated entries
+ * included), each x bf16 [m, cols], each y bf16 [m, rows]. */
+typedef struct sws_layer_io {
+  const void* const* x;
+  void* const* y;
+  int64_t m;
+} sws_layer_io;
+
+/* ---- planner (host only, no GPU needed) -------------------------------- */
+
+/* Flat layout (blog section "flat layout", steps 1-2): the sharded entries of
+ * each layer are concatenated in declaration order at offsets o_j that are
+ * multiples of 16 (every entry's byte size is rounded up to 16), |T| is
+ * rounded up to a multiple of 16*N, and C = |T|/N. An entry is sharded iff
+ * rows % N == 0; otherwise it is replicated and the call returns
+ * SWS_W_SKIPPED. n_shards in [1, 256]; rows, cols >= 0; flags must be 0.
+ * On success *out receives a plan owned by the caller (sws_plan_destroy). */
+int sws_plan_create(const sws_entry* entries, int32_t n_entries, int32_t n_shards, uint32_t flags,
+                    sws_plan** out);
+/* Number of layers (highest layer id + 1) and shards. */
+int sws_plan_info(const sws_plan* plan, int32_t* n_layers, int32_t* n_shards, int32_t* n_entries);
+/* |T| of a layer and its chunk size C (both 0 for a layer with no sharded
+ * entry) and how many entries (sharded or not) the layer has. */
+int sws_plan_layer(const sws_plan* plan, int32_t layer, int64_t* total_bytes, int64_t* chunk_bytes,
+                   int32_t* n_entries);
+/* Offset o_j of entry j inside its layer's T (-1 if replicated), its size in
+ * bytes and whether it is sharded. */
+int sws_plan_entry(const sws_plan* plan, int32_t j, int64_t* offset, int64_t* nbytes, int32_t* sharded);
+/* max over layers of |T| - the size each of the two slots needs. */
+int64_t sws_plan_slot_bytes(const sws_plan* plan);
+void sws_plan_destroy(sws_plan* plan);
+
+/* ---- one-time relayout -------------------------------------------------- */
+
+/* Remaps a layer from the loader's per-weight row shards to flat chunks (blog
+ * section "加载：行 shard 先行，finalize 再重排", step 2): chunk i receives T
+ * bytes [i*C, (i+1)*C); a byte at local offset u of sharded entry j comes from
+ * row shard u / (s_j/N) at offset u % (s_j/N); padding bytes are written as 0.
+ *   row_shards: host array of device pointers, [k*N + r] = shard r of the k-th
+ *               sharded entry of the layer (declaration order), each
+ *               (rows/N)*cols*elem bytes, contiguous. Any alignment.
+ *   chunks:     host array of N device pointers, C bytes each, 16-B aligned.
+ * Enqueued on `stream`; source and destination must not overlap. */
+int sws_relayout(const sws_plan* plan, int32_t layer, const void* const* row_shards, void* const* chunks,
+                 sws_stream_t stream);
+
+/* ---- context: resident chunks, two slots, scales, workspace ------------- */
+
+/* Bytes of workspace a context needs for linears with up to max_m rows of
+ * activations (split-K partial sums, counters, the prefill quantiser's output
+ * and the device status word). */
+int64_t sws_workspace_bytes(const sws_plan* plan, int64_t max_m);
+
+/* Creates a context over caller-owned device memory:
+ *   chunks:     host array [n_layers * N] of device pointers, layer-major;
+ *               chunk (l, i) holds C_l bytes. Entries for layers without
+ *               sharded weights may be NULL.
+ *   slot0/1:    two device buffers of at least sws_plan_slot_bytes() bytes.
+ *   scales:     host array [n_entries] of device pointers to float32 block
+ *               scales [ceil(rows/128), ceil(cols/128)] row-major for E4M3
+ *               entries (NULL for other types).
+ *   replicated: host array [n_entries] of device pointers to the full weight
+ *               of each replicated entry (NULL for sharded ones); may be NULL
+ *               when every entry is sharded.
+ *   workspace:  device buffer of workspace_bytes >= sws_workspace_bytes(plan,
+ *               max_m) for the largest m later passed to sws_linear. It is
+ *               zeroed here on the legacy default stream, synchronously.
+ * Every pointer array is copied; the plan must outlive the context. */
+int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void* slot1,
+                   const float* const* scales, const void* const* replicated, void* workspace,
+                   int64_t workspace_bytes, sws_ctx** out);
+void sws_ctx_destroy(sws_ctx* ctx);
+
+/* One layer's gather (blog "flat layout" step 3, all_gather_into_tensor):
+ * slot[i*C : (i+1)*C] = chunk(layer, i) for i in [0, N), a pure byte copy on
+ * `stream` by a TMA bulk-copy kernel. Tags the slot with `layer` (host-side,
+ * in issue order). */
+int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
+
+/* Y = X W_j^T for entry j (blog section "核心抽象": the GEMM sees the full W):
+ *   Y[m, o] = bf16_rne( sum_i x[m, i] * e4m3(q[o, i]) * s[o/128, i/128] ),
+ * fp32 accumulation. W_j is the view slot + o_j (src = SWS_SRC_SLOT0/1; the
+ * slot's tag must equal the entry's layer, else SWS_E_STATE), the chunks
+ * themselves (SWS_SRC_FUSED), or the replicated buffer for entries outside T
+ * (src ignored). x: bf16 [m, cols] row-major; y: bf16 [m, rows] row-major.
+ * m in [0, 2^31): m <= 64 runs the split-K decode kernel (tensor-core MMA on
+ * f16 operands: W is converted exactly, x is rounded to f16, which is exact
+ * for |x| in [2^-24, 65504]); m > 64 runs the prefill path (x quantised by
+ * sws_quantize_x into the workspace, then the tcgen05 block-scaled FP8 GEMM).
+ * Requires E4M3 weights, cols % 16 == 0, and, for m > 64, cols % 128 == 0.
+ * Linears that share a context must not overlap on the GPU (they share the
+ * workspace). */
+int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t m, void* y,
+               sws_stream_t stream);
+
+/* Lookahead over layers first..last (blog "提前一层" and "SGLang 中的实现"):
+ * gather(first) is issued on `side` after `side` waits for work already
+ * queued on `main`; then for each layer l: `side` waits done(l-1) and gathers
+ * layer l+1 into slot (l+1-first) % 2, recording ready(l+1); `main` waits
+ * ready(l) once, runs every linear of layer l on slot (l-first) % 2 and
+ * records done(l). At most two layers' full weights are resident. With
+ * SWS_RUN_FUSED no gather runs and the linears read the chunks directly.
+ * io[l - first] gives layer l's activations and outputs. On return `main`
+ * carries all the work (side-stream work is joined into it). */
+int sws_run_layers(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
+                   sws_stream_t main, sws_stream_t side);
+
+/* After a run with SWS_RUN_TIMING: synchronises on the recorded events and
+ * writes, per layer of that run (n values each, n = last - first + 1):
+ *   exposed_ms[l] - time `main` stood waiting for ready(l) (from the end of
+ *                   layer l-1's linears to the start of layer l's; for the
+ *                   first layer, from the run's start),
+ *   layer_ms[l]   - time from the start to the end of layer l's linears. */
+int sws_run_timing(sws_ctx* ctx, float* exposed_ms, float* layer_ms, int32_t n);
+
+/* Prefill activation quantiser: for each row m and 128-column group g,
+ * ex[m, g] = 2^k with k the smallest integer such that amax <= 448 * 2^k
+ * (1 when the group is all zero), and xq[m, i] = e4m3_rne(x[m, i] / ex[m, g])
+ * (ties to even, saturating). x bf16 [m, k] row-major, xq u8 [m, k],
+ * ex float32 [m, ceil(k/128)]; k % 16 == 0. */
+int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws_stream_t stream);
+
+/* Device-side status of a context: 0, or the SWS_E_* code a kernel recorded
+ * (e.g. SWS_E_TIMEOUT when a wait on a TMA completion gave up). Synchronises
+ * the device. `clear` != 0 resets it. */
+int sws_ctx_status(sws_ctx* ctx, int32_t clear);
+
+/* ---- tracing ------------------------------------------------------------ */
+
+/* Optional device timestamps: each later gather / linear launch of the
+ * context appends one record of 4 uint64 to `records` (device memory,
+ * capacity records): {tag, start_ns, end_ns, 0} where tag = kind << 56 |
+ * layer << 32 | entry (kind 1 = gather, 2 = linear), start_ns is the earliest
+ * %globaltimer read by any CTA at entry and end_ns the latest at exit. Passing
+ * NULL turns tracing off. Records are reset (start = ~0, end = 0) on `stream`.
+ * Returns the number of records written so far through sws_trace_count. */
+int sws_trace_begin(sws_ctx* ctx, uint64_t* records, int32_t capacity, sws_stream_t stream);
+int32_t sws_trace_count(const sws_ctx* ctx);
+
+/* ---- misc --------------------------------------------------------------- */
+const char* sws_last_error(void);
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t sws_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWS_H_ */

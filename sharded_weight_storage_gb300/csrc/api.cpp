@@ -1,0 +1,395 @@
+// Context, linear dispatch and the lookahead slot scheduler.
+//
+// Scheduler: weight-sharding blog (zdszero.github.io/weight_sharding.html),
+// sections "提前一层：lookahead 与 ping-pong slot" and "SGLang 中的实现":
+//   pre_dispatch(first): gather the first layer on the side stream;
+//   per layer l: maybe_dispatch(l+1) - the side stream waits done(l-1), the
+//   gate on the slot that layer l-1 read, then gathers layer l+1 into it and
+//   records ready(l+1); the layer waits ready(l) once ("wait_ready_once",
+//   section "CUDA graph 与 draft 模型"), runs its linears and records done(l).
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "sws_internal.h"
+
+using namespace sws;
+
+struct sws_ctx {
+  const sws_plan* plan = nullptr;
+  int device = 0;
+  std::vector<uint8_t*> chunks;  // [n_layers * N]
+  uint8_t* slot[2] = {nullptr, nullptr};
+  int32_t slot_tag[2] = {-1, -1};
+  std::vector<const float*> scales;
+  std::vector<const uint8_t*> replicated;
+  uint8_t* ws = nullptr;
+  int64_t ws_bytes = 0;
+  int64_t ws_decode = 0;  // bytes of the decode region at the start of ws
+  cudaEvent_t ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+  cudaEvent_t call_start = nullptr, join = nullptr;
+  // timing of the last SWS_RUN_TIMING run
+  std::vector<cudaEvent_t> t_wait, t_begin, t_end;
+  int32_t timed_n = 0;
+  // device trace records
+  uint64_t* trace = nullptr;
+  int32_t trace_cap = 0, trace_next = 0;
+};
+
+namespace {
+
+int32_t* status_word(sws_ctx* c) { return reinterpret_cast<int32_t*>(c->ws); }
+
+uint64_t* next_trace(sws_ctx* c) {
+  if (!c->trace || c->trace_next >= c->trace_cap) return nullptr;
+  return c->trace + 4 * (int64_t)(c->trace_next++);
+}
+
+int64_t prefill_bytes(int64_t m, int64_t cols) {
+  if (m <= 64) return 0;
+  return roundup(m * cols, 256) + roundup(m * cdiv(cols, 128) * 4, 256);
+}
+
+int ensure_events(sws_ctx* c, size_t n) {
+  while (c->t_wait.size() < n) {
+    cudaEvent_t a, b, d;
+    SWS_CUDA_TRY(cudaEventCreate(&a));
+    SWS_CUDA_TRY(cudaEventCreate(&b));
+    SWS_CUDA_TRY(cudaEventCreate(&d));
+    c->t_wait.push_back(a);
+    c->t_begin.push_back(b);
+    c->t_end.push_back(d);
+  }
+  return SWS_OK;
+}
+
+int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
+  const sws_plan* p = c->plan;
+  const LayerPlan& lp = p->layers[layer];
+  c->slot_tag[slot] = layer;
+  if (lp.total == 0) return SWS_OK;
+  GatherLaunch g;
+  g.n = p->n_shards;
+  for (int i = 0; i < g.n; ++i) {
+    g.chunks[i] = c->chunks[(int64_t)layer * g.n + i];
+    if (!g.chunks[i]) return fail(SWS_E_INVALID, "gather: chunk %d of layer %d is NULL", i, layer);
+  }
+  g.chunk_bytes = lp.chunk;
+  g.dst = c->slot[slot];
+  g.status = status_word(c);
+  g.trace = next_trace(c);
+  g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
+  cudaError_t e = launch_gather(g, s);
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
+}
+
+int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s) {
+  const sws_plan* p = c->plan;
+  if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "linear: entry %d", j);
+  const EntryPlan& e = p->entries[j];
+  if (e.dtype != SWS_E4M3) return fail(SWS_E_UNSUPPORTED, "linear: entry %d is not E4M3", j);
+  if (m < 0 || m >= ((int64_t)1 << 31)) return fail(SWS_E_INVALID, "linear: m=%lld", (long long)m);
+  if (m == 0 || e.rows == 0) return SWS_OK;
+  if (!x || !y) return fail(SWS_E_INVALID, "linear: x or y is NULL");
+  if (!aligned16(x) || !aligned16(y)) return fail(SWS_E_ALIGN, "linear: x or y is not 16-byte aligned");
+  if (!c->scales[j]) return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
+  if (e.cols % 16 != 0) return fail(SWS_E_UNSUPPORTED, "linear: cols=%lld is not a multiple of 16", (long long)e.cols);
+  const LayerPlan& lp = p->layers[e.layer];
+  const uint8_t* w = nullptr;
+  bool fused = false;
+  if (!e.sharded) {
+    w = c->replicated[j];
+    if (!w) return fail(SWS_E_INVALID, "linear: replicated entry %d has no buffer", j);
+  } else if (src == SWS_SRC_SLOT0 || src == SWS_SRC_SLOT1) {
+    if (c->slot_tag[src] != e.layer)
+      return fail(SWS_E_STATE, "linear: slot %d holds layer %d, entry %d belongs to layer %d", src, c->slot_tag[src], j,
+                  e.layer);
+    w = c->slot[src] + e.offset;
+  } else if (src == SWS_SRC_FUSED) {
+    fused = true;
+  } else {
+    return fail(SWS_E_INVALID, "linear: src=%d", src);
+  }
+  uint64_t* rec = next_trace(c);
+  const uint64_t tag = (kTraceLinear << 56) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
+  if (m <= 64) {
+    DecodeLaunch d;
+    d.w = fused ? nullptr : w;
+    d.n_chunks = fused ? p->n_shards : 0;
+    for (int i = 0; i < 256; ++i) d.chunks[i] = nullptr;
+    if (fused)
+      for (int i = 0; i < p->n_shards; ++i) {
+        d.chunks[i] = c->chunks[(int64_t)e.layer * p->n_shards + i];
+        if (!d.chunks[i]) return fail(SWS_E_INVALID, "linear: chunk %d of layer %d is NULL", i, e.layer);
+      }
+    d.chunk_bytes = lp.chunk;
+    d.t_offset = fused ? e.offset : 0;
+    d.scales = c->scales[j];
+    d.x = static_cast<const uint16_t*>(x);
+    d.y = static_cast<uint16_t*>(y);
+    d.m = m;
+    d.rows = e.rows;
+    d.cols = e.cols;
+    d.workspace = c->ws;
+    d.workspace_bytes = c->ws_decode;
+    d.trace = rec;
+    d.tag = tag;
+    return launch_decode(d, s);
+  }
+  if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
+  if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+  const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
+  if (c->ws_bytes < need)
+    return fail(SWS_E_WORKSPACE, "linear: workspace %lld < %lld bytes for m=%lld", (long long)c->ws_bytes,
+                (long long)need, (long long)m);
+  uint8_t* xq = c->ws + c->ws_decode;
+  float* ex = reinterpret_cast<float*>(xq + roundup(m * e.cols, 256));
+  int rc = launch_quantize_x(static_cast<const uint16_t*>(x), m, e.cols, xq, ex, s);
+  if (rc != SWS_OK) return rc;
+  PrefillLaunch pl;
+  pl.w = w;
+  pl.scales = c->scales[j];
+  pl.xq = xq;
+  pl.ex = ex;
+  pl.y = static_cast<uint16_t*>(y);
+  pl.m = m;
+  pl.rows = e.rows;
+  pl.cols = e.cols;
+  pl.status = status_word(c);
+  pl.trace = rec;
+  pl.tag = tag;
+  return launch_prefill(pl, s);
+}
+
+int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io, cudaStream_t s) {
+  const LayerPlan& lp = c->plan->layers[layer];
+  if (lp.all.empty()) return SWS_OK;
+  if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
+  for (size_t k = 0; k < lp.all.size(); ++k) {
+    int rc = linear_impl(c, lp.all[k], src, io.x[k], io.m, io.y[k], s);
+    if (rc != SWS_OK) return rc;
+  }
+  return SWS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
+  if (!p || max_m < 0) return -1;
+  int64_t dec = 0;
+  if (decode_workspace_bytes(std::min<int64_t>(std::max<int64_t>(max_m, 1), 64), 1, 16, &dec) != SWS_OK) return -1;
+  int64_t pre = 0;
+  for (const EntryPlan& e : p->entries) pre = std::max(pre, prefill_bytes(max_m, e.cols));
+  return dec + pre;
+}
+
+int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void* slot1, const float* const* scales,
+                   const void* const* replicated, void* workspace, int64_t workspace_bytes, sws_ctx** out) {
+  if (!out) return fail(SWS_E_INVALID, "ctx_create: out is NULL");
+  *out = nullptr;
+  if (!plan) return fail(SWS_E_INVALID, "ctx_create: plan is NULL");
+  int rc = check_device();
+  if (rc != SWS_OK) return rc;
+  const int32_t n = plan->n_shards, L = (int32_t)plan->layers.size(), E = (int32_t)plan->entries.size();
+  if (L > 0 && !chunks) return fail(SWS_E_INVALID, "ctx_create: chunks is NULL");
+  for (int32_t l = 0; l < L; ++l)
+    for (int32_t i = 0; i < n; ++i) {
+      void* ptr = chunks[(int64_t)l * n + i];
+      if (plan->layers[l].total > 0 && !ptr) return fail(SWS_E_INVALID, "ctx_create: chunk (%d, %d) is NULL", l, i);
+      if (ptr && !aligned16(ptr)) return fail(SWS_E_ALIGN, "ctx_create: chunk (%d, %d) is not 16-byte aligned", l, i);
+    }
+  if (plan->slot_bytes > 0 && (!slot0 || !slot1)) return fail(SWS_E_INVALID, "ctx_create: a slot is NULL");
+  if (!aligned16(slot0) || !aligned16(slot1)) return fail(SWS_E_ALIGN, "ctx_create: slot not 16-byte aligned");
+  if (E > 0 && !scales) return fail(SWS_E_INVALID, "ctx_create: scales is NULL");
+  for (int32_t j = 0; j < E; ++j) {
+    if (plan->entries[j].dtype == SWS_E4M3 && !scales[j])
+      return fail(SWS_E_INVALID, "ctx_create: E4M3 entry %d has no scales", j);
+    if (scales[j] && !aligned16(scales[j])) return fail(SWS_E_ALIGN, "ctx_create: scales of entry %d unaligned", j);
+    if (!plan->entries[j].sharded) {
+      const void* r = replicated ? replicated[j] : nullptr;
+      if (r && !aligned16(r)) return fail(SWS_E_ALIGN, "ctx_create: replicated buffer of entry %d unaligned", j);
+    }
+  }
+  const int64_t need = sws_workspace_bytes(plan, 1);
+  if (!workspace || workspace_bytes < need)
+    return fail(SWS_E_WORKSPACE, "ctx_create: workspace %lld < %lld bytes", (long long)workspace_bytes,
+                (long long)need);
+  if (!aligned16(workspace)) return fail(SWS_E_ALIGN, "ctx_create: workspace not 16-byte aligned");
+  sws_ctx* c = new (std::nothrow) sws_ctx();
+  if (!c) return fail(SWS_E_INVALID, "ctx_create: out of host memory");
+  c->plan = plan;
+  cudaGetDevice(&c->device);
+  c->chunks.assign((size_t)L * n, nullptr);
+  for (int64_t i = 0; i < (int64_t)L * n; ++i) c->chunks[i] = static_cast<uint8_t*>(chunks[i]);
+  c->slot[0] = static_cast<uint8_t*>(slot0);
+  c->slot[1] = static_cast<uint8_t*>(slot1);
+  c->scales.assign(E, nullptr);
+  c->replicated.assign(E, nullptr);
+  for (int32_t j = 0; j < E; ++j) {
+    c->scales[j] = scales[j];
+    if (replicated && !plan->entries[j].sharded) c->replicated[j] = static_cast<const uint8_t*>(replicated[j]);
+  }
+  c->ws = static_cast<uint8_t*>(workspace);
+  c->ws_bytes = workspace_bytes;
+  int64_t dec64 = 0;
+  decode_workspace_bytes(64, 1, 16, &dec64);
+  c->ws_decode = std::min(dec64, workspace_bytes);
+  // Only the status word and the split-K arrival counters must start at zero.
+  cudaError_t e = cudaMemset(workspace, 0, (size_t)(kCtlBytes + kMaxCounters * 4));
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "ctx_create: cudaMemset(workspace)");
+  }
+  for (int s = 0; s < 2; ++s) {
+    if ((e = cudaEventCreateWithFlags(&c->ready[s], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->done[s], cudaEventDisableTiming)) != cudaSuccess) {
+      sws_ctx_destroy(c);
+      return cuda_fail(e, "ctx_create: cudaEventCreate");
+    }
+  }
+  if ((e = cudaEventCreateWithFlags(&c->call_start, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess) {
+    sws_ctx_destroy(c);
+    return cuda_fail(e, "ctx_create: cudaEventCreate");
+  }
+  *out = c;
+  return SWS_OK;
+}
+
+void sws_ctx_destroy(sws_ctx* c) {
+  if (!c) return;
+  for (int s = 0; s < 2; ++s) {
+    if (c->ready[s]) cudaEventDestroy(c->ready[s]);
+    if (c->done[s]) cudaEventDestroy(c->done[s]);
+  }
+  if (c->call_start) cudaEventDestroy(c->call_start);
+  if (c->join) cudaEventDestroy(c->join);
+  for (size_t i = 0; i < c->t_wait.size(); ++i) {
+    cudaEventDestroy(c->t_wait[i]);
+    cudaEventDestroy(c->t_begin[i]);
+    cudaEventDestroy(c->t_end[i]);
+  }
+  delete c;
+}
+
+int sws_gather_to_slot(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "gather_to_slot: ctx is NULL");
+  if (layer < 0 || layer >= (int32_t)c->plan->layers.size()) return fail(SWS_E_INVALID, "gather_to_slot: layer %d", layer);
+  if (slot != 0 && slot != 1) return fail(SWS_E_INVALID, "gather_to_slot: slot %d", slot);
+  return gather_impl(c, layer, slot, (cudaStream_t)stream);
+}
+
+int sws_linear(sws_ctx* c, int32_t entry, int32_t src, const void* x, int64_t m, void* y, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "linear: ctx is NULL");
+  return linear_impl(c, entry, src, x, m, y, (cudaStream_t)stream);
+}
+
+int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
+                   sws_stream_t main_s, sws_stream_t side_s) {
+  if (!c) return fail(SWS_E_INVALID, "run_layers: ctx is NULL");
+  const int32_t L = (int32_t)c->plan->layers.size();
+  if (last < first) return SWS_OK;
+  if (first < 0 || last >= L) return fail(SWS_E_INVALID, "run_layers: range [%d, %d] outside [0, %d)", first, last, L);
+  if (!io) return fail(SWS_E_INVALID, "run_layers: io is NULL");
+  if (flags & ~(SWS_RUN_FUSED | SWS_RUN_TIMING)) return fail(SWS_E_INVALID, "run_layers: flags 0x%x", flags);
+  cudaStream_t ms = (cudaStream_t)main_s, ss = (cudaStream_t)side_s;
+  const bool timing = (flags & SWS_RUN_TIMING) != 0;
+  const int32_t n = last - first + 1;
+  if (timing) {
+    int rc = ensure_events(c, (size_t)n);
+    if (rc != SWS_OK) return rc;
+    c->timed_n = n;
+  } else {
+    c->timed_n = 0;
+  }
+  if (flags & SWS_RUN_FUSED) {
+    for (int32_t l = first; l <= last; ++l) {
+      if (timing) {
+        SWS_CUDA_TRY(cudaEventRecord(c->t_wait[l - first], ms));
+        SWS_CUDA_TRY(cudaEventRecord(c->t_begin[l - first], ms));
+      }
+      int rc = layer_linears(c, l, SWS_SRC_FUSED, io[l - first], ms);
+      if (rc != SWS_OK) return rc;
+      if (timing) SWS_CUDA_TRY(cudaEventRecord(c->t_end[l - first], ms));
+    }
+    return SWS_OK;
+  }
+  if (ss == ms) return fail(SWS_E_INVALID, "run_layers: main and side streams must differ");
+  auto slot_of = [&](int32_t l) { return (l - first) & 1; };
+  // pre_dispatch(first): the side stream starts after work already on main.
+  SWS_CUDA_TRY(cudaEventRecord(c->call_start, ms));
+  if (timing) SWS_CUDA_TRY(cudaEventRecord(c->t_wait[0], ms));
+  SWS_CUDA_TRY(cudaStreamWaitEvent(ss, c->call_start, 0));
+  int rc = gather_impl(c, first, slot_of(first), ss);
+  if (rc != SWS_OK) return rc;
+  SWS_CUDA_TRY(cudaEventRecord(c->ready[slot_of(first)], ss));
+  for (int32_t l = first; l <= last; ++l) {
+    const int32_t nxt = l + 1;
+    if (nxt <= last) {  // maybe_dispatch(l + 1)
+      if (l - 1 >= first) SWS_CUDA_TRY(cudaStreamWaitEvent(ss, c->done[slot_of(l - 1)], 0));
+      rc = gather_impl(c, nxt, slot_of(nxt), ss);
+      if (rc != SWS_OK) return rc;
+      SWS_CUDA_TRY(cudaEventRecord(c->ready[slot_of(nxt)], ss));
+    }
+    if (timing && l > first) SWS_CUDA_TRY(cudaEventRecord(c->t_wait[l - first], ms));
+    SWS_CUDA_TRY(cudaStreamWaitEvent(ms, c->ready[slot_of(l)], 0));  // wait once
+    if (timing) SWS_CUDA_TRY(cudaEventRecord(c->t_begin[l - first], ms));
+    rc = layer_linears(c, l, slot_of(l), io[l - first], ms);
+    if (rc != SWS_OK) return rc;
+    if (timing) SWS_CUDA_TRY(cudaEventRecord(c->t_end[l - first], ms));
+    SWS_CUDA_TRY(cudaEventRecord(c->done[slot_of(l)], ms));  // update_done_event(l)
+  }
+  SWS_CUDA_TRY(cudaEventRecord(c->join, ss));
+  SWS_CUDA_TRY(cudaStreamWaitEvent(ms, c->join, 0));
+  return SWS_OK;
+}
+
+int sws_run_timing(sws_ctx* c, float* exposed_ms, float* layer_ms, int32_t n) {
+  if (!c) return fail(SWS_E_INVALID, "run_timing: ctx is NULL");
+  if (c->timed_n == 0) return fail(SWS_E_STATE, "run_timing: the last run had no SWS_RUN_TIMING");
+  if (n < c->timed_n) return fail(SWS_E_INVALID, "run_timing: n=%d < %d layers", n, c->timed_n);
+  SWS_CUDA_TRY(cudaEventSynchronize(c->t_end[c->timed_n - 1]));
+  for (int32_t i = 0; i < c->timed_n; ++i) {
+    float a = 0.f, b = 0.f;
+    SWS_CUDA_TRY(cudaEventElapsedTime(&a, c->t_wait[i], c->t_begin[i]));
+    SWS_CUDA_TRY(cudaEventElapsedTime(&b, c->t_begin[i], c->t_end[i]));
+    if (exposed_ms) exposed_ms[i] = a;
+    if (layer_ms) layer_ms[i] = b;
+  }
+  return SWS_OK;
+}
+
+int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws_stream_t stream) {
+  return launch_quantize_x(static_cast<const uint16_t*>(x), m, k, static_cast<uint8_t*>(xq), ex,
+                           (cudaStream_t)stream);
+}
+
+int sws_ctx_status(sws_ctx* c, int32_t clear) {
+  if (!c) return fail(SWS_E_INVALID, "ctx_status: ctx is NULL");
+  int32_t v = 0;
+  SWS_CUDA_TRY(cudaDeviceSynchronize());
+  SWS_CUDA_TRY(cudaMemcpy(&v, c->ws, sizeof v, cudaMemcpyDeviceToHost));
+  if (clear) SWS_CUDA_TRY(cudaMemset(c->ws, 0, sizeof v));
+  return v;
+}
+
+int sws_trace_begin(sws_ctx* c, uint64_t* records, int32_t capacity, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "trace_begin: ctx is NULL");
+  if (records && (capacity < 0 || !aligned16(records))) return fail(SWS_E_INVALID, "trace_begin: bad buffer");
+  c->trace = records;
+  c->trace_cap = records ? capacity : 0;
+  c->trace_next = 0;
+  if (records) {
+    cudaError_t e = launch_trace_reset(records, capacity, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace_begin: reset kernel");
+  }
+  return SWS_OK;
+}
+
+int32_t sws_trace_count(const sws_ctx* c) { return c ? c->trace_next : -1; }
+
+}  // extern "C"

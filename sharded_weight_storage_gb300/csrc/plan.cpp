@@ -1,0 +1,196 @@
+// Host-side flat-layout planner and the relayout segment builder.
+//
+// Layout rule: weight-sharding blog (zdszero.github.io/weight_sharding.html),
+// section "一层一次 AllGather：flat layout", steps 1-2: a layer's weights are
+// concatenated in order, each padded to 16 bytes, the total padded to a
+// multiple of 16*N, and T is cut into N byte-equal chunks of C = |T|/N.
+// Eligibility: section "只 shard 真正 replicated 的权重": weights whose row
+// count does not divide by N are skipped (kept replicated) with a warning.
+// Relayout: section "加载：行 shard 先行，finalize 再重排", step 2.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <new>
+
+#include "sws_internal.h"
+
+namespace sws {
+
+static thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SWS_E_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_bytes(int32_t dtype) {
+  switch (dtype) {
+    case SWS_E4M3: return 1;
+    case SWS_BF16: return 2;
+    case SWS_F32: return 4;
+    case SWS_U8: return 1;
+    default: return 0;
+  }
+}
+
+}  // namespace sws
+
+using namespace sws;
+
+extern "C" {
+
+const char* sws_last_error(void) { return g_last_error.c_str(); }
+
+int32_t sws_version(void) { return 100; }
+
+int sws_plan_create(const sws_entry* entries, int32_t n_entries, int32_t n_shards, uint32_t flags,
+                    sws_plan** out) {
+  if (!out) return fail(SWS_E_INVALID, "plan_create: out is NULL");
+  *out = nullptr;
+  if (n_entries < 0 || (n_entries > 0 && !entries)) return fail(SWS_E_INVALID, "plan_create: bad entry list");
+  if (n_shards < 1 || n_shards > 256) return fail(SWS_E_INVALID, "plan_create: N=%d outside [1, 256]", n_shards);
+  if (flags != 0) return fail(SWS_E_INVALID, "plan_create: unknown flags 0x%x", flags);
+  sws_plan* p = new (std::nothrow) sws_plan();
+  if (!p) return fail(SWS_E_INVALID, "plan_create: out of host memory");
+  p->n_shards = n_shards;
+  p->flags = flags;
+  int32_t n_layers = 0;
+  for (int32_t j = 0; j < n_entries; ++j) {
+    const sws_entry& e = entries[j];
+    int eb = elem_bytes(e.dtype);
+    if (e.layer < 0 || e.layer >= (1 << 20) || e.rows < 0 || e.cols < 0 || eb == 0 ||
+        (e.cols > 0 && e.rows > (int64_t(1) << 40) / (e.cols * eb))) {
+      delete p;
+      return fail(SWS_E_INVALID, "plan_create: entry %d has layer %d, shape [%lld, %lld], dtype %d", j, e.layer,
+                  (long long)e.rows, (long long)e.cols, e.dtype);
+    }
+    n_layers = std::max(n_layers, e.layer + 1);
+  }
+  p->layers.resize(n_layers);
+  p->entries.resize(n_entries);
+  bool skipped = false;
+  for (int32_t j = 0; j < n_entries; ++j) {
+    const sws_entry& e = entries[j];
+    EntryPlan& ep = p->entries[j];
+    LayerPlan& lp = p->layers[e.layer];
+    ep.layer = e.layer;
+    ep.dtype = e.dtype;
+    ep.rows = e.rows;
+    ep.cols = e.cols;
+    ep.elem = elem_bytes(e.dtype);
+    ep.bytes = e.rows * e.cols * ep.elem;
+    ep.sharded = (e.rows % n_shards) == 0;
+    ep.index_in_layer = (int32_t)lp.all.size();
+    lp.all.push_back(j);
+    if (!ep.sharded) {
+      skipped = true;
+      continue;
+    }
+    ep.offset = lp.total;           // o_j
+    lp.total += roundup(ep.bytes, 16);  // each entry padded to 16 B
+    lp.sharded.push_back(j);
+  }
+  for (LayerPlan& lp : p->layers) {
+    lp.total = roundup(lp.total, 16 * (int64_t)n_shards);  // total padded to 16*N
+    lp.chunk = lp.total / n_shards;                         // C = |T|/N
+    p->slot_bytes = std::max(p->slot_bytes, lp.total);
+  }
+  *out = p;
+  if (skipped) {
+    fail(SWS_W_SKIPPED, "plan_create: some entries have rows %% N != 0 and stay replicated");
+    return SWS_W_SKIPPED;
+  }
+  return SWS_OK;
+}
+
+int sws_plan_info(const sws_plan* p, int32_t* n_layers, int32_t* n_shards, int32_t* n_entries) {
+  if (!p) return fail(SWS_E_INVALID, "plan_info: plan is NULL");
+  if (n_layers) *n_layers = (int32_t)p->layers.size();
+  if (n_shards) *n_shards = p->n_shards;
+  if (n_entries) *n_entries = (int32_t)p->entries.size();
+  return SWS_OK;
+}
+
+int sws_plan_layer(const sws_plan* p, int32_t layer, int64_t* total, int64_t* chunk, int32_t* n_entries) {
+  if (!p) return fail(SWS_E_INVALID, "plan_layer: plan is NULL");
+  if (layer < 0 || layer >= (int32_t)p->layers.size()) return fail(SWS_E_INVALID, "plan_layer: layer %d", layer);
+  const LayerPlan& lp = p->layers[layer];
+  if (total) *total = lp.total;
+  if (chunk) *chunk = lp.chunk;
+  if (n_entries) *n_entries = (int32_t)lp.all.size();
+  return SWS_OK;
+}
+
+int sws_plan_entry(const sws_plan* p, int32_t j, int64_t* offset, int64_t* nbytes, int32_t* sharded) {
+  if (!p) return fail(SWS_E_INVALID, "plan_entry: plan is NULL");
+  if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "plan_entry: entry %d", j);
+  const EntryPlan& e = p->entries[j];
+  if (offset) *offset = e.offset;
+  if (nbytes) *nbytes = e.bytes;
+  if (sharded) *sharded = e.sharded ? 1 : 0;
+  return SWS_OK;
+}
+
+int64_t sws_plan_slot_bytes(const sws_plan* p) { return p ? p->slot_bytes : -1; }
+
+void sws_plan_destroy(sws_plan* p) { delete p; }
+
+int sws_relayout(const sws_plan* p, int32_t layer, const void* const* row_shards, void* const* chunks,
+                 sws_stream_t stream) {
+  if (!p) return fail(SWS_E_INVALID, "relayout: plan is NULL");
+  if (layer < 0 || layer >= (int32_t)p->layers.size()) return fail(SWS_E_INVALID, "relayout: layer %d", layer);
+  const LayerPlan& lp = p->layers[layer];
+  const int32_t n = p->n_shards;
+  if (lp.total == 0) return SWS_OK;
+  if (!chunks) return fail(SWS_E_INVALID, "relayout: chunks is NULL");
+  if (!lp.sharded.empty() && !row_shards) return fail(SWS_E_INVALID, "relayout: row_shards is NULL");
+  for (int32_t i = 0; i < n; ++i) {
+    if (!chunks[i]) return fail(SWS_E_INVALID, "relayout: chunk %d is NULL", i);
+    if (!aligned16(chunks[i])) return fail(SWS_E_ALIGN, "relayout: chunk %d is not 16-byte aligned", i);
+  }
+  for (size_t k = 0; k < lp.sharded.size(); ++k)
+    for (int32_t r = 0; r < n; ++r)
+      if (p->entries[lp.sharded[k]].bytes > 0 && !row_shards[k * n + r])
+        return fail(SWS_E_INVALID, "relayout: row shard %d of sharded entry %zu is NULL", r, k);
+  // Walk T once, cutting it into maximal runs that stay inside one chunk and
+  // one source (a row shard, or padding).
+  std::vector<CopySeg> segs;
+  const int64_t c = lp.chunk;
+  auto emit = [&](int64_t g0, int64_t g1, const uint8_t* src) {  // T bytes [g0, g1)
+    while (g0 < g1) {
+      int64_t ci = g0 / c, in_chunk = g0 - ci * c;
+      int64_t len = std::min(g1 - g0, c - in_chunk);
+      segs.push_back(CopySeg{src, static_cast<uint8_t*>(chunks[ci]) + in_chunk, len});
+      if (src) src += len;
+      g0 += len;
+    }
+  };
+  int64_t g = 0;
+  for (size_t k = 0; k < lp.sharded.size(); ++k) {
+    const EntryPlan& e = p->entries[lp.sharded[k]];
+    const int64_t per = e.bytes / n;  // bytes of one row shard
+    for (int32_t r = 0; r < n && per > 0; ++r)
+      emit(e.offset + r * per, e.offset + (r + 1) * per, static_cast<const uint8_t*>(row_shards[k * n + r]));
+    int64_t end = e.offset + e.bytes;
+    int64_t next = (k + 1 < lp.sharded.size()) ? p->entries[lp.sharded[k + 1]].offset : lp.total;
+    if (next > end) emit(end, next, nullptr);  // padding after the entry
+    g = next;
+  }
+  if (lp.sharded.empty()) emit(0, lp.total, nullptr);
+  (void)g;
+  cudaError_t e = launch_relayout(segs, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "relayout kernel launch");
+  return SWS_OK;
+}
+
+}  // extern "C"

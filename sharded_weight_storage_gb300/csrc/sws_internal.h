@@ -1,0 +1,128 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "sws.h"
+
+namespace sws {
+
+// ---- errors -----------------------------------------------------------------
+// Records a message for sws_last_error() and returns `code`.
+int fail(int code, const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+#define SWS_CUDA_TRY(expr)                                   \
+  do {                                                       \
+    cudaError_t _e = (expr);                                 \
+    if (_e != cudaSuccess) return ::sws::cuda_fail(_e, #expr); \
+  } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t roundup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int elem_bytes(int32_t dtype);  // 0 for an unknown type
+
+// ---- plan ------------------------------------------------------------------
+struct EntryPlan {
+  int32_t layer = 0, dtype = 0;
+  int64_t rows = 0, cols = 0, elem = 1, bytes = 0;
+  bool sharded = false;
+  int64_t offset = -1;       // o_j inside the layer's T, -1 if replicated
+  int32_t index_in_layer = 0; // position among all entries of the layer
+};
+
+struct LayerPlan {
+  std::vector<int32_t> sharded;  // entry ids packed into T, in order
+  std::vector<int32_t> all;      // every entry id of the layer, in order
+  int64_t total = 0, chunk = 0;
+};
+
+// ---- device status word and trace records (inside the workspace) -----------
+// Workspace layout (bytes):
+//   [0, 256)        control: status word (int32 at 0)
+//   [256, 256+CNT)  split-K arrival counters (int32 per row block)
+//   then            split-K partial sums (fp32)
+//   then            prefill quantiser output (xq bytes, then ex floats)
+constexpr int64_t kCtlBytes = 256;
+constexpr int64_t kMaxCounters = 1 << 16;
+
+// Kinds written into trace tags.
+constexpr uint64_t kTraceGather = 1, kTraceLinear = 2;
+
+// Device-side wait limit for mbarrier / TMA waits, in nanoseconds of
+// %globaltimer. A wait that runs out sets the status word and the kernel exits.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---- kernel launchers (defined in the .cu files) -----------------------------
+int device_sm_count();
+int check_device();  // SWS_OK if the current device is sm_103, else an error code
+
+struct GatherLaunch {
+  const uint8_t* chunks[256];
+  int32_t n;
+  int64_t chunk_bytes;
+  uint8_t* dst;
+  int32_t* status;
+  uint64_t* trace;  // record (4 x u64) or nullptr
+  uint64_t tag;     // written into the record's tag field
+};
+cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t s);
+
+struct CopySeg {
+  const uint8_t* src;  // nullptr: fill with zeros
+  uint8_t* dst;
+  int64_t len;
+};
+cudaError_t launch_relayout(const std::vector<CopySeg>& segs, cudaStream_t s);
+
+// Weight address map: for the slot path, row o starts at base + o * cols.
+// For the fused path, byte g = off + o * cols + k of T lives in
+// chunks[g / chunk] at g % chunk.
+struct DecodeLaunch {
+  const uint8_t* w;          // slot view (or nullptr for fused)
+  const uint8_t* chunks[256];
+  int32_t n_chunks;
+  int64_t chunk_bytes;
+  int64_t t_offset;          // o_j for fused addressing
+  const float* scales;
+  const uint16_t* x;         // bf16 [m, cols]
+  uint16_t* y;               // bf16 [m, rows]
+  int64_t m, rows, cols;
+  uint8_t* workspace;        // control + counters + partials
+  int64_t workspace_bytes;
+  uint64_t* trace;
+  uint64_t tag;
+};
+int decode_workspace_bytes(int64_t m, int64_t rows, int64_t cols, int64_t* bytes);
+int launch_decode(const DecodeLaunch& a, cudaStream_t s);
+
+int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, float* ex, cudaStream_t s);
+
+struct PrefillLaunch {
+  const uint8_t* w;      // fp8 [rows, cols] (slot view or replicated buffer)
+  const float* scales;   // [ceil(rows/128), cols/128]
+  const uint8_t* xq;     // fp8 [m, cols]
+  const float* ex;       // [m, cols/128]
+  uint16_t* y;           // bf16 [m, rows]
+  int64_t m, rows, cols;
+  int32_t* status;
+  uint64_t* trace;
+  uint64_t tag;
+};
+int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
+
+cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);
+
+}  // namespace sws
+
+struct sws_plan {
+  int32_t n_shards = 1;
+  uint32_t flags = 0;
+  std::vector<sws::EntryPlan> entries;
+  std::vector<sws::LayerPlan> layers;
+  int64_t slot_bytes = 0;
+};

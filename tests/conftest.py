@@ -14,3 +14,17 @@ def pytest_configure(config):
 
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def swslib():
+    """Builds libsws.so in-tree if it is missing or stale, then loads it."""
+    from sharded_weight_storage_gb300 import build as B
+    B.build()
+    import sharded_weight_storage_gb300 as S
+    return S
+
+
+def cuda_ok():
+    import torch
+    return torch.cuda.is_available()

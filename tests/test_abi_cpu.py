@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: every symbol the header declares is exported, the
+planner agrees with the oracle, and bad arguments give the documented codes."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+from conftest import ROOT
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "sws.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sws_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(swslib):
+    lib = swslib.lib()
+    names = _header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+    from sharded_weight_storage_gb300 import _lib
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_version(swslib):
+    assert swslib.lib().sws_version() >= 100
+
+
+def _compare_plan(S, ents, n):
+    plan = S.Plan([(l, S.E4M3 if eb == 1 else {2: S.BF16, 4: S.F32}[eb], r, c) for (l, r, c, eb) in ents], n)
+    ref = O.plan_layout(ents, n)
+    n_layers, n_shards, n_entries = plan.info()
+    assert n_shards == n and n_entries == len(ents)
+    assert n_layers == (max(e[0] for e in ents) + 1 if ents else 0)
+    for l in range(n_layers):
+        total, chunk, ne = plan.layer(l)
+        ly = ref.layers.get(l)
+        if ly is None:
+            assert total == 0 and chunk == 0 and ne == 0
+            continue
+        assert (total, chunk) == (ly.total, ly.chunk)
+        assert ne == sum(1 for e in ents if e[0] == l)
+    for j in range(len(ents)):
+        off, nb, sh = plan.entry(j)
+        assert sh == ref.sharded[j]
+        assert nb == ents[j][1] * ents[j][2] * ents[j][3]
+        if sh:
+            assert off == ref.layers[ents[j][0]].offsets[j]
+        else:
+            assert off == -1
+    assert plan.slot_bytes == ref.slot_bytes
+
+
+@pytest.mark.parametrize("w", [WL.TINY, WL.SHARED_EXPERT, WL.ATTN_KDA, WL.PREFILL], ids=lambda w: w.name)
+def test_planner_matches_oracle_on_workloads(swslib, w):
+    _compare_plan(swslib, [(0, e.rows, e.cols, 1) for e in w.entries], w.n_shards)
+
+
+def test_planner_matches_oracle_on_92_layer_stack(swslib):
+    w = WL.STACK92
+    _compare_plan(swslib, [(l, e.rows, e.cols, 1) for l in range(w.n_layers) for e in w.entries], w.n_shards)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 7, 8, 16, 256])
+def test_planner_matches_oracle_random(swslib, n):
+    rng = np.random.default_rng(1000 + n)
+    import warnings
+    for _ in range(25):
+        ents = []
+        for _ in range(int(rng.integers(1, 9))):
+            rows = int(rng.integers(0, 6)) * n if rng.random() < 0.75 else int(rng.integers(1, 50))
+            ents.append((int(rng.integers(0, 4)), rows, int(rng.integers(0, 90)), int(rng.choice([1, 2, 4]))))
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            _compare_plan(swslib, ents, n)
+
+
+def test_skipped_entries_warn_and_stay_out_of_T(swslib):
+    S = swslib
+    with pytest.warns(RuntimeWarning):
+        plan = S.Plan([(0, S.E4M3, 6, 16), (0, S.E4M3, 8, 16)], 4)
+    assert plan.status == S.W_SKIPPED
+    assert plan.entry(0) == (-1, 96, False)
+    assert plan.entry(1) == (0, 128, True)
+    assert plan.layer(0) == (128, 32, 2)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=0), dict(n=257), dict(rows=-1), dict(cols=-5), dict(dtype=9), dict(layer=-1), dict(flags=1),
+])
+def test_plan_create_rejects_bad_arguments(swslib, bad):
+    S = swslib
+    n = bad.get("n", 4)
+    ent = (bad.get("layer", 0), bad.get("dtype", S.E4M3), bad.get("rows", 8), bad.get("cols", 16))
+    with pytest.raises(S.SwsError) as ei:
+        S.Plan([ent], n, bad.get("flags", 0))
+    assert ei.value.code == S.E_INVALID
+
+
+def test_empty_plan_and_empty_layers(swslib):
+    S = swslib
+    plan = S.Plan([], 4)
+    assert plan.info() == (0, 4, 0) and plan.slot_bytes == 0
+    plan = S.Plan([(2, S.E4M3, 4, 16)], 4)
+    assert plan.layer(0) == (0, 0, 0) and plan.layer(1) == (0, 0, 0)
+    assert plan.layer(2) == (64, 16, 1)
+    with pytest.raises(S.SwsError):
+        plan.layer(3)
+    with pytest.raises(S.SwsError):
+        plan.entry(1)
+
+
+def test_workspace_bytes_grows_with_prefill_m(swslib):
+    S = swslib
+    plan = S.Plan([(0, S.E4M3, 256, 512)], 4)
+    a, b, c = S.workspace_bytes(plan, 1), S.workspace_bytes(plan, 64), S.workspace_bytes(plan, 4096)
+    assert 0 < a <= b < c
+    assert c - b >= 4096 * 512 + 4096 * 4 * 4
+
+
+def test_relayout_validates_before_any_launch(swslib):
+    S = swslib
+    plan = S.Plan([(0, S.E4M3, 8, 16)], 4)
+    with pytest.raises(S.SwsError) as ei:
+        S.relayout(plan, 0, [16] * 4, [0, 0, 0, 0])
+    assert ei.value.code == S.E_INVALID
+    with pytest.raises(S.SwsError) as ei:
+        S.relayout(plan, 0, [16] * 4, [17, 32, 48, 64])
+    assert ei.value.code == S.E_ALIGN
+    with pytest.raises(S.SwsError):
+        S.relayout(plan, 1, [16] * 4, [16, 32, 48, 64])

@@ -1,0 +1,138 @@
+"""Lookahead scheduler on the GPU: per-layer outputs against the oracle, the
+happens-before edges of the oracle's schedule model checked on device
+timestamps, at most two layers resident, and the fused (no-slot) mode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from helpers import assert_close, bf16_tensor_to_f64, build_stack, draw_layers, workload_entries
+
+pytestmark = pytest.mark.gpu
+
+STACK = WL.scaled_workload(WL.STACK92, rows_div=16, cols_div=16, n_layers=7, name="stack7_div16")
+
+
+@pytest.fixture(scope="module")
+def S(swslib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return swslib
+
+
+@pytest.fixture(scope="module")
+def stack(S):
+    ents = workload_entries(STACK)
+    layers = draw_layers(STACK)
+    st = build_stack(S, ents, STACK.n_shards, layers)
+    return st, layers
+
+
+def _io(st, first, last, m, key=STACK.key):
+    xs, ys, io = {}, {}, []
+    for l in range(first, last + 1):
+        js = st.layer_entries(l)
+        xl = [WL.draw_x(key, j, m, st.entries[j][3]).cuda() for j in js]
+        yl = [torch.full((m, st.entries[j][2]), float("nan"), dtype=torch.bfloat16, device="cuda") for j in js]
+        for j, a, b in zip(js, xl, yl):
+            xs[j], ys[j] = a, b
+        io.append(([a.data_ptr() for a in xl], [b.data_ptr() for b in yl], m))
+    return xs, ys, io
+
+
+def _records(rec, n):
+    r = rec[: 4 * n].view(n, 4).cpu().numpy().astype(np.uint64)
+    out = []
+    for tag, t0, t1, _ in r:
+        kind, layer = int(tag) >> 56, (int(tag) >> 32) & 0xFFFFFF
+        out.append((kind, layer, int(t0), int(t1)))
+    return out
+
+
+@pytest.mark.parametrize("first,last", [(0, 6), (1, 5), (2, 2), (3, 4)])
+def test_run_layers_outputs_and_ordering(S, stack, first, last):
+    st, layers = stack
+    m = 8
+    xs, ys, io = _io(st, first, last, m)
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    rec = torch.zeros(4 * 256, dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
+    st.ctx.trace_begin(rec.data_ptr(), 256, main.cuda_stream)
+    st.ctx.run_layers(first, last, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    n_rec = st.ctx.trace_count()
+    st.ctx.trace_begin(0, 0, 0)
+    exposed, layer_ms = st.ctx.run_timing(last - first + 1)
+    assert all(v >= 0 for v in exposed + layer_ms)
+    assert st.ctx.status() == 0
+    # outputs
+    for l in range(first, last + 1):
+        for j in st.layer_entries(l):
+            x = xs[j].cpu()
+            ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(x)), layers[l].codes[j], layers[l].scales[j])
+            assert_close(bf16_tensor_to_f64(ys[j]), ref, f"layer {l} entry {j}")
+    # ordering on device timestamps
+    recs = _records(rec, n_rec)
+    gathers = {l: (t0, t1) for k, l, t0, t1 in recs if k == 1}
+    lin = {}
+    for k, l, t0, t1 in recs:
+        if k == 2:
+            a, b = lin.get(l, (t0, t1))
+            lin[l] = (min(a, t0), max(b, t1))
+    assert sorted(gathers) == list(range(first, last + 1))
+    assert sorted(lin) == list(range(first, last + 1))
+    for (kb, lb), (ka, la) in O.happens_before(first, last):
+        before = gathers[lb] if kb == "gather" else lin[lb]
+        after = gathers[la] if ka == "gather" else lin[la]
+        assert after[0] >= before[1], f"{kb}({lb}) must end before {ka}({la}) starts"
+    # at most two layers hold full weights at any time
+    events = []
+    for l in range(first, last + 1):
+        events += [(gathers[l][0], 1), (lin[l][1], -1)]
+    live = peak = 0
+    for _, d in sorted(events, key=lambda e: (e[0], e[1])):
+        live += d
+        peak = max(peak, live)
+    assert peak <= O.max_live_layers(first, last) <= 2
+
+
+def test_fused_mode_matches_slot_mode_bitwise(S, stack):
+    st, layers = stack
+    m = 32
+    xs, ys, io = _io(st, 0, 6, m)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    st.ctx.run_layers(0, 6, io, 0, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    ref = {j: y.clone() for j, y in ys.items()}
+    for y in ys.values():
+        y.fill_(float("nan"))
+    torch.cuda.synchronize()
+    st.ctx.run_layers(0, 6, io, S.RUN_FUSED, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    for j in ys:
+        assert torch.equal(ys[j], ref[j]), f"entry {j}"
+
+
+def test_run_layers_repeated_calls_reuse_slots(S, stack):
+    st, layers = stack
+    m = 1
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    for first, last in [(0, 3), (4, 6), (0, 6), (5, 6)]:
+        xs, ys, io = _io(st, first, last, m)
+        st.ctx.run_layers(first, last, io, 0, main.cuda_stream, side.cuda_stream)
+        main.synchronize()
+        for l in range(first, last + 1):
+            for j in st.layer_entries(l):
+                ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[l].codes[j], layers[l].scales[j])
+                assert_close(bf16_tensor_to_f64(ys[j]), ref, f"({first},{last}) layer {l} entry {j}")
+
+
+def test_run_layers_rejects_bad_ranges(S, stack):
+    st, _ = stack
+    with pytest.raises(S.SwsError):
+        st.ctx.run_layers(0, 7, [([], [], 1)] * 8, 0, 0, torch.cuda.Stream().cuda_stream)
+    with pytest.raises(S.SwsError):
+        s = torch.cuda.Stream().cuda_stream
+        st.ctx.run_layers(0, 0, [([0, 0], [0, 0], 1)], 0, s, s)

@@ -192,3 +192,9 @@ def row_shards(codes: np.ndarray, n: int) -> List[np.ndarray]:
     assert rows % n == 0
     k = rows // n
     return [np.ascontiguousarray(codes[r * k:(r + 1) * k]) for r in range(n)]
+
+
+def apply_row_signs(codes, signs):
+    """Layer codes of a stack: base codes with each row's sign bit flipped where
+    signs[row] == 0x80. Works on numpy arrays and torch tensors alike."""
+    return codes ^ signs[:, None]
