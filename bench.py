@@ -199,8 +199,8 @@ def run_ours(args, dist):
     import numpy as np
     import torch
 
-    from sharded_weight_storage_gb300 import build as B
-    B.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sharded_weight_storage_gb300 as S
     import workloads as WL
     from sharded_weight_storage_gb300.storage import ShardedStack

@@ -19,8 +19,8 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 @pytest.fixture(scope="session")
 def swslib():
     """Builds libsws.so in-tree if it is missing or stale, then loads it."""
-    from sharded_weight_storage_gb300 import build as B
-    B.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sharded_weight_storage_gb300 as S
     return S
 
