@@ -173,6 +173,30 @@ int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t s
 int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t m, void* y,
                sws_stream_t stream);
 
+/* Decode linear that allocates nothing. The paper has no counterpart to this
+ * call; it serves callers that cannot give the library memory. An inference engine
+ * that sizes its KV-cache pool from the memory left free after loading the
+ * weights has no headroom for allocations made later, and a device allocation
+ * in the middle of a decode step can stall the whole GPU; such a caller passes
+ * only its inputs and outputs here. Same result as sws_linear for m <= 64
+ * (within rounding: the split-K partition may differ):
+ *   w:      E4M3 weight [rows, cols] row-major (e.g. a slot view slot + o_j),
+ *   scales: float32 block scales [ceil(rows/128), ceil(cols/128)],
+ *   x:      bf16 [m, cols], y: bf16 [m, rows]; all 16-byte aligned.
+ * Limits: 0 <= m <= 64, cols % 16 == 0, at most 4096 row blocks (2,097,152
+ * rows for m <= 16, 1,048,576 rows for 16 < m <= 64); anything larger is
+ * rejected with SWS_E_INVALID / SWS_E_UNSUPPORTED before any launch.
+ * Scratch: a fixed 8 MiB + 16 KiB array inside the library's device image
+ * (every GPU that loads the library holds it until the process exits). It is
+ * shared by all calls on a device and keeps the last call's contents; the
+ * arrival counters in it are cleared on `stream` before each launch. Calls
+ * whose work overlaps on the GPU race on it, so serialise them (one stream).
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture. No cudaMalloc / cudaFree is ever called. */
+int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t cols, const void* x, int64_t m,
+                       void* y, sws_stream_t stream);
+
 /* Lookahead over layers first..last (blog "提前一层" and "SGLang 中的实现"):
  * gather(first) is issued on `side` after `side` waits for work already
  * queued on `main`; then for each layer l: `side` waits done(l-1) and gathers

@@ -54,6 +54,8 @@ _PROTOS = [
     ("sws_ctx_destroy", None, [C.c_void_p]),
     ("sws_gather_to_slot", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_linear", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
+    ("sws_linear_noalloc", C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int64,
+                                     C.c_void_p, C.c_void_p]),
     ("sws_run_layers", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_uint32, C.c_void_p,
                                  C.c_void_p]),
     ("sws_run_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32]),

@@ -420,3 +420,122 @@ int launch_decode(const DecodeLaunch& a, cudaStream_t s) {
 }
 
 }  // namespace sws
+
+// ---------------------------------------------------------------------------
+// Decode linear that allocates nothing.
+//
+// Some callers cannot hand this library a workspace or let it allocate one: an
+// inference engine that sizes its KV-cache pool from the free memory left after
+// the weights are placed has no headroom for allocations made later, and a
+// cudaMalloc issued in the middle of a decode step can synchronise the whole
+// device. This variant of the split-K decode kernel keeps its scratch (the
+// split-K partial sums and the per-row-block arrival counters) in a fixed
+// array that lives in the library's device image, so a call needs only the
+// caller's inputs and outputs.
+//
+// The array is shared by every call on a device and keeps the last call's
+// contents; the arrival counters are cleared on the stream before each launch.
+// Two calls whose work overlaps on the GPU race on the array.
+// ---------------------------------------------------------------------------
+namespace sws {
+namespace {
+
+constexpr int64_t kNoAllocPartialBytes = int64_t(8) << 20;  // 8 MiB of fp32 partial sums
+constexpr int64_t kNoAllocCounters = 4096;                    // row blocks, one int32 each
+constexpr int64_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocCounters * 4;
+constexpr int kMaxDevices = 64;
+
+// Partial sums first (256-byte aligned), counters after them.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The first call on
+// a device resolves it with cudaGetSymbolAddress (with that device current);
+// later calls reuse the cached address.
+int noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SWS_E_UNSUPPORTED, "linear_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaGetSymbolAddress(scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_noalloc_addr[dev]);
+  return SWS_OK;
+}
+
+template <int NT>
+cudaError_t launch_noalloc_nt(DecodeParams p, int64_t row_blocks, cudaStream_t s) {
+  constexpr int R = rows_per_warp_tiles<NT>();
+  constexpr int64_t kSlotBytes = int64_t(kWarps) * R * NT * 32 * 4 * 4;
+  constexpr int64_t kGridCap = kNoAllocPartialBytes / (2 * kSlotBytes);  // two partial slots per CTA
+  p.units = row_blocks * p.slabs;
+  const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, kGridCap});
+  decode_kernel<NT, R, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace sws
+
+extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t cols, const void* x,
+                                  int64_t m, void* y, sws_stream_t stream) {
+  using namespace sws;
+  if (m < 0 || m > 64) return fail(SWS_E_INVALID, "linear_noalloc: m=%lld outside [0, 64]", (long long)m);
+  if (rows < 0 || cols < 0) return fail(SWS_E_INVALID, "linear_noalloc: shape [%lld, %lld]", (long long)rows,
+                                        (long long)cols);
+  if (cols % 16 != 0)
+    return fail(SWS_E_UNSUPPORTED, "linear_noalloc: cols=%lld is not a multiple of 16", (long long)cols);
+  if (m == 0 || rows == 0) return SWS_OK;
+  if (!w || !scales || !x || !y) return fail(SWS_E_INVALID, "linear_noalloc: NULL pointer");
+  if (!aligned16(w) || !aligned16(scales) || !aligned16(x) || !aligned16(y))
+    return fail(SWS_E_ALIGN, "linear_noalloc: a pointer is not 16-byte aligned");
+  const int nt = nt_for(m);
+  const int64_t row_blocks = cdiv(rows, rows_per_cta(nt));
+  if (row_blocks > kNoAllocCounters)
+    return fail(SWS_E_INVALID, "linear_noalloc: rows=%lld exceeds the limit of %lld rows at m=%lld",
+                (long long)rows, (long long)(kNoAllocCounters * rows_per_cta(nt)), (long long)m);
+  int rc = check_device();
+  if (rc != SWS_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cols == 0) {
+    cudaError_t e = cudaMemsetAsync(y, 0, (size_t)(m * rows * 2), s);
+    return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: cudaMemsetAsync(y)");
+  }
+  uint8_t* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != SWS_OK) return rc;
+  int32_t* counters = reinterpret_cast<int32_t*>(scratch + kNoAllocPartialBytes);
+  cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)(row_blocks * 4), s);
+  if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaMemsetAsync(counters)");
+  DecodeParams p;
+  p.w = static_cast<const uint8_t*>(w);
+  for (int i = 0; i < 256; ++i) p.chunks[i] = nullptr;
+  p.chunk_bytes = 1;
+  p.t_offset = 0;
+  p.scales = scales;
+  p.scale_cols = cdiv(cols, 128);
+  p.x = static_cast<const uint16_t*>(x);
+  p.y = static_cast<uint16_t*>(y);
+  p.rows = rows;
+  p.cols = cols;
+  p.m = (int32_t)m;
+  p.slabs = (int32_t)cdiv(cols, kSlabK);
+  p.counters = counters;
+  p.partials = reinterpret_cast<float*>(scratch);
+  p.trace = nullptr;
+  p.tag = 0;
+  switch (nt) {
+    case 1: e = launch_noalloc_nt<1>(p, row_blocks, s); break;
+    case 2: e = launch_noalloc_nt<2>(p, row_blocks, s); break;
+    case 4: e = launch_noalloc_nt<4>(p, row_blocks, s); break;
+    default: e = launch_noalloc_nt<8>(p, row_blocks, s); break;
+  }
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
+}
