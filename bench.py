@@ -40,6 +40,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stack-layers", type=int, default=92, help="layers of the lookahead stack (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["gather", "decode", "fused", "step", "noalloc"], default=None,
+                    help="profiling driver: build the shared-expert layer and run one kernel --reps times")
+    ap.add_argument("--m", type=int, default=HEADLINE_M)
+    ap.add_argument("--entry", type=int, default=0, help="0 = gate_up, 1 = down")
+    ap.add_argument("--reps", type=int, default=4)
     return ap.parse_args()
 
 
@@ -523,9 +528,58 @@ def config_block(world):
             "parallelism": f"replicas x{world} (no collective)"}
 
 
+def run_only(args, dist):
+    """Launches one kernel of the shared-expert layer --reps times (for ncu)."""
+    import ctypes as C
+
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import sharded_weight_storage_gb300 as S
+    import workloads as WL
+    from sharded_weight_storage_gb300.storage import ShardedStack
+
+    w = WL.SHARED_EXPERT
+    ents = [(0, e.rows, e.cols) for e in w.entries]
+    lw = WL.layer_weights(w, 0)
+    st = ShardedStack([(0, S.E4M3, r, c) for (_, r, c) in ents], w.n_shards, max_m=64)
+    st.load_layer(0, {j: torch.from_numpy(lw.codes[j]) for j in range(len(ents))},
+                  {j: torch.from_numpy(lw.scales[j]) for j in range(len(ents))})
+    ctx = st.make_ctx()
+    ctx.gather_to_slot(0, 0, 0)
+    j, m = args.entry, args.m
+    x = WL.draw_x(w.key, j, m, ents[j][2]).cuda()
+    y = torch.empty((m, ents[j][1]), dtype=torch.bfloat16, device="cuda")
+    off = st.entry_info[j][0]
+    for _ in range(args.reps):
+        if args.only == "gather":
+            ctx.gather_to_slot(0, 0, 0)
+        elif args.only == "decode":
+            ctx.linear(j, S.SRC_SLOT0, x.data_ptr(), m, y.data_ptr(), 0)
+        elif args.only == "fused":
+            ctx.linear(j, S.SRC_FUSED, x.data_ptr(), m, y.data_ptr(), 0)
+        elif args.only == "noalloc":
+            S.lib().sws_linear_noalloc(C.c_void_p(st.slots[0].data_ptr() + off), C.c_void_p(st.scales[j].data_ptr()),
+                                       ents[j][1], ents[j][2], C.c_void_p(x.data_ptr()), m,
+                                       C.c_void_p(y.data_ptr()), None)
+        else:
+            ctx.gather_to_slot(0, 0, 0)
+            for jj in range(len(ents)):
+                xx = WL.draw_x(w.key, jj, m, ents[jj][2]).cuda()
+                yy = torch.empty((m, ents[jj][1]), dtype=torch.bfloat16, device="cuda")
+                ctx.linear(jj, S.SRC_SLOT0, xx.data_ptr(), m, yy.data_ptr(), 0)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    print(f"only={args.only} m={m} entry={j} reps={args.reps}: ok")
+
+
 def main():
     args = parse()
     dist = Dist()
+    if args.only:
+        run_only(args, dist)
+        return
     if args.impl == "reference":
         line = run_reference(args, dist)
         if line is not None:
