@@ -9,15 +9,21 @@
 // Design (HBM-bound at decode sizes; every weight byte is read exactly once):
 //   * Swap-AB warp-level tensor-core MMA (mma.sync m16n8k16, f16 operands,
 //     fp32 accumulate): the weight supplies 16-row A tiles, the activations the
-//     8-column B tiles, so m <= 64 costs 1..8 n-tiles.
-//   * Weights stream straight from HBM into registers with 16-byte
-//     non-allocating loads (one slab of 128 K ahead), and are widened with the
-//     exact e4m3x2 -> f16x2 conversion. Because a dot product does not care
-//     about the order of k, each thread reads contiguous bytes and the
+//     8-column B tiles, so m <= 64 costs 1..8 n-tiles. e4m3 -> f16 is exact
+//     (one cvt per two weights); the dot product ignores the order of k, so
+//     each thread takes 32 contiguous weight bytes per 128-K slab and the
 //     activations use the same permutation of k.
+//   * Slot path: 128-K weight slabs of the CTA's rows are staged in shared
+//     memory by 2-D TMA (128-byte swizzle, zero fill past the edges) through a
+//     ring of 3-6 stages with mbarrier completion, issued by one thread, so
+//     that >= 128 KB per SM are in flight without holding registers.
+//   * Fused path (no slot): the same ring and arithmetic, but every thread
+//     copies 16-byte weight pieces with cp.async straight from the chunk that
+//     holds them (byte g of T lives in chunk g / C at offset g % C), walking
+//     the chunk map incrementally down its rows.
 //   * Activations are converted bf16 -> f16 once per CTA and staged in shared
 //     memory (double-buffered, XOR-swizzled so that fragment loads are free of
-//     bank conflicts); one __syncthreads per 128-K slab.
+//     bank conflicts); one CTA barrier per 128-K slab.
 //   * Block scales: a warp's rows lie inside one 128-row scale block, so the
 //     scale is one scalar per warp and slab. The accumulator holds
 //     sum_b (s_b / s_cur) P_b and is rescaled by s_prev / s_cur when the scale
@@ -27,9 +33,8 @@
 //     covers a whole row block writes Y directly; partial runs write fp32 sums
 //     to the workspace and the last CTA to arrive on a row block (atomic
 //     counter, no waiting) adds them in K order and writes Y.
-//   * Fused variant: the same kernel reads each 16-byte weight piece from the
-//     chunk that holds it (byte g of T lives in chunk g / C at g % C), so no
-//     slot is written.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -49,6 +54,7 @@ constexpr int kSlabK = 128;
 constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
 
 struct DecodeParams {
+  CUtensorMap tmap;  // slot path: 2-D map of the weight view [rows, cols] u8
   const uint8_t* w;
   const uint8_t* chunks[256];
   int64_t chunk_bytes;
@@ -59,21 +65,14 @@ struct DecodeParams {
   uint16_t* y;
   int64_t rows, cols;
   int32_t m;
-  int32_t slabs;       // ceil(cols / 128)
-  int64_t units;       // row blocks * slabs
+  int32_t slabs;  // ceil(cols / 128)
+  int64_t units;  // row blocks * slabs
   int32_t* counters;
   float* partials;
+  int32_t* status;
   uint64_t* trace;
   uint64_t tag;
 };
-
-__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t r;
@@ -97,250 +96,405 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dev::smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(dev::smem_addr(bar))
+      : "memory");
+}
+
 // Which CTA's unit range [u*G/U ...) contains unit u.
 __device__ __forceinline__ int64_t cta_of(int64_t u, int64_t G, int64_t U) { return ((u + 1) * G - 1) / U; }
 
-template <int NT, int R, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr int kRowsWarp = 16 * R;
-  constexpr int kRowsCta = kWarps * kRowsWarp;
-  constexpr int kXRows = NT * 8;
-  constexpr int kXUnits = kXRows * 16;  // 16-byte units per X slab
-  constexpr int kXPer = (kXUnits + kThreads - 1) / kThreads;
-  constexpr int kSlot = kWarps * R * NT * 32 * 4;  // floats per partial slot
+// Position of 16-byte activation unit u (8 f16 of k) in row m of a staged
+// slab: spreads the 4 units a thread reads, and neighbouring rows, over all
+// 32 banks.
+__device__ __forceinline__ int xpos(int u, int m) { return u ^ (((u >> 3) & 1) << 1) ^ (m & 1); }
 
-  __shared__ __align__(16) uint4 xs[2][kXUnits];
-  __shared__ int s_last;
+// ---- activation staging: bf16 global -> f16 shared, one 128-K slab --------
+template <int NT>
+struct XStage {
+  static constexpr int kUnits = NT * 8 * 16;  // 16-byte units per slab
+  static constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
+  uint4 r[kPer];
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
-  const int64_t U = p.units, G = gridDim.x, c = blockIdx.x;
-  const int64_t u0 = c * U / G, u1 = (c + 1) * U / G;
-  if (tid == 0) dev::trace_start(p.trace);
-  const int64_t C = p.chunk_bytes;
-
-  // ---- weight loads ------------------------------------------------------
-  // Thread (g, tig) of warp w, row tile rt, half h (rows g and g+8) reads the
-  // 16 bytes at k = kb*128 + l*64 + 16*tig for l = 0, 1.
-  auto load_w = [&](int64_t u, uint4 (&dst)[R][2][2]) {
-    const int64_t rb = u / p.slabs, kb = u - rb * p.slabs;
+  __device__ __forceinline__ void load(const DecodeParams& p, int64_t kb, int tid) {
 #pragma unroll
-    for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t o = rb * kRowsCta + warp * kRowsWarp + rt * 16 + g + 8 * h;
-#pragma unroll
-        for (int l = 0; l < 2; ++l) {
-          const int64_t k = kb * kSlabK + l * 64 + 16 * tig;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (o < p.rows && k < p.cols) {
-            if (FUSED) {
-              const int64_t gb = p.t_offset + o * p.cols + k;
-              const int64_t ci = gb / C;
-              v = ldg_stream(p.chunks[ci] + (gb - ci * C));
-            } else {
-              v = ldg_stream(p.w + o * p.cols + k);
-            }
-          }
-          dst[rt][h][l] = v;
-        }
-      }
-  };
-  // ---- activation staging (bf16 -> f16, swizzled) --------------------------
-  auto load_x = [&](int64_t u, uint4 (&dst)[kXPer]) {
-    const int64_t kb = u % p.slabs;
-#pragma unroll
-    for (int i = 0; i < kXPer; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       const int v = tid + i * kThreads;
       const int mrow = v >> 4, q = v & 15;
       const int64_t k = kb * kSlabK + q * 8;
       uint4 val = make_uint4(0, 0, 0, 0);
-      if (v < kXUnits && mrow < p.m && k < p.cols)
+      if (v < kUnits && mrow < p.m && k < p.cols)
         val = __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)mrow * p.cols + k));
-      dst[i] = val;
+      r[i] = val;
     }
-  };
-  auto store_x = [&](int buf, const uint4 (&src)[kXPer]) {
+  }
+  __device__ __forceinline__ void store(uint4* xs, int tid) const {
 #pragma unroll
-    for (int i = 0; i < kXPer; ++i) {
+    for (int i = 0; i < kPer; ++i) {
       const int v = tid + i * kThreads;
-      if (v < kXUnits) {
+      if (v < kUnits) {
         const int mrow = v >> 4, q = v & 15;
         uint4 h;
-        h.x = bf16x2_to_f16x2(src[i].x);
-        h.y = bf16x2_to_f16x2(src[i].y);
-        h.z = bf16x2_to_f16x2(src[i].z);
-        h.w = bf16x2_to_f16x2(src[i].w);
-        xs[buf][mrow * 16 + (q ^ (mrow & 1))] = h;
+        h.x = bf16x2_to_f16x2(r[i].x);
+        h.y = bf16x2_to_f16x2(r[i].y);
+        h.z = bf16x2_to_f16x2(r[i].z);
+        h.w = bf16x2_to_f16x2(r[i].w);
+        xs[mrow * 16 + xpos(q, mrow)] = h;
       }
     }
-  };
+  }
+};
 
-  float acc[R][NT][4];
+// ---- MMAs of one 64-K half-slab ---------------------------------------------
+// wq[rt][h] holds the 16 weight bytes of row (g + 8h) of row tile rt at
+// k = 32*tig + 16*l + [0, 16); the activation fragments come from units
+// 4*tig + 2*l and 4*tig + 2*l + 1 of each n-tile row.
+template <int NT, int R>
+__device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
+                                         int g, int tig) {
+  uint32_t a[R][2][8];
+#pragma unroll
+  for (int rt = 0; rt < R; ++rt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 wv = wq[rt][h];
+      a[rt][h][0] = e4m3x2_to_f16x2(wv.x);
+      a[rt][h][1] = e4m3x2_to_f16x2(wv.x >> 16);
+      a[rt][h][2] = e4m3x2_to_f16x2(wv.y);
+      a[rt][h][3] = e4m3x2_to_f16x2(wv.y >> 16);
+      a[rt][h][4] = e4m3x2_to_f16x2(wv.z);
+      a[rt][h][5] = e4m3x2_to_f16x2(wv.z >> 16);
+      a[rt][h][6] = e4m3x2_to_f16x2(wv.w);
+      a[rt][h][7] = e4m3x2_to_f16x2(wv.w >> 16);
+    }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int mrow = nt * 8 + g;
+    const int u = 4 * tig + 2 * l;
+    const uint4 b0 = xb[mrow * 16 + xpos(u, mrow)];
+    const uint4 b1 = xb[mrow * 16 + xpos(u + 1, mrow)];
+    const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int rt = 0; rt < R; ++rt)
+        mma16816(acc[rt][nt], a[rt][0][2 * kk], a[rt][1][2 * kk], a[rt][0][2 * kk + 1], a[rt][1][2 * kk + 1],
+                 bw[2 * kk], bw[2 * kk + 1]);
+  }
+}
+
+template <int NT, int R>
+__device__ __forceinline__ void rescale(float (&acc)[R][NT][4], float f) {
+#pragma unroll
+  for (int rt = 0; rt < R; ++rt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rt][nt][e] *= f;
+}
+
+template <int NT, int R>
+__device__ __forceinline__ void zero(float (&acc)[R][NT][4]) {
 #pragma unroll
   for (int rt = 0; rt < R; ++rt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.f;
-  float cs = 0.f;  // scale the accumulator currently refers to
+}
 
-  uint4 wcur[R][2][2], wnxt[R][2][2];
-  uint4 xst[kXPer];
-  if (u0 < u1) {
-    load_w(u0, wcur);
-    load_x(u0, xst);
-    store_x(0, xst);
+// Scale bookkeeping for one slab of a warp; returns false when the slab's
+// scale is zero (it contributes nothing and is skipped).
+template <int NT, int R>
+__device__ __forceinline__ bool apply_scale(float (&acc)[R][NT][4], float& cs, float s) {
+  if (s == 0.f) return false;
+  if (cs != 0.f && s != cs) rescale<NT, R>(acc, cs / s);
+  cs = s;
+  return true;
+}
+
+// ---- end of a run -------------------------------------------------------------
+// Runs that cover a whole row block write Y at once. A partial run only stores
+// its fp32 sums in its slot (first or last run of the CTA); the arrival count
+// and the reduction wait until the CTA has streamed all its weights, so no
+// fence, barrier or atomic round trip stalls the weight pipeline mid-stream.
+template <int NT, int R>
+__device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const DecodeParams& p, int64_t row0, int g,
+                                        int tig) {
+#pragma unroll
+  for (int rt = 0; rt < R; ++rt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t o = row0 + rt * 16 + g + 8 * (e >> 1);
+        const int mm = nt * 8 + 2 * tig + (e & 1);
+        if (o < p.rows && mm < p.m) {
+          const __nv_bfloat16 b = __float2bfloat16_rn(acc[rt][nt][e]);
+          p.y[(int64_t)mm * p.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+        }
+      }
+}
+
+struct RunGeom {
+  int64_t G, U, u0, c;
+  __device__ __forceinline__ int64_t first_cta(const DecodeParams& p, int64_t rb) const { return cta_of(rb * p.slabs, G, U); }
+  __device__ __forceinline__ int64_t last_cta(const DecodeParams& p, int64_t rb) const {
+    return cta_of(rb * p.slabs + p.slabs - 1, G, U);
   }
+  __device__ __forceinline__ bool partial(const DecodeParams& p, int64_t rb) const {
+    return first_cta(p, rb) != last_cta(p, rb);
+  }
+  // Partial slot of CTA cc for row block rb: 0 for its first run, 1 otherwise.
+  __device__ __forceinline__ int64_t slot(const DecodeParams& p, int64_t cc, int64_t rb) const {
+    return 2 * cc + (rb == (cc * U / G) / p.slabs ? 0 : 1);
+  }
+};
 
-  for (int64_t u = u0; u < u1; ++u) {
-    const int buf = (int)((u - u0) & 1);
-    __syncthreads();  // xs[buf] is complete; xs[buf ^ 1] is no longer read
-    const bool more = u + 1 < u1;
-    if (more) {
-      load_w(u + 1, wnxt);
-      load_x(u + 1, xst);
+template <int NT, int R>
+__device__ __forceinline__ void end_run(float (&acc)[R][NT][4], const DecodeParams& p, const RunGeom& geo,
+                                        int64_t rb, int64_t row0, int warp, int lane) {
+  constexpr int kSlot = kWarps * R * NT * 32 * 4;  // floats per partial slot
+  if (!geo.partial(p, rb)) {
+    write_y<NT, R>(acc, p, row0, lane >> 2, lane & 3);
+  } else {
+    float4* slot = reinterpret_cast<float4*>(p.partials + geo.slot(p, geo.c, rb) * (int64_t)kSlot);
+#pragma unroll
+    for (int rt = 0; rt < R; ++rt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        slot[((warp * R + rt) * NT + nt) * 32 + lane] =
+            make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]);
+  }
+  zero<NT, R>(acc);
+}
+
+// After the CTA's last slab: count arrivals on the (at most two) partial row
+// blocks of this CTA; the last CTA to arrive on one adds the partials of all
+// its contributors in K order and writes Y, then re-arms the counter.
+template <int NT, int R, int kRowsCta, int kRowsWarp>
+__device__ __forceinline__ void settle_partials(const DecodeParams& p, const RunGeom& geo, int64_t rb_first,
+                                                int64_t rb_last, int warp, int lane, int* s_last) {
+  constexpr int kSlot = kWarps * R * NT * 32 * 4;
+  const int tid = warp * 32 + lane;
+  const bool pf = geo.partial(p, rb_first), pl = rb_last != rb_first && geo.partial(p, rb_last);
+  if (!pf && !pl) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int last = 0;
+    if (pf) last |= (atomicAdd(p.counters + rb_first, 1) == (int)(geo.last_cta(p, rb_first) - geo.first_cta(p, rb_first)));
+    if (pl) last |= (atomicAdd(p.counters + rb_last, 1) == (int)(geo.last_cta(p, rb_last) - geo.first_cta(p, rb_last))) << 1;
+    *s_last = last;
+  }
+  __syncthreads();
+  const int last = *s_last;
+  if (!last) return;
+  __threadfence();
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    if (!(last & (1 << which))) continue;
+    const int64_t rb = which == 0 ? rb_first : rb_last;
+    const int64_t cf = geo.first_cta(p, rb), cl = geo.last_cta(p, rb);
+    float acc[R][NT][4];
+    zero<NT, R>(acc);
+    // Per accumulator tile, the loads of up to four contributors are issued
+    // together and added in K order, so the sum does not depend on which CTA
+    // arrived last.
+    for (int64_t c0 = cf; c0 <= cl; c0 += 4) {
+      const float4* sl[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t cc = c0 + q <= cl ? c0 + q : cl;
+        sl[q] = reinterpret_cast<const float4*>(p.partials + geo.slot(p, cc, rb) * (int64_t)kSlot);
+      }
+      const int nq = (int)(cl - c0 + 1 < 4 ? cl - c0 + 1 : 4);
+#pragma unroll
+      for (int rt = 0; rt < R; ++rt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int idx = ((warp * R + rt) * NT + nt) * 32 + lane;
+          float4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = __ldcg(sl[q] + idx);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q < nq) {
+              acc[rt][nt][0] += v[q].x;
+              acc[rt][nt][1] += v[q].y;
+              acc[rt][nt][2] += v[q].z;
+              acc[rt][nt][3] += v[q].w;
+            }
+        }
     }
+    write_y<NT, R>(acc, p, rb * kRowsCta + warp * kRowsWarp, lane >> 2, lane & 3);
+    if (tid == 0) p.counters[rb] = 0;
+  }
+}
+
+// ---- the kernel ---------------------------------------------------------------
+// FUSED = false: weight slabs come from the view by TMA (thread 0 issues).
+// FUSED = true:  every thread copies 16-byte pieces straight from the chunks
+//                with cp.async into the same swizzled layout.
+template <int NT, int R, int S, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int kRowsWarp = 16 * R;
+  constexpr int kRowsCta = kWarps * kRowsWarp;
+  constexpr int kStage = kRowsCta * kSlabK;  // bytes of one staged weight slab
+  constexpr int kBoxRows = kRowsCta > 256 ? 256 : kRowsCta;
+  constexpr int kBoxes = kRowsCta / kBoxRows;
+  using XS = XStage<NT>;
+
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(16) uint4 xs[2][XS::kUnits];
+  __shared__ __align__(8) uint64_t full[S];
+  __shared__ int s_last;
+  // 128-byte swizzled TMA tiles need a 1024-byte aligned destination.
+  uint8_t* wst = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int64_t U = p.units, G = gridDim.x, c = blockIdx.x;
+  const int64_t u0 = c * U / G, u1 = (c + 1) * U / G, n = u1 - u0;
+  if (tid == 0) {
+    dev::trace_start(p.trace);
+    if (!FUSED) {
+      for (int s = 0; s < S; ++s) dev::mbar_init(&full[s], 1);
+      dev::fence_mbar_init();
+    }
+  }
+  __syncthreads();
+
+  // Stage slab i (unit u0 + i) into ring slot i % S.
+  auto issue = [&](int64_t i) {
+    const int64_t u = u0 + i, rb = u / p.slabs, kb = u - rb * p.slabs;
+    uint8_t* dst = wst + (int)(i % S) * kStage;
+    if (!FUSED) {
+      uint64_t* bar = &full[(int)(i % S)];
+      dev::mbar_arrive_expect_tx(bar, kStage);
+#pragma unroll
+      for (int b = 0; b < kBoxes; ++b)
+        tma_load_2d(dst + b * kBoxRows * kSlabK, &p.tmap, (int32_t)(kb * kSlabK),
+                    (int32_t)(rb * kRowsCta + b * kBoxRows), bar);
+    } else {
+      // thread -> 16-byte column piece cu of rows rr, rr + 32, ...; byte
+      // g = t_offset + o * cols + k of T lives in chunk g / C at g % C.
+      const int cu = tid & 7;
+      const int64_t k = kb * kSlabK + 16 * cu;
+      const int64_t C = p.chunk_bytes;
+      int64_t gb = p.t_offset + (rb * kRowsCta + (tid >> 3)) * p.cols + k;
+      int64_t ci = gb / C, off = gb - ci * C;
+      const int64_t step = 32 * p.cols;
+#pragma unroll 4
+      for (int j = 0; j < kRowsCta / 32; ++j) {
+        const int rr = (tid >> 3) + 32 * j;
+        const int64_t o = rb * kRowsCta + rr;
+        const bool valid = o < p.rows && k < p.cols;
+        const uint8_t* src = p.chunks[valid ? ci : 0] + (valid ? off : 0);
+        dev::cp_async16(dst + rr * kSlabK + ((cu ^ (rr & 7)) << 4), src, valid ? 16u : 0u);
+        off += step;
+        while (off >= C) {
+          off -= C;
+          ++ci;
+        }
+      }
+      dev::cp_async_commit();
+    }
+  };
+
+  if (FUSED) {
+    for (int64_t i = 0; i < S - 1; ++i) {
+      if (i < n) issue(i); else dev::cp_async_commit();
+    }
+  } else if (tid == 0) {
+    for (int64_t i = 0; i < n && i < S - 1; ++i) issue(i);
+  }
+  // Activations are fetched two slabs ahead (register sets xa / xb take turns,
+  // the loop is unrolled by two so they stay in registers), and block scales
+  // 32 slabs at a time, one per lane, a block ahead, so no global-load latency
+  // sits on the per-slab path.
+  XS xa, xb;
+  auto scale_of = [&](int64_t i) -> float {
+    if (i >= n) return 0.f;
+    const int64_t u = u0 + i, rb = u / p.slabs, kb = u - rb * p.slabs;
+    const int64_t row0 = rb * kRowsCta + warp * kRowsWarp;
+    return row0 < p.rows ? __ldg(p.scales + (row0 >> 7) * p.scale_cols + kb) : 0.f;
+  };
+  float sc_cur = scale_of(lane), sc_next = scale_of(32 + lane);
+  if (n > 0) {
+    xa.load(p, u0 % p.slabs, tid);
+    xa.store(xs[0], tid);
+  }
+  if (n > 1) xb.load(p, (u0 + 1) % p.slabs, tid);
+  float acc[R][NT][4];
+  zero<NT, R>(acc);
+  float cs = 0.f;  // scale the accumulator currently refers to
+  const RunGeom geo{G, U, u0, c};
+  bool timed_out = false;
+
+  // One slab: `nx` receives slab i + 2 (it held slab i, already staged);
+  // `cx` holds slab i + 1, staged at the end.
+  auto slab = [&](int64_t i, XS& nx, XS& cx) {
+    const int64_t u = u0 + i;
+    const int st = (int)(i % S);
+    bool ok = true;
+    if (FUSED) dev::cp_async_wait<S - 2>();
+    else ok = dev::mbar_wait(&full[st], (uint32_t)((i / S) & 1), kWaitLimitNs);
+    // Slab i has landed for everyone; slab i-1's stage and X buffer are free.
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        dev::set_status(p.status, SWS_E_TIMEOUT);
+        for (int64_t j = i; j < n && j < i + S - 1; ++j)  // drain copies still in flight (bounded)
+          dev::mbar_wait(&full[(int)(j % S)], (uint32_t)((j / S) & 1), kWaitLimitNs / 4);
+      }
+      timed_out = true;
+      return;
+    }
+    if (FUSED) {
+      if (i + S - 1 < n) issue(i + S - 1); else dev::cp_async_commit();
+    } else if (tid == 0 && i + S - 1 < n) {
+      issue(i + S - 1);
+    }
+    if (i + 2 < n) nx.load(p, (u + 2) % p.slabs, tid);
+    if ((i & 31) == 0 && i > 0) {
+      sc_cur = sc_next;
+      sc_next = scale_of(i + 32 + lane);
+    }
+    const float s = __shfl_sync(0xffffffffu, sc_cur, (int)(i & 31));
     const int64_t rb = u / p.slabs, kb = u - rb * p.slabs;
     const int64_t row0 = rb * kRowsCta + warp * kRowsWarp;
-    const bool run_start = (u == u0) || kb == 0;
-    const bool run_end = (u + 1 == u1) || kb + 1 == p.slabs;
-    if (run_start) cs = 0.f;
-    // ---- this warp's scale for the slab, and the accumulator rescale ----
-    float s = 0.f;
-    if (row0 < p.rows) s = __ldg(p.scales + (row0 >> 7) * p.scale_cols + kb);
-    if (s != 0.f) {
-      if (cs != 0.f && s != cs) {
-        const float ratio = cs / s;
-#pragma unroll
-        for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[rt][nt][e] *= ratio;
-      }
-      cs = s;
-      // ---- MMAs over the slab: two 64-K halves of four k16 steps ----
-      const uint4* xb = xs[buf];
+    if (u == u0 || kb == 0) cs = 0.f;
+    if (apply_scale<NT, R>(acc, cs, s)) {
+      const uint8_t* wb = wst + st * kStage;
 #pragma unroll
       for (int l = 0; l < 2; ++l) {
-        uint32_t a[R][2][8];  // [rt][row g / g+8][f16x2 words for k positions]
+        uint4 wq[R][2];
 #pragma unroll
         for (int rt = 0; rt < R; ++rt)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint4 wv = wcur[rt][h][l];
-            a[rt][h][0] = e4m3x2_to_f16x2(wv.x);
-            a[rt][h][1] = e4m3x2_to_f16x2(wv.x >> 16);
-            a[rt][h][2] = e4m3x2_to_f16x2(wv.y);
-            a[rt][h][3] = e4m3x2_to_f16x2(wv.y >> 16);
-            a[rt][h][4] = e4m3x2_to_f16x2(wv.z);
-            a[rt][h][5] = e4m3x2_to_f16x2(wv.z >> 16);
-            a[rt][h][6] = e4m3x2_to_f16x2(wv.w);
-            a[rt][h][7] = e4m3x2_to_f16x2(wv.w >> 16);
+            const int r = warp * kRowsWarp + rt * 16 + g + 8 * h;
+            wq[rt][h] = *reinterpret_cast<const uint4*>(wb + r * kSlabK + (((2 * tig + l) ^ g) << 4));
           }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int mrow = nt * 8 + g;
-          const int u0x = 8 * l + 2 * tig;
-          const uint4 b0 = xb[mrow * 16 + (u0x ^ (mrow & 1))];
-          const uint4 b1 = xb[mrow * 16 + ((u0x + 1) ^ (mrow & 1))];
-          const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int rt = 0; rt < R; ++rt)
-              mma16816(acc[rt][nt], a[rt][0][2 * kk], a[rt][1][2 * kk], a[rt][0][2 * kk + 1], a[rt][1][2 * kk + 1],
-                       bw[2 * kk], bw[2 * kk + 1]);
-        }
+        mma_half<NT, R>(acc, wq, xs[i & 1], l, g, tig);
       }
     }
-    if (more) store_x(buf ^ 1, xst);
-
-    if (run_end) {
-      // ---- finish the run: apply the last scale, then write or reduce ----
-#pragma unroll
-      for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[rt][nt][e] *= cs;
-      const int64_t ks = rb * p.slabs;
-      const int64_t cf = cta_of(ks, G, U), cl = cta_of(ks + p.slabs - 1, G, U);
-      bool write_y = true;
-      if (cf != cl) {
-        // partial run: publish, count arrivals; the last CTA sums in K order
-        const int64_t my_first_rb = u0 / p.slabs;
-        float* slot = p.partials + (2 * c + (rb == my_first_rb ? 0 : 1)) * (int64_t)kSlot;
-#pragma unroll
-        for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            reinterpret_cast<float4*>(slot)[((warp * R + rt) * NT + nt) * 32 + lane] =
-                make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]);
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-          const int old = atomicAdd(p.counters + rb, 1);
-          s_last = (old == (int)(cl - cf));
-        }
-        __syncthreads();
-        write_y = s_last != 0;
-        if (write_y) {
-          __threadfence();
-#pragma unroll
-          for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.f;
-          for (int64_t cc = cf; cc <= cl; ++cc) {
-            const int64_t first_rb = (cc * U / G) / p.slabs;
-            const float* sl = p.partials + (2 * cc + (rb == first_rb ? 0 : 1)) * (int64_t)kSlot;
-#pragma unroll
-            for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(sl) + ((warp * R + rt) * NT + nt) * 32 + lane);
-                acc[rt][nt][0] += v.x;
-                acc[rt][nt][1] += v.y;
-                acc[rt][nt][2] += v.z;
-                acc[rt][nt][3] += v.w;
-              }
-          }
-          if (tid == 0) p.counters[rb] = 0;
-        }
-      }
-      if (write_y) {
-#pragma unroll
-        for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int64_t o = row0 + rt * 16 + g + 8 * (e >> 1);
-              const int mm = nt * 8 + 2 * tig + (e & 1);
-              if (o < p.rows && mm < p.m) {
-                const __nv_bfloat16 b = __float2bfloat16_rn(acc[rt][nt][e]);
-                p.y[(int64_t)mm * p.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
-              }
-            }
-      }
-#pragma unroll
-      for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.f;
+    if (i + 1 < n) cx.store(xs[(i + 1) & 1], tid);
+    if (i + 1 == n || kb + 1 == p.slabs) {
+      rescale<NT, R>(acc, cs);
+      end_run<NT, R>(acc, p, geo, rb, row0, warp, lane);
     }
-    if (more) {
-#pragma unroll
-      for (int rt = 0; rt < R; ++rt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int l = 0; l < 2; ++l) wcur[rt][h][l] = wnxt[rt][h][l];
-    }
+  };
+  for (int64_t i = 0; i < n && !timed_out; i += 2) {
+    slab(i, xa, xb);
+    if (i + 1 < n && !timed_out) slab(i + 1, xb, xa);
   }
+  if (!timed_out && n > 0)
+    settle_partials<NT, R, kRowsCta, kRowsWarp>(p, geo, u0 / p.slabs, (u1 - 1) / p.slabs, warp, lane, &s_last);
+  if (FUSED) dev::cp_async_wait<0>();
   if (tid == 0) {
     __threadfence();
     dev::trace_end(p.trace, p.tag);
@@ -349,19 +503,90 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
 template <int NT>
 constexpr int rows_per_warp_tiles() { return NT <= 2 ? 4 : 2; }
-
-template <int NT, bool FUSED>
-cudaError_t launch_nt(const DecodeParams& p0, int64_t row_blocks, cudaStream_t s) {
-  constexpr int R = rows_per_warp_tiles<NT>();
-  DecodeParams p = p0;
-  p.units = row_blocks * p.slabs;
-  const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid});
-  decode_kernel<NT, R, FUSED><<<(unsigned)grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
+// Ring depth: 192 KB of weight stages, leaving room for the staged activations.
+template <int NT>
+constexpr int stages_for() { return NT <= 2 ? 3 : NT == 4 ? 6 : 5; }
 
 int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D map of an e4m3 weight [rows, cols] (row stride cols bytes): boxes of 128
+// bytes of k by box_rows rows, 128-byte swizzle, zero fill outside.
+int encode_weight_map(CUtensorMap* m, const void* w, int64_t rows, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(SWS_E_CUDA, "decode: cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {(cuuint32_t)kSlabK, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SWS_E_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SWS_OK;
+}
+
+template <int NT, bool FUSED>
+cudaError_t launch_nt(DecodeParams& p, int64_t row_blocks, int64_t grid_cap, cudaStream_t s) {
+  constexpr int R = rows_per_warp_tiles<NT>();
+  constexpr int S = stages_for<NT>();
+  constexpr int kRowsCta = kWarps * 16 * R;
+  constexpr int kSmem = S * kRowsCta * kSlabK + 1024;
+  auto kern = decode_kernel<NT, R, S, FUSED>;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
+  if (attr != cudaSuccess) return attr;
+  p.units = row_blocks * p.slabs;
+  const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
+  kern<<<(unsigned)grid, kThreads, kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Fills everything but the tensor map / chunk table and the scratch pointers.
+void fill_params(DecodeParams& p, const float* scales, const uint16_t* x, uint16_t* y, int64_t m, int64_t rows,
+                 int64_t cols) {
+  p.w = nullptr;
+  for (int i = 0; i < 256; ++i) p.chunks[i] = nullptr;
+  p.chunk_bytes = 1;
+  p.t_offset = 0;
+  p.scales = scales;
+  p.scale_cols = cdiv(cols, 128);
+  p.x = x;
+  p.y = y;
+  p.rows = rows;
+  p.cols = cols;
+  p.m = (int32_t)m;
+  p.slabs = (int32_t)cdiv(cols, kSlabK);
+  p.status = nullptr;
+  p.trace = nullptr;
+  p.tag = 0;
+}
+
+cudaError_t dispatch(DecodeParams& p, int nt, bool fused, int64_t row_blocks, int64_t grid_cap, cudaStream_t s) {
+  switch (nt) {
+    case 1: return fused ? launch_nt<1, true>(p, row_blocks, grid_cap, s) : launch_nt<1, false>(p, row_blocks, grid_cap, s);
+    case 2: return fused ? launch_nt<2, true>(p, row_blocks, grid_cap, s) : launch_nt<2, false>(p, row_blocks, grid_cap, s);
+    case 4: return fused ? launch_nt<4, true>(p, row_blocks, grid_cap, s) : launch_nt<4, false>(p, row_blocks, grid_cap, s);
+    default: return fused ? launch_nt<8, true>(p, row_blocks, grid_cap, s) : launch_nt<8, false>(p, row_blocks, grid_cap, s);
+  }
+}
+
+int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
 }  // namespace
 
@@ -369,11 +594,9 @@ int decode_workspace_bytes(int64_t m, int64_t rows, int64_t cols, int64_t* bytes
   (void)cols;
   if (m < 0 || m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)m);
   const int nt = nt_for(std::max<int64_t>(m, 1));
-  const int r = nt <= 2 ? 4 : 2;
-  const int64_t slot_floats = (int64_t)kWarps * r * nt * 32 * 4;
   const int64_t row_blocks = cdiv(rows, rows_per_cta(nt));
   if (row_blocks > kMaxCounters) return fail(SWS_E_UNSUPPORTED, "decode: %lld rows is too many", (long long)rows);
-  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot_floats * 4;
+  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot_bytes_for(nt);
   return SWS_OK;
 }
 
@@ -390,32 +613,25 @@ int launch_decode(const DecodeLaunch& a, cudaStream_t s) {
     return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode: cudaMemsetAsync");
   }
   DecodeParams p;
-  p.w = a.w;
+  fill_params(p, a.scales, a.x, a.y, a.m, a.rows, a.cols);
   const bool fused = a.w == nullptr;
-  for (int i = 0; i < 256; ++i) p.chunks[i] = i < a.n_chunks ? a.chunks[i] : nullptr;
-  p.chunk_bytes = a.chunk_bytes > 0 ? a.chunk_bytes : 1;
-  p.t_offset = a.t_offset;
-  p.scales = a.scales;
-  p.scale_cols = cdiv(a.cols, 128);
-  p.x = a.x;
-  p.y = a.y;
-  p.rows = a.rows;
-  p.cols = a.cols;
-  p.m = (int32_t)a.m;
-  p.slabs = (int32_t)cdiv(a.cols, kSlabK);
+  const int nt = nt_for(a.m);
+  if (fused) {
+    for (int i = 0; i < a.n_chunks && i < 256; ++i) p.chunks[i] = a.chunks[i];
+    p.chunk_bytes = a.chunk_bytes > 0 ? a.chunk_bytes : 1;
+    p.t_offset = a.t_offset;
+  } else {
+    p.w = a.w;
+    rc = encode_weight_map(&p.tmap, a.w, a.rows, a.cols, std::min(256, rows_per_cta(nt)));
+    if (rc != SWS_OK) return rc;
+  }
   p.counters = reinterpret_cast<int32_t*>(a.workspace + kCtlBytes);
   p.partials = reinterpret_cast<float*>(a.workspace + kCtlBytes + kMaxCounters * 4);
+  p.status = reinterpret_cast<int32_t*>(a.workspace);
   p.trace = a.trace;
   p.tag = a.tag;
-  const int nt = nt_for(a.m);
   const int64_t row_blocks = cdiv(a.rows, rows_per_cta(nt));
-  cudaError_t e;
-  switch (nt) {
-    case 1: e = fused ? launch_nt<1, true>(p, row_blocks, s) : launch_nt<1, false>(p, row_blocks, s); break;
-    case 2: e = fused ? launch_nt<2, true>(p, row_blocks, s) : launch_nt<2, false>(p, row_blocks, s); break;
-    case 4: e = fused ? launch_nt<4, true>(p, row_blocks, s) : launch_nt<4, false>(p, row_blocks, s); break;
-    default: e = fused ? launch_nt<8, true>(p, row_blocks, s) : launch_nt<8, false>(p, row_blocks, s); break;
-  }
+  cudaError_t e = dispatch(p, nt, fused, row_blocks, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 
@@ -470,17 +686,6 @@ int noalloc_scratch(uint8_t** out) {
   return SWS_OK;
 }
 
-template <int NT>
-cudaError_t launch_noalloc_nt(DecodeParams p, int64_t row_blocks, cudaStream_t s) {
-  constexpr int R = rows_per_warp_tiles<NT>();
-  constexpr int64_t kSlotBytes = int64_t(kWarps) * R * NT * 32 * 4 * 4;
-  constexpr int64_t kGridCap = kNoAllocPartialBytes / (2 * kSlotBytes);  // two partial slots per CTA
-  p.units = row_blocks * p.slabs;
-  const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, kGridCap});
-  decode_kernel<NT, R, false><<<(unsigned)grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 }  // namespace sws
 
@@ -515,27 +720,14 @@ extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t ro
   cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)(row_blocks * 4), s);
   if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaMemsetAsync(counters)");
   DecodeParams p;
+  fill_params(p, scales, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), m, rows, cols);
   p.w = static_cast<const uint8_t*>(w);
-  for (int i = 0; i < 256; ++i) p.chunks[i] = nullptr;
-  p.chunk_bytes = 1;
-  p.t_offset = 0;
-  p.scales = scales;
-  p.scale_cols = cdiv(cols, 128);
-  p.x = static_cast<const uint16_t*>(x);
-  p.y = static_cast<uint16_t*>(y);
-  p.rows = rows;
-  p.cols = cols;
-  p.m = (int32_t)m;
-  p.slabs = (int32_t)cdiv(cols, kSlabK);
+  rc = encode_weight_map(&p.tmap, w, rows, cols, std::min(256, rows_per_cta(nt)));
+  if (rc != SWS_OK) return rc;
   p.counters = counters;
   p.partials = reinterpret_cast<float*>(scratch);
-  p.trace = nullptr;
-  p.tag = 0;
-  switch (nt) {
-    case 1: e = launch_noalloc_nt<1>(p, row_blocks, s); break;
-    case 2: e = launch_noalloc_nt<2>(p, row_blocks, s); break;
-    case 4: e = launch_noalloc_nt<4>(p, row_blocks, s); break;
-    default: e = launch_noalloc_nt<8>(p, row_blocks, s); break;
-  }
+  // Two partial slots per CTA must fit in the fixed array.
+  const int64_t grid_cap = kNoAllocPartialBytes / (2 * slot_bytes_for(nt));
+  e = dispatch(p, nt, false, row_blocks, grid_cap, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
 }
