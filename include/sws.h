@@ -173,6 +173,14 @@ int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t s
 int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t m, void* y,
                sws_stream_t stream);
 
+/* Every linear of one layer (declaration order, replicated entries included),
+ * with io->x[k] / io->y[k] for its k-th entry and a common m: the decode-sized
+ * ones (m <= 64) run as grouped launches, up to 8 linears per launch - one for
+ * the views (slot src, or replicated buffers) and one for chunk-map reads
+ * (SWS_SRC_FUSED) - so a layer pays one launch instead of one per weight.
+ * Same results and rules as sws_linear for each entry. */
+int sws_layer_linears(sws_ctx* ctx, int32_t layer, int32_t src, const sws_layer_io* io, sws_stream_t stream);
+
 /* Decode linear that allocates nothing. The paper has no counterpart to this
  * call; it serves callers that cannot give the library memory. An inference engine
  * that sizes its KV-cache pool from the memory left free after loading the

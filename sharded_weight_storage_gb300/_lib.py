@@ -54,6 +54,7 @@ _PROTOS = [
     ("sws_ctx_destroy", None, [C.c_void_p]),
     ("sws_gather_to_slot", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_linear", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
+    ("sws_layer_linears", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_void_p]),
     ("sws_linear_noalloc", C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int64,
                                      C.c_void_p, C.c_void_p]),
     ("sws_run_layers", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_uint32, C.c_void_p,
@@ -190,6 +191,12 @@ class Ctx:
     def linear(self, entry: int, src: int, x: int, m: int, y: int, stream: int = 0):
         check(lib().sws_linear(self.handle, entry, src, C.c_void_p(x), m, C.c_void_p(y), C.c_void_p(stream or None)),
               "linear")
+
+    def layer_linears(self, layer: int, src: int, xs: Sequence[int], ys: Sequence[int], m: int, stream: int = 0):
+        xa, ya = _ptrs(xs), _ptrs(ys)
+        io = _LayerIO(C.cast(xa, C.POINTER(C.c_void_p)), C.cast(ya, C.POINTER(C.c_void_p)), m)
+        check(lib().sws_layer_linears(self.handle, layer, src, C.byref(io), C.c_void_p(stream or None)),
+              "layer_linears")
 
     def run_layers(self, first: int, last: int, io: Sequence[tuple], flags: int, main: int, side: int):
         """io[l - first] = (x_ptrs, y_ptrs, m) for layer l."""

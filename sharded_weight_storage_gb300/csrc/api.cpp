@@ -85,7 +85,29 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
 }
 
-int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s) {
+// Where entry j's weight lives for source `src`: a view (slot or replicated
+// buffer) or, for the fused source, the chunks of its layer.
+int weight_source(sws_ctx* c, int32_t j, int32_t src, const uint8_t** w, bool* fused) {
+  const EntryPlan& e = c->plan->entries[j];
+  *w = nullptr;
+  *fused = false;
+  if (!e.sharded) {
+    *w = c->replicated[j];
+    if (!*w) return fail(SWS_E_INVALID, "linear: replicated entry %d has no buffer", j);
+  } else if (src == SWS_SRC_SLOT0 || src == SWS_SRC_SLOT1) {
+    if (c->slot_tag[src] != e.layer)
+      return fail(SWS_E_STATE, "linear: slot %d holds layer %d, entry %d belongs to layer %d", src, c->slot_tag[src], j,
+                  e.layer);
+    *w = c->slot[src] + e.offset;
+  } else if (src == SWS_SRC_FUSED) {
+    *fused = true;
+  } else {
+    return fail(SWS_E_INVALID, "linear: src=%d", src);
+  }
+  return SWS_OK;
+}
+
+int check_linear_args(sws_ctx* c, int32_t j, const void* x, int64_t m, void* y) {
   const sws_plan* p = c->plan;
   if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "linear: entry %d", j);
   const EntryPlan& e = p->entries[j];
@@ -96,49 +118,39 @@ int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, vo
   if (!aligned16(x) || !aligned16(y)) return fail(SWS_E_ALIGN, "linear: x or y is not 16-byte aligned");
   if (!c->scales[j]) return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
   if (e.cols % 16 != 0) return fail(SWS_E_UNSUPPORTED, "linear: cols=%lld is not a multiple of 16", (long long)e.cols);
-  const LayerPlan& lp = p->layers[e.layer];
-  const uint8_t* w = nullptr;
-  bool fused = false;
-  if (!e.sharded) {
-    w = c->replicated[j];
-    if (!w) return fail(SWS_E_INVALID, "linear: replicated entry %d has no buffer", j);
-  } else if (src == SWS_SRC_SLOT0 || src == SWS_SRC_SLOT1) {
-    if (c->slot_tag[src] != e.layer)
-      return fail(SWS_E_STATE, "linear: slot %d holds layer %d, entry %d belongs to layer %d", src, c->slot_tag[src], j,
-                  e.layer);
-    w = c->slot[src] + e.offset;
-  } else if (src == SWS_SRC_FUSED) {
-    fused = true;
-  } else {
-    return fail(SWS_E_INVALID, "linear: src=%d", src);
+  return SWS_OK;
+}
+
+void init_group(sws_ctx* c, DecodeGroup& g, int32_t layer, int64_t m, bool fused) {
+  const sws_plan* p = c->plan;
+  g.n = 0;
+  g.m = m;
+  g.fused = fused;
+  for (int i = 0; i < 256; ++i) g.chunks[i] = nullptr;
+  g.n_chunks = 0;
+  if (fused) {
+    g.n_chunks = p->n_shards;
+    for (int i = 0; i < p->n_shards; ++i) g.chunks[i] = c->chunks[(int64_t)layer * p->n_shards + i];
   }
-  uint64_t* rec = next_trace(c);
-  const uint64_t tag = (kTraceLinear << 56) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
-  if (m <= 64) {
-    DecodeLaunch d;
-    d.w = fused ? nullptr : w;
-    d.n_chunks = fused ? p->n_shards : 0;
-    for (int i = 0; i < 256; ++i) d.chunks[i] = nullptr;
-    if (fused)
-      for (int i = 0; i < p->n_shards; ++i) {
-        d.chunks[i] = c->chunks[(int64_t)e.layer * p->n_shards + i];
-        if (!d.chunks[i]) return fail(SWS_E_INVALID, "linear: chunk %d of layer %d is NULL", i, e.layer);
-      }
-    d.chunk_bytes = lp.chunk;
-    d.t_offset = fused ? e.offset : 0;
-    d.scales = c->scales[j];
-    d.x = static_cast<const uint16_t*>(x);
-    d.y = static_cast<uint16_t*>(y);
-    d.m = m;
-    d.rows = e.rows;
-    d.cols = e.cols;
-    d.workspace = c->ws;
-    d.workspace_bytes = c->ws_decode;
-    d.trace = rec;
-    d.tag = tag;
-    return launch_decode(d, s);
-  }
-  if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
+  g.chunk_bytes = p->layers[layer].chunk;
+  g.workspace = c->ws;
+  g.workspace_bytes = c->ws_decode;
+}
+
+int launch_group(sws_ctx* c, DecodeGroup& g, int32_t layer, int32_t first_entry, cudaStream_t s) {
+  if (g.n == 0) return SWS_OK;
+  if (g.fused)
+    for (int i = 0; i < g.n_chunks; ++i)
+      if (!g.chunks[i]) return fail(SWS_E_INVALID, "linear: chunk %d of layer %d is NULL", i, layer);
+  g.trace = next_trace(c);
+  g.tag = (kTraceLinear << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)first_entry;
+  int rc = launch_decode(g, s);
+  g.n = 0;
+  return rc;
+}
+
+int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+  const EntryPlan& e = c->plan->entries[j];
   if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
   const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
   if (c->ws_bytes < need)
@@ -158,20 +170,72 @@ int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, vo
   pl.rows = e.rows;
   pl.cols = e.cols;
   pl.status = status_word(c);
-  pl.trace = rec;
-  pl.tag = tag;
+  pl.trace = next_trace(c);
+  pl.tag = (kTraceLinear << 56) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
   return launch_prefill(pl, s);
 }
 
+int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s) {
+  int rc = check_linear_args(c, j, x, m, y);
+  if (rc != SWS_OK) return rc;
+  const EntryPlan& e = c->plan->entries[j];
+  if (m == 0 || e.rows == 0) return SWS_OK;
+  const uint8_t* w = nullptr;
+  bool fused = false;
+  rc = weight_source(c, j, src, &w, &fused);
+  if (rc != SWS_OK) return rc;
+  if (m > 64) {
+    if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
+    return prefill_linear(c, j, w, x, m, y, s);
+  }
+  DecodeGroup g;
+  init_group(c, g, e.layer, m, fused);
+  g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), e.rows,
+                             e.cols, e.offset};
+  return launch_group(c, g, e.layer, j, s);
+}
+
+// All linears of a layer: decode-sized ones go out as at most two grouped
+// launches (views by TMA, chunk-map reads), up to kMaxDecodeGroup per launch.
 int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io, cudaStream_t s) {
   const LayerPlan& lp = c->plan->layers[layer];
   if (lp.all.empty()) return SWS_OK;
   if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
-  for (size_t k = 0; k < lp.all.size(); ++k) {
-    int rc = linear_impl(c, lp.all[k], src, io.x[k], io.m, io.y[k], s);
-    if (rc != SWS_OK) return rc;
+  const int64_t m = io.m;
+  if (m > 64) {
+    for (size_t k = 0; k < lp.all.size(); ++k) {
+      int rc = linear_impl(c, lp.all[k], src, io.x[k], m, io.y[k], s);
+      if (rc != SWS_OK) return rc;
+    }
+    return SWS_OK;
   }
-  return SWS_OK;
+  DecodeGroup gv, gf;
+  init_group(c, gv, layer, m, false);
+  init_group(c, gf, layer, m, true);
+  int32_t first_v = -1, first_f = -1;
+  for (size_t k = 0; k < lp.all.size(); ++k) {
+    const int32_t j = lp.all[k];
+    int rc = check_linear_args(c, j, io.x[k], m, io.y[k]);
+    if (rc != SWS_OK) return rc;
+    const EntryPlan& e = c->plan->entries[j];
+    if (m == 0 || e.rows == 0) continue;
+    const uint8_t* w = nullptr;
+    bool fused = false;
+    rc = weight_source(c, j, src, &w, &fused);
+    if (rc != SWS_OK) return rc;
+    DecodeGroup& g = fused ? gf : gv;
+    int32_t& first = fused ? first_f : first_v;
+    if (g.n == kMaxDecodeGroup) {
+      rc = launch_group(c, g, layer, first, s);
+      if (rc != SWS_OK) return rc;
+    }
+    if (g.n == 0) first = j;
+    g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(io.x[k]), static_cast<uint16_t*>(io.y[k]),
+                               e.rows, e.cols, e.offset};
+  }
+  int rc = launch_group(c, gv, layer, first_v, s);
+  if (rc != SWS_OK) return rc;
+  return launch_group(c, gf, layer, first_f, s);
 }
 
 }  // namespace
@@ -181,7 +245,7 @@ extern "C" {
 int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   if (!p || max_m < 0) return -1;
   int64_t dec = 0;
-  if (decode_workspace_bytes(std::min<int64_t>(std::max<int64_t>(max_m, 1), 64), 1, 16, &dec) != SWS_OK) return -1;
+  if (decode_workspace_bytes(std::min<int64_t>(std::max<int64_t>(max_m, 1), 64), &dec) != SWS_OK) return -1;
   int64_t pre = 0;
   for (const EntryPlan& e : p->entries) pre = std::max(pre, prefill_bytes(max_m, e.cols));
   return dec + pre;
@@ -236,7 +300,7 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
   c->ws = static_cast<uint8_t*>(workspace);
   c->ws_bytes = workspace_bytes;
   int64_t dec64 = 0;
-  decode_workspace_bytes(64, 1, 16, &dec64);
+  decode_workspace_bytes(64, &dec64);
   c->ws_decode = std::min(dec64, workspace_bytes);
   // Only the status word and the split-K arrival counters must start at zero.
   cudaError_t e = cudaMemset(workspace, 0, (size_t)(kCtlBytes + kMaxCounters * 4));
@@ -286,6 +350,14 @@ int sws_gather_to_slot(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t str
 int sws_linear(sws_ctx* c, int32_t entry, int32_t src, const void* x, int64_t m, void* y, sws_stream_t stream) {
   if (!c) return fail(SWS_E_INVALID, "linear: ctx is NULL");
   return linear_impl(c, entry, src, x, m, y, (cudaStream_t)stream);
+}
+
+int sws_layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io* io, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "layer_linears: ctx is NULL");
+  if (layer < 0 || layer >= (int32_t)c->plan->layers.size())
+    return fail(SWS_E_INVALID, "layer_linears: layer %d", layer);
+  if (!io) return fail(SWS_E_INVALID, "layer_linears: io is NULL");
+  return layer_linears(c, layer, src, *io, (cudaStream_t)stream);
 }
 
 int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,

@@ -4,7 +4,8 @@
 //
 // The linear the weight-sharding blog keeps unchanged (section "核心抽象":
 // the GEMM sees the full W; Y = X W^T with W [out, in]); block scales are
-// 128 x 128, float32.
+// 128 x 128, float32. One launch computes a group of up to eight such linears
+// (all linears of a layer share m), so launch, ramp-up and drain are paid once.
 //
 // Design (HBM-bound at decode sizes; every weight byte is read exactly once):
 //   * Swap-AB warp-level tensor-core MMA (mma.sync m16n8k16, f16 operands,
@@ -28,11 +29,12 @@
 //     scale is one scalar per warp and slab. The accumulator holds
 //     sum_b (s_b / s_cur) P_b and is rescaled by s_prev / s_cur when the scale
 //     changes, then multiplied by the last scale at the end of a run.
-//   * Split-K across CTAs: the (row block, K slab) units are cut into equal
-//     contiguous ranges, one per CTA of a grid sized to the SM count. A CTA that
-//     covers a whole row block writes Y directly; partial runs write fp32 sums
-//     to the workspace and the last CTA to arrive on a row block (atomic
-//     counter, no waiting) adds them in K order and writes Y.
+//   * Split-K across CTAs: the (row block, K slab) units of all linears of the
+//     group are concatenated and cut into equal contiguous ranges, one per CTA
+//     of a grid sized to the SM count. A CTA that covers a whole row block
+//     writes Y directly; partial runs store fp32 sums in the workspace and, once
+//     the CTA has streamed all its weights, the last CTA to arrive on a row
+//     block (atomic counter, no waiting) adds them in K order and writes Y.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -53,20 +55,27 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSlabK = 128;
 constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
 
-struct DecodeParams {
+// One linear of a group.
+struct DecodeEntry {
   CUtensorMap tmap;  // slot path: 2-D map of the weight view [rows, cols] u8
-  const uint8_t* w;
-  const uint8_t* chunks[256];
-  int64_t chunk_bytes;
-  int64_t t_offset;
   const float* scales;
-  int64_t scale_cols;
-  const uint16_t* x;
-  uint16_t* y;
+  const uint16_t* x;  // bf16 [m, cols]
+  uint16_t* y;        // bf16 [m, rows]
   int64_t rows, cols;
+  int64_t t_offset;    // fused path: o_j, the entry's offset in T
+  int64_t scale_cols;  // ceil(cols / 128)
+  int64_t unit_begin;  // first unit of this entry in the group's unit space
+  int64_t rb_begin;    // first row block of this entry in the group
+  int32_t slabs;       // ceil(cols / 128)
+};
+
+struct DecodeParams {
+  DecodeEntry e[kMaxDecodeGroup];
+  int32_t n_entries;
   int32_t m;
-  int32_t slabs;  // ceil(cols / 128)
-  int64_t units;  // row blocks * slabs
+  int64_t units;  // total units (row block x K slab) of the group
+  const uint8_t* chunks[256];  // fused path: the layer's chunks
+  int64_t chunk_bytes;
   int32_t* counters;
   float* partials;
   int32_t* status;
@@ -105,13 +114,49 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Which CTA's unit range [u*G/U ...) contains unit u.
+// Which CTA's unit range [c*U/G, (c+1)*U/G) contains unit u.
 __device__ __forceinline__ int64_t cta_of(int64_t u, int64_t G, int64_t U) { return ((u + 1) * G - 1) / U; }
 
 // Position of 16-byte activation unit u (8 f16 of k) in row m of a staged
 // slab: spreads the 4 units a thread reads, and neighbouring rows, over all
 // 32 banks.
 __device__ __forceinline__ int xpos(int u, int m) { return u ^ (((u >> 3) & 1) << 1) ^ (m & 1); }
+
+// Where a unit of the group's unit space lies.
+struct UnitPos {
+  int j;        // entry
+  int64_t rbl;  // row block inside the entry
+  int64_t kb;   // K slab
+  int64_t rbg;  // row block in the group
+};
+
+__device__ __forceinline__ int entry_of_unit(const DecodeParams& p, int64_t u) {
+  int j = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxDecodeGroup; ++q)
+    if (q < p.n_entries && u >= p.e[q].unit_begin) j = q;
+  return j;
+}
+
+__device__ __forceinline__ int entry_of_rb(const DecodeParams& p, int64_t rbg) {
+  int j = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxDecodeGroup; ++q)
+    if (q < p.n_entries && rbg >= p.e[q].rb_begin) j = q;
+  return j;
+}
+
+__device__ __forceinline__ UnitPos unit_pos(const DecodeParams& p, int64_t u) {
+  UnitPos r;
+  r.j = entry_of_unit(p, u);
+  const DecodeEntry& e = p.e[r.j];
+  const uint32_t local = (uint32_t)(u - e.unit_begin);  // units per entry < 2^31
+  const uint32_t rbl = local / (uint32_t)e.slabs;
+  r.rbl = rbl;
+  r.kb = local - rbl * (uint32_t)e.slabs;
+  r.rbg = e.rb_begin + r.rbl;
+  return r;
+}
 
 // ---- activation staging: bf16 global -> f16 shared, one 128-K slab --------
 template <int NT>
@@ -120,15 +165,15 @@ struct XStage {
   static constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
   uint4 r[kPer];
 
-  __device__ __forceinline__ void load(const DecodeParams& p, int64_t kb, int tid) {
+  __device__ __forceinline__ void load(const DecodeEntry& e, int m, int64_t kb, int tid) {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int v = tid + i * kThreads;
       const int mrow = v >> 4, q = v & 15;
       const int64_t k = kb * kSlabK + q * 8;
       uint4 val = make_uint4(0, 0, 0, 0);
-      if (v < kUnits && mrow < p.m && k < p.cols)
-        val = __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)mrow * p.cols + k));
+      if (v < kUnits && mrow < m && k < e.cols)
+        val = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)mrow * e.cols + k));
       r[i] = val;
     }
   }
@@ -223,46 +268,54 @@ __device__ __forceinline__ bool apply_scale(float (&acc)[R][NT][4], float& cs, f
 // and the reduction wait until the CTA has streamed all its weights, so no
 // fence, barrier or atomic round trip stalls the weight pipeline mid-stream.
 template <int NT, int R>
-__device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const DecodeParams& p, int64_t row0, int g,
-                                        int tig) {
+__device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const DecodeEntry& e, int m, int64_t row0,
+                                        int g, int tig) {
 #pragma unroll
   for (int rt = 0; rt < R; ++rt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t o = row0 + rt * 16 + g + 8 * (e >> 1);
-        const int mm = nt * 8 + 2 * tig + (e & 1);
-        if (o < p.rows && mm < p.m) {
-          const __nv_bfloat16 b = __float2bfloat16_rn(acc[rt][nt][e]);
-          p.y[(int64_t)mm * p.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+      for (int q = 0; q < 4; ++q) {
+        const int64_t o = row0 + rt * 16 + g + 8 * (q >> 1);
+        const int mm = nt * 8 + 2 * tig + (q & 1);
+        if (o < e.rows && mm < m) {
+          const __nv_bfloat16 b = __float2bfloat16_rn(acc[rt][nt][q]);
+          e.y[(int64_t)mm * e.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
         }
       }
 }
 
+// Row-block bookkeeping of the split-K partition (all in group row blocks).
 struct RunGeom {
-  int64_t G, U, u0, c;
-  __device__ __forceinline__ int64_t first_cta(const DecodeParams& p, int64_t rb) const { return cta_of(rb * p.slabs, G, U); }
-  __device__ __forceinline__ int64_t last_cta(const DecodeParams& p, int64_t rb) const {
-    return cta_of(rb * p.slabs + p.slabs - 1, G, U);
+  int64_t G, U, c;
+  __device__ __forceinline__ int64_t first_unit(const DecodeParams& p, int64_t rbg) const {
+    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
+    return e.unit_begin + (rbg - e.rb_begin) * e.slabs;
   }
-  __device__ __forceinline__ bool partial(const DecodeParams& p, int64_t rb) const {
-    return first_cta(p, rb) != last_cta(p, rb);
+  __device__ __forceinline__ int64_t first_cta(const DecodeParams& p, int64_t rbg) const {
+    return cta_of(first_unit(p, rbg), G, U);
   }
-  // Partial slot of CTA cc for row block rb: 0 for its first run, 1 otherwise.
-  __device__ __forceinline__ int64_t slot(const DecodeParams& p, int64_t cc, int64_t rb) const {
-    return 2 * cc + (rb == (cc * U / G) / p.slabs ? 0 : 1);
+  __device__ __forceinline__ int64_t last_cta(const DecodeParams& p, int64_t rbg) const {
+    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
+    return cta_of(first_unit(p, rbg) + e.slabs - 1, G, U);
+  }
+  __device__ __forceinline__ bool partial(const DecodeParams& p, int64_t rbg) const {
+    return first_cta(p, rbg) != last_cta(p, rbg);
+  }
+  // Partial slot of CTA cc for row block rbg: 0 for its first run, 1 otherwise.
+  __device__ __forceinline__ int64_t slot(const DecodeParams& p, int64_t cc, int64_t rbg) const {
+    return 2 * cc + (rbg == unit_pos(p, cc * U / G).rbg ? 0 : 1);
   }
 };
 
 template <int NT, int R>
 __device__ __forceinline__ void end_run(float (&acc)[R][NT][4], const DecodeParams& p, const RunGeom& geo,
-                                        int64_t rb, int64_t row0, int warp, int lane) {
+                                        const UnitPos& up, int64_t row0, int warp, int lane) {
   constexpr int kSlot = kWarps * R * NT * 32 * 4;  // floats per partial slot
-  if (!geo.partial(p, rb)) {
-    write_y<NT, R>(acc, p, row0, lane >> 2, lane & 3);
+  if (!geo.partial(p, up.rbg)) {
+    write_y<NT, R>(acc, p.e[up.j], p.m, row0, lane >> 2, lane & 3);
   } else {
-    float4* slot = reinterpret_cast<float4*>(p.partials + geo.slot(p, geo.c, rb) * (int64_t)kSlot);
+    float4* slot = reinterpret_cast<float4*>(p.partials + geo.slot(p, geo.c, up.rbg) * (int64_t)kSlot);
 #pragma unroll
     for (int rt = 0; rt < R; ++rt)
 #pragma unroll
@@ -287,8 +340,11 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
   __syncthreads();
   if (tid == 0) {
     int last = 0;
-    if (pf) last |= (atomicAdd(p.counters + rb_first, 1) == (int)(geo.last_cta(p, rb_first) - geo.first_cta(p, rb_first)));
-    if (pl) last |= (atomicAdd(p.counters + rb_last, 1) == (int)(geo.last_cta(p, rb_last) - geo.first_cta(p, rb_last))) << 1;
+    if (pf)
+      last |= (atomicAdd(p.counters + rb_first, 1) == (int)(geo.last_cta(p, rb_first) - geo.first_cta(p, rb_first)));
+    if (pl)
+      last |= (atomicAdd(p.counters + rb_last, 1) == (int)(geo.last_cta(p, rb_last) - geo.first_cta(p, rb_last)))
+              << 1;
     *s_last = last;
   }
   __syncthreads();
@@ -298,8 +354,9 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
     if (!(last & (1 << which))) continue;
-    const int64_t rb = which == 0 ? rb_first : rb_last;
-    const int64_t cf = geo.first_cta(p, rb), cl = geo.last_cta(p, rb);
+    const int64_t rbg = which == 0 ? rb_first : rb_last;
+    const int j = entry_of_rb(p, rbg);
+    const int64_t cf = geo.first_cta(p, rbg), cl = geo.last_cta(p, rbg);
     float acc[R][NT][4];
     zero<NT, R>(acc);
     // Per accumulator tile, the loads of up to four contributors are issued
@@ -310,7 +367,7 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int64_t cc = c0 + q <= cl ? c0 + q : cl;
-        sl[q] = reinterpret_cast<const float4*>(p.partials + geo.slot(p, cc, rb) * (int64_t)kSlot);
+        sl[q] = reinterpret_cast<const float4*>(p.partials + geo.slot(p, cc, rbg) * (int64_t)kSlot);
       }
       const int nq = (int)(cl - c0 + 1 < 4 ? cl - c0 + 1 : 4);
 #pragma unroll
@@ -331,13 +388,13 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
             }
         }
     }
-    write_y<NT, R>(acc, p, rb * kRowsCta + warp * kRowsWarp, lane >> 2, lane & 3);
-    if (tid == 0) p.counters[rb] = 0;
+    write_y<NT, R>(acc, p.e[j], p.m, (rbg - p.e[j].rb_begin) * kRowsCta + warp * kRowsWarp, lane >> 2, lane & 3);
+    if (tid == 0) p.counters[rbg] = 0;
   }
 }
 
 // ---- the kernel ---------------------------------------------------------------
-// FUSED = false: weight slabs come from the view by TMA (thread 0 issues).
+// FUSED = false: weight slabs come from the views by TMA (thread 0 issues).
 // FUSED = true:  every thread copies 16-byte pieces straight from the chunks
 //                with cp.async into the same swizzled layout.
 template <int NT, int R, int S, bool FUSED>
@@ -370,29 +427,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   // Stage slab i (unit u0 + i) into ring slot i % S.
   auto issue = [&](int64_t i) {
-    const int64_t u = u0 + i, rb = u / p.slabs, kb = u - rb * p.slabs;
+    const UnitPos up = unit_pos(p, u0 + i);
+    const DecodeEntry& e = p.e[up.j];
     uint8_t* dst = wst + (int)(i % S) * kStage;
     if (!FUSED) {
       uint64_t* bar = &full[(int)(i % S)];
       dev::mbar_arrive_expect_tx(bar, kStage);
 #pragma unroll
       for (int b = 0; b < kBoxes; ++b)
-        tma_load_2d(dst + b * kBoxRows * kSlabK, &p.tmap, (int32_t)(kb * kSlabK),
-                    (int32_t)(rb * kRowsCta + b * kBoxRows), bar);
+        tma_load_2d(dst + b * kBoxRows * kSlabK, &e.tmap, (int32_t)(up.kb * kSlabK),
+                    (int32_t)(up.rbl * kRowsCta + b * kBoxRows), bar);
     } else {
       // thread -> 16-byte column piece cu of rows rr, rr + 32, ...; byte
       // g = t_offset + o * cols + k of T lives in chunk g / C at g % C.
       const int cu = tid & 7;
-      const int64_t k = kb * kSlabK + 16 * cu;
+      const int64_t k = up.kb * kSlabK + 16 * cu;
       const int64_t C = p.chunk_bytes;
-      int64_t gb = p.t_offset + (rb * kRowsCta + (tid >> 3)) * p.cols + k;
+      int64_t gb = e.t_offset + (up.rbl * kRowsCta + (tid >> 3)) * e.cols + k;
       int64_t ci = gb / C, off = gb - ci * C;
-      const int64_t step = 32 * p.cols;
+      const int64_t step = 32 * e.cols;
 #pragma unroll 4
-      for (int j = 0; j < kRowsCta / 32; ++j) {
-        const int rr = (tid >> 3) + 32 * j;
-        const int64_t o = rb * kRowsCta + rr;
-        const bool valid = o < p.rows && k < p.cols;
+      for (int jr = 0; jr < kRowsCta / 32; ++jr) {
+        const int rr = (tid >> 3) + 32 * jr;
+        const int64_t o = up.rbl * kRowsCta + rr;
+        const bool valid = o < e.rows && k < e.cols;
         const uint8_t* src = p.chunks[valid ? ci : 0] + (valid ? off : 0);
         dev::cp_async16(dst + rr * kSlabK + ((cu ^ (rr & 7)) << 4), src, valid ? 16u : 0u);
         off += step;
@@ -412,33 +470,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   } else if (tid == 0) {
     for (int64_t i = 0; i < n && i < S - 1; ++i) issue(i);
   }
+
   // Activations are fetched two slabs ahead (register sets xa / xb take turns,
   // the loop is unrolled by two so they stay in registers), and block scales
   // 32 slabs at a time, one per lane, a block ahead, so no global-load latency
   // sits on the per-slab path.
   XS xa, xb;
+  auto stage_x = [&](XS& dst, int64_t i) {
+    const UnitPos up = unit_pos(p, u0 + i);
+    dst.load(p.e[up.j], p.m, up.kb, tid);
+  };
   auto scale_of = [&](int64_t i) -> float {
     if (i >= n) return 0.f;
-    const int64_t u = u0 + i, rb = u / p.slabs, kb = u - rb * p.slabs;
-    const int64_t row0 = rb * kRowsCta + warp * kRowsWarp;
-    return row0 < p.rows ? __ldg(p.scales + (row0 >> 7) * p.scale_cols + kb) : 0.f;
+    const UnitPos up = unit_pos(p, u0 + i);
+    const DecodeEntry& e = p.e[up.j];
+    const int64_t row0 = up.rbl * kRowsCta + warp * kRowsWarp;
+    return row0 < e.rows ? __ldg(e.scales + (row0 >> 7) * e.scale_cols + up.kb) : 0.f;
   };
   float sc_cur = scale_of(lane), sc_next = scale_of(32 + lane);
   if (n > 0) {
-    xa.load(p, u0 % p.slabs, tid);
+    stage_x(xa, 0);
     xa.store(xs[0], tid);
   }
-  if (n > 1) xb.load(p, (u0 + 1) % p.slabs, tid);
+  if (n > 1) stage_x(xb, 1);
   float acc[R][NT][4];
   zero<NT, R>(acc);
   float cs = 0.f;  // scale the accumulator currently refers to
-  const RunGeom geo{G, U, u0, c};
+  const RunGeom geo{G, U, c};
   bool timed_out = false;
 
   // One slab: `nx` receives slab i + 2 (it held slab i, already staged);
   // `cx` holds slab i + 1, staged at the end.
   auto slab = [&](int64_t i, XS& nx, XS& cx) {
-    const int64_t u = u0 + i;
     const int st = (int)(i % S);
     bool ok = true;
     if (FUSED) dev::cp_async_wait<S - 2>();
@@ -447,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         dev::set_status(p.status, SWS_E_TIMEOUT);
-        for (int64_t j = i; j < n && j < i + S - 1; ++j)  // drain copies still in flight (bounded)
-          dev::mbar_wait(&full[(int)(j % S)], (uint32_t)((j / S) & 1), kWaitLimitNs / 4);
+        for (int64_t jj = i; jj < n && jj < i + S - 1; ++jj)  // drain copies still in flight (bounded)
+          dev::mbar_wait(&full[(int)(jj % S)], (uint32_t)((jj / S) & 1), kWaitLimitNs / 4);
       }
       timed_out = true;
       return;
@@ -458,15 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     } else if (tid == 0 && i + S - 1 < n) {
       issue(i + S - 1);
     }
-    if (i + 2 < n) nx.load(p, (u + 2) % p.slabs, tid);
+    if (i + 2 < n) stage_x(nx, i + 2);
     if ((i & 31) == 0 && i > 0) {
       sc_cur = sc_next;
       sc_next = scale_of(i + 32 + lane);
     }
     const float s = __shfl_sync(0xffffffffu, sc_cur, (int)(i & 31));
-    const int64_t rb = u / p.slabs, kb = u - rb * p.slabs;
-    const int64_t row0 = rb * kRowsCta + warp * kRowsWarp;
-    if (u == u0 || kb == 0) cs = 0.f;
+    const UnitPos up = unit_pos(p, u0 + i);
+    const int64_t row0 = up.rbl * kRowsCta + warp * kRowsWarp;
+    if (i == 0 || up.kb == 0) cs = 0.f;
     if (apply_scale<NT, R>(acc, cs, s)) {
       const uint8_t* wb = wst + st * kStage;
 #pragma unroll
@@ -483,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
     if (i + 1 < n) cx.store(xs[(i + 1) & 1], tid);
-    if (i + 1 == n || kb + 1 == p.slabs) {
+    if (i + 1 == n || up.kb + 1 == p.e[up.j].slabs) {
       rescale<NT, R>(acc, cs);
-      end_run<NT, R>(acc, p, geo, rb, row0, warp, lane);
+      end_run<NT, R>(acc, p, geo, up, row0, warp, lane);
     }
   };
   for (int64_t i = 0; i < n && !timed_out; i += 2) {
@@ -493,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (i + 1 < n && !timed_out) slab(i + 1, xb, xa);
   }
   if (!timed_out && n > 0)
-    settle_partials<NT, R, kRowsCta, kRowsWarp>(p, geo, u0 / p.slabs, (u1 - 1) / p.slabs, warp, lane, &s_last);
+    settle_partials<NT, R, kRowsCta, kRowsWarp>(p, geo, unit_pos(p, u0).rbg, unit_pos(p, u1 - 1).rbg, warp, lane,
+                                                &s_last);
   if (FUSED) dev::cp_async_wait<0>();
   if (tid == 0) {
     __threadfence();
@@ -509,6 +573,7 @@ constexpr int stages_for() { return NT <= 2 ? 3 : NT == 4 ? 6 : 5; }
 
 int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
+int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -541,7 +606,7 @@ int encode_weight_map(CUtensorMap* m, const void* w, int64_t rows, int64_t cols,
 }
 
 template <int NT, bool FUSED>
-cudaError_t launch_nt(DecodeParams& p, int64_t row_blocks, int64_t grid_cap, cudaStream_t s) {
+cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int R = rows_per_warp_tiles<NT>();
   constexpr int S = stages_for<NT>();
   constexpr int kRowsCta = kWarps * 16 * R;
@@ -551,87 +616,97 @@ cudaError_t launch_nt(DecodeParams& p, int64_t row_blocks, int64_t grid_cap, cud
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
   if (attr != cudaSuccess) return attr;
-  p.units = row_blocks * p.slabs;
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
   kern<<<(unsigned)grid, kThreads, kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
-// Fills everything but the tensor map / chunk table and the scratch pointers.
-void fill_params(DecodeParams& p, const float* scales, const uint16_t* x, uint16_t* y, int64_t m, int64_t rows,
-                 int64_t cols) {
-  p.w = nullptr;
-  for (int i = 0; i < 256; ++i) p.chunks[i] = nullptr;
-  p.chunk_bytes = 1;
-  p.t_offset = 0;
-  p.scales = scales;
-  p.scale_cols = cdiv(cols, 128);
-  p.x = x;
-  p.y = y;
-  p.rows = rows;
-  p.cols = cols;
-  p.m = (int32_t)m;
-  p.slabs = (int32_t)cdiv(cols, kSlabK);
-  p.status = nullptr;
-  p.trace = nullptr;
-  p.tag = 0;
-}
-
-cudaError_t dispatch(DecodeParams& p, int nt, bool fused, int64_t row_blocks, int64_t grid_cap, cudaStream_t s) {
+cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, int64_t grid_cap, cudaStream_t s) {
   switch (nt) {
-    case 1: return fused ? launch_nt<1, true>(p, row_blocks, grid_cap, s) : launch_nt<1, false>(p, row_blocks, grid_cap, s);
-    case 2: return fused ? launch_nt<2, true>(p, row_blocks, grid_cap, s) : launch_nt<2, false>(p, row_blocks, grid_cap, s);
-    case 4: return fused ? launch_nt<4, true>(p, row_blocks, grid_cap, s) : launch_nt<4, false>(p, row_blocks, grid_cap, s);
-    default: return fused ? launch_nt<8, true>(p, row_blocks, grid_cap, s) : launch_nt<8, false>(p, row_blocks, grid_cap, s);
+    case 1: return fused ? launch_nt<1, true>(p, grid_cap, s) : launch_nt<1, false>(p, grid_cap, s);
+    case 2: return fused ? launch_nt<2, true>(p, grid_cap, s) : launch_nt<2, false>(p, grid_cap, s);
+    case 4: return fused ? launch_nt<4, true>(p, grid_cap, s) : launch_nt<4, false>(p, grid_cap, s);
+    default: return fused ? launch_nt<8, true>(p, grid_cap, s) : launch_nt<8, false>(p, grid_cap, s);
   }
 }
 
-int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
-
-}  // namespace
-
-int decode_workspace_bytes(int64_t m, int64_t rows, int64_t cols, int64_t* bytes) {
-  (void)cols;
-  if (m < 0 || m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)m);
-  const int nt = nt_for(std::max<int64_t>(m, 1));
-  const int64_t row_blocks = cdiv(rows, rows_per_cta(nt));
-  if (row_blocks > kMaxCounters) return fail(SWS_E_UNSUPPORTED, "decode: %lld rows is too many", (long long)rows);
-  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot_bytes_for(nt);
+// Validates a group and fills the kernel parameters, except the scratch
+// pointers. *empty is set when nothing is left to launch (every item has no
+// rows or no columns; outputs of zero-column items are zeroed on `s`).
+int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, bool* empty, cudaStream_t s) {
+  *empty = true;
+  if (g.n < 1 || g.n > kMaxDecodeGroup) return fail(SWS_E_INVALID, "decode: group of %d linears", g.n);
+  if (g.m < 0 || g.m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)g.m);
+  const int nt = nt_for(std::max<int64_t>(g.m, 1));
+  const int rows_cta = rows_per_cta(nt);
+  p.n_entries = 0;
+  p.m = (int32_t)g.m;
+  p.units = 0;
+  for (int i = 0; i < 256; ++i) p.chunks[i] = i < g.n_chunks ? g.chunks[i] : nullptr;
+  p.chunk_bytes = g.chunk_bytes > 0 ? g.chunk_bytes : 1;
+  int64_t rb = 0;
+  for (int i = 0; i < g.n; ++i) {
+    const DecodeItem& it = g.item[i];
+    if (it.cols % 16 != 0)
+      return fail(SWS_E_UNSUPPORTED, "decode: cols=%lld is not a multiple of 16", (long long)it.cols);
+    if (g.m == 0 || it.rows == 0) continue;
+    if (it.cols == 0) {
+      cudaError_t e = cudaMemsetAsync(it.y, 0, (size_t)(g.m * it.rows * 2), s);
+      if (e != cudaSuccess) return cuda_fail(e, "decode: cudaMemsetAsync");
+      continue;
+    }
+    DecodeEntry& e = p.e[p.n_entries++];
+    if (!g.fused) {
+      int rc = encode_weight_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
+      if (rc != SWS_OK) return rc;
+    }
+    e.scales = it.scales;
+    e.x = it.x;
+    e.y = it.y;
+    e.rows = it.rows;
+    e.cols = it.cols;
+    e.t_offset = it.t_offset;
+    e.scale_cols = cdiv(it.cols, 128);
+    e.slabs = (int32_t)cdiv(it.cols, kSlabK);
+    e.unit_begin = p.units;
+    e.rb_begin = rb;
+    const int64_t nrb = cdiv(it.rows, rows_cta);
+    rb += nrb;
+    p.units += nrb * e.slabs;
+  }
+  if (rb > kMaxCounters) return fail(SWS_E_UNSUPPORTED, "decode: %lld row blocks in one launch", (long long)rb);
+  if (p.units >= ((int64_t)1 << 31)) return fail(SWS_E_UNSUPPORTED, "decode: group too large");
+  *row_blocks = rb;
+  *empty = p.n_entries == 0;
   return SWS_OK;
 }
 
-int launch_decode(const DecodeLaunch& a, cudaStream_t s) {
-  if (a.m <= 0 || a.rows == 0) return SWS_OK;
-  if (a.cols % 16 != 0) return fail(SWS_E_UNSUPPORTED, "decode: cols=%lld is not a multiple of 16", (long long)a.cols);
+}  // namespace
+
+int decode_workspace_bytes(int64_t m, int64_t* bytes) {
+  if (m < 0 || m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)m);
+  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot_bytes_for(nt_for(std::max<int64_t>(m, 1)));
+  return SWS_OK;
+}
+
+int launch_decode(const DecodeGroup& g, cudaStream_t s) {
+  if (g.m == 0) return SWS_OK;
   int64_t need = 0;
-  int rc = decode_workspace_bytes(a.m, a.rows, a.cols, &need);
+  int rc = decode_workspace_bytes(g.m, &need);
   if (rc != SWS_OK) return rc;
-  if (a.workspace_bytes < need)
-    return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)a.workspace_bytes, (long long)need);
-  if (a.cols == 0) {
-    cudaError_t e = cudaMemsetAsync(a.y, 0, (size_t)(a.m * a.rows * 2), s);
-    return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode: cudaMemsetAsync");
-  }
+  if (g.workspace_bytes < need)
+    return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);
   DecodeParams p;
-  fill_params(p, a.scales, a.x, a.y, a.m, a.rows, a.cols);
-  const bool fused = a.w == nullptr;
-  const int nt = nt_for(a.m);
-  if (fused) {
-    for (int i = 0; i < a.n_chunks && i < 256; ++i) p.chunks[i] = a.chunks[i];
-    p.chunk_bytes = a.chunk_bytes > 0 ? a.chunk_bytes : 1;
-    p.t_offset = a.t_offset;
-  } else {
-    p.w = a.w;
-    rc = encode_weight_map(&p.tmap, a.w, a.rows, a.cols, std::min(256, rows_per_cta(nt)));
-    if (rc != SWS_OK) return rc;
-  }
-  p.counters = reinterpret_cast<int32_t*>(a.workspace + kCtlBytes);
-  p.partials = reinterpret_cast<float*>(a.workspace + kCtlBytes + kMaxCounters * 4);
-  p.status = reinterpret_cast<int32_t*>(a.workspace);
-  p.trace = a.trace;
-  p.tag = a.tag;
-  const int64_t row_blocks = cdiv(a.rows, rows_per_cta(nt));
-  cudaError_t e = dispatch(p, nt, fused, row_blocks, kMaxGrid, s);
+  int64_t row_blocks = 0;
+  bool empty = true;
+  rc = build_params(p, g, &row_blocks, &empty, s);
+  if (rc != SWS_OK || empty) return rc;
+  p.counters = reinterpret_cast<int32_t*>(g.workspace + kCtlBytes);
+  p.partials = reinterpret_cast<float*>(g.workspace + kCtlBytes + kMaxCounters * 4);
+  p.status = reinterpret_cast<int32_t*>(g.workspace);
+  p.trace = g.trace;
+  p.tag = g.tag;
+  cudaError_t e = dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 
@@ -709,25 +784,30 @@ extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t ro
   int rc = check_device();
   if (rc != SWS_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cols == 0) {
-    cudaError_t e = cudaMemsetAsync(y, 0, (size_t)(m * rows * 2), s);
-    return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: cudaMemsetAsync(y)");
-  }
+  DecodeGroup g;
+  g.n = 1;
+  g.m = m;
+  g.fused = false;
+  g.item[0] = DecodeItem{static_cast<const uint8_t*>(w), scales, static_cast<const uint16_t*>(x),
+                         static_cast<uint16_t*>(y), rows, cols, 0};
+  DecodeParams p;
+  int64_t nrb = 0;
+  bool empty = true;
+  rc = build_params(p, g, &nrb, &empty, s);
+  if (rc != SWS_OK || empty) return rc;
   uint8_t* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc != SWS_OK) return rc;
   int32_t* counters = reinterpret_cast<int32_t*>(scratch + kNoAllocPartialBytes);
-  cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)(row_blocks * 4), s);
+  cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)(nrb * 4), s);
   if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaMemsetAsync(counters)");
-  DecodeParams p;
-  fill_params(p, scales, static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), m, rows, cols);
-  p.w = static_cast<const uint8_t*>(w);
-  rc = encode_weight_map(&p.tmap, w, rows, cols, std::min(256, rows_per_cta(nt)));
-  if (rc != SWS_OK) return rc;
   p.counters = counters;
   p.partials = reinterpret_cast<float*>(scratch);
+  p.status = nullptr;
+  p.trace = nullptr;
+  p.tag = 0;
   // Two partial slots per CTA must fit in the fixed array.
   const int64_t grid_cap = kNoAllocPartialBytes / (2 * slot_bytes_for(nt));
-  e = dispatch(p, nt, false, row_blocks, grid_cap, s);
+  e = dispatch(p, nt, false, grid_cap, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
 }

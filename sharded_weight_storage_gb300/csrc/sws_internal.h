@@ -79,26 +79,36 @@ struct CopySeg {
 };
 cudaError_t launch_relayout(const std::vector<CopySeg>& segs, cudaStream_t s);
 
-// Weight address map: for the slot path, row o starts at base + o * cols.
-// For the fused path, byte g = off + o * cols + k of T lives in
-// chunks[g / chunk] at g % chunk.
-struct DecodeLaunch {
-  const uint8_t* w;          // slot view (or nullptr for fused)
-  const uint8_t* chunks[256];
-  int32_t n_chunks;
-  int64_t chunk_bytes;
-  int64_t t_offset;          // o_j for fused addressing
+// Decode linears (m <= 64): a group of up to kMaxDecodeGroup linears that
+// share m runs as one launch. Slot path: each item's weight is a view `w`
+// [rows, cols] (TMA). Fused path: each item's bytes are T[t_offset, ...) read
+// through the layer's chunks (byte g of T lives in chunks[g / C] at g % C).
+constexpr int kMaxDecodeGroup = 8;
+struct DecodeItem {
+  const uint8_t* w;  // slot / replicated view (unused on the fused path)
   const float* scales;
-  const uint16_t* x;         // bf16 [m, cols]
-  uint16_t* y;               // bf16 [m, rows]
-  int64_t m, rows, cols;
-  uint8_t* workspace;        // control + counters + partials
-  int64_t workspace_bytes;
-  uint64_t* trace;
-  uint64_t tag;
+  const uint16_t* x;  // bf16 [m, cols]
+  uint16_t* y;        // bf16 [m, rows]
+  int64_t rows, cols;
+  int64_t t_offset;  // fused path: o_j
 };
-int decode_workspace_bytes(int64_t m, int64_t rows, int64_t cols, int64_t* bytes);
-int launch_decode(const DecodeLaunch& a, cudaStream_t s);
+struct DecodeGroup {
+  DecodeItem item[kMaxDecodeGroup];
+  int32_t n = 0;
+  int64_t m = 0;
+  bool fused = false;
+  const uint8_t* chunks[256];
+  int32_t n_chunks = 0;
+  int64_t chunk_bytes = 0;
+  uint8_t* workspace = nullptr;  // control + counters + partials
+  int64_t workspace_bytes = 0;
+  uint64_t* trace = nullptr;
+  uint64_t tag = 0;
+};
+// Workspace a decode launch with this m needs (independent of the shapes, up
+// to kMaxCounters row blocks per launch).
+int decode_workspace_bytes(int64_t m, int64_t* bytes);
+int launch_decode(const DecodeGroup& g, cudaStream_t s);
 
 int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, float* ex, cudaStream_t s);
 

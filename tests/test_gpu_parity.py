@@ -264,3 +264,53 @@ def test_quantize_x_bit_exact(S, m, k):
     rq, re = O.quantize_x(WL.bf16_to_f64(WL.bf16_bits(x)))
     assert np.array_equal(ex.cpu().numpy(), re)
     assert np.array_equal(xq.cpu().numpy(), rq)
+
+
+# ---------------------------------------------------------------------------
+# grouped layer linears (one launch per layer and source path)
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("m", [1, 9, 33, 64])
+def test_layer_linears_grouped_kda(S, m):
+    w = SMALL_KDA
+    ents = workload_entries(w, 1)
+    layers = draw_layers(w, 1)
+    st = build_stack(S, ents, w.n_shards, layers)
+    st.ctx.gather_to_slot(0, 1, 0)
+    xs = [WL.draw_x(w.key, j, m, c).cuda() for j, (_, r, c) in enumerate(ents)]
+    for src in (S.SRC_SLOT1, S.SRC_FUSED):
+        ys = [torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda") for (_, r, c) in ents]
+        st.ctx.layer_linears(0, src, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
+        torch.cuda.synchronize()
+        for j in range(len(ents)):
+            ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[0].codes[j], layers[0].scales[j])
+            assert_close(bf16_tensor_to_f64(ys[j]), ref, f"entry {j} src {src} m {m}")
+
+
+def test_layer_linears_ten_entries_with_replicated(S):
+    # 10 entries (two launches of the views group), two of them replicated
+    # (rows % N != 0) and therefore read from their own buffers even on the
+    # fused source.
+    from helpers import LayerData
+    rng = np.random.default_rng(21)
+    shapes = [(0, 4 * (8 + 13 * j) if j not in (3, 7) else 4 * (8 + 13 * j) + 1, 16 * (3 + 5 * j)) for j in range(10)]
+    codes, scales = {}, {}
+    for j, (_, r, c) in enumerate(shapes):
+        q = rng.integers(0, 256, size=(r, c), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0x3C
+        codes[j] = q
+        scales[j] = (2.0 ** rng.uniform(-8, -4, size=(-(-r // 128), -(-c // 128)))).astype(np.float32)
+    with _nowarn():
+        st = build_stack(S, shapes, 4, [LayerData(codes, scales)])
+    assert [st.entry_info[j][2] for j in range(10)] == [j not in (3, 7) for j in range(10)]
+    st.ctx.gather_to_slot(0, 0, 0)
+    m = 12
+    xs = [WL.draw_x(31, j, m, c).cuda() for j, (_, r, c) in enumerate(shapes)]
+    for src in (S.SRC_SLOT0, S.SRC_FUSED):
+        ys = [torch.empty((m, r), dtype=torch.bfloat16, device="cuda") for (_, r, c) in shapes]
+        st.ctx.layer_linears(0, src, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
+        torch.cuda.synchronize()
+        for j in range(10):
+            ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), codes[j], scales[j])
+            assert_close(bf16_tensor_to_f64(ys[j]), ref, f"entry {j} src {src}")
