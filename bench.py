@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stack-layers", type=int, default=92, help="layers of the lookahead stack (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["gather", "decode", "fused", "step", "noalloc"], default=None,
+    ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc"], default=None,
                     help="profiling driver: build the shared-expert layer and run one kernel --reps times")
     ap.add_argument("--m", type=int, default=HEADLINE_M)
     ap.add_argument("--entry", type=int, default=0, help="0 = gate_up, 1 = down")
@@ -549,12 +549,16 @@ def run_only(args, dist):
     j, m = args.entry, args.m
     x = WL.draw_x(w.key, j, m, ents[j][2]).cuda()
     y = torch.empty((m, ents[j][1]), dtype=torch.bfloat16, device="cuda")
+    xl = [WL.draw_x(w.key, jj, m, ents[jj][2]).cuda() for jj in range(len(ents))]
+    yl = [torch.empty((m, ents[jj][1]), dtype=torch.bfloat16, device="cuda") for jj in range(len(ents))]
     off = st.entry_info[j][0]
     for _ in range(args.reps):
         if args.only == "gather":
             ctx.gather_to_slot(0, 0, 0)
         elif args.only == "decode":
             ctx.linear(j, S.SRC_SLOT0, x.data_ptr(), m, y.data_ptr(), 0)
+        elif args.only == "layer":
+            ctx.layer_linears(0, S.SRC_SLOT0, [xx.data_ptr() for xx in xl], [yy.data_ptr() for yy in yl], m, 0)
         elif args.only == "fused":
             ctx.linear(j, S.SRC_FUSED, x.data_ptr(), m, y.data_ptr(), 0)
         elif args.only == "noalloc":
