@@ -36,7 +36,6 @@
 //     the CTA has streamed all its weights, the last CTA to arrive on a row
 //     block (atomic counter, no waiting) adds them in K order and writes Y.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -575,36 +574,6 @@ int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
 int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point.
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// 2-D map of an e4m3 weight [rows, cols] (row stride cols bytes): boxes of 128
-// bytes of k by box_rows rows, 128-byte swizzle, zero fill outside.
-int encode_weight_map(CUtensorMap* m, const void* w, int64_t rows, int64_t cols, int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return fail(SWS_E_CUDA, "decode: cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t gstride[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {(cuuint32_t)kSlabK, (cuuint32_t)box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), gdim, gstride, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(SWS_E_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return SWS_OK;
-}
-
 template <int NT, bool FUSED>
 cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int R = rows_per_warp_tiles<NT>();
@@ -657,7 +626,7 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
     }
     DecodeEntry& e = p.e[p.n_entries++];
     if (!g.fused) {
-      int rc = encode_weight_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
+      int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
       if (rc != SWS_OK) return rc;
     }
     e.scales = it.scales;

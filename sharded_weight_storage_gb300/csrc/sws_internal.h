@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -56,6 +57,10 @@ constexpr uint64_t kTraceGather = 1, kTraceLinear = 2;
 // Device-side wait limit for mbarrier / TMA waits, in nanoseconds of
 // %globaltimer. A wait that runs out sets the status word and the kernel exits.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// 2-D tensor map of a byte matrix [rows, cols] (row stride cols, cols % 16 ==
+// 0): boxes of 128 bytes by box_rows rows, 128-byte swizzle, zero fill outside.
+int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
