@@ -39,6 +39,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stack-layers", type=int, default=92, help="layers of the lookahead stack (0 skips it)")
+    ap.add_argument("--prefill-layers", type=int, default=8, help="layers of the prefill run (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc"], default=None,
                     help="profiling driver: build the shared-expert layer and run one kernel --reps times")
@@ -145,6 +146,17 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def fp8_peak():
+    """Dense FP8 peak: the measured bf16 cuBLAS peak times the nominal fp8/bf16
+    ratio (4.5 / 2.25 = 2); (burst, sustained, source)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return 2 * float(d["bf16_tflops"]), 2 * float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured bf16 x 2"
+    return 2 * 1900.0, 2 * 1700.0, "fallback bf16 x 2"
 
 
 # ---------------------------------------------------------------------------
@@ -448,6 +460,98 @@ def run_stack(args, dist, n_layers):
     return out
 
 
+def run_prefill(args, dist, n_layers):
+    """Prefill on the KDA-layer weights (N = 8): per-linear tcgen05 GEMM
+    throughput at M = 2048 and 8192, whole-layer time, and lookahead over
+    n_layers layers with the gather overlapped."""
+    import torch
+
+    import sharded_weight_storage_gb300 as S
+    import workloads as WL
+    from sharded_weight_storage_gb300.storage import ShardedStack
+
+    dev = torch.device("cuda", dist.local)
+    w = WL.PREFILL
+    n = w.n_shards
+    ne = len(w.entries)
+    ents = [(l, e.rows, e.cols) for l in range(n_layers) for e in w.entries]
+    base = WL.base_layer(w, 0)
+    base_dev = [torch.from_numpy(c).to(dev) for c in base.codes]
+    base_sc = [torch.from_numpy(s).to(dev) for s in base.scales]
+    del base
+    mmax = max(w.m_values)
+    st = ShardedStack([(l, S.E4M3, r, c) for (l, r, c) in ents], n, max_m=mmax, device=str(dev))
+    for l in range(n_layers):
+        codes, scales = {}, {}
+        for j, e in enumerate(w.entries):
+            signs = torch.from_numpy(WL.draw_row_signs(w.key, l, j, e.rows)).to(dev)
+            codes[l * ne + j] = WL.apply_row_signs(base_dev[j], signs)
+            scales[l * ne + j] = base_sc[j]
+        st.load_layer(l, codes, scales)
+    del base_dev
+    ctx = st.make_ctx()
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    burst, sustained, src = fp8_peak()
+    out = {"workload": f"KDA-like layer x{n_layers}, N={n}, FP8 e4m3 weights and quantised activations",
+           "fp8_peak_tflops": burst, "fp8_peak_source": src, "per_m": {}}
+
+    def timed(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    with torch.cuda.stream(stream):
+        ctx.gather_to_slot(0, 0, sp)
+        for m in w.m_values:
+            ctx.gather_to_slot(0, 0, sp)  # the lookahead run below retags both slots
+            xs = [WL.draw_x(w.key, j, m, e.cols).to(dev) for j, e in enumerate(w.entries)]
+            ys = [torch.empty((m, e.rows), dtype=torch.bfloat16, device=dev) for e in w.entries]
+            per = {}
+            flops_layer = 0
+            for j, e in enumerate(w.entries):
+                call = lambda j=j: ctx.linear(j, 0, xs[j].data_ptr(), m, ys[j].data_ptr(), sp)
+                call()
+                t = timed(call)
+                fl = 2.0 * m * e.rows * e.cols
+                flops_layer += fl
+                per[e.name] = {"us": t * 1e3, "TFLOPS": fl / t / 1e9, "frac_of_fp8_peak": fl / t / 1e9 / burst}
+            # quantiser alone for the widest activation
+            xq = torch.empty((m, 8192), dtype=torch.uint8, device=dev)
+            ex = torch.empty((m, 64), dtype=torch.float32, device=dev)
+            xw = WL.draw_x(w.key, 99, m, 8192).to(dev)
+            q_ms = timed(lambda: S.quantize_x(xw.data_ptr(), m, 8192, xq.data_ptr(), ex.data_ptr(), sp))
+            lay = lambda: ctx.layer_linears(0, 0, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, sp)
+            lay()
+            t_layer = timed(lay)
+            io = [([x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m) for _ in range(n_layers)]
+            side = torch.cuda.Stream(device=dev)
+            ctx.run_layers(0, n_layers - 1, io, 0, sp, side.cuda_stream)
+            t_run = timed(lambda: ctx.run_layers(0, n_layers - 1, io, 0, sp, side.cuda_stream), reps=3)
+            ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, sp, side.cuda_stream)
+            exposed, layer_ms = ctx.run_timing(n_layers)
+            out["per_m"][m] = {
+                "linears": per, "layer_us": t_layer * 1e3, "layer_TFLOPS": flops_layer / t_layer / 1e9,
+                "layer_frac_of_fp8_peak": flops_layer / t_layer / 1e9 / burst,
+                "quantize_8192_cols_us": q_ms * 1e3,
+                "lookahead_step_ms": t_run, "lookahead_TFLOPS": n_layers * flops_layer / t_run / 1e9,
+                "exposed_gather_us_per_layer": 1e3 * statistics.mean(exposed[1:]) if n_layers > 1 else 1e3 * exposed[0],
+                "exposed_frac_of_step": sum(exposed) / t_run,
+            }
+            del xs, ys, xq, ex, xw
+    torch.cuda.synchronize()
+    del st, ctx
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline only; never on the GPU path)
 # ---------------------------------------------------------------------------
@@ -590,6 +694,7 @@ def main():
         return
     r = run_ours(args, dist)
     stack = run_stack(args, dist, args.stack_layers) if args.stack_layers > 0 else None
+    prefill = run_prefill(args, dist, args.prefill_layers) if args.prefill_layers > 0 else None
     if dist.rank != 0:
         dist.close()
         return
@@ -628,6 +733,7 @@ def main():
         "gather_alone": r["gather_alone"],
         "per_m": r["per_m"],
         "lookahead_stack": stack,
+        "prefill": prefill,
         "weight_GBps_step": total / ms_step / 1e6,
     }
     if dist.world == 1 and not args.no_cpu_baseline:
