@@ -88,10 +88,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return r;
 }
 
+// bf16 pair -> f16 pair: exact for |x| in [2^-24, 65504]; larger magnitudes
+// saturate to +-65504, smaller ones round to the f16 subnormal grid.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
   uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
