@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--m", type=int, default=HEADLINE_M)
     ap.add_argument("--entry", type=int, default=0, help="0 = gate_up, 1 = down")
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--decode-kernel", choices=["auto", "mma", "tcgen05"], default="auto",
+                    help="which kernel serves decode linears from views")
     return ap.parse_args()
 
 
@@ -192,6 +194,10 @@ def ncu_traffic(kernel_key, sha):
     return d.get("dram_bytes_per_launch")
 
 
+def set_decode_kernel(S, name):
+    S.set_option(S.OPT_DECODE_KERNEL, {"auto": S.DECODE_AUTO, "mma": S.DECODE_MMA, "tcgen05": S.DECODE_TCGEN05}[name])
+
+
 class Timer:
     """CUDA events on one stream; pairs are resolved after a synchronize."""
 
@@ -223,6 +229,7 @@ def run_ours(args, dist):
     from sharded_weight_storage_gb300.storage import ShardedStack
 
     dev = torch.device("cuda", dist.local)
+    set_decode_kernel(S, args.decode_kernel)
     w = WL.SHARED_EXPERT
     n = w.n_shards
     ents = [(0, e.rows, e.cols) for e in w.entries]
@@ -642,6 +649,7 @@ def run_only(args, dist):
     import workloads as WL
     from sharded_weight_storage_gb300.storage import ShardedStack
 
+    set_decode_kernel(S, args.decode_kernel)
     w = WL.SHARED_EXPERT
     ents = [(0, e.rows, e.cols) for e in w.entries]
     lw = WL.layer_weights(w, 0)

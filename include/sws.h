@@ -249,6 +249,17 @@ int sws_ctx_status(sws_ctx* ctx, int32_t clear);
 int sws_trace_begin(sws_ctx* ctx, uint64_t* records, int32_t capacity, sws_stream_t stream);
 int32_t sws_trace_count(const sws_ctx* ctx);
 
+/* ---- options -------------------------------------------------------------- */
+#define SWS_OPT_DECODE_KERNEL 1 /* which kernel serves decode linears (m <= 64) from views */
+#define SWS_DECODE_AUTO 0       /* chosen by m (default) */
+#define SWS_DECODE_MMA 1        /* warp-level mma.sync kernel */
+#define SWS_DECODE_TCGEN05 2    /* tcgen05 / TMEM kernel */
+/* Process-wide option, read at each launch. Both decode kernels compute the
+ * same linear (sws_linear) within the same tolerance; chunk-map (fused) reads
+ * always use the mma.sync kernel. SWS_E_INVALID for an unknown option or
+ * value. */
+int sws_set_option(int32_t option, int64_t value);
+
 /* ---- misc --------------------------------------------------------------- */
 const char* sws_last_error(void);
 /* Library version as major*10000 + minor*100 + patch. */

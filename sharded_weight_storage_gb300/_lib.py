@@ -16,6 +16,8 @@ E_INVALID, E_ALIGN, E_STATE, E_CUDA, E_TIMEOUT, E_UNSUPPORTED, E_WORKSPACE = -1,
 E4M3, BF16, F32, U8 = 0, 1, 2, 3
 SRC_SLOT0, SRC_SLOT1, SRC_FUSED = 0, 1, 2
 RUN_FUSED, RUN_TIMING = 1, 2
+OPT_DECODE_KERNEL = 1
+DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05 = 0, 1, 2
 
 _NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}
@@ -64,6 +66,7 @@ _PROTOS = [
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
     ("sws_trace_count", C.c_int32, [C.c_void_p]),
+    ("sws_set_option", C.c_int, [C.c_int32, C.c_int64]),
     ("sws_last_error", C.c_char_p, []),
     ("sws_version", C.c_int32, []),
 ]
@@ -158,6 +161,10 @@ def workspace_bytes(plan: Plan, max_m: int) -> int:
     if v < 0:
         raise SwsError(E_INVALID, "workspace_bytes: " + last_error())
     return v
+
+
+def set_option(option: int, value: int):
+    check(lib().sws_set_option(option, value), "set_option")
 
 
 def quantize_x(x: int, m: int, k: int, xq: int, ex: int, stream: int = 0):

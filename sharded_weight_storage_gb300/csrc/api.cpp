@@ -464,4 +464,16 @@ int sws_trace_begin(sws_ctx* c, uint64_t* records, int32_t capacity, sws_stream_
 
 int32_t sws_trace_count(const sws_ctx* c) { return c ? c->trace_next : -1; }
 
+int sws_set_option(int32_t option, int64_t value) {
+  switch (option) {
+    case SWS_OPT_DECODE_KERNEL:
+      if (value < SWS_DECODE_AUTO || value > SWS_DECODE_TCGEN05)
+        return fail(SWS_E_INVALID, "set_option: decode kernel %lld", (long long)value);
+      set_decode_kernel((int)value);
+      return SWS_OK;
+    default:
+      return fail(SWS_E_INVALID, "set_option: unknown option %d", option);
+  }
+}
+
 }  // extern "C"

@@ -1,0 +1,142 @@
+// Shared pieces of the decode linears (m <= 64): launch parameters of a group
+// of linears, the (row block, K slab) unit space of the split-K partition, and
+// small conversion / copy helpers. Included by decode_gemm.cu (mma.sync
+// kernel) and decode_tc.cu (tcgen05 kernel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "sws_internal.h"
+
+namespace sws {
+namespace dec {
+
+constexpr int kSlabK = 128;
+constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
+
+// One linear of a group.
+struct DecodeEntry {
+  CUtensorMap tmap;   // slot path: 2-D map of the weight view [rows, cols] u8
+  CUtensorMap xmap;   // tcgen05 path: 2-D map of the activations [m, cols] bf16
+  const float* scales;
+  const uint16_t* x;  // bf16 [m, cols]
+  uint16_t* y;        // bf16 [m, rows]
+  int64_t rows, cols;
+  int64_t t_offset;    // fused path: o_j, the entry's offset in T
+  int64_t scale_cols;  // ceil(cols / 128)
+  int64_t unit_begin;  // first unit of this entry in the group's unit space
+  int64_t rb_begin;    // first row block of this entry in the group
+  int32_t slabs;       // ceil(cols / 128)
+};
+
+struct DecodeParams {
+  DecodeEntry e[kMaxDecodeGroup];
+  int32_t n_entries;
+  int32_t m;
+  int64_t units;  // total units (row block x K slab) of the group
+  const uint8_t* chunks[256];  // fused path: the layer's chunks
+  int64_t chunk_bytes;
+  int32_t* counters;
+  float* partials;
+  int32_t* status;
+  uint64_t* trace;
+  uint64_t tag;
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_bytes));
+  return r;
+}
+
+// bf16 pair -> f16 pair: exact for |x| in [2^-24, 65504]; larger magnitudes
+// saturate to +-65504, smaller ones round to the f16 subnormal grid.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dev::smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(dev::smem_addr(bar))
+      : "memory");
+}
+
+// Which CTA's unit range [c*U/G, (c+1)*U/G) contains unit u.
+__device__ __forceinline__ int64_t cta_of(int64_t u, int64_t G, int64_t U) { return ((u + 1) * G - 1) / U; }
+
+// Where a unit of the group's unit space lies.
+struct UnitPos {
+  int j;        // entry
+  int64_t rbl;  // row block inside the entry
+  int64_t kb;   // K slab
+  int64_t rbg;  // row block in the group
+};
+
+__device__ __forceinline__ int entry_of_unit(const DecodeParams& p, int64_t u) {
+  int j = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxDecodeGroup; ++q)
+    if (q < p.n_entries && u >= p.e[q].unit_begin) j = q;
+  return j;
+}
+
+__device__ __forceinline__ int entry_of_rb(const DecodeParams& p, int64_t rbg) {
+  int j = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxDecodeGroup; ++q)
+    if (q < p.n_entries && rbg >= p.e[q].rb_begin) j = q;
+  return j;
+}
+
+__device__ __forceinline__ UnitPos unit_pos(const DecodeParams& p, int64_t u) {
+  UnitPos r;
+  r.j = entry_of_unit(p, u);
+  const DecodeEntry& e = p.e[r.j];
+  const uint32_t local = (uint32_t)(u - e.unit_begin);  // units per entry < 2^31
+  const uint32_t rbl = local / (uint32_t)e.slabs;
+  r.rbl = rbl;
+  r.kb = local - rbl * (uint32_t)e.slabs;
+  r.rbg = e.rb_begin + r.rbl;
+  return r;
+}
+
+// Row-block bookkeeping of the split-K partition (all in group row blocks).
+struct RunGeom {
+  int64_t G, U, c;
+  __device__ __forceinline__ int64_t first_unit(const DecodeParams& p, int64_t rbg) const {
+    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
+    return e.unit_begin + (rbg - e.rb_begin) * e.slabs;
+  }
+  __device__ __forceinline__ int64_t first_cta(const DecodeParams& p, int64_t rbg) const {
+    return cta_of(first_unit(p, rbg), G, U);
+  }
+  __device__ __forceinline__ int64_t last_cta(const DecodeParams& p, int64_t rbg) const {
+    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
+    return cta_of(first_unit(p, rbg) + e.slabs - 1, G, U);
+  }
+  __device__ __forceinline__ bool partial(const DecodeParams& p, int64_t rbg) const {
+    return first_cta(p, rbg) != last_cta(p, rbg);
+  }
+  // Partial slot of CTA cc for row block rbg: 0 for its first run, 1 otherwise.
+  __device__ __forceinline__ int64_t slot(const DecodeParams& p, int64_t cc, int64_t rbg) const {
+    return 2 * cc + (rbg == unit_pos(p, cc * U / G).rbg ? 0 : 1);
+  }
+};
+
+// tcgen05 decode kernel (decode_tc.cu): units of 256 weight rows; launches a
+// group whose params were built with that unit height and activation maps.
+constexpr int kTcUnitRows = 256;
+cudaError_t launch_decode_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s);
+int64_t tc_slot_bytes(int64_t m);
+
+}  // namespace dec
+}  // namespace sws

@@ -43,59 +43,22 @@
 #include <algorithm>
 #include <mutex>
 
+#include "decode_common.cuh"
 #include "ptx.cuh"
 #include "sws_internal.h"
 
 namespace sws {
 namespace {
 
+using namespace dec;
+
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlabK = 128;
-constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
 
-// One linear of a group.
-struct DecodeEntry {
-  CUtensorMap tmap;  // slot path: 2-D map of the weight view [rows, cols] u8
-  const float* scales;
-  const uint16_t* x;  // bf16 [m, cols]
-  uint16_t* y;        // bf16 [m, rows]
-  int64_t rows, cols;
-  int64_t t_offset;    // fused path: o_j, the entry's offset in T
-  int64_t scale_cols;  // ceil(cols / 128)
-  int64_t unit_begin;  // first unit of this entry in the group's unit space
-  int64_t rb_begin;    // first row block of this entry in the group
-  int32_t slabs;       // ceil(cols / 128)
-};
-
-struct DecodeParams {
-  DecodeEntry e[kMaxDecodeGroup];
-  int32_t n_entries;
-  int32_t m;
-  int64_t units;  // total units (row block x K slab) of the group
-  const uint8_t* chunks[256];  // fused path: the layer's chunks
-  int64_t chunk_bytes;
-  int32_t* counters;
-  float* partials;
-  int32_t* status;
-  uint64_t* trace;
-  uint64_t tag;
-};
-
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_bytes));
-  return r;
-}
-
-// bf16 pair -> f16 pair: exact for |x| in [2^-24, 65504]; larger magnitudes
-// saturate to +-65504, smaller ones round to the f16 subnormal grid.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
+// Position of 16-byte activation unit u (8 f16 of k) in row m of a staged
+// slab: spreads the 4 units a thread reads, and neighbouring rows, over all
+// 32 banks.
+__device__ __forceinline__ int xpos(int u, int m) { return u ^ (((u >> 3) & 1) << 1) ^ (m & 1); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -104,59 +67,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(dev::smem_addr(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(dev::smem_addr(bar))
-      : "memory");
-}
-
-// Which CTA's unit range [c*U/G, (c+1)*U/G) contains unit u.
-__device__ __forceinline__ int64_t cta_of(int64_t u, int64_t G, int64_t U) { return ((u + 1) * G - 1) / U; }
-
-// Position of 16-byte activation unit u (8 f16 of k) in row m of a staged
-// slab: spreads the 4 units a thread reads, and neighbouring rows, over all
-// 32 banks.
-__device__ __forceinline__ int xpos(int u, int m) { return u ^ (((u >> 3) & 1) << 1) ^ (m & 1); }
-
-// Where a unit of the group's unit space lies.
-struct UnitPos {
-  int j;        // entry
-  int64_t rbl;  // row block inside the entry
-  int64_t kb;   // K slab
-  int64_t rbg;  // row block in the group
-};
-
-__device__ __forceinline__ int entry_of_unit(const DecodeParams& p, int64_t u) {
-  int j = 0;
-#pragma unroll
-  for (int q = 1; q < kMaxDecodeGroup; ++q)
-    if (q < p.n_entries && u >= p.e[q].unit_begin) j = q;
-  return j;
-}
-
-__device__ __forceinline__ int entry_of_rb(const DecodeParams& p, int64_t rbg) {
-  int j = 0;
-#pragma unroll
-  for (int q = 1; q < kMaxDecodeGroup; ++q)
-    if (q < p.n_entries && rbg >= p.e[q].rb_begin) j = q;
-  return j;
-}
-
-__device__ __forceinline__ UnitPos unit_pos(const DecodeParams& p, int64_t u) {
-  UnitPos r;
-  r.j = entry_of_unit(p, u);
-  const DecodeEntry& e = p.e[r.j];
-  const uint32_t local = (uint32_t)(u - e.unit_begin);  // units per entry < 2^31
-  const uint32_t rbl = local / (uint32_t)e.slabs;
-  r.rbl = rbl;
-  r.kb = local - rbl * (uint32_t)e.slabs;
-  r.rbg = e.rb_begin + r.rbl;
-  return r;
 }
 
 // ---- activation staging: bf16 global -> f16 shared, one 128-K slab --------
@@ -285,29 +195,6 @@ __device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const Deco
         }
       }
 }
-
-// Row-block bookkeeping of the split-K partition (all in group row blocks).
-struct RunGeom {
-  int64_t G, U, c;
-  __device__ __forceinline__ int64_t first_unit(const DecodeParams& p, int64_t rbg) const {
-    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
-    return e.unit_begin + (rbg - e.rb_begin) * e.slabs;
-  }
-  __device__ __forceinline__ int64_t first_cta(const DecodeParams& p, int64_t rbg) const {
-    return cta_of(first_unit(p, rbg), G, U);
-  }
-  __device__ __forceinline__ int64_t last_cta(const DecodeParams& p, int64_t rbg) const {
-    const DecodeEntry& e = p.e[entry_of_rb(p, rbg)];
-    return cta_of(first_unit(p, rbg) + e.slabs - 1, G, U);
-  }
-  __device__ __forceinline__ bool partial(const DecodeParams& p, int64_t rbg) const {
-    return first_cta(p, rbg) != last_cta(p, rbg);
-  }
-  // Partial slot of CTA cc for row block rbg: 0 for its first run, 1 otherwise.
-  __device__ __forceinline__ int64_t slot(const DecodeParams& p, int64_t cc, int64_t rbg) const {
-    return 2 * cc + (rbg == unit_pos(p, cc * U / G).rbg ? 0 : 1);
-  }
-};
 
 template <int NT, int R>
 __device__ __forceinline__ void end_run(float (&acc)[R][NT][4], const DecodeParams& p, const RunGeom& geo,
@@ -604,12 +491,13 @@ cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, int64_t grid_cap
 // Validates a group and fills the kernel parameters, except the scratch
 // pointers. *empty is set when nothing is left to launch (every item has no
 // rows or no columns; outputs of zero-column items are zeroed on `s`).
-int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, bool* empty, cudaStream_t s) {
+int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, bool* empty, cudaStream_t s,
+                 bool tc = false) {
   *empty = true;
   if (g.n < 1 || g.n > kMaxDecodeGroup) return fail(SWS_E_INVALID, "decode: group of %d linears", g.n);
   if (g.m < 0 || g.m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)g.m);
   const int nt = nt_for(std::max<int64_t>(g.m, 1));
-  const int rows_cta = rows_per_cta(nt);
+  const int rows_cta = tc ? kTcUnitRows : rows_per_cta(nt);
   p.n_entries = 0;
   p.m = (int32_t)g.m;
   p.units = 0;
@@ -629,6 +517,10 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
     DecodeEntry& e = p.e[p.n_entries++];
     if (!g.fused) {
       int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
+      if (rc != SWS_OK) return rc;
+    }
+    if (tc) {  // activation slabs [N, 128] bf16, N = m rounded up to 16
+      int rc = encode_bf16_rows_map(&e.xmap, it.x, g.m, it.cols, kSlabK, (int)(((g.m + 15) / 16) * 16));
       if (rc != SWS_OK) return rc;
     }
     e.scales = it.scales;
@@ -654,9 +546,24 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
 
 }  // namespace
 
+namespace {
+int g_decode_kernel = kDecodeAuto;
+}
+
+void set_decode_kernel(int k) { g_decode_kernel = k; }
+
+// The tcgen05 kernel runs a 128 x N x 16 MMA for every 16 k whatever m is, so
+// it pays off once the warp-level MMAs of the mma.sync kernel limit the rate.
+int decode_kernel_for(int64_t m) {
+  if (g_decode_kernel != kDecodeAuto) return g_decode_kernel;
+  return m > 16 ? kDecodeTc : kDecodeMma;
+}
+
 int decode_workspace_bytes(int64_t m, int64_t* bytes) {
   if (m < 0 || m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)m);
-  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot_bytes_for(nt_for(std::max<int64_t>(m, 1)));
+  const int64_t mm = std::max<int64_t>(m, 1);
+  const int64_t slot = std::max<int64_t>(slot_bytes_for(nt_for(mm)), tc_slot_bytes(mm));
+  *bytes = kCtlBytes + kMaxCounters * 4 + 2 * (int64_t)kMaxGrid * slot;
   return SWS_OK;
 }
 
@@ -670,14 +577,15 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   DecodeParams p;
   int64_t row_blocks = 0;
   bool empty = true;
-  rc = build_params(p, g, &row_blocks, &empty, s);
+  const bool tc = !g.fused && decode_kernel_for(g.m) == kDecodeTc;
+  rc = build_params(p, g, &row_blocks, &empty, s, tc);
   if (rc != SWS_OK || empty) return rc;
   p.counters = reinterpret_cast<int32_t*>(g.workspace + kCtlBytes);
   p.partials = reinterpret_cast<float*>(g.workspace + kCtlBytes + kMaxCounters * 4);
   p.status = reinterpret_cast<int32_t*>(g.workspace);
   p.trace = g.trace;
   p.tag = g.tag;
-  cudaError_t e = dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
+  cudaError_t e = tc ? launch_decode_tc(p, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 

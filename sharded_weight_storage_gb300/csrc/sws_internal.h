@@ -61,6 +61,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // 2-D tensor map of a byte matrix [rows, cols] (row stride cols, cols % 16 ==
 // 0): boxes of 128 bytes by box_rows rows, 128-byte swizzle, zero fill outside.
 int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+// 2-D tensor map of a bf16 matrix [rows, cols] (row stride 2*cols bytes,
+// cols % 8 == 0): boxes of box_cols x box_rows elements, no swizzle.
+int encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows);
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
@@ -114,6 +117,10 @@ struct DecodeGroup {
 // to kMaxCounters row blocks per launch).
 int decode_workspace_bytes(int64_t m, int64_t* bytes);
 int launch_decode(const DecodeGroup& g, cudaStream_t s);
+// Which decode kernel serves a view-path launch: SWS_DECODE_AUTO picks by m.
+enum DecodeKernel { kDecodeAuto = 0, kDecodeMma = 1, kDecodeTc = 2 };
+void set_decode_kernel(int k);
+int decode_kernel_for(int64_t m);
 
 int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, float* ex, cudaStream_t s);
 

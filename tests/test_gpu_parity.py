@@ -314,3 +314,69 @@ def test_layer_linears_ten_entries_with_replicated(S):
         for j in range(10):
             ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), codes[j], scales[j])
             assert_close(bf16_tensor_to_f64(ys[j]), ref, f"entry {j} src {src}")
+
+
+# ---------------------------------------------------------------------------
+# both decode kernels (warp-level mma.sync and tcgen05) on the same checks
+# ---------------------------------------------------------------------------
+
+
+@pytest.fixture(params=["mma", "tcgen05"])
+def decode_kernel(S, request):
+    S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_MMA if request.param == "mma" else S.DECODE_TCGEN05)
+    yield request.param
+    S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_AUTO)
+
+
+@pytest.mark.parametrize("m", [1, 5, 16, 17, 31, 33, 48, 64])
+def test_decode_kernels_full_output(S, decode_kernel, m):
+    w = SMALL_KDA
+    ents = workload_entries(w, 1)
+    layers = draw_layers(w, 1)
+    st = build_stack(S, ents, w.n_shards, layers)
+    st.ctx.gather_to_slot(0, 0, 0)
+    xs = [WL.draw_x(w.key, j, m, c).cuda() for j, (_, r, c) in enumerate(ents)]
+    for j in range(len(ents)):
+        y = _run_linear(st, j, S.SRC_SLOT0, xs[j], m)
+        ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[0].codes[j], layers[0].scales[j])
+        assert_close(bf16_tensor_to_f64(y), ref, f"{decode_kernel} entry {j} m {m}")
+    ys = [torch.empty((m, r), dtype=torch.bfloat16, device="cuda") for (_, r, c) in ents]
+    st.ctx.layer_linears(0, S.SRC_SLOT0, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
+    torch.cuda.synchronize()
+    for j in range(len(ents)):
+        ref = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[0].codes[j], layers[0].scales[j])
+        assert_close(bf16_tensor_to_f64(ys[j]), ref, f"{decode_kernel} grouped entry {j} m {m}")
+    assert st.ctx.status() == 0
+
+
+def test_decode_kernels_ragged_and_special(S, decode_kernel):
+    rng = np.random.default_rng(77)
+    shapes = [(0, 4 * 101, 16 * 9), (0, 4 * 3, 16), (0, 4 * 300, 16 * 200), (0, 4 * 64, 16 * 24)]
+    codes, scales = {}, {}
+    for j, (_, r, c) in enumerate(shapes):
+        q = rng.integers(0, 256, size=(r, c), dtype=np.uint8)
+        q[(q & 0x7F) == 0x7F] = 0x3C
+        codes[j] = q
+        scales[j] = (2.0 ** rng.uniform(-8, -4, size=(-(-r // 128), -(-c // 128)))).astype(np.float32)
+    scales[3][:] = 0.0  # an all-zero-scale weight gives exactly zero
+    from helpers import LayerData
+    ld = LayerData(codes, scales)
+    st = build_stack(S, shapes, 4, [ld])
+    st.ctx.gather_to_slot(0, 1, 0)
+    for m in (1, 7, 20, 64):
+        for j in range(len(shapes)):
+            _check_linear_full(st, ld, j, S.SRC_SLOT1, m, 98)
+    x = WL.draw_x(1, 0, 40, shapes[3][2]).cuda()
+    y = _run_linear(st, 3, S.SRC_SLOT1, x, 40)
+    assert not y.float().abs().max().item()
+
+
+def test_decode_kernels_full_size_sampled(S, decode_kernel):
+    w = WL.SHARED_EXPERT
+    ents = workload_entries(w, 1)
+    layers = draw_layers(w, 1)
+    st = build_stack(S, ents, w.n_shards, layers)
+    st.ctx.gather_to_slot(0, 0, 0)
+    for m in (8, 32, 64):
+        for j in range(len(ents)):
+            _check_linear_sampled(st, layers[0], j, S.SRC_SLOT0, m, w.key, seed=3)
