@@ -238,17 +238,30 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
   return launch_group(c, gf, layer, first_f, s);
 }
 
+// Activation split region of the tcgen05 decode path: enough for the largest
+// layer (all of a layer's linears in one launch).
+int64_t split_region_bytes(const sws_plan* p, int64_t m) {
+  int64_t most = 0;
+  for (const LayerPlan& l : p->layers) {
+    int64_t slabs = 0;
+    for (int32_t j : l.all) slabs += cdiv(p->entries[j].cols, 128);
+    most = std::max(most, slabs);
+  }
+  return decode_split_bytes(m, most);
+}
+
 }  // namespace
 
 extern "C" {
 
 int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   if (!p || max_m < 0) return -1;
+  const int64_t mm = std::min<int64_t>(std::max<int64_t>(max_m, 1), 64);
   int64_t dec = 0;
-  if (decode_workspace_bytes(std::min<int64_t>(std::max<int64_t>(max_m, 1), 64), &dec) != SWS_OK) return -1;
+  if (decode_workspace_bytes(mm, &dec) != SWS_OK) return -1;
   int64_t pre = 0;
   for (const EntryPlan& e : p->entries) pre = std::max(pre, prefill_bytes(max_m, e.cols));
-  return dec + pre;
+  return dec + split_region_bytes(p, mm) + pre;
 }
 
 int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void* slot1, const float* const* scales,
@@ -301,7 +314,7 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
   c->ws_bytes = workspace_bytes;
   int64_t dec64 = 0;
   decode_workspace_bytes(64, &dec64);
-  c->ws_decode = std::min(dec64, workspace_bytes);
+  c->ws_decode = std::min(dec64 + split_region_bytes(plan, 64), workspace_bytes);
   // Only the status word and the split-K arrival counters must start at zero.
   cudaError_t e = cudaMemset(workspace, 0, (size_t)(kCtlBytes + kMaxCounters * 4));
   if (e != cudaSuccess) {

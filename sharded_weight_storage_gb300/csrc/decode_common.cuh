@@ -20,11 +20,11 @@ constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
 // One linear of a group.
 struct DecodeEntry {
   CUtensorMap tmap;   // slot path: 2-D map of the weight view [rows, cols] u8
-  CUtensorMap xmap;   // tcgen05 path: 2-D map of the activations [m, cols] bf16
   const float* scales;
   const uint16_t* x;  // bf16 [m, cols]
   uint16_t* y;        // bf16 [m, rows]
   int64_t rows, cols;
+  uint8_t* xs;         // tcgen05 path: the entry's activation split blocks (one per K slab)
   int64_t t_offset;    // fused path: o_j, the entry's offset in T
   int64_t scale_cols;  // ceil(cols / 128)
   int64_t unit_begin;  // first unit of this entry in the group's unit space
@@ -132,9 +132,14 @@ struct RunGeom {
   }
 };
 
-// tcgen05 decode kernel (decode_tc.cu): units of 256 weight rows; launches a
-// group whose params were built with that unit height and activation maps.
+// tcgen05 decode kernel (decode_tc.cu): units of 256 weight rows. A launch
+// first splits the activations into per-slab blocks (xs of every entry), then
+// runs the GEMM on them; the params must have been built with that unit height.
 constexpr int kTcUnitRows = 256;
+__host__ __device__ constexpr int64_t tc_n_pad(int64_t m) { return (m + 15) / 16 * 16; }
+// Split block of one entry and K slab for n_pad = m rounded up to 16:
+// [hi e4m3 n_pad x 128 | lo e4m3 n_pad x 128 | e fp32 n_pad].
+__host__ __device__ constexpr int64_t tc_split_block_bytes(int64_t n_pad) { return 260 * n_pad; }
 cudaError_t launch_decode_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s);
 int64_t tc_slot_bytes(int64_t m);
 

@@ -492,7 +492,8 @@ cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, int64_t grid_cap
 // pointers. *empty is set when nothing is left to launch (every item has no
 // rows or no columns; outputs of zero-column items are zeroed on `s`).
 int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, bool* empty, cudaStream_t s,
-                 bool tc = false) {
+                 uint8_t* tc_split = nullptr) {
+  const bool tc = tc_split != nullptr;
   *empty = true;
   if (g.n < 1 || g.n > kMaxDecodeGroup) return fail(SWS_E_INVALID, "decode: group of %d linears", g.n);
   if (g.m < 0 || g.m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)g.m);
@@ -519,9 +520,10 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
       int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
       if (rc != SWS_OK) return rc;
     }
-    if (tc) {  // activation slabs [N, 128] bf16, N = m rounded up to 16
-      int rc = encode_bf16_rows_map(&e.xmap, it.x, g.m, it.cols, kSlabK, (int)(((g.m + 15) / 16) * 16));
-      if (rc != SWS_OK) return rc;
+    e.xs = nullptr;
+    if (tc) {  // the entry's activation split blocks, one per K slab
+      e.xs = tc_split;
+      tc_split += cdiv(it.cols, kSlabK) * tc_split_block_bytes(tc_n_pad(g.m));
     }
     e.scales = it.scales;
     e.x = it.x;
@@ -559,6 +561,10 @@ int decode_kernel_for(int64_t m) {
   return m > 16 ? kDecodeTc : kDecodeMma;
 }
 
+int64_t decode_split_bytes(int64_t m, int64_t slabs) {
+  return slabs * tc_split_block_bytes(tc_n_pad(std::max<int64_t>(m, 1)));
+}
+
 int decode_workspace_bytes(int64_t m, int64_t* bytes) {
   if (m < 0 || m > 64) return fail(SWS_E_INVALID, "decode: m=%lld outside [0, 64]", (long long)m);
   const int64_t mm = std::max<int64_t>(m, 1);
@@ -572,13 +578,20 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   int64_t need = 0;
   int rc = decode_workspace_bytes(g.m, &need);
   if (rc != SWS_OK) return rc;
+  const bool tc = !g.fused && decode_kernel_for(g.m) == kDecodeTc;
+  if (tc) {  // the activation split region follows the partial sums
+    int64_t slabs = 0;
+    for (int i = 0; i < g.n; ++i) slabs += cdiv(g.item[i].cols, kSlabK);
+    need += decode_split_bytes(g.m, slabs);
+  }
   if (g.workspace_bytes < need)
     return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);
   DecodeParams p;
   int64_t row_blocks = 0;
   bool empty = true;
-  const bool tc = !g.fused && decode_kernel_for(g.m) == kDecodeTc;
-  rc = build_params(p, g, &row_blocks, &empty, s, tc);
+  int64_t dec = 0;
+  decode_workspace_bytes(g.m, &dec);
+  rc = build_params(p, g, &row_blocks, &empty, s, tc ? g.workspace + dec : nullptr);
   if (rc != SWS_OK || empty) return rc;
   p.counters = reinterpret_cast<int32_t*>(g.workspace + kCtlBytes);
   p.partials = reinterpret_cast<float*>(g.workspace + kCtlBytes + kMaxCounters * 4);

@@ -4,22 +4,40 @@
 //
 //   Y[m, o] = bf16_rne( sum_kb s[o/128, kb] * sum_{i in kb} x[m, i] * e4m3(q[o, i]) )
 //
-// Swap-AB: the weight rows are the MMA's M = 128 dimension and the
-// activations its N = 16..64 dimension (m rounded up to 16).
-//   * warp 0, one thread: TMA producer. Per unit (256 weight rows x 128 K) it
-//     loads the e4m3 weight slab (128-byte swizzle) and the raw bf16 activation
-//     slab [N, 128] into one of 4-5 shared-memory stages.
-//   * warps 2-9 (each owns one quarter of the TMEM lanes of one of the unit's
-//     two 128-row tiles): convert every weight row exactly (e4m3 -> f16)
-//     straight into TMEM, where it is the MMA's A
-//     operand, and the activations (bf16 -> f16, saturating) into the 128-byte
-//     swizzled B layout in shared memory; then, one unit behind, read the MMA's
-//     per-slab result from TMEM and add it, times the slab's 128 x 128 block
-//     scale, into fp32 registers (exact block scaling, as in the prefill GEMM).
-//   * warp 1: allocates TMEM and issues tcgen05.mma kind::f16 with A in TMEM:
-//     2 tiles x 8 MMAs (128 x N x 16) per unit into two D buffers.
-// Converted weights never pass through shared memory, so shared-memory traffic
-// stays at about 2 bytes per weight byte (TMA write + conversion read).
+// The weights are never converted: the e4m3 weight slab goes from HBM (TMA,
+// 128-byte swizzle) straight into the MMA as its A operand, and the MMA is
+// tcgen05.mma kind::f8f6f4. The bf16 activations are made FP8 without loss:
+// per (row m, 128-K slab) with a power-of-two scale e = 2^(floor(log2 amax) - 7)
+// every x/e lies in [-256, 256) and is the exact sum of two e4m3 numbers,
+//   x/e = hi + lo,  hi = e4m3_rne(x/e),  lo = e4m3_rne(x/e - hi),
+// for all |x| >= amax / 1024 (smaller elements keep an error below
+// e * 2^-10 <= amax * 2^-17). So sum_i x_i w_i = e * (sum_i hi_i w_i + sum_i lo_i w_i):
+// the two terms are two more columns of the MMA, added when the result is
+// read out.
+//
+// A launch is two kernels on the stream:
+//   1. split_x_kernel: every (entry, K slab) block of activations -> its hi and
+//      lo e4m3 operands (already in the 128-byte swizzled order of a
+//      1024-byte aligned shared-memory tile) and the scales e, in the workspace.
+//      This is m x K work per linear, done once instead of once per row block.
+//   2. decode_tc_kernel, launched as a programmatic dependent of (1): its
+//      weight loads start while (1) runs; only the activation loads wait for
+//      (1) to finish (griddepcontrol.wait).
+// decode_tc_kernel (swap-AB: weight rows are the MMA's M = 128 dimension, the
+// activations its N = 16..64 dimension, m rounded up to 16):
+//   * warp 0, one thread: producer. Per unit (256 weight rows x 128 K) one TMA
+//     load of the weight slab, one bulk copy of the slab's split block and two
+//     4-byte async copies of the unit's weight scales, into one of 4-6 stages.
+//   * warp 1: allocates TMEM and issues, per unit, 2 tiles x 4 MMAs
+//     (128 x 2N x 32: the hi and lo operands side by side as one 2N-row B
+//     operand, so each weight byte is read from shared memory once) into one
+//     of two to four D buffers.
+//   * warps 2-9 (each one quarter of the TMEM lanes of one 128-row tile): read
+//     the unit's result from TMEM and add hi + lo, times s[o/128, kb] * e[m], into
+//     fp32 registers; at the end of a run, write Y or the split-K partial.
+// Shared-memory traffic is one TMA write and one MMA read per weight byte.
+// Every wait is bounded; the worker warps leave their loop together (a barrier
+// reduction of their failure flags), so no named barrier is left half-joined.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -40,18 +58,31 @@ constexpr int kTcRows = 256;  // weight rows per unit: two 128-row MMA tiles
 constexpr int kTcWarps = 10;  // 0 producer, 1 MMA, 2..9 workers (one per tile and TMEM lane quarter)
 constexpr int kWorkers = 8;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kTmemCols = 512;
+
+__host__ __device__ constexpr int pow2_at_least(int v) {
+  int r = 32;
+  while (r < v) r *= 2;
+  return r;
+}
 
 template <int N>
 struct TcCfg {
-  static constexpr int kWBytes = kTcRows * kSlabK;     // e4m3 weight slab
-  static constexpr int kXRawBytes = N * kSlabK * 2;    // bf16 activations [N][128]
-  static constexpr int kStageBytes = kWBytes + kXRawBytes;
-  static constexpr int kXBytes = N * kSlabK * 2;       // f16 B operand: two 128-byte atoms per row
-  static constexpr int kStages = N <= 32 ? 5 : 4;
-  static constexpr int kSmem = kStages * kStageBytes + 2 * kXBytes + 1024;
-  static constexpr int kSlotFloats = kTcRows * N;      // partial-sum slot of one CTA
+  static constexpr int kWBytes = kTcRows * kSlabK;              // e4m3 weight slab, 128-byte swizzle
+  static constexpr int kTermBytes = N * kSlabK;                 // one e4m3 B operand [N][128]
+  static constexpr int kXBytes = (int)tc_split_block_bytes(N);  // hi, lo, e
+  static constexpr int kSwOff = kWBytes + kXBytes;              // two fp32 weight scales
+  static constexpr int kStageBytes = (kSwOff + 16 + 1023) / 1024 * 1024;
+  static constexpr int kStages = N <= 16 ? 6 : N <= 32 ? 5 : 4;
+  static constexpr int kSmem = kStages * kStageBytes + 1024;
+  static constexpr int kDBufs = N <= 32 ? 4 : 2;  // TMEM accumulator buffers of 2 tiles x 2N columns
+  static constexpr int kTmemCols = pow2_at_least(kDBufs * 4 * N);
+  static constexpr int kSlotFloats = kTcRows * N;  // partial-sum slot of one CTA
 };
+static_assert(TcCfg<16>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
+static_assert(TcCfg<32>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
+static_assert(TcCfg<48>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
+static_assert(TcCfg<64>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
+static_assert(TcCfg<64>::kTmemCols <= 512, "decode_tc: TMEM columns");
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
@@ -63,19 +94,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// kind::f16 instruction descriptor: A, B f16, D f32, K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+// kind::f8f6f4 instruction descriptor: A, B e4m3, D f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f8(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D (TMEM) (+)= A (TMEM) x B (shared memory).
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D (TMEM) (+)= A (shared memory) x B (shared memory).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -86,40 +117,180 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 32 lanes x 16 consecutive fp32 columns, without waiting for completion.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 4-byte async copy global -> shared (zero fill when src_bytes == 0).
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dev::smem_addr(smem_dst)), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+// Arrives on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Barrier among the 8 worker warps only (named barrier 1).
 __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Scale of 128-row tile t of a unit (0 past the last row).
-__device__ __forceinline__ float tile_scale(const DecodeParams& p, const UnitPos& up, int t) {
-  const DecodeEntry& e = p.e[up.j];
-  const int64_t row0 = up.rbl * kTcRows + t * 128;
-  return row0 < e.rows ? __ldg(e.scales + (row0 >> 7) * e.scale_cols + up.kb) : 0.f;
+// Barrier among the worker warps that also returns whether any of them passed
+// `pred` true.
+__device__ __forceinline__ bool workers_sync_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
+
+// Every lane waits; the warp fails if any lane ran out of time.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  const bool ok = dev::mbar_wait(bar, parity, kWaitLimitNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Two fp32 -> e4m3 (round to nearest even, saturating); `lo` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
+  const uint32_t h = e4m3x2_to_f16x2(two_bytes);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// ---- 1. activation split ---------------------------------------------------------
+
+// Eight consecutive threads per (entry, K slab, row), 16 activations each. The
+// thread count is a multiple of 128, so whole warps are either in or out.
+__global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad) {
+  // Let the GEMM launch now: it waits for this grid's results before it reads them.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = (int)(tid & 7);
+  int64_t task = tid >> 3;  // (entry, slab, row)
+  int j = 0;
+  for (; j < p.n_entries; ++j) {
+    const int64_t t = (int64_t)p.e[j].slabs * n_pad;
+    if (task < t) break;
+    task -= t;
+  }
+  if (j >= p.n_entries) return;
+  const DecodeEntry& e = p.e[j];
+  const int64_t kb = task / n_pad;
+  const int r = (int)(task - kb * n_pad);
+  const int64_t col = kb * kSlabK + g * 16;
+  float v[16];
+  if (r < p.m && col < e.cols) {  // cols is a multiple of 16: a group is all in or all out
+    const uint4* src = reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col);
+    const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
+    const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  }
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  // e = 2^(E - 134) for amax with biased exponent E, so amax / e is in
+  // [128, 256); 1 for an all-zero (or below 2^-119) row slab.
+  const uint32_t E = __float_as_uint(a) >> 23;
+  const bool big = E > 7;
+  const float es = big ? __uint_as_float((E - 7) << 23) : 1.f;
+  const float inv = big ? __uint_as_float((261 - E) << 23) : 1.f;
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float s0 = v[4 * i] * inv, s1 = v[4 * i + 1] * inv;
+    const float s2 = v[4 * i + 2] * inv, s3 = v[4 * i + 3] * inv;
+    const uint32_t h01 = f32x2_to_e4m3x2(s0, s1), h23 = f32x2_to_e4m3x2(s2, s3);
+    const float2 b01 = e4m3x2_to_f32x2(h01), b23 = e4m3x2_to_f32x2(h23);
+    const uint32_t l01 = f32x2_to_e4m3x2(s0 - b01.x, s1 - b01.y);
+    const uint32_t l23 = f32x2_to_e4m3x2(s2 - b23.x, s3 - b23.y);
+    hi[i] = h01 | (h23 << 16);
+    lo[i] = l01 | (l23 << 16);
+  }
+  // Row r at r * 128, 16-byte chunk g at (g ^ (r & 7)) * 16: the 128-byte
+  // swizzle of a 1024-byte aligned tile.
+  uint8_t* blk = e.xs + kb * tc_split_block_bytes(n_pad);
+  const int off = r * 128 + ((g ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(blk + n_pad * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  if (g == 0) reinterpret_cast<float*>(blk + 2 * n_pad * 128)[r] = es;
+}
+
+// ---- 2. GEMM ---------------------------------------------------------------------
+
+// Walks a CTA's consecutive units like an odometer (K slab, then row block,
+// then entry), so the per-unit loop needs no division and reads the launch
+// parameters only when the entry changes.
+struct UnitCursor {
+  int j;
+  int64_t rbl, kb;
+  int32_t slabs;
+  int64_t nrb, rb_begin, rows, scale_cols;
+  const float* scales;
+  const uint8_t* xs;
+  __device__ __forceinline__ void load(const DecodeParams& p) {
+    const DecodeEntry& e = p.e[j];
+    slabs = e.slabs;
+    rows = e.rows;
+    nrb = (e.rows + kTcRows - 1) / kTcRows;
+    rb_begin = e.rb_begin;
+    scale_cols = e.scale_cols;
+    scales = e.scales;
+    xs = e.xs;
+  }
+  __device__ __forceinline__ void init(const DecodeParams& p, int64_t u) {
+    const UnitPos up = unit_pos(p, u);
+    j = up.j;
+    rbl = up.rbl;
+    kb = up.kb;
+    load(p);
+  }
+  __device__ __forceinline__ void next(const DecodeParams& p) {
+    if (++kb < slabs) return;
+    kb = 0;
+    if (++rbl < nrb) return;
+    rbl = 0;
+    if (++j < p.n_entries) load(p);
+  }
+  __device__ __forceinline__ UnitPos pos() const {
+    UnitPos r;
+    r.j = j;
+    r.rbl = rbl;
+    r.kb = kb;
+    r.rbg = rb_begin + rbl;
+    return r;
+  }
+};
 
 // Each worker thread owns row `row` of tile `t` (0 or 1) of every unit.
 template <int N>
@@ -154,6 +325,7 @@ __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& 
 
 // After the CTA's last unit: arrival counts on its (at most two) partial row
 // blocks; the last CTA to arrive adds the partials in K order and writes Y.
+// Called by all worker threads together.
 template <int N>
 __device__ __forceinline__ void tc_settle(const DecodeParams& p, const RunGeom& geo, int64_t u_first,
                                           int64_t u_last, int wt, int t, int row, int* s_last) {
@@ -204,13 +376,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   using Cf = TcCfg<N>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t dsm[];
-  __shared__ __align__(8) uint64_t sfull[S], sempty[S], abfull[2], abempty[2], dfull[2], dempty[2], mdone;
+  constexpr int kDBufs = Cf::kDBufs;
+  __shared__ __align__(8) uint64_t sfull[S], sempty[S], dfull[kDBufs], dempty[kDBufs], mdone;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_last;
   // Swizzled TMA tiles and MMA operands need 1024-byte aligned bases.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  uint8_t* xbuf = smem + S * Cf::kStageBytes;  // two f16 B operands
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t U = p.units, G = gridDim.x, c = blockIdx.x;
   const int64_t u0 = c * U / G, u1 = (c + 1) * U / G, n = u1 - u0;
@@ -218,12 +390,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   if (tid == 0) {
     dev::trace_start(p.trace);
     for (int s = 0; s < S; ++s) {
-      dev::mbar_init(&sfull[s], 1);
-      dev::mbar_init(&sempty[s], kWorkers);
+      dev::mbar_init(&sfull[s], 2);              // expect_tx arrival + the scale copies' arrival
+      dev::mbar_init(&sempty[s], 1 + kWorkers);  // MMA commit + the workers (they read e)
     }
-    for (int b = 0; b < 2; ++b) {
-      dev::mbar_init(&abfull[b], kWorkers);
-      dev::mbar_init(&abempty[b], 1);
+    for (int b = 0; b < kDBufs; ++b) {
       dev::mbar_init(&dfull[b], 1);
       dev::mbar_init(&dempty[b], kWorkers);
     }
@@ -233,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dev::smem_addr(&s_tmem)),
-                 "r"(kTmemCols)
+                 "r"(Cf::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
@@ -244,22 +414,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   const RunGeom geo{G, U, c};
 
   if (warp == 0) {
-    // ---- TMA producer ------------------------------------------------------
+    // ---- producer ------------------------------------------------------------
     if (lane == 0) {
+      for (int j = 0; j < p.n_entries; ++j)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.e[j].tmap)) : "memory");
+      const int64_t early = n < S ? n : S;  // units whose weight loads go out before the split is done
+      const uint8_t* early_src[S];          // their split blocks
+      bool split_ready = false;
+      UnitCursor cur;
+      cur.init(p, u0);
       int64_t i = 0;
-      for (; i < n && !s_abort; ++i) {
+      for (; i < n && !s_abort; ++i, cur.next(p)) {
         const int s = (int)(i % S);
         if (!dev::mbar_wait(&sempty[s], (uint32_t)(((i / S) & 1) ^ 1), kWaitLimitNs)) {
           dev::set_status(p.status, SWS_E_TIMEOUT);
           s_abort = 1;
           break;
         }
-        const UnitPos up = unit_pos(p, u0 + i);
-        const DecodeEntry& e = p.e[up.j];
         uint8_t* st = smem + s * Cf::kStageBytes;
-        dev::mbar_arrive_expect_tx(&sfull[s], Cf::kStageBytes);
-        tma_load_2d(st, &e.tmap, (int32_t)(up.kb * kSlabK), (int32_t)(up.rbl * kTcRows), &sfull[s]);
-        tma_load_2d(st + Cf::kWBytes, &e.xmap, (int32_t)(up.kb * kSlabK), 0, &sfull[s]);
+        dev::mbar_arrive_expect_tx(&sfull[s], Cf::kWBytes + Cf::kXBytes);
+        tma_load_2d(st, &p.e[cur.j].tmap, (int32_t)(cur.kb * kSlabK), (int32_t)(cur.rbl * kTcRows), &sfull[s]);
+        float* sw = reinterpret_cast<float*>(st + Cf::kSwOff);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int64_t row0 = cur.rbl * kTcRows + t * 128;
+          const bool in = row0 < cur.rows;
+          cp_async4(sw + t, cur.scales + (in ? (row0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+        }
+        cp_async_arrive_noinc(&sfull[s]);
+        const uint8_t* src = cur.xs + cur.kb * Cf::kXBytes;
+        if (split_ready) {
+          dev::bulk_g2s(st + Cf::kWBytes, src, Cf::kXBytes, &sfull[s]);
+        } else {
+          early_src[i] = src;
+          if (i + 1 == early) {
+            grid_dependency_wait();
+            split_ready = true;
+            for (int64_t k = 0; k <= i; ++k)
+              dev::bulk_g2s(smem + k * Cf::kStageBytes + Cf::kWBytes, early_src[k], Cf::kXBytes, &sfull[k]);
+          }
+        }
+      }
+      if (!split_ready) {  // aborted early: complete the stages already issued
+        grid_dependency_wait();
+        for (int64_t k = 0; k < i; ++k)
+          dev::bulk_g2s(smem + k * Cf::kStageBytes + Cf::kWBytes, early_src[k], Cf::kXBytes, &sfull[k]);
       }
       // Before the CTA may exit, every issued stage must have landed.
       for (int64_t k = i - S; k < i; ++k)
@@ -268,25 +467,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   } else if (warp == 1) {
     // ---- MMA issuer ----------------------------------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, N);
+      // B is the split block's hi and lo operands as one 2N-row operand, so
+      // each weight tile is read once: D[:, 0:N] = A hi^T, D[:, N:2N] = A lo^T.
+      constexpr uint32_t idesc = idesc_f8(128, 2 * N);
       bool issued = false;
       for (int64_t i = 0; i < n && !s_abort; ++i) {
-        const int b = (int)(i & 1);
-        if (!dev::mbar_wait(&abfull[b], (uint32_t)((i >> 1) & 1), kWaitLimitNs) ||
-            !dev::mbar_wait(&dempty[b], (uint32_t)(((i >> 1) & 1) ^ 1), kWaitLimitNs)) {
+        const int s = (int)(i % S), b = (int)(i % kDBufs);
+        if (!dev::mbar_wait(&sfull[s], (uint32_t)((i / S) & 1), kWaitLimitNs) ||
+            !dev::mbar_wait(&dempty[b], (uint32_t)(((i / kDBufs) & 1) ^ 1), kWaitLimitNs)) {
           dev::set_status(p.status, SWS_E_TIMEOUT);
           s_abort = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t xs = dev::smem_addr(xbuf + b * Cf::kXBytes);
+        const uint32_t wa = dev::smem_addr(smem + s * Cf::kStageBytes);
+        const uint32_t xb = wa + Cf::kWBytes;
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int k = 0; k < kSlabK / 16; ++k)
-            mma_f16_ta(tmem + 256 + b * 2 * N + t * N, tmem + b * 128 + t * 64 + k * 8,
-                       smem_desc_sw128(xs + (k >> 2) * (N * 128) + (k & 3) * 32), idesc, k > 0);
-        mma_commit(&abempty[b]);
+          for (int k = 0; k < kSlabK / 32; ++k)
+            mma_f8(tmem + b * 4 * N + t * 2 * N, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32),
+                   smem_desc_sw128(xb + k * 32), idesc, k != 0);
+        mma_commit(&sempty[s]);
         mma_commit(&dfull[b]);
         issued = true;
       }
@@ -296,105 +498,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       }
     }
   } else {
-    // ---- workers: convert unit i, promote unit i - 1 ---------------------------------
-    const int q = warp & 3;          // TMEM lane quarter of this warp
-    const int t = (warp - 2) >> 2;   // the unit's 128-row tile this warp works on
-    const int row = q * 32 + lane;   // row inside the tile = TMEM lane
-    const int wt = tid - 64;         // worker thread 0..255
+    // ---- workers: promote each unit's slab result ---------------------------------
+    const int q = warp & 3;         // TMEM lane quarter of this warp
+    const int t = (warp - 2) >> 2;  // the unit's 128-row tile this warp promotes
+    const int row = q * 32 + lane;  // row inside the tile = TMEM lane
+    const int wt = tid - 64;        // worker thread 0..255
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float acc[N];
 #pragma unroll
     for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
-    float sc_new = 0.f, sc_old = 0.f;
-    bool ok = true;
-    for (int64_t i = 0; i <= n && ok; ++i) {
-      if (i < n) {
-        const int s = (int)(i % S), b = (int)(i & 1);
-        if (!dev::mbar_wait(&sfull[s], (uint32_t)((i / S) & 1), kWaitLimitNs) ||
-            !dev::mbar_wait(&abempty[b], (uint32_t)(((i >> 1) & 1) ^ 1), kWaitLimitNs)) {
-          dev::set_status(p.status, SWS_E_TIMEOUT);
-          s_abort = 1;
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const UnitPos up = unit_pos(p, u0 + i);
-        sc_new = tile_scale(p, up, t);  // used when this unit is promoted, one step later
-        const uint8_t* st = smem + s * Cf::kStageBytes;
-        // weight row `row` of tile t, e4m3 -> f16 into TMEM (A operand)
-        const int r = t * 128 + row;
-        const uint8_t* wr = st + r * kSlabK;
+    bool fail = false;
+    UnitCursor cur;
+    cur.init(p, u0);
+    for (int64_t i = 0; i < n; ++i, cur.next(p)) {
+      const int s = (int)(i % S), b = (int)(i % kDBufs);
+      fail = !warp_wait(&sfull[s], (uint32_t)((i / S) & 1)) || !warp_wait(&dfull[b], (uint32_t)((i / kDBufs) & 1));
+      if (fail) break;
+      tc_fence_after();
+      const uint8_t* st = smem + s * Cf::kStageBytes;
+      const float* ex = reinterpret_cast<const float*>(st + Cf::kWBytes + 2 * Cf::kTermBytes);
+      const float sw = reinterpret_cast<const float*>(st + Cf::kSwOff)[t];
+      const uint32_t dcol = tmem + lane_off + b * 4 * N + t * 2 * N;  // hi columns; lo N further
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t h[32];
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t rh[16], rl[16];
+        tmem_ld16_nowait(dcol + c0, rh);
+        tmem_ld16_nowait(dcol + N + c0, rl);
+        tmem_wait_ld();
 #pragma unroll
-          for (int cq = 0; cq < 4; ++cq) {
-            const int cc = hh * 4 + cq;
-            const uint4 w = *reinterpret_cast<const uint4*>(wr + ((cc ^ (r & 7)) << 4));
-            h[cq * 8 + 0] = e4m3x2_to_f16x2(w.x);
-            h[cq * 8 + 1] = e4m3x2_to_f16x2(w.x >> 16);
-            h[cq * 8 + 2] = e4m3x2_to_f16x2(w.y);
-            h[cq * 8 + 3] = e4m3x2_to_f16x2(w.y >> 16);
-            h[cq * 8 + 4] = e4m3x2_to_f16x2(w.z);
-            h[cq * 8 + 5] = e4m3x2_to_f16x2(w.z >> 16);
-            h[cq * 8 + 6] = e4m3x2_to_f16x2(w.w);
-            h[cq * 8 + 7] = e4m3x2_to_f16x2(w.w >> 16);
-          }
-          tmem_st32(tmem + lane_off + b * 128 + t * 64 + hh * 32, h);
-        }
-        // activations: bf16 [N][128] -> f16 B operand (two 128-byte swizzled atoms per row)
-        uint8_t* xb = xbuf + b * Cf::kXBytes;
-#pragma unroll
-        for (int k = wt; k < N * 16; k += 32 * kWorkers) {
-          const int xr = k >> 4, hc = k & 15, atom = hc >> 3, cc = hc & 7;
-          const uint4 raw = *reinterpret_cast<const uint4*>(st + Cf::kWBytes + xr * 256 + hc * 16);
-          uint4 o;
-          o.x = bf16x2_to_f16x2(raw.x);
-          o.y = bf16x2_to_f16x2(raw.y);
-          o.z = bf16x2_to_f16x2(raw.z);
-          o.w = bf16x2_to_f16x2(raw.w);
-          *reinterpret_cast<uint4*>(xb + atom * (N * 128) + xr * 128 + ((cc ^ (xr & 7)) << 4)) = o;
-        }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        dev::fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          dev::mbar_arrive(&sempty[s]);
-          dev::mbar_arrive(&abfull[b]);
-        }
+        for (int k = 0; k < 16; ++k)
+          acc[c0 + k] = fmaf(sw * ex[c0 + k], __uint_as_float(rh[k]) + __uint_as_float(rl[k]), acc[c0 + k]);
       }
-      if (i >= 1) {
-        const int64_t ip = i - 1;
-        const int b = (int)(ip & 1);
-        if (!dev::mbar_wait(&dfull[b], (uint32_t)((ip >> 1) & 1), kWaitLimitNs)) {
-          dev::set_status(p.status, SWS_E_TIMEOUT);
-          s_abort = 1;
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < N / 16; ++c0) {
-          float v[16];
-          tmem_ld16(tmem + lane_off + 256 + b * 2 * N + t * N + c0 * 16, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) acc[c0 * 16 + k] = fmaf(sc_old, v[k], acc[c0 * 16 + k]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&dempty[b]);
-        const UnitPos up = unit_pos(p, u0 + ip);
-        if (ip + 1 == n || up.kb + 1 == p.e[up.j].slabs) tc_end_run<N>(acc, p, geo, up, t, row);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        dev::mbar_arrive(&dempty[b]);
+        dev::mbar_arrive(&sempty[s]);
       }
-      sc_old = sc_new;
+      if (i + 1 == n || cur.kb + 1 == cur.slabs) tc_end_run<N>(acc, p, geo, cur.pos(), t, row);
     }
-    if (ok && n > 0) tc_settle<N>(p, geo, u0, u1 - 1, wt, t, row, &s_last);
+    // All workers leave the loop before any named barrier of the settle.
+    if (workers_sync_any(fail)) {
+      if (fail) dev::set_status(p.status, SWS_E_TIMEOUT);
+      s_abort = 1;
+    } else if (n > 0) {
+      tc_settle<N>(p, geo, u0, u1 - 1, wt, t, row, &s_last);
+    }
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Cf::kTmemCols)
+                 : "memory");
   }
   if (tid == 0) {
     __threadfence();
@@ -411,24 +566,39 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
     attr = cudaFuncSetAttribute(decode_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr != cudaSuccess) return attr;
+  // 1. split the activations of every entry
+  int64_t threads = 0;
+  for (int j = 0; j < p.n_entries; ++j) threads += (int64_t)p.e[j].slabs * N * 8;
+  split_x_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, N);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. the GEMM, as a programmatic dependent launch of (1)
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
-  decode_tc_kernel<N><<<(unsigned)grid, kTcThreads, kSmem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
 }
 
 }  // namespace
 
 namespace dec {
 cudaError_t launch_decode_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
-  const int npad = ((p.m + 15) / 16) * 16;
-  switch (npad) {
+  switch ((int)tc_n_pad(p.m)) {
     case 16: return launch_tc_n<16>(p, grid_cap, s);
     case 32: return launch_tc_n<32>(p, grid_cap, s);
     case 48: return launch_tc_n<48>(p, grid_cap, s);
     default: return launch_tc_n<64>(p, grid_cap, s);
   }
 }
-int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * (((m + 15) / 16) * 16) * 4; }
+int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }
 }  // namespace dec
 
 }  // namespace sws

@@ -47,6 +47,7 @@ struct LayerPlan {
 //   [0, 256)        control: status word (int32 at 0)
 //   [256, 256+CNT)  split-K arrival counters (int32 per row block)
 //   then            split-K partial sums (fp32)
+//   then            tcgen05 decode: activation split blocks
 //   then            prefill quantiser output (xq bytes, then ex floats)
 constexpr int64_t kCtlBytes = 256;
 constexpr int64_t kMaxCounters = 1 << 16;
@@ -61,9 +62,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // 2-D tensor map of a byte matrix [rows, cols] (row stride cols, cols % 16 ==
 // 0): boxes of 128 bytes by box_rows rows, 128-byte swizzle, zero fill outside.
 int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
-// 2-D tensor map of a bf16 matrix [rows, cols] (row stride 2*cols bytes,
-// cols % 8 == 0): boxes of box_cols x box_rows elements, no swizzle.
-int encode_bf16_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows);
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
@@ -116,6 +114,9 @@ struct DecodeGroup {
 // Workspace a decode launch with this m needs (independent of the shapes, up
 // to kMaxCounters row blocks per launch).
 int decode_workspace_bytes(int64_t m, int64_t* bytes);
+// Activation split region a tcgen05 decode launch needs after that workspace:
+// one block per K slab of its linears (slabs = sum of ceil(cols / 128)).
+int64_t decode_split_bytes(int64_t m, int64_t slabs);
 int launch_decode(const DecodeGroup& g, cudaStream_t s);
 // Which decode kernel serves a view-path launch: SWS_DECODE_AUTO picks by m.
 enum DecodeKernel { kDecodeAuto = 0, kDecodeMma = 1, kDecodeTc = 2 };

@@ -369,6 +369,21 @@ def test_decode_kernels_ragged_and_special(S, decode_kernel):
     x = WL.draw_x(1, 0, 40, shapes[3][2]).cuda()
     y = _run_linear(st, 3, S.SRC_SLOT1, x, 40)
     assert not y.float().abs().max().item()
+    # one-hot rows select dequantised columns. The tcgen05 kernel scales each
+    # slab's exact result once, so its output is the column rounded once to
+    # fp32 and then to bf16; the mma.sync kernel re-bases its accumulator when
+    # the block scale changes (a few fp32 roundings) and meets the tolerance.
+    _, r, c = shapes[2]
+    for m in (1, 20, 64):
+        cols = rng.integers(0, c, size=m)
+        xo = torch.zeros((m, c), dtype=torch.bfloat16)
+        xo[np.arange(m), torch.from_numpy(cols)] = 1.0
+        y = _run_linear(st, 2, S.SRC_SLOT1, xo.cuda(), m)
+        want = O.e4m3_decode(codes[2][:, cols].T) * scales[2][np.arange(r) // 128][:, cols // 128].T.astype(np.float64)
+        if decode_kernel == "tcgen05":
+            assert torch.equal(y.cpu(), torch.from_numpy(want).float().to(torch.bfloat16)), f"m {m}"
+        else:
+            assert_close(bf16_tensor_to_f64(y), want, f"{decode_kernel} one-hot m {m}")
 
 
 def test_decode_kernels_full_size_sampled(S, decode_kernel):
