@@ -251,13 +251,14 @@ int32_t sws_trace_count(const sws_ctx* ctx);
 
 /* ---- options -------------------------------------------------------------- */
 #define SWS_OPT_DECODE_KERNEL 1 /* which kernel serves decode linears (m <= 64) from views */
-#define SWS_DECODE_AUTO 0       /* chosen by m (default) */
+#define SWS_DECODE_AUTO 0       /* the library's choice (default): tcgen05 */
 #define SWS_DECODE_MMA 1        /* warp-level mma.sync kernel */
 #define SWS_DECODE_TCGEN05 2    /* tcgen05 / TMEM kernel */
 /* Process-wide option, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance; chunk-map (fused) reads
- * always use the mma.sync kernel. SWS_E_INVALID for an unknown option or
- * value. */
+ * always use the mma.sync kernel. A tcgen05 launch is three kernels on the
+ * stream (activation split, GEMM, split-K settle); an mma.sync launch is one.
+ * SWS_E_INVALID for an unknown option or value. */
 int sws_set_option(int32_t option, int64_t value);
 
 /* ---- misc --------------------------------------------------------------- */

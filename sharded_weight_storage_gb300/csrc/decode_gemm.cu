@@ -181,6 +181,10 @@ __device__ __forceinline__ bool apply_scale(float (&acc)[R][NT][4], float& cs, f
 template <int NT, int R>
 __device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const DecodeEntry& e, int m, int64_t row0,
                                         int g, int tig) {
+  // Into registers first: a store could alias the parameter block, and the
+  // compiler would read these again after every store.
+  uint16_t* const y = e.y;
+  const int64_t rows = e.rows;
 #pragma unroll
   for (int rt = 0; rt < R; ++rt)
 #pragma unroll
@@ -189,9 +193,9 @@ __device__ __forceinline__ void write_y(const float (&acc)[R][NT][4], const Deco
       for (int q = 0; q < 4; ++q) {
         const int64_t o = row0 + rt * 16 + g + 8 * (q >> 1);
         const int mm = nt * 8 + 2 * tig + (q & 1);
-        if (o < e.rows && mm < m) {
+        if (o < rows && mm < m) {
           const __nv_bfloat16 b = __float2bfloat16_rn(acc[rt][nt][q]);
-          e.y[(int64_t)mm * e.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+          y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
         }
       }
 }
@@ -554,11 +558,13 @@ int g_decode_kernel = kDecodeAuto;
 
 void set_decode_kernel(int k) { g_decode_kernel = k; }
 
-// The tcgen05 kernel runs a 128 x N x 16 MMA for every 16 k whatever m is, so
-// it pays off once the warp-level MMAs of the mma.sync kernel limit the rate.
+// The tcgen05 kernel streams the weights at the HBM rate for every m <= 64
+// (its MMAs and activation split are small next to the weight bytes); the
+// mma.sync kernel serves the fused path and can be selected for comparison.
 int decode_kernel_for(int64_t m) {
   if (g_decode_kernel != kDecodeAuto) return g_decode_kernel;
-  return m > 16 ? kDecodeTc : kDecodeMma;
+  (void)m;
+  return kDecodeTc;
 }
 
 int64_t decode_split_bytes(int64_t m, int64_t slabs) {

@@ -15,14 +15,19 @@
 // the two terms are two more columns of the MMA, added when the result is
 // read out.
 //
-// A launch is two kernels on the stream:
+// A launch is three kernels on the stream:
 //   1. split_x_kernel: every (entry, K slab) block of activations -> its hi and
 //      lo e4m3 operands (already in the 128-byte swizzled order of a
 //      1024-byte aligned shared-memory tile) and the scales e, in the workspace.
 //      This is m x K work per linear, done once instead of once per row block.
 //   2. decode_tc_kernel, launched as a programmatic dependent of (1): its
 //      weight loads start while (1) runs; only the activation loads wait for
-//      (1) to finish (griddepcontrol.wait).
+//      (1) to finish (griddepcontrol.wait). Row blocks that one CTA covers
+//      whole are written to Y; a CTA's first and last run may share their row
+//      block with neighbouring CTAs (split-K) and store fp32 partial sums.
+//   3. settle_kernel, a programmatic dependent of (2): adds the partial sums
+//      of every shared row block in K order and writes Y. Settling in its own
+//      grid keeps the GEMM free of fences, atomics and cold code at its end.
 // decode_tc_kernel (swap-AB: weight rows are the MMA's M = 128 dimension, the
 // activations its N = 16..64 dimension, m rounded up to 16):
 //   * warp 0, one thread: producer. Per unit (256 weight rows x 128 K) one TMA
@@ -34,10 +39,10 @@
 //     of two to four D buffers.
 //   * warps 2-9 (each one quarter of the TMEM lanes of one 128-row tile): read
 //     the unit's result from TMEM and add hi + lo, times s[o/128, kb] * e[m], into
-//     fp32 registers; at the end of a run, write Y or the split-K partial.
+//     fp32 registers; at the end of a run, write Y or the partial sums.
 // Shared-memory traffic is one TMA write and one MMA read per weight byte.
-// Every wait is bounded; the worker warps leave their loop together (a barrier
-// reduction of their failure flags), so no named barrier is left half-joined.
+// Every wait is bounded; a wait that runs out records SWS_E_TIMEOUT and the
+// CTA finishes with its copies landed and TMEM released.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -142,24 +147,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Barrier among the 8 worker warps only (named barrier 1).
-__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// Barrier among the worker warps that also returns whether any of them passed
-// `pred` true.
-__device__ __forceinline__ bool workers_sync_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 256, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
-
 // Every lane waits; the warp fails if any lane ran out of time.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   const bool ok = dev::mbar_wait(bar, parity, kWaitLimitNs);
@@ -185,6 +172,7 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
 __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad) {
   // Let the GEMM launch now: it waits for this grid's results before it reads them.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) dev::trace_start(p.trace);  // the linear's trace spans all three kernels
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int g = (int)(tid & 7);
   int64_t task = tid >> 3;  // (entry, slab, row)
@@ -294,20 +282,29 @@ struct UnitCursor {
 
 // Each worker thread owns row `row` of tile `t` (0 or 1) of every unit.
 template <int N>
+// The launch parameters are read into registers first: a store through a
+// generic pointer could alias them, and the compiler would read them again
+// (from parameter memory) after every store.
 __device__ __forceinline__ void tc_write_y(const float (&acc)[N], const DecodeParams& p, const UnitPos& up, int t,
                                            int row) {
   const DecodeEntry& e = p.e[up.j];
+  uint16_t* const y = e.y;
+  const int64_t rows = e.rows;
+  const int m = p.m;
   const int64_t o = up.rbl * kTcRows + t * 128 + row;
-  if (o < e.rows) {
+  if (o < rows) {
 #pragma unroll
     for (int mm = 0; mm < N; ++mm)
-      if (mm < p.m) {
+      if (mm < m) {
         const __nv_bfloat16 b = __float2bfloat16_rn(acc[mm]);
-        e.y[(int64_t)mm * e.rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+        y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
       }
   }
 }
 
+// End of a run of units on one row block (acc holds its sums): a run that
+// covers the whole row block writes Y; a partial run stores its sums in the
+// CTA's slot (first or last run) for the settle kernel.
 template <int N>
 __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& p, const RunGeom& geo,
                                            const UnitPos& up, int t, int row) {
@@ -323,54 +320,6 @@ __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& 
   for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
 }
 
-// After the CTA's last unit: arrival counts on its (at most two) partial row
-// blocks; the last CTA to arrive adds the partials in K order and writes Y.
-// Called by all worker threads together.
-template <int N>
-__device__ __forceinline__ void tc_settle(const DecodeParams& p, const RunGeom& geo, int64_t u_first,
-                                          int64_t u_last, int wt, int t, int row, int* s_last) {
-  const UnitPos uf = unit_pos(p, u_first), ul = unit_pos(p, u_last);
-  const bool pf = geo.partial(p, uf.rbg), pl = ul.rbg != uf.rbg && geo.partial(p, ul.rbg);
-  if (!pf && !pl) return;
-  __threadfence();
-  workers_sync();
-  if (wt == 0) {
-    int last = 0;
-    if (pf)
-      last |= (atomicAdd(p.counters + uf.rbg, 1) == (int)(geo.last_cta(p, uf.rbg) - geo.first_cta(p, uf.rbg)));
-    if (pl)
-      last |= (atomicAdd(p.counters + ul.rbg, 1) == (int)(geo.last_cta(p, ul.rbg) - geo.first_cta(p, ul.rbg))) << 1;
-    *s_last = last;
-  }
-  workers_sync();
-  const int last = *s_last;
-  if (!last) return;
-  __threadfence();
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    if (!(last & (1 << which))) continue;
-    const UnitPos& up = which == 0 ? uf : ul;
-    const int64_t cf = geo.first_cta(p, up.rbg), cl = geo.last_cta(p, up.rbg);
-    float acc[N];
-#pragma unroll
-    for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
-    for (int64_t cc = cf; cc <= cl; ++cc) {  // K order: the sum does not depend on who arrived last
-      const float4* s4 = reinterpret_cast<const float4*>(
-          p.partials + geo.slot(p, cc, up.rbg) * (int64_t)TcCfg<N>::kSlotFloats + (t * 128 + row) * N);
-#pragma unroll
-      for (int q = 0; q < N / 4; ++q) {
-        const float4 v = __ldcg(s4 + q);
-        acc[4 * q] += v.x;
-        acc[4 * q + 1] += v.y;
-        acc[4 * q + 2] += v.z;
-        acc[4 * q + 3] += v.w;
-      }
-    }
-    tc_write_y<N>(acc, p, up, t, row);
-    if (wt == 0) p.counters[up.rbg] = 0;
-  }
-}
-
 template <int N>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
   using Cf = TcCfg<N>;
@@ -380,7 +329,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   __shared__ __align__(8) uint64_t sfull[S], sempty[S], dfull[kDBufs], dempty[kDBufs], mdone;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_last;
   // Swizzled TMA tiles and MMA operands need 1024-byte aligned bases.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -410,6 +358,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   }
   __syncthreads();
   tc_fence_after();
+  // No early launch_dependents here: settle blocks that launch early and wait
+  // beside the GEMM's CTAs slow the GEMM down more than the settle's launch
+  // latency costs.
   const uint32_t tmem = s_tmem;
   const RunGeom geo{G, U, c};
 
@@ -502,7 +453,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     const int q = warp & 3;         // TMEM lane quarter of this warp
     const int t = (warp - 2) >> 2;  // the unit's 128-row tile this warp promotes
     const int row = q * 32 + lane;  // row inside the tile = TMEM lane
-    const int wt = tid - 64;        // worker thread 0..255
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float acc[N];
 #pragma unroll
@@ -537,12 +487,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       }
       if (i + 1 == n || cur.kb + 1 == cur.slabs) tc_end_run<N>(acc, p, geo, cur.pos(), t, row);
     }
-    // All workers leave the loop before any named barrier of the settle.
-    if (workers_sync_any(fail)) {
-      if (fail) dev::set_status(p.status, SWS_E_TIMEOUT);
+    if (fail) {
+      dev::set_status(p.status, SWS_E_TIMEOUT);
       s_abort = 1;
-    } else if (n > 0) {
-      tc_settle<N>(p, geo, u0, u1 - 1, wt, t, row, &s_last);
     }
   }
   __syncthreads();
@@ -552,6 +499,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
                  : "memory");
   }
   if (tid == 0) {
+    __threadfence();
+    dev::trace_end(p.trace, p.tag);
+  }
+}
+
+// ---- 3. split-K settle ------------------------------------------------------------
+
+// One block per CTA boundary c = 1..G-1 of the GEMM's partition: if the
+// boundary falls inside a row block, and is the first boundary in it, the
+// block adds the partial sums of the CTAs that share the row block in K (CTA)
+// order, so the result does not depend on timing, and writes Y. Thread r owns
+// rows r and r + 128 of the row block. The blocks are small (128 threads, few
+// registers) so that they fit beside a GEMM CTA and launch before it ends.
+constexpr int kSettleThreads = 128;
+
+template <int N>
+__global__ void __launch_bounds__(kSettleThreads) settle_kernel(const __grid_constant__ DecodeParams p, int32_t G) {
+  grid_dependency_wait();  // the GEMM's partial sums are complete and visible
+  const int64_t U = p.units, c = blockIdx.x + 1;
+  const RunGeom geo{G, U, c};
+  const UnitPos up = unit_pos(p, c * U / G);
+  if (up.kb == 0) return;  // the boundary is a row-block start: nothing is split here
+  if (c > 1) {             // an earlier boundary inside the same row block settles it
+    const UnitPos prev = unit_pos(p, (c - 1) * U / G);
+    if (prev.rbg == up.rbg && prev.kb != 0) return;
+  }
+  const int64_t cf = geo.first_cta(p, up.rbg), cl = geo.last_cta(p, up.rbg);
+  const DecodeEntry& e = p.e[up.j];
+  uint16_t* const y = e.y;
+  const int64_t rows = e.rows;
+  const int m = p.m;
+  constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
+#pragma unroll 1
+  for (int row = threadIdx.x; row < kTcRows; row += kSettleThreads) {
+    const int64_t o = up.rbl * kTcRows + row;
+    if (o >= rows) break;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N / 4; q0 += 4) {  // 16 columns at a time
+      float4 acc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t cc = cf; cc <= cl; ++cc) {
+        const float4* s4 = reinterpret_cast<const float4*>(p.partials + geo.slot(p, cc, up.rbg) * kSlot + row * N) + q0;
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = __ldcg(s4 + q);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[q].x += v[q].x;
+          acc[q].y += v[q].y;
+          acc[q].z += v[q].z;
+          acc[q].w += v[q].w;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int mm = 4 * (q0 + q) + k;
+          if (mm < m) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
+            y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
     __threadfence();
     dev::trace_end(p.trace, p.tag);
   }
@@ -584,7 +601,13 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
+  if (e != cudaSuccess || grid < 2) return e;
+  // 3. the split-K settle, as a programmatic dependent launch of (2)
+  cfg.gridDim = dim3((unsigned)(grid - 1));
+  cfg.blockDim = dim3(kSettleThreads);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, settle_kernel<N>, p, (int32_t)grid);
 }
 
 }  // namespace

@@ -99,12 +99,18 @@ def test_run_layers_outputs_and_ordering(S, stack, first, last):
 
 
 def test_fused_mode_matches_slot_mode_bitwise(S, stack):
+    # The chunk-map (fused) reads run the mma.sync kernel; with the same kernel
+    # on the slot views the two weight sources must give identical bits.
     st, layers = stack
     m = 32
     xs, ys, io = _io(st, 0, 6, m)
     main, side = torch.cuda.Stream(), torch.cuda.Stream()
-    st.ctx.run_layers(0, 6, io, 0, main.cuda_stream, side.cuda_stream)
-    main.synchronize()
+    S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_MMA)
+    try:
+        st.ctx.run_layers(0, 6, io, 0, main.cuda_stream, side.cuda_stream)
+        main.synchronize()
+    finally:
+        S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_AUTO)
     ref = {j: y.clone() for j, y in ys.items()}
     for y in ys.values():
         y.fill_(float("nan"))
