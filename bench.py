@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import datetime
 import json
 import os
 import statistics
@@ -35,12 +36,14 @@ L2_FLUSH_BYTES = 512 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--stack-layers", type=int, default=92, help="layers of the lookahead stack (0 skips it)")
     ap.add_argument("--prefill-layers", type=int, default=8, help="layers of the prefill run (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-soak-s", type=float, default=0.5,
+                    help="untimed run of the same step for clock samples when the timed region is too short")
     ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc"], default=None,
                     help="profiling driver: build the shared-expert layer and run one kernel --reps times")
     ap.add_argument("--m", type=int, default=HEADLINE_M)
@@ -91,7 +94,9 @@ class Dist:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons every 50 ms, each sample with its
+    own timestamp, so a summary can keep only the samples inside a window."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -103,10 +108,11 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            time.sleep(0.3)  # let the sampler start before the caller's window opens
         except OSError:
             self.proc = None
         return self
@@ -122,20 +128,27 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.t.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t_from=None, t_to=None):
+        """Median SM clock, max clock and active throttle reasons of the samples
+        taken between host times t_from and t_to (seconds since the epoch)."""
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             p = [x.strip() for x in ln.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                smax = float(p[2])
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(p[2]), float(p[3])
             except ValueError:
                 continue
-            for n, v in zip(names, p[5:9]):
+            if (t_from is not None and ts < t_from) or (t_to is not None and ts > t_to):
+                continue
+            sm.append(clk)
+            smax = cmax
+            for n, v in zip(names, p[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
@@ -287,17 +300,32 @@ def run_ours(args, dist):
     dist.barrier()
     torch.cuda.synchronize()
     tm = Timer(stream)
-    with ClockSampler(dist.local) as clk, torch.cuda.stream(stream):
-        t0 = tm.ev()
-        for _ in range(args.steps):
-            step(HEADLINE_M, tm)
-        t1 = tm.ev()
-        torch.cuda.synchronize()
+    with ClockSampler(dist.local) as clk:
+        with torch.cuda.stream(stream):
+            h0 = time.time()
+            t0 = tm.ev()
+            for _ in range(args.steps):
+                step(HEADLINE_M, tm)
+            t1 = tm.ev()
+            torch.cuda.synchronize()
+            h1 = time.time()
+            clocks = clk.summary(h0, h1)
+            clocks["window"] = "timed region"
+            if clocks["samples"] < 3 and args.clock_soak_s > 0:
+                # The timed region is shorter than a few sampling intervals: keep
+                # the same step running, untimed, for 0.5 s and report those samples.
+                h2 = time.time()
+                while time.time() - h2 < args.clock_soak_s:
+                    for _ in range(50):
+                        step(HEADLINE_M)
+                    torch.cuda.synchronize()
+                clocks = clk.summary(h2, time.time())
+                clocks["window"] = (f"{args.clock_soak_s} s of the same step right after the timed region "
+                                    "(timed region too short to sample)")
     dist.barrier()
     torch.cuda.synchronize()
     window_ms = t0.elapsed_time(t1)
     window_ms = dist.max(window_ms)
-    clocks = clk.summary()
     wb, scb, actb = layer_bytes(ents, HEADLINE_M)
     step_bytes = 2 * total + wb + scb + actb
     per_kernel = {k: statistics.mean(tm.ms(k)) for k in ("gather", "linears")}

@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     if (lane == 0) {
       for (int j = 0; j < p.n_entries; ++j)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.e[j].tmap)) : "memory");
+      const uint64_t stream_policy = l2_evict_first_policy();
       const int64_t early = n < S ? n : S;  // units whose weight loads go out before the split is done
       const uint8_t* early_src[S];          // their split blocks
       bool split_ready = false;
@@ -384,7 +385,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         }
         uint8_t* st = smem + s * Cf::kStageBytes;
         dev::mbar_arrive_expect_tx(&sfull[s], Cf::kWBytes + Cf::kXBytes);
-        tma_load_2d(st, &p.e[cur.j].tmap, (int32_t)(cur.kb * kSlabK), (int32_t)(cur.rbl * kTcRows), &sfull[s]);
+        tma_load_2d_hint(st, &p.e[cur.j].tmap, (int32_t)(cur.kb * kSlabK), (int32_t)(cur.rbl * kTcRows), &sfull[s],
+                         stream_policy);
         float* sw = reinterpret_cast<float*>(st + Cf::kSwOff);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -506,16 +508,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 
 // ---- 3. split-K settle ------------------------------------------------------------
 
-// One block per CTA boundary c = 1..G-1 of the GEMM's partition: if the
-// boundary falls inside a row block, and is the first boundary in it, the
-// block adds the partial sums of the CTAs that share the row block in K (CTA)
-// order, so the result does not depend on timing, and writes Y. Thread r owns
-// rows r and r + 128 of the row block. The blocks are small (128 threads, few
-// registers) so that they fit beside a GEMM CTA and launch before it ends.
-constexpr int kSettleThreads = 128;
-
+// One block per CTA boundary c = 1..G-1 of the GEMM's partition and 16-column
+// group (blockIdx.y): if the boundary falls inside a row block, and is the
+// first boundary in it, the block adds the partial sums of the CTAs that share
+// the row block in K (CTA) order, so the result does not depend on timing, and
+// writes those 16 columns of Y. Thread r owns row r of the row block; it
+// issues the loads of up to four contributions before adding them.
 template <int N>
-__global__ void __launch_bounds__(kSettleThreads) settle_kernel(const __grid_constant__ DecodeParams p, int32_t G) {
+__global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p, int32_t G) {
   grid_dependency_wait();  // the GEMM's partial sums are complete and visible
   const int64_t U = p.units, c = blockIdx.x + 1;
   const RunGeom geo{G, U, c};
@@ -530,39 +530,44 @@ __global__ void __launch_bounds__(kSettleThreads) settle_kernel(const __grid_con
   uint16_t* const y = e.y;
   const int64_t rows = e.rows;
   const int m = p.m;
-  constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
-#pragma unroll 1
-  for (int row = threadIdx.x; row < kTcRows; row += kSettleThreads) {
-    const int64_t o = up.rbl * kTcRows + row;
-    if (o >= rows) break;
-#pragma unroll 1
-    for (int q0 = 0; q0 < N / 4; q0 += 4) {  // 16 columns at a time
-      float4 acc[4];
+  const int row = threadIdx.x, c0 = blockIdx.y * 16;
+  const int64_t o = up.rbl * kTcRows + row;
+  if (o < rows) {
+    constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
+    float4 acc[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int64_t cc = cf; cc <= cl; ++cc) {
-        const float4* s4 = reinterpret_cast<const float4*>(p.partials + geo.slot(p, cc, up.rbg) * kSlot + row * N) + q0;
-        float4 v[4];
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t cb = cf; cb <= cl; cb += 4) {
+      float4 v[4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = __ldcg(s4 + q);
+      for (int k = 0; k < 4; ++k)
+        if (cb + k <= cl) {
+          const float4* s4 =
+              reinterpret_cast<const float4*>(p.partials + geo.slot(p, cb + k, up.rbg) * kSlot + row * N + c0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[q].x += v[q].x;
-          acc[q].y += v[q].y;
-          acc[q].z += v[q].z;
-          acc[q].w += v[q].w;
+          for (int q = 0; q < 4; ++q) v[k][q] = __ldcg(s4 + q);
         }
-      }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+      for (int k = 0; k < 4; ++k)
+        if (cb + k <= cl) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int mm = 4 * (q0 + q) + k;
-          if (mm < m) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
-            y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+          for (int q = 0; q < 4; ++q) {
+            acc[q].x += v[k][q].x;
+            acc[q].y += v[k][q].y;
+            acc[q].z += v[k][q].z;
+            acc[q].w += v[k][q].w;
           }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float a[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int mm = c0 + 4 * q + k;
+        if (mm < m) {
+          const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
+          y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
         }
       }
     }
@@ -604,8 +609,8 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
   if (e != cudaSuccess || grid < 2) return e;
   // 3. the split-K settle, as a programmatic dependent launch of (2)
-  cfg.gridDim = dim3((unsigned)(grid - 1));
-  cfg.blockDim = dim3(kSettleThreads);
+  cfg.gridDim = dim3((unsigned)(grid - 1), N / 16);
+  cfg.blockDim = dim3(kTcRows);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, settle_kernel<N>, p, (int32_t)grid);
 }
