@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
-    ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc"], default=None,
+    ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill"],
+                    default=None,
                     help="profiling driver: build the shared-expert layer and run one kernel --reps times")
     ap.add_argument("--m", type=int, default=HEADLINE_M)
     ap.add_argument("--entry", type=int, default=0, help="0 = gate_up, 1 = down")
@@ -687,6 +688,24 @@ def run_only(args, dist):
     from sharded_weight_storage_gb300.storage import ShardedStack
 
     set_decode_kernel(S, args.decode_kernel)
+    if args.only == "prefill":  # one KDA-layer linear (entry --entry) at m = --m tokens
+        w = WL.PREFILL
+        ents = [(0, e.rows, e.cols) for e in w.entries]
+        lw = WL.layer_weights(WL.scaled_workload(w, n_layers=1), 0)
+        st = ShardedStack([(0, S.E4M3, r, c) for (_, r, c) in ents], w.n_shards, max_m=args.m)
+        st.load_layer(0, {j: torch.from_numpy(lw.codes[j]) for j in range(len(ents))},
+                      {j: torch.from_numpy(lw.scales[j]) for j in range(len(ents))})
+        ctx = st.make_ctx()
+        ctx.gather_to_slot(0, 0, 0)
+        j, m = args.entry, args.m
+        x = WL.draw_x(w.key, j, m, ents[j][2]).cuda()
+        y = torch.empty((m, ents[j][1]), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.reps):
+            ctx.linear(j, S.SRC_SLOT0, x.data_ptr(), m, y.data_ptr(), 0)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        print(f"only=prefill m={m} entry={j} reps={args.reps}: ok")
+        return
     w = WL.SHARED_EXPERT
     ents = [(0, e.rows, e.cols) for e in w.entries]
     lw = WL.layer_weights(w, 0)

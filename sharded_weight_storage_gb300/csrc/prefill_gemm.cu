@@ -239,14 +239,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float* exr = p.ex + (m < p.M ? m : 0) * G;
       const float* swr = p.sw + (nb < sw_rows ? nb : 0) * G;
       const bool live = m < p.M && nb < sw_rows;
-      auto factor = [&](int kb) -> float { return (live && kb < G) ? __ldg(exr + kb) * __ldg(swr + kb) : 0.f; };
+      // Raw scale loads, multiplied only when used: a product taken at load
+      // time would make the thread wait for both loads right away.
+      auto load_ex = [&](int kb) -> float { return (live && kb < G) ? __ldg(exr + kb) : 0.f; };
+      auto load_sw = [&](int kb) -> float { return (live && kb < G) ? __ldg(swr + kb) : 0.f; };
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      // Scale factors are fetched four slabs ahead (ring f[d] holds slab kb0 + d).
-      float f[4];
+      // Scale factors are fetched four slabs ahead (rings fe[d], fw[d] hold slab kb0 + d).
+      float fe[4], fw[4];
 #pragma unroll
-      for (int d = 0; d < 4; ++d) f[d] = factor(d);
+      for (int d = 0; d < 4; ++d) {
+        fe[d] = load_ex(d);
+        fw[d] = load_sw(d);
+      }
       bool ok = true;
       for (int kb0 = 0; kb0 < G && ok; kb0 += 4) {
 #pragma unroll
@@ -259,8 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               set_abort(p, &s_abort);
             } else {
               tc_fence_after();
-              const float fk = f[d];
-              f[d] = factor(kb + 4);
+              const float fk = fe[d] * fw[d];
+              fe[d] = load_ex(kb + 4);
+              fw[d] = load_sw(kb + 4);
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 float v[16];
