@@ -242,7 +242,9 @@ int sws_ctx_status(sws_ctx* ctx, int32_t clear);
 /* Optional device timestamps: each later gather / linear launch of the
  * context appends one record of 4 uint64 to `records` (device memory,
  * capacity records): {tag, start_ns, end_ns, 0} where tag = kind << 56 |
- * layer << 32 | entry (kind 1 = gather, 2 = linear), start_ns is the earliest
+ * kernel << 48 | layer << 32 | entry (kind 1 = gather, 2 = linear; kernel, for
+ * linears: 1 mma.sync on views, 2 mma.sync through the chunk map, 3 tcgen05
+ * on views, 4 tcgen05 through the chunk map, 5 prefill), start_ns is the earliest
  * %globaltimer read by any CTA at entry and end_ns the latest at exit. Passing
  * NULL turns tracing off. Records are reset (start = ~0, end = 0) on `stream`.
  * Returns the number of records written so far through sws_trace_count. */

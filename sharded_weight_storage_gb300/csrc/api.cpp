@@ -171,7 +171,7 @@ int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64
   pl.cols = e.cols;
   pl.status = status_word(c);
   pl.trace = next_trace(c);
-  pl.tag = (kTraceLinear << 56) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
+  pl.tag = (kTraceLinear << 56) | (kTracePrefill << 48) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
   return launch_prefill(pl, s);
 }
 

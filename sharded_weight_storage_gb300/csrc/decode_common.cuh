@@ -17,14 +17,19 @@ namespace dec {
 constexpr int kSlabK = 128;
 constexpr int kMaxGrid = 256;  // upper bound used to size the workspace
 
-// One linear of a group.
+// One linear of a group, or (tcgen05 chunk-map launches) one segment of a
+// linear: the rows of the linear that lie whole inside one chunk.
 struct DecodeEntry {
-  CUtensorMap tmap;   // slot path: 2-D map of the weight view [rows, cols] u8
+  CUtensorMap tmap;   // 2-D map of the weight rows [rows, cols] u8 (slot view, or the segment in its chunk)
   const float* scales;
   const uint16_t* x;  // bf16 [m, cols]
   uint16_t* y;        // bf16 [m, rows]
-  int64_t rows, cols;
-  uint8_t* xs;         // tcgen05 path: the entry's activation split blocks (one per K slab)
+  int64_t rows, cols;  // rows of this entry / segment
+  int64_t row_base;    // first row of the linear this entry covers (segments), else 0
+  int64_t y_rows;      // rows of the linear: the row stride of y (and of the scale rows)
+  int32_t linear;      // which linear of the group
+  int32_t split_owner; // 1 for the entry that splits the linear's activations
+  uint8_t* xs;         // tcgen05 path: the linear's activation split blocks (one per K slab)
   int64_t t_offset;    // fused path: o_j, the entry's offset in T
   int64_t scale_cols;  // ceil(cols / 128)
   int64_t unit_begin;  // first unit of this entry in the group's unit space
@@ -32,13 +37,27 @@ struct DecodeEntry {
   int32_t slabs;       // ceil(cols / 128)
 };
 
+// Chunk-map (fused) reads on the tcgen05 path: every entry is a segment (the
+// rows of a linear that lie whole inside one chunk, with a tensor map over that
+// chunk), so no unit reads across a chunk boundary. A row that a boundary
+// splits (a "straddling" row) belongs to no segment: the settle kernel
+// computes that row of Y directly.
+constexpr int kMaxDecodeEntries = 40;
+constexpr int kMaxStraddle = 32;
+struct Straddles {
+  int32_t n;
+  int32_t entry[kMaxStraddle];  // an entry (segment) of the linear, for its pointers
+  int64_t row[kMaxStraddle];    // the row within the linear
+};
+
 struct DecodeParams {
-  DecodeEntry e[kMaxDecodeGroup];
+  DecodeEntry e[kMaxDecodeEntries];
   int32_t n_entries;
   int32_t m;
   int64_t units;  // total units (row block x K slab) of the group
   const uint8_t* chunks[256];  // fused path: the layer's chunks
   int64_t chunk_bytes;
+  Straddles st;   // tcgen05 chunk-map launches only
   int32_t* counters;
   float* partials;
   int32_t* status;
@@ -101,17 +120,13 @@ struct UnitPos {
 
 __device__ __forceinline__ int entry_of_unit(const DecodeParams& p, int64_t u) {
   int j = 0;
-#pragma unroll
-  for (int q = 1; q < kMaxDecodeGroup; ++q)
-    if (q < p.n_entries && u >= p.e[q].unit_begin) j = q;
+  for (int q = 1; q < p.n_entries && u >= p.e[q].unit_begin; ++q) j = q;
   return j;
 }
 
 __device__ __forceinline__ int entry_of_rb(const DecodeParams& p, int64_t rbg) {
   int j = 0;
-#pragma unroll
-  for (int q = 1; q < kMaxDecodeGroup; ++q)
-    if (q < p.n_entries && rbg >= p.e[q].rb_begin) j = q;
+  for (int q = 1; q < p.n_entries && rbg >= p.e[q].rb_begin; ++q) j = q;
   return j;
 }
 
@@ -158,7 +173,7 @@ __host__ __device__ constexpr int64_t tc_n_pad(int64_t m) { return (m + 15) / 16
 // Split block of one entry and K slab for n_pad = m rounded up to 16:
 // [hi e4m3 n_pad x 128 | lo e4m3 n_pad x 128 | e fp32 n_pad].
 __host__ __device__ constexpr int64_t tc_split_block_bytes(int64_t n_pad) { return 260 * n_pad; }
-cudaError_t launch_decode_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int64_t grid_cap, cudaStream_t s);
 int64_t tc_slot_bytes(int64_t m);
 
 }  // namespace dec

@@ -533,6 +533,10 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
     e.x = it.x;
     e.y = it.y;
     e.rows = it.rows;
+    e.row_base = 0;
+    e.y_rows = it.rows;
+    e.linear = i;
+    e.split_owner = 1;
     e.cols = it.cols;
     e.t_offset = it.t_offset;
     e.scale_cols = cdiv(it.cols, 128);
@@ -579,32 +583,105 @@ int decode_workspace_bytes(int64_t m, int64_t* bytes) {
   return SWS_OK;
 }
 
+// Chunk-map (fused) launch on the tcgen05 path. Each linear becomes one entry
+// per chunk it has whole rows in (a segment: rows rf..rl, a tensor map over
+// that chunk's bytes), so no unit reads across a chunk boundary; the rows a
+// boundary splits are listed for the settle kernel. `lin` holds the group's
+// linears as build_params made them (with their split blocks); *ok stays false
+// when the segments or split rows exceed the tables (the mma.sync kernel then
+// serves the launch).
+int build_fused_segments(DecodeParams& p, const DecodeParams& lin, const DecodeGroup& g, bool* ok) {
+  *ok = false;
+  p = lin;
+  p.n_entries = 0;
+  p.units = 0;
+  p.st.n = 0;
+  const int64_t C = g.chunk_bytes;
+  int64_t rb = 0;
+  for (int j = 0; j < lin.n_entries; ++j) {
+    const DecodeEntry& L = lin.e[j];
+    const int64_t o = L.t_offset, cols = L.cols, rows = L.rows, end = o + rows * cols;
+    const int64_t c0 = o / C, c1 = (end - 1) / C;
+    bool owner = true;
+    for (int64_t c = c0; c <= c1; ++c) {
+      const int64_t lo = c * C, hi = lo + C;
+      if (c > c0 && (lo - o) % cols != 0) {  // the boundary at lo splits row (lo - o) / cols
+        if (p.st.n >= kMaxStraddle) return SWS_OK;
+        p.st.row[p.st.n] = (lo - o) / cols;
+        p.st.entry[p.st.n] = -1 - j;  // resolved to a segment of linear j below
+        ++p.st.n;
+      }
+      const int64_t rf = lo <= o ? 0 : (lo - o + cols - 1) / cols;
+      const int64_t rl = std::min<int64_t>(rows, (hi - o) / cols) - 1;
+      if (rf > rl) continue;
+      if (p.n_entries >= kMaxDecodeEntries) return SWS_OK;
+      if (c >= g.n_chunks || !g.chunks[c]) return fail(SWS_E_INVALID, "decode: chunk %lld is missing", (long long)c);
+      DecodeEntry& e = p.e[p.n_entries];
+      e = L;
+      int rc = encode_u8_tile_map(&e.tmap, g.chunks[c] + (o + rf * cols - lo), rl - rf + 1, cols, kTcUnitRows);
+      if (rc != SWS_OK) return rc;
+      e.rows = rl - rf + 1;
+      e.row_base = rf;
+      e.y_rows = rows;
+      e.linear = j;
+      e.split_owner = owner ? 1 : 0;
+      owner = false;
+      e.unit_begin = p.units;
+      e.rb_begin = rb;
+      const int64_t nrb = cdiv(e.rows, kTcUnitRows);
+      rb += nrb;
+      p.units += nrb * e.slabs;
+      ++p.n_entries;
+    }
+    if (owner) return SWS_OK;  // no whole row of this linear in any chunk
+  }
+  for (int k = 0; k < p.st.n; ++k) {  // any segment of the linear gives the straddling row's pointers
+    const int j = -1 - p.st.entry[k];
+    for (int q = 0; q < p.n_entries; ++q)
+      if (p.e[q].linear == j) {
+        p.st.entry[k] = q;
+        break;
+      }
+  }
+  if (rb > kMaxCounters || p.units >= ((int64_t)1 << 31)) return SWS_OK;
+  *ok = true;
+  return SWS_OK;
+}
+
 int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   if (g.m == 0) return SWS_OK;
-  int64_t need = 0;
-  int rc = decode_workspace_bytes(g.m, &need);
+  int64_t dec = 0;
+  int rc = decode_workspace_bytes(g.m, &dec);
   if (rc != SWS_OK) return rc;
-  const bool tc = !g.fused && decode_kernel_for(g.m) == kDecodeTc;
-  if (tc) {  // the activation split region follows the partial sums
-    int64_t slabs = 0;
-    for (int i = 0; i < g.n; ++i) slabs += cdiv(g.item[i].cols, kSlabK);
-    need += decode_split_bytes(g.m, slabs);
-  }
+  int64_t slabs = 0;
+  for (int i = 0; i < g.n; ++i) slabs += cdiv(g.item[i].cols, kSlabK);
+  const int64_t split = decode_split_bytes(g.m, slabs);  // the activation split region follows the partial sums
+  bool tc = decode_kernel_for(g.m) == kDecodeTc;
+  const int64_t need = dec + (tc ? split : 0);
   if (g.workspace_bytes < need)
     return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);
   DecodeParams p;
   int64_t row_blocks = 0;
   bool empty = true;
-  int64_t dec = 0;
-  decode_workspace_bytes(g.m, &dec);
   rc = build_params(p, g, &row_blocks, &empty, s, tc ? g.workspace + dec : nullptr);
   if (rc != SWS_OK || empty) return rc;
+  if (tc && g.fused) {
+    DecodeParams lin = p;
+    bool ok = false;
+    rc = build_fused_segments(p, lin, g, &ok);
+    if (rc != SWS_OK) return rc;
+    if (!ok) {  // beyond the chunk-map tables: the mma.sync kernel reads this group
+      tc = false;
+      rc = build_params(p, g, &row_blocks, &empty, s, nullptr);
+      if (rc != SWS_OK || empty) return rc;
+    }
+  }
   p.counters = reinterpret_cast<int32_t*>(g.workspace + kCtlBytes);
   p.partials = reinterpret_cast<float*>(g.workspace + kCtlBytes + kMaxCounters * 4);
   p.status = reinterpret_cast<int32_t*>(g.workspace);
   p.trace = g.trace;
-  p.tag = g.tag;
-  cudaError_t e = tc ? launch_decode_tc(p, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
+  p.tag = g.tag | ((tc ? (g.fused ? kTraceTcFused : kTraceTc) : (g.fused ? kTraceMmaFused : kTraceMma)) << 48);
+  cudaError_t e = tc ? launch_decode_tc(p, g.fused, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 

@@ -75,7 +75,7 @@ struct TcCfg {
   static constexpr int kWBytes = kTcRows * kSlabK;              // e4m3 weight slab, 128-byte swizzle
   static constexpr int kTermBytes = N * kSlabK;                 // one e4m3 B operand [N][128]
   static constexpr int kXBytes = (int)tc_split_block_bytes(N);  // hi, lo, e
-  static constexpr int kSwOff = kWBytes + kXBytes;              // two fp32 weight scales
+  static constexpr int kSwOff = kWBytes + kXBytes;              // four fp32 weight scales
   static constexpr int kStageBytes = (kSwOff + 16 + 1023) / 1024 * 1024;
   static constexpr int kStages = N <= 16 ? 6 : N <= 32 ? 5 : 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024;
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ De
   int64_t task = tid >> 3;  // (entry, slab, row)
   int j = 0;
   for (; j < p.n_entries; ++j) {
+    if (!p.e[j].split_owner) continue;  // another segment of the same linear splits it
     const int64_t t = (int64_t)p.e[j].slabs * n_pad;
     if (task < t) break;
     task -= t;
@@ -243,13 +244,18 @@ struct UnitCursor {
   int j;
   int64_t rbl, kb;
   int32_t slabs;
-  int64_t nrb, rb_begin, rows, scale_cols;
+  int64_t nrb, rb_begin, rows, scale_cols, row_base, unit_begin, y_rows;
   const float* scales;
   const uint8_t* xs;
+  uint16_t* y;
   __device__ __forceinline__ void load(const DecodeParams& p) {
     const DecodeEntry& e = p.e[j];
     slabs = e.slabs;
     rows = e.rows;
+    row_base = e.row_base;
+    unit_begin = e.unit_begin;
+    y_rows = e.y_rows;
+    y = e.y;
     nrb = (e.rows + kTcRows - 1) / kTcRows;
     rb_begin = e.rb_begin;
     scale_cols = e.scale_cols;
@@ -280,39 +286,29 @@ struct UnitCursor {
   }
 };
 
-// Each worker thread owns row `row` of tile `t` (0 or 1) of every unit.
-template <int N>
-// The launch parameters are read into registers first: a store through a
-// generic pointer could alias them, and the compiler would read them again
-// (from parameter memory) after every store.
-__device__ __forceinline__ void tc_write_y(const float (&acc)[N], const DecodeParams& p, const UnitPos& up, int t,
-                                           int row) {
-  const DecodeEntry& e = p.e[up.j];
-  uint16_t* const y = e.y;
-  const int64_t rows = e.rows;
-  const int m = p.m;
-  const int64_t o = up.rbl * kTcRows + t * 128 + row;
-  if (o < rows) {
-#pragma unroll
-    for (int mm = 0; mm < N; ++mm)
-      if (mm < m) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(acc[mm]);
-        y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
-      }
-  }
-}
-
 // End of a run of units on one row block (acc holds its sums): a run that
 // covers the whole row block writes Y; a partial run stores its sums in the
-// CTA's slot (first or last run) for the settle kernel.
+// CTA's slot (first or last run) for the settle kernel. Everything comes from
+// the cursor's registers: no launch-parameter reads at the end of a run.
 template <int N>
 __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& p, const RunGeom& geo,
-                                           const UnitPos& up, int t, int row) {
-  if (!geo.partial(p, up.rbg)) {
-    tc_write_y<N>(acc, p, up, t, row);
+                                           const UnitCursor& cur, int64_t first_rbg, int t, int row) {
+  const int64_t fu = cur.unit_begin + cur.rbl * cur.slabs;  // the row block's first unit
+  const bool partial = cta_of(fu, geo.G, geo.U) != cta_of(fu + cur.slabs - 1, geo.G, geo.U);
+  const int64_t o = cur.rbl * kTcRows + t * 128 + row;      // row of the entry
+  if (!partial) {
+    if (o < cur.rows) {
+      const int m = p.m;
+#pragma unroll
+      for (int mm = 0; mm < N; ++mm)
+        if (mm < m) {
+          const __nv_bfloat16 b = __float2bfloat16_rn(acc[mm]);
+          cur.y[(int64_t)mm * cur.y_rows + cur.row_base + o] = *reinterpret_cast<const uint16_t*>(&b);
+        }
+    }
   } else {
-    float4* d = reinterpret_cast<float4*>(p.partials + geo.slot(p, geo.c, up.rbg) * (int64_t)TcCfg<N>::kSlotFloats +
-                                          (t * 128 + row) * N);
+    const int64_t slot = 2 * geo.c + (cur.rb_begin + cur.rbl == first_rbg ? 0 : 1);
+    float4* d = reinterpret_cast<float4*>(p.partials + slot * (int64_t)TcCfg<N>::kSlotFloats + (t * 128 + row) * N);
 #pragma unroll
     for (int q = 0; q < N / 4; ++q) d[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
   }
@@ -370,13 +366,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       for (int j = 0; j < p.n_entries; ++j)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.e[j].tmap)) : "memory");
       const uint64_t stream_policy = l2_evict_first_policy();
-      const int64_t early = n < S ? n : S;  // units whose weight loads go out before the split is done
-      const uint8_t* early_src[S];          // their split blocks
+      // Split-block copies of the first stages wait for the split kernel; the
+      // weight loads of those stages go out before it has finished.
+      const uint8_t* pend_src[S];
       bool split_ready = false;
+      auto finish_split = [&](int64_t issued) {
+        grid_dependency_wait();
+        split_ready = true;
+        for (int64_t k = 0; k < issued; ++k)
+          dev::bulk_g2s(smem + k * Cf::kStageBytes + Cf::kWBytes, pend_src[k], Cf::kXBytes, &sfull[k]);
+      };
       UnitCursor cur;
       cur.init(p, u0);
       int64_t i = 0;
       for (; i < n && !s_abort; ++i, cur.next(p)) {
+        if (!split_ready && i == S) finish_split(S);  // stage 0's reuse needs its split data
         const int s = (int)(i % S);
         if (!dev::mbar_wait(&sempty[s], (uint32_t)(((i / S) & 1) ^ 1), kWaitLimitNs)) {
           dev::set_status(p.status, SWS_E_TIMEOUT);
@@ -387,32 +391,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         dev::mbar_arrive_expect_tx(&sfull[s], Cf::kWBytes + Cf::kXBytes);
         tma_load_2d_hint(st, &p.e[cur.j].tmap, (int32_t)(cur.kb * kSlabK), (int32_t)(cur.rbl * kTcRows), &sfull[s],
                          stream_policy);
+        // Block scales of each 128-row tile's first and last row (a segment's
+        // tile may cross a 128-row scale block of its linear).
         float* sw = reinterpret_cast<float*>(st + Cf::kSwOff);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int64_t row0 = cur.rbl * kTcRows + t * 128;
-          const bool in = row0 < cur.rows;
-          cp_async4(sw + t, cur.scales + (in ? (row0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+          const int64_t lr0 = cur.rbl * kTcRows + t * 128;  // first row of the tile in the entry
+          const bool in = lr0 < cur.rows;
+          const int64_t g0 = cur.row_base + lr0;
+          const int64_t g1 = cur.row_base + (lr0 + 127 < cur.rows ? lr0 + 127 : cur.rows - 1);
+          cp_async4(sw + 2 * t, cur.scales + (in ? (g0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+          cp_async4(sw + 2 * t + 1, cur.scales + (in ? (g1 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
         }
         cp_async_arrive_noinc(&sfull[s]);
         const uint8_t* src = cur.xs + cur.kb * Cf::kXBytes;
-        if (split_ready) {
+        if (split_ready)
           dev::bulk_g2s(st + Cf::kWBytes, src, Cf::kXBytes, &sfull[s]);
-        } else {
-          early_src[i] = src;
-          if (i + 1 == early) {
-            grid_dependency_wait();
-            split_ready = true;
-            for (int64_t k = 0; k <= i; ++k)
-              dev::bulk_g2s(smem + k * Cf::kStageBytes + Cf::kWBytes, early_src[k], Cf::kXBytes, &sfull[k]);
-          }
-        }
+        else
+          pend_src[i] = src;
       }
-      if (!split_ready) {  // aborted early: complete the stages already issued
-        grid_dependency_wait();
-        for (int64_t k = 0; k < i; ++k)
-          dev::bulk_g2s(smem + k * Cf::kStageBytes + Cf::kWBytes, early_src[k], Cf::kXBytes, &sfull[k]);
-      }
+      if (!split_ready) finish_split(i);  // also completes the stages of an early abort
       // Before the CTA may exit, every issued stage must have landed.
       for (int64_t k = i - S; k < i; ++k)
         if (k >= 0) dev::mbar_wait(&sfull[(int)(k % S)], (uint32_t)((k / S) & 1), kWaitLimitNs / 4);
@@ -462,6 +460,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     bool fail = false;
     UnitCursor cur;
     cur.init(p, u0);
+    const int64_t first_rbg = cur.rb_begin + cur.rbl;
     for (int64_t i = 0; i < n; ++i, cur.next(p)) {
       const int s = (int)(i % S), b = (int)(i % kDBufs);
       fail = !warp_wait(&sfull[s], (uint32_t)((i / S) & 1)) || !warp_wait(&dfull[b], (uint32_t)((i / kDBufs) & 1));
@@ -469,7 +468,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       tc_fence_after();
       const uint8_t* st = smem + s * Cf::kStageBytes;
       const float* ex = reinterpret_cast<const float*>(st + Cf::kWBytes + 2 * Cf::kTermBytes);
-      const float sw = reinterpret_cast<const float*>(st + Cf::kSwOff)[t];
+      // this row's 128-row scale block: the tile's first or last one
+      const float* swt = reinterpret_cast<const float*>(st + Cf::kSwOff) + 2 * t;
+      const int64_t g0 = cur.row_base + cur.rbl * kTcRows + t * 128;
+      const float sw = ((g0 + row) >> 7) == (g0 >> 7) ? swt[0] : swt[1];
       const uint32_t dcol = tmem + lane_off + b * 4 * N + t * 2 * N;  // hi columns; lo N further
 #pragma unroll
       for (int c0 = 0; c0 < N; c0 += 16) {
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         dev::mbar_arrive(&dempty[b]);
         dev::mbar_arrive(&sempty[s]);
       }
-      if (i + 1 == n || cur.kb + 1 == cur.slabs) tc_end_run<N>(acc, p, geo, cur.pos(), t, row);
+      if (i + 1 == n || cur.kb + 1 == cur.slabs) tc_end_run<N>(acc, p, geo, cur, first_rbg, t, row);
     }
     if (fail) {
       dev::set_status(p.status, SWS_E_TIMEOUT);
@@ -508,30 +510,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 
 // ---- 3. split-K settle ------------------------------------------------------------
 
-// One block per CTA boundary c = 1..G-1 of the GEMM's partition and 16-column
-// group (blockIdx.y): if the boundary falls inside a row block, and is the
-// first boundary in it, the block adds the partial sums of the CTAs that share
-// the row block in K (CTA) order, so the result does not depend on timing, and
-// writes those 16 columns of Y. Thread r owns row r of the row block; it
-// issues the loads of up to four contributions before adding them.
+// Which row blocks the GEMM's partition split between CTAs, worked out on the
+// host from the same partition (so the kernel does no unit arithmetic).
+struct SettleTask {
+  int32_t j;       // entry
+  int32_t rbl;     // row block in the entry
+  int32_t cf, cl;  // the CTAs that share it, in K order
+};
+struct SettlePlan {
+  int32_t n;                           // tasks
+  int32_t cta_first_rbg[kMaxGrid];     // each CTA's first row block (its partial slot 0)
+  SettleTask task[kMaxGrid];
+};
+
+// One block per settle task (a row block the GEMM's partition split between
+// CTAs cf..cl) and 16-column group (blockIdx.y): the block adds the partial
+// sums of those CTAs in K (CTA) order, so the result does not depend on
+// timing, and writes those 16 columns of Y. Thread r owns row r of the row
+// block; it issues the loads of up to four contributions before adding them.
+// Chunk-map launches add one block per straddling row and 16-column group
+// (blockIdx.x >= sp.n): that row is in no segment, so the block computes it
+// directly from the chunks (straddle_row).
 template <int N>
-__global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p, int32_t G) {
-  grid_dependency_wait();  // the GEMM's partial sums are complete and visible
-  const int64_t U = p.units, c = blockIdx.x + 1;
-  const RunGeom geo{G, U, c};
-  const UnitPos up = unit_pos(p, c * U / G);
-  if (up.kb == 0) return;  // the boundary is a row-block start: nothing is split here
-  if (c > 1) {             // an earlier boundary inside the same row block settles it
-    const UnitPos prev = unit_pos(p, (c - 1) * U / G);
-    if (prev.rbg == up.rbg && prev.kb != 0) return;
+__device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
+
+template <int N, bool FUSED>
+__global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p,
+                                                         const __grid_constant__ SettlePlan sp) {
+  grid_dependency_wait();  // the GEMM's results are complete and visible
+  if (FUSED && (int32_t)blockIdx.x >= sp.n) {
+    straddle_row<N>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
+    return;
   }
-  const int64_t cf = geo.first_cta(p, up.rbg), cl = geo.last_cta(p, up.rbg);
+  const SettleTask tk = sp.task[blockIdx.x];
+  UnitPos up;
+  up.j = tk.j;
+  up.rbl = tk.rbl;
+  up.rbg = p.e[tk.j].rb_begin + tk.rbl;
+  const int64_t cf = tk.cf, cl = tk.cl;
   const DecodeEntry& e = p.e[up.j];
   uint16_t* const y = e.y;
-  const int64_t rows = e.rows;
+  const int64_t rows = e.rows, ystride = e.y_rows, base = e.row_base;
   const int m = p.m;
   const int row = threadIdx.x, c0 = blockIdx.y * 16;
-  const int64_t o = up.rbl * kTcRows + row;
+  const int64_t o = up.rbl * kTcRows + row;  // row of the entry (segment); straddling rows are in none
   if (o < rows) {
     constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
     float4 acc[4];
@@ -543,7 +565,7 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
       for (int k = 0; k < 4; ++k)
         if (cb + k <= cl) {
           const float4* s4 =
-              reinterpret_cast<const float4*>(p.partials + geo.slot(p, cb + k, up.rbg) * kSlot + row * N + c0);
+              reinterpret_cast<const float4*>(p.partials + (2 * (cb + k) + (up.rbg == sp.cta_first_rbg[cb + k] ? 0 : 1)) * kSlot + row * N + c0);
 #pragma unroll
           for (int q = 0; q < 4; ++q) v[k][q] = __ldcg(s4 + q);
         }
@@ -567,7 +589,7 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
         const int mm = c0 + 4 * q + k;
         if (mm < m) {
           const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
-          y[(int64_t)mm * rows + o] = *reinterpret_cast<const uint16_t*>(&b);
+          y[(int64_t)mm * ystride + base + o] = *reinterpret_cast<const uint16_t*>(&b);
         }
       }
     }
@@ -579,7 +601,116 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
   }
 }
 
+// Row st.row of a linear, read through the chunk map (a chunk boundary falls
+// inside it), for outputs m = c0 .. c0 + 15. The block stages the row in 4 KB
+// windows (32 slabs; 16-byte pieces never straddle a boundary, which is a
+// multiple of 16), so each window costs one memory round trip. Warp w takes
+// slabs w, w + 8, ... of a window and each lane four weights of a slab; a lane
+// accumulates s[kb] * x * w over its slabs for every m, and the warps' sums are
+// added once at the end, warp by warp in a fixed order.
 template <int N>
+__device__ void straddle_row(const DecodeParams& p, int sidx, int c0) {
+  constexpr int kWin = 32 * kSlabK;  // bytes per window
+  constexpr int kWarps = kTcRows / 32;
+  __shared__ __align__(16) uint8_t wbuf[kWin];
+  __shared__ float sbuf[32];
+  __shared__ float part[kWarps][16];
+  const DecodeEntry& e = p.e[p.st.entry[sidx]];  // a segment of the linear: its pointers
+  const int64_t r = p.st.row[sidx];                // row of the linear
+  const int64_t cols = e.cols, rows = e.y_rows, C = p.chunk_bytes, t0 = e.t_offset + r * cols;
+  const float* srow = e.scales + (r >> 7) * e.scale_cols;
+  uint16_t* const y = e.y;
+  const int slabs = e.slabs, m = p.m;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) acc[h] = 0.f;
+  for (int64_t w0 = 0; w0 < cols; w0 += kWin) {
+    __syncthreads();  // the previous window is consumed
+    for (int t = threadIdx.x; t < kWin / 16; t += blockDim.x) {
+      const int64_t k = w0 + 16 * t;
+      if (k < cols) {
+        const int64_t g = t0 + k;
+        *reinterpret_cast<uint4*>(wbuf + 16 * t) = *reinterpret_cast<const uint4*>(p.chunks[g / C] + g % C);
+      }
+    }
+    const int kb0 = (int)(w0 / kSlabK);
+    if (threadIdx.x < 32) sbuf[threadIdx.x] = kb0 + (int)threadIdx.x < slabs ? __ldg(srow + kb0 + threadIdx.x) : 0.f;
+    __syncthreads();
+    for (int sl = warp; sl < 32; sl += kWarps) {
+      const int64_t k = w0 + sl * kSlabK + lane * 4;
+      if (k >= cols) break;  // cols % 16 == 0: four weights are all in or all out
+      const uint32_t w4 = *reinterpret_cast<const uint32_t*>(wbuf + sl * kSlabK + lane * 4);
+      const float2 w01 = e4m3x2_to_f32x2(w4), w23 = e4m3x2_to_f32x2(w4 >> 16);
+      const float sc = sbuf[sl];
+      const float a0 = sc * w01.x, a1 = sc * w01.y, a2 = sc * w23.x, a3 = sc * w23.y;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        if (c0 + h < m) {
+          const uint2 x4 = *reinterpret_cast<const uint2*>(e.x + (int64_t)(c0 + h) * cols + k);
+          float v = acc[h];
+          v = fmaf(__uint_as_float(x4.x << 16), a0, v);
+          v = fmaf(__uint_as_float(x4.x & 0xffff0000u), a1, v);
+          v = fmaf(__uint_as_float(x4.y << 16), a2, v);
+          acc[h] = fmaf(__uint_as_float(x4.y & 0xffff0000u), a3, v);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
+    if (lane == 0) part[warp][h] = acc[h];
+  }
+  __syncthreads();
+  if (threadIdx.x < 16) {
+    const int h = threadIdx.x;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v += part[w][h];
+    if (c0 + h < m && r < rows) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      y[(int64_t)(c0 + h) * rows + r] = *reinterpret_cast<const uint16_t*>(&b);
+    }
+  }
+}
+
+// Host copy of the partition's arithmetic (unit_pos, cta_of, RunGeom).
+void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
+  const int64_t U = p.units;
+  auto pos = [&](int64_t u) {
+    int j = 0;
+    for (int q = 1; q < p.n_entries && u >= p.e[q].unit_begin; ++q) j = q;
+    const int64_t local = u - p.e[j].unit_begin;
+    UnitPos r;
+    r.j = j;
+    r.rbl = local / p.e[j].slabs;
+    r.kb = local - r.rbl * p.e[j].slabs;
+    r.rbg = p.e[j].rb_begin + r.rbl;
+    return r;
+  };
+  auto cta = [&](int64_t u) { return ((u + 1) * G - 1) / U; };
+  sp->n = 0;
+  for (int64_t c = 0; c < G; ++c) sp->cta_first_rbg[c] = (int32_t)pos(c * U / G).rbg;
+  for (int64_t c = 1; c < G; ++c) {
+    const UnitPos up = pos(c * U / G);
+    if (up.kb == 0) continue;  // the boundary is a row-block start: nothing is split here
+    if (c > 1) {               // an earlier boundary inside the same row block settles it
+      const UnitPos prev = pos((c - 1) * U / G);
+      if (prev.rbg == up.rbg && prev.kb != 0) continue;
+    }
+    const DecodeEntry& e = p.e[up.j];
+    const int64_t fu = e.unit_begin + up.rbl * e.slabs;
+    SettleTask& t = sp->task[sp->n++];
+    t.j = up.j;
+    t.rbl = (int32_t)up.rbl;
+    t.cf = (int32_t)cta(fu);
+    t.cl = (int32_t)cta(fu + e.slabs - 1);
+  }
+}
+
+template <int N, bool FUSED>
 cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int kSmem = TcCfg<N>::kSmem;
   static std::once_flag once;
@@ -590,7 +721,8 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   if (attr != cudaSuccess) return attr;
   // 1. split the activations of every entry
   int64_t threads = 0;
-  for (int j = 0; j < p.n_entries; ++j) threads += (int64_t)p.e[j].slabs * N * 8;
+  for (int j = 0; j < p.n_entries; ++j)
+    if (p.e[j].split_owner) threads += (int64_t)p.e[j].slabs * N * 8;
   split_x_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, N);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -607,24 +739,34 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.attrs = at;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
-  if (e != cudaSuccess || grid < 2) return e;
-  // 3. the split-K settle, as a programmatic dependent launch of (2)
-  cfg.gridDim = dim3((unsigned)(grid - 1), N / 16);
+  // 3. the split-K settle (and the straddling rows of a chunk-map launch), as
+  //    a programmatic dependent launch of (2)
+  if (e != cudaSuccess) return e;
+  SettlePlan sp;
+  settle_plan(p, grid, &sp);
+  const int64_t blocks = sp.n + (FUSED ? p.st.n : 0);
+  if (blocks < 1) return cudaSuccess;
+  cfg.gridDim = dim3((unsigned)blocks, N / 16);
   cfg.blockDim = dim3(kTcRows);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, settle_kernel<N>, p, (int32_t)grid);
+  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED>, p, sp);
+}
+
+template <bool FUSED>
+cudaError_t launch_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
+  switch ((int)tc_n_pad(p.m)) {
+    case 16: return launch_tc_n<16, FUSED>(p, grid_cap, s);
+    case 32: return launch_tc_n<32, FUSED>(p, grid_cap, s);
+    case 48: return launch_tc_n<48, FUSED>(p, grid_cap, s);
+    default: return launch_tc_n<64, FUSED>(p, grid_cap, s);
+  }
 }
 
 }  // namespace
 
 namespace dec {
-cudaError_t launch_decode_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
-  switch ((int)tc_n_pad(p.m)) {
-    case 16: return launch_tc_n<16>(p, grid_cap, s);
-    case 32: return launch_tc_n<32>(p, grid_cap, s);
-    case 48: return launch_tc_n<48>(p, grid_cap, s);
-    default: return launch_tc_n<64>(p, grid_cap, s);
-  }
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int64_t grid_cap, cudaStream_t s) {
+  return fused ? launch_tc<true>(p, grid_cap, s) : launch_tc<false>(p, grid_cap, s);
 }
 int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }
 }  // namespace dec

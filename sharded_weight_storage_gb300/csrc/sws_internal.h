@@ -54,6 +54,8 @@ constexpr int64_t kMaxCounters = 1 << 16;
 
 // Kinds written into trace tags.
 constexpr uint64_t kTraceGather = 1, kTraceLinear = 2;
+// Kernel of a linear launch, in bits 48..55 of its trace tag.
+constexpr uint64_t kTraceMma = 1, kTraceMmaFused = 2, kTraceTc = 3, kTraceTcFused = 4, kTracePrefill = 5;
 
 // Device-side wait limit for mbarrier / TMA waits, in nanoseconds of
 // %globaltimer. A wait that runs out sets the status word and the kernel exits.
