@@ -276,14 +276,6 @@ struct UnitCursor {
     rbl = 0;
     if (++j < p.n_entries) load(p);
   }
-  __device__ __forceinline__ UnitPos pos() const {
-    UnitPos r;
-    r.j = j;
-    r.rbl = rbl;
-    r.kb = kb;
-    r.rbg = rb_begin + rbl;
-    return r;
-  }
 };
 
 // End of a run of units on one row block (acc holds its sums): a run that

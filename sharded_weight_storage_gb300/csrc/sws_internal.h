@@ -62,8 +62,10 @@ constexpr uint64_t kTraceMma = 1, kTraceMmaFused = 2, kTraceTc = 3, kTraceTcFuse
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // 2-D tensor map of a byte matrix [rows, cols] (row stride cols, cols % 16 ==
-// 0): boxes of 128 bytes by box_rows rows, 128-byte swizzle, zero fill outside.
-int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+// 0): boxes of box_cols (128 or 64) bytes by box_rows rows, with the swizzle of
+// that width (128- or 64-byte), zero fill outside.
+int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows,
+                       int box_cols = 128);
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
