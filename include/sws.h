@@ -18,7 +18,9 @@
  *   - Memory: the caller allocates and owns every device buffer (chunks, row
  *     shards, slots, scales, activations, outputs, workspace) and keeps it
  *     alive until the work queued on it has finished. The library allocates
- *     host objects and CUDA events only; it never calls cudaMalloc.
+ *     host objects, CUDA events and one CUDA stream per context (prefill
+ *     layers quantise the next linear's activations on it); it never calls
+ *     cudaMalloc.
  *   - Alignment: every device pointer passed in must be 16-byte aligned
  *     (SWS_E_ALIGN otherwise).
  *   - Streams: sws_stream_t is a cudaStream_t; NULL is the legacy default
@@ -127,8 +129,9 @@ int sws_relayout(const sws_plan* plan, int32_t layer, const void* const* row_sha
 /* ---- context: resident chunks, two slots, scales, workspace ------------- */
 
 /* Bytes of workspace a context needs for linears with up to max_m rows of
- * activations (split-K partial sums, counters, the prefill quantiser's output
- * and the device status word). */
+ * activations (split-K partial sums, counters, the tcgen05 decode path's
+ * activation split blocks, two buffers of prefill quantiser output and the
+ * device status word). */
 int64_t sws_workspace_bytes(const sws_plan* plan, int64_t max_m);
 
 /* Creates a context over caller-owned device memory:

@@ -36,6 +36,10 @@ struct sws_ctx {
   // device trace records
   uint64_t* trace = nullptr;
   int32_t trace_cap = 0, trace_next = 0;
+  // prefill layers: the next linear's activations are quantised on qstream
+  // while the current GEMM runs (two workspace buffers)
+  cudaStream_t qstream = nullptr;
+  cudaEvent_t q_done[2] = {nullptr, nullptr}, g_done[2] = {nullptr, nullptr};
 };
 
 namespace {
@@ -149,22 +153,25 @@ int launch_group(sws_ctx* c, DecodeGroup& g, int32_t layer, int32_t first_entry,
   return rc;
 }
 
-int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+// Quantised activations of a prefill linear: xq [m, cols] then ex [m, cols/128].
+struct PrefillBuf {
+  uint8_t* xq;
+  float* ex;
+};
+PrefillBuf prefill_buf(sws_ctx* c, int b, int64_t per_buf, int64_t m, int64_t cols) {
+  PrefillBuf r;
+  r.xq = c->ws + c->ws_decode + b * per_buf;
+  r.ex = reinterpret_cast<float*>(r.xq + roundup(m * cols, 256));
+  return r;
+}
+
+int prefill_gemm(sws_ctx* c, int32_t j, const uint8_t* w, const PrefillBuf& q, int64_t m, void* y, cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
-  if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
-  const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
-  if (c->ws_bytes < need)
-    return fail(SWS_E_WORKSPACE, "linear: workspace %lld < %lld bytes for m=%lld", (long long)c->ws_bytes,
-                (long long)need, (long long)m);
-  uint8_t* xq = c->ws + c->ws_decode;
-  float* ex = reinterpret_cast<float*>(xq + roundup(m * e.cols, 256));
-  int rc = launch_quantize_x(static_cast<const uint16_t*>(x), m, e.cols, xq, ex, s);
-  if (rc != SWS_OK) return rc;
   PrefillLaunch pl;
   pl.w = w;
   pl.scales = c->scales[j];
-  pl.xq = xq;
-  pl.ex = ex;
+  pl.xq = q.xq;
+  pl.ex = q.ex;
   pl.y = static_cast<uint16_t*>(y);
   pl.m = m;
   pl.rows = e.rows;
@@ -173,6 +180,69 @@ int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64
   pl.trace = next_trace(c);
   pl.tag = (kTraceLinear << 56) | (kTracePrefill << 48) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
   return launch_prefill(pl, s);
+}
+
+int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+  const EntryPlan& e = c->plan->entries[j];
+  if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+  const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
+  if (c->ws_bytes < need)
+    return fail(SWS_E_WORKSPACE, "linear: workspace %lld < %lld bytes for m=%lld", (long long)c->ws_bytes,
+                (long long)need, (long long)m);
+  const PrefillBuf q = prefill_buf(c, 0, 0, m, e.cols);
+  int rc = launch_quantize_x(static_cast<const uint16_t*>(x), m, e.cols, q.xq, q.ex, s);
+  if (rc != SWS_OK) return rc;
+  return prefill_gemm(c, j, w, q, m, y, s);
+}
+
+int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s);
+
+// A prefill layer: linear k's activations are quantised on the context's side
+// stream into buffer k % 2 while GEMM k - 1 runs on `s`; GEMM k waits for its
+// quantiser, and quantiser k waits for GEMM k - 2, the last reader of its
+// buffer. Without room for two buffers the linears run one after another.
+int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_io& io, cudaStream_t s) {
+  const int64_t m = io.m;
+  int64_t per_buf = 0;
+  for (int32_t j : lp.all) {
+    if (c->plan->entries[j].cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+    per_buf = std::max(per_buf, prefill_bytes(m, c->plan->entries[j].cols));
+  }
+  if (lp.all.size() < 2 || c->ws_bytes < c->ws_decode + 2 * per_buf) {
+    for (size_t k = 0; k < lp.all.size(); ++k) {
+      int rc = linear_impl(c, lp.all[k], src, io.x[k], m, io.y[k], s);
+      if (rc != SWS_OK) return rc;
+    }
+    return SWS_OK;
+  }
+  cudaError_t ce = cudaEventRecord(c->call_start, s);  // the activations are ready in s's order
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(c->qstream, c->call_start, 0);
+  if (ce != cudaSuccess) return cuda_fail(ce, "prefill layer: stream order");
+  for (size_t k = 0; k < lp.all.size(); ++k) {
+    const int32_t j = lp.all[k];
+    int rc = check_linear_args(c, j, io.x[k], m, io.y[k]);
+    if (rc != SWS_OK) return rc;
+    const EntryPlan& e = c->plan->entries[j];
+    if (e.rows == 0) continue;
+    const uint8_t* w = nullptr;
+    bool fused = false;
+    rc = weight_source(c, j, src, &w, &fused);
+    if (rc != SWS_OK) return rc;
+    if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
+    const int b = (int)(k & 1);
+    const PrefillBuf q = prefill_buf(c, b, per_buf, m, e.cols);
+    if (k >= 2 && (ce = cudaStreamWaitEvent(c->qstream, c->g_done[b], 0)) != cudaSuccess)
+      return cuda_fail(ce, "prefill layer: wait");
+    rc = launch_quantize_x(static_cast<const uint16_t*>(io.x[k]), m, e.cols, q.xq, q.ex, c->qstream);
+    if (rc != SWS_OK) return rc;
+    if ((ce = cudaEventRecord(c->q_done[b], c->qstream)) != cudaSuccess ||
+        (ce = cudaStreamWaitEvent(s, c->q_done[b], 0)) != cudaSuccess)
+      return cuda_fail(ce, "prefill layer: quantiser order");
+    rc = prefill_gemm(c, j, w, q, m, io.y[k], s);
+    if (rc != SWS_OK) return rc;
+    if ((ce = cudaEventRecord(c->g_done[b], s)) != cudaSuccess) return cuda_fail(ce, "prefill layer: record");
+  }
+  return SWS_OK;
 }
 
 int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s) {
@@ -202,13 +272,7 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
   if (lp.all.empty()) return SWS_OK;
   if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
   const int64_t m = io.m;
-  if (m > 64) {
-    for (size_t k = 0; k < lp.all.size(); ++k) {
-      int rc = linear_impl(c, lp.all[k], src, io.x[k], m, io.y[k], s);
-      if (rc != SWS_OK) return rc;
-    }
-    return SWS_OK;
-  }
+  if (m > 64) return prefill_layer(c, lp, src, io, s);
   DecodeGroup gv, gf;
   init_group(c, gv, layer, m, false);
   init_group(c, gf, layer, m, true);
@@ -261,7 +325,7 @@ int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   if (decode_workspace_bytes(mm, &dec) != SWS_OK) return -1;
   int64_t pre = 0;
   for (const EntryPlan& e : p->entries) pre = std::max(pre, prefill_bytes(max_m, e.cols));
-  return dec + split_region_bytes(p, mm) + pre;
+  return dec + split_region_bytes(p, mm) + 2 * pre;  // two buffers: quantiser k + 1 beside GEMM k
 }
 
 int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void* slot1, const float* const* scales,
@@ -333,6 +397,16 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
     sws_ctx_destroy(c);
     return cuda_fail(e, "ctx_create: cudaEventCreate");
   }
+  for (int b = 0; b < 2; ++b)
+    if ((e = cudaEventCreateWithFlags(&c->q_done[b], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->g_done[b], cudaEventDisableTiming)) != cudaSuccess) {
+      sws_ctx_destroy(c);
+      return cuda_fail(e, "ctx_create: cudaEventCreate");
+    }
+  if ((e = cudaStreamCreateWithFlags(&c->qstream, cudaStreamNonBlocking)) != cudaSuccess) {
+    sws_ctx_destroy(c);
+    return cuda_fail(e, "ctx_create: cudaStreamCreate");
+  }
   *out = c;
   return SWS_OK;
 }
@@ -345,6 +419,11 @@ void sws_ctx_destroy(sws_ctx* c) {
   }
   if (c->call_start) cudaEventDestroy(c->call_start);
   if (c->join) cudaEventDestroy(c->join);
+  for (int b = 0; b < 2; ++b) {
+    if (c->q_done[b]) cudaEventDestroy(c->q_done[b]);
+    if (c->g_done[b]) cudaEventDestroy(c->g_done[b]);
+  }
+  if (c->qstream) cudaStreamDestroy(c->qstream);
   for (size_t i = 0; i < c->t_wait.size(); ++i) {
     cudaEventDestroy(c->t_wait[i]);
     cudaEventDestroy(c->t_begin[i]);
