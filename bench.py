@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--stack-layers", type=int, default=92, help="layers of the lookahead stack (0 skips it)")
     ap.add_argument("--prefill-layers", type=int, default=8, help="layers of the prefill run (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the KDA-layer and tiny-layer decode sections")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
     ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill"],
@@ -499,8 +500,85 @@ def run_stack(args, dist, n_layers):
         "resident_formula_all_ranks": r_bytes + 2 * st.plan.slot_bytes,
         "resident_formula_per_rank": r_bytes // n + 2 * st.plan.slot_bytes,
         "launches_per_step": n_layers * (1 + decode_kernel_info(args.decode_kernel)[2]),
+        "gather_ctas": 2 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count,
     }
     del st, ctx, io
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_decode_config(args, dist, w, relayout: bool):
+    """Decode linears of one layer of workload w at each of its m values: the
+    gather, slot linears, chunk-map (fused) linears and gather + linears (µs,
+    GB/s), and optionally the one-time relayout from row shards."""
+    import torch
+
+    import sharded_weight_storage_gb300 as S
+    import sharded_weight_storage_gb300._lib as L
+    import workloads as WL
+    from sharded_weight_storage_gb300.storage import ShardedStack
+
+    dev = torch.device("cuda", dist.local)
+    ents = [(0, e.rows, e.cols) for e in w.entries]
+    lw = WL.layer_weights(WL.scaled_workload(w, n_layers=1), 0)
+    st = ShardedStack([(0, S.E4M3, r, c) for (_, r, c) in ents], w.n_shards, max_m=64, device=str(dev))
+    codes = {j: torch.from_numpy(lw.codes[j]).to(dev) for j in range(len(ents))}
+    st.load_layer(0, codes, {j: torch.from_numpy(lw.scales[j]) for j in range(len(ents))})
+    ctx = st.make_ctx()
+    total = st.layout[0][0]
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty(1024, dtype=torch.float32, device=dev)
+
+    def timed(fn, reps=20, flush=True):
+        out = []
+        for _ in range(reps):
+            if flush:
+                torch.amax(scratch.view(1024, -1), dim=1, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            out.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) for a, b in out])
+
+    out = {"workload": f"{w.name}: {len(ents)} linears, |T| = {total} B, N = {w.n_shards}", "per_m": {}}
+    with torch.cuda.stream(stream):
+        if relayout:
+            n = w.n_shards
+            parts = [codes[j][r * (ents[j][1] // n):(r + 1) * (ents[j][1] // n)].contiguous()
+                     for j in range(len(ents)) for r in range(n)]
+            chunk_ptrs = [c.data_ptr() for c in st.chunks[0]]
+            rl = lambda: L.relayout(st.plan, 0, [q.data_ptr() for q in parts], chunk_ptrs, sp)
+            rl()
+            r_ms = timed(rl, reps=10)
+            out["relayout"] = {"us": r_ms * 1e3, "GBps": 2 * total / r_ms / 1e6}
+            del parts
+        ctx.gather_to_slot(0, 0, sp)
+        g_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp))
+        out["gather"] = {"us": g_ms * 1e3, "GBps": 2 * total / g_ms / 1e6}
+        for m in w.m_values:
+            xs = [WL.draw_x(w.key, j, m, c).to(dev) for j, (_, r, c) in enumerate(ents)]
+            ys = [torch.empty((m, r), dtype=torch.bfloat16, device=dev) for (_, r, c) in ents]
+            lins = lambda src: ctx.layer_linears(0, src, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys],
+                                                 m, sp)
+            for _ in range(3):
+                lins(S.SRC_SLOT0)
+                lins(S.SRC_FUSED)
+            lb = sum(layer_bytes(ents, m))
+            slot_ms = timed(lambda: lins(S.SRC_SLOT0))
+            fused_ms = timed(lambda: lins(S.SRC_FUSED))
+            step_ms = timed(lambda: (ctx.gather_to_slot(0, 0, sp), lins(S.SRC_SLOT0)))
+            out["per_m"][m] = {
+                "slot_linears_us": slot_ms * 1e3, "slot_linears_GBps": lb / slot_ms / 1e6,
+                "fused_linears_us": fused_ms * 1e3, "fused_linears_GBps": lb / fused_ms / 1e6,
+                "gather_plus_linears_us": step_ms * 1e3, "gather_plus_linears_GBps": (2 * total + lb) / step_ms / 1e6,
+            }
+    assert ctx.status() == 0
+    del st, ctx
     torch.cuda.empty_cache()
     return out
 
@@ -758,6 +836,11 @@ def main():
         return
     r = run_ours(args, dist)
     stack = run_stack(args, dist, args.stack_layers) if args.stack_layers > 0 else None
+    configs = None
+    if not args.no_configs:
+        import workloads as WL
+        configs = {"attn_kda_layer": run_decode_config(args, dist, WL.ATTN_KDA, relayout=True),
+                   "tiny_flat_layer": run_decode_config(args, dist, WL.TINY, relayout=True)}
     prefill = run_prefill(args, dist, args.prefill_layers) if args.prefill_layers > 0 else None
     if dist.rank != 0:
         dist.close()
@@ -798,6 +881,7 @@ def main():
         "gather_alone": r["gather_alone"],
         "per_m": r["per_m"],
         "lookahead_stack": stack,
+        "decode_configs": configs,
         "prefill": prefill,
         "weight_GBps_step": total / ms_step / 1e6,
     }
