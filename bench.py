@@ -467,11 +467,32 @@ def run_stack(args, dist, n_layers):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / k
 
+    def graph_steps(k, flags):
+        # The whole stack recorded once into a CUDA graph, then replayed: the
+        # host issues one launch per step instead of ~4 per layer.
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            ctx.run_layers(0, n_layers - 1, io, flags, main.cuda_stream, side.cuda_stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(main):
+            for _ in range(2):
+                g.replay()
+            a.record(main)
+            for _ in range(k):
+                g.replay()
+            b.record(main)
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) / k
+
     k = max(3, args.steps // 2)
     steps(max(2, args.warmup // 2), 0)
     slot_ms = dist.max(steps(k, 0))
     steps(1, S.RUN_FUSED)
     fused_ms = dist.max(steps(k, S.RUN_FUSED))
+    graph_ms = dist.max(graph_steps(k, 0))
+    graph_fused_ms = dist.max(graph_steps(k, S.RUN_FUSED))
     exposed, layer_ms = [], []
     for _ in range(3):
         ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
@@ -489,6 +510,8 @@ def run_stack(args, dist, n_layers):
         "layers": n_layers, "gen_s": round(gen_s, 1),
         "step_ms": slot_ms, "per_layer_us": slot_ms * 1e3 / n_layers,
         "fused_step_ms": fused_ms, "fused_per_layer_us": fused_ms * 1e3 / n_layers,
+        "graph_step_ms": graph_ms, "graph_per_layer_us": graph_ms * 1e3 / n_layers,
+        "graph_fused_step_ms": graph_fused_ms, "graph_fused_per_layer_us": graph_fused_ms * 1e3 / n_layers,
         "exposed_gather_us_per_layer": 1e3 * statistics.mean(ex[1:]) if n_layers > 1 else 1e3 * ex[0],
         "exposed_gather_first_layer_us": 1e3 * ex[0],
         "exposed_frac_of_step": sum(ex) / sum(lm + ex) if sum(lm + ex) > 0 else 0.0,

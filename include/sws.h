@@ -216,7 +216,14 @@ int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t
  * records done(l). At most two layers' full weights are resident. With
  * SWS_RUN_FUSED no gather runs and the linears read the chunks directly.
  * io[l - first] gives layer l's activations and outputs. On return `main`
- * carries all the work (side-stream work is joined into it). */
+ * carries all the work (side-stream work is joined into it).
+ * Stream capture: without SWS_RUN_TIMING the call only enqueues kernels and
+ * event record/wait pairs (no synchronisation, no allocation, no query), so
+ * it records into a CUDA graph when `main` is capturing: the fork to `side`
+ * and the join back are captured edges, and replaying the graph repeats the
+ * run on the pointers given at capture time (activations and outputs are read
+ * and written in place, so refill x between replays). SWS_RUN_TIMING records
+ * timing events and is not capturable (SWS_E_INVALID while capturing). */
 int sws_run_layers(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
                    sws_stream_t main, sws_stream_t side);
 

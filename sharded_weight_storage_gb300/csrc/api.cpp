@@ -464,6 +464,10 @@ int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* 
   const bool timing = (flags & SWS_RUN_TIMING) != 0;
   const int32_t n = last - first + 1;
   if (timing) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    SWS_CUDA_TRY(cudaStreamIsCapturing(ms, &cap));
+    if (cap != cudaStreamCaptureStatusNone)
+      return fail(SWS_E_INVALID, "run_layers: SWS_RUN_TIMING records timing events and cannot be captured");
     int rc = ensure_events(c, (size_t)n);
     if (rc != SWS_OK) return rc;
     c->timed_n = n;

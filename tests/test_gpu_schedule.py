@@ -162,3 +162,37 @@ def test_run_layers_rejects_bad_ranges(S, stack):
     with pytest.raises(S.SwsError):
         s = torch.cuda.Stream().cuda_stream
         st.ctx.run_layers(0, 0, [([0, 0], [0, 0], 1)], 0, s, s)
+
+
+@pytest.mark.parametrize("m", [8, 40])
+def test_run_layers_captures_into_a_cuda_graph(S, stack, m):
+    # The lookahead schedule (gathers on the side stream, event waits, the
+    # programmatic dependent launches of the decode linears) records into one
+    # CUDA graph; replaying it gives the eager run's bits, and replays with new
+    # activations in the same buffers give their results.
+    st, layers = stack
+    xs, ys, io = _io(st, 0, 6, m)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    st.ctx.run_layers(0, 6, io, 0, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    ref = {j: y.clone() for j, y in ys.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        with pytest.raises(S.SwsError):  # timing events cannot be captured
+            st.ctx.run_layers(0, 6, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
+        st.ctx.run_layers(0, 6, io, 0, main.cuda_stream, side.cuda_stream)
+    for y in ys.values():
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for j in ys:
+        assert torch.equal(ys[j], ref[j]), f"entry {j}: graph replay differs from the eager run"
+    for x in xs.values():  # new inputs, same buffers
+        x.copy_(torch.flip(x, dims=[1]))
+    g.replay()
+    torch.cuda.synchronize()
+    for l in range(0, 7):
+        for j in st.layer_entries(l):
+            want = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[l].codes[j], layers[l].scales[j])
+            assert_close(bf16_tensor_to_f64(ys[j]), want, f"replay 2, layer {l} entry {j}")
+    assert st.ctx.status() == 0
