@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--m", type=int, default=HEADLINE_M)
     ap.add_argument("--entry", type=int, default=0, help="0 = gate_up, 1 = down")
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--prefill-kernel", choices=["auto", "single", "pair"], default="auto",
+                    help="prefill GEMM: one CTA per tile, a CTA pair per tile, or the library's choice")
     ap.add_argument("--decode-kernel", choices=["auto", "mma", "tcgen05"], default="auto",
                     help="which kernel serves decode linears from views")
     return ap.parse_args()
@@ -213,6 +215,10 @@ def set_decode_kernel(S, name):
     S.set_option(S.OPT_DECODE_KERNEL, {"auto": S.DECODE_AUTO, "mma": S.DECODE_MMA, "tcgen05": S.DECODE_TCGEN05}[name])
 
 
+def set_prefill_kernel(S, name):
+    S.set_option(S.OPT_PREFILL_KERNEL, {"auto": S.PREFILL_AUTO, "single": S.PREFILL_SINGLE, "pair": S.PREFILL_PAIR}[name])
+
+
 def decode_kernel_info(name):
     """(dominant kernel name, its sources, launches per decode group) of a
     slot-path decode launch: the library's default is the tcgen05 kernel, which
@@ -254,6 +260,7 @@ def run_ours(args, dist):
 
     dev = torch.device("cuda", dist.local)
     set_decode_kernel(S, args.decode_kernel)
+    set_prefill_kernel(S, args.prefill_kernel)
     w = WL.SHARED_EXPERT
     n = w.n_shards
     ents = [(0, e.rows, e.cols) for e in w.entries]
@@ -669,6 +676,13 @@ def run_prefill(args, dist, n_layers):
                 fl = 2.0 * m * e.rows * e.cols
                 flops_layer += fl
                 per[e.name] = {"us": t * 1e3, "TFLOPS": fl / t / 1e9, "frac_of_fp8_peak": fl / t / 1e9 / burst}
+                for kname in ("single", "pair"):  # each GEMM kernel forced, quantiser included
+                    set_prefill_kernel(S, kname)
+                    call()
+                    tk = timed(call)
+                    per[e.name][kname + "_us"] = tk * 1e3
+                    per[e.name][kname + "_frac_of_fp8_peak"] = fl / tk / 1e9 / burst
+                set_prefill_kernel(S, args.prefill_kernel)
             # quantiser alone for the widest activation
             xq = torch.empty((m, 8192), dtype=torch.uint8, device=dev)
             ex = torch.empty((m, 64), dtype=torch.float32, device=dev)
@@ -789,6 +803,7 @@ def run_only(args, dist):
     from sharded_weight_storage_gb300.storage import ShardedStack
 
     set_decode_kernel(S, args.decode_kernel)
+    set_prefill_kernel(S, args.prefill_kernel)
     if args.only == "prefill":  # one KDA-layer linear (entry --entry) at m = --m tokens
         w = WL.PREFILL
         ents = [(0, e.rows, e.cols) for e in w.entries]

@@ -254,7 +254,8 @@ int sws_ctx_status(sws_ctx* ctx, int32_t clear);
  * capacity records): {tag, start_ns, end_ns, 0} where tag = kind << 56 |
  * kernel << 48 | layer << 32 | entry (kind 1 = gather, 2 = linear; kernel, for
  * linears: 1 mma.sync on views, 2 mma.sync through the chunk map, 3 tcgen05
- * on views, 4 tcgen05 through the chunk map, 5 prefill), start_ns is the earliest
+ * on views, 4 tcgen05 through the chunk map, 5 prefill, 6 prefill on a CTA
+ * pair), start_ns is the earliest
  * %globaltimer read by any CTA at entry and end_ns the latest at exit. Passing
  * NULL turns tracing off. Records are reset (start = ~0, end = 0) on `stream`.
  * Returns the number of records written so far through sws_trace_count. */
@@ -266,10 +267,17 @@ int32_t sws_trace_count(const sws_ctx* ctx);
 #define SWS_DECODE_AUTO 0       /* the library's choice (default): tcgen05 */
 #define SWS_DECODE_MMA 1        /* warp-level mma.sync kernel */
 #define SWS_DECODE_TCGEN05 2    /* tcgen05 / TMEM kernel */
-/* Process-wide option, read at each launch. Both decode kernels compute the
+#define SWS_OPT_PREFILL_KERNEL 2 /* which kernel serves prefill linears (m > 64) */
+#define SWS_PREFILL_AUTO 0       /* the library's choice (default): one CTA per tile */
+#define SWS_PREFILL_SINGLE 1     /* one CTA per 128 x 256 output tile */
+#define SWS_PREFILL_PAIR 2       /* a cluster of two CTAs (tcgen05 .cta_group::2) per 256 x 256 tile;
+                                    SWS_E_UNSUPPORTED at launch if no such cluster fits */
+/* Process-wide options, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance; chunk-map (fused) reads
  * always use the mma.sync kernel. A tcgen05 launch is three kernels on the
  * stream (activation split, GEMM, split-K settle); an mma.sync launch is one.
+ * Both prefill kernels compute the same sums in the same slab order per output
+ * element and give bit-identical results.
  * SWS_E_INVALID for an unknown option or value. */
 int sws_set_option(int32_t option, int64_t value);
 

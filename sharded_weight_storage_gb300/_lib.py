@@ -18,6 +18,8 @@ SRC_SLOT0, SRC_SLOT1, SRC_FUSED = 0, 1, 2
 RUN_FUSED, RUN_TIMING = 1, 2
 OPT_DECODE_KERNEL = 1
 DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05 = 0, 1, 2
+OPT_PREFILL_KERNEL = 2
+PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
 
 _NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}

@@ -567,6 +567,11 @@ int sws_set_option(int32_t option, int64_t value) {
         return fail(SWS_E_INVALID, "set_option: decode kernel %lld", (long long)value);
       set_decode_kernel((int)value);
       return SWS_OK;
+    case SWS_OPT_PREFILL_KERNEL:
+      if (value < SWS_PREFILL_AUTO || value > SWS_PREFILL_PAIR)
+        return fail(SWS_E_INVALID, "set_option: prefill kernel %lld", (long long)value);
+      set_prefill_kernel((int)value);
+      return SWS_OK;
     default:
       return fail(SWS_E_INVALID, "set_option: unknown option %d", option);
   }

@@ -9,21 +9,38 @@
 // the GEMM is a dense contraction and the gather is easy to hide (section
 // "提前一层：lookahead 与 ping-pong slot").
 //
-// Design (one persistent CTA per SM, 10 warps, warp-specialised):
-//   * warp 0, one thread: TMA producer. Per 128-K slab it loads the 128 x 128
-//     activation tile and the 256 x 128 weight tile (e4m3, 128-byte swizzle,
-//     zero fill past the edges) into one of 4 shared-memory stages.
-//   * warp 1: allocates 512 TMEM columns; one thread issues the MMAs:
-//     4 x tcgen05.mma kind::f8f6f4 (128 x 256 x 32) per slab into one of two
-//     TMEM slab buffers (128 lanes x 256 fp32 columns each), then commits to
-//     the stage's "empty" barrier and the buffer's "full" barrier.
-//   * warps 2-9: promotion. The weight scales are not powers of two, so they
-//     cannot feed the MMA's own block scaling; each slab result is read from
-//     TMEM (tcgen05.ld) and added into fp32 registers with the factor
-//     ex[m, kb] * s_w[n/128, kb] (each thread owns one row m and 128 columns).
-//     After the last slab of a tile the row is rounded to bf16 and stored.
-//   * Every mbarrier wait is bounded; a wait that runs out records
-//     SWS_E_TIMEOUT and the CTA finishes with TMEM released.
+// Two kernels compute it; both are persistent and warp-specialised: one
+// thread loads operand tiles with TMA, one thread issues the MMAs into TMEM
+// slab buffers (one buffer per 128-K slab), and promotion warps turn each slab
+// into fp32 register sums. The weight scales are not powers of two, so they
+// cannot feed the MMA's own block scaling: each slab result is read from TMEM
+// (tcgen05.ld) and added with the factor ex[m, kb] * s_w[n/128, kb] (each
+// promotion thread owns one row m and a run of columns). After the last slab
+// of a tile the rows are rounded to bf16 and stored. The factors reach the
+// promotion threads through a shared-memory ring filled by cp.async eight
+// slabs ahead.
+//
+// prefill_kernel: one CTA per 128 x 256 tile (128 activation rows, 256 weight
+// rows); 4 stages of 48 KB; 4 x tcgen05.mma kind::f8f6f4 (128 x 256 x 32)
+// per slab into one of two 256-column buffers; 8 promotion warps x 128
+// columns.
+//
+// prefill_pair_kernel (selected by option; slower here, see below): a cluster
+// of two CTAs on an SM pair per 256 x 256 tile, with tcgen05 .cta_group::2.
+// Each CTA loads 128 activation rows and 128 weight rows per slab (32 KB)
+// into one of 6 stages; the pair's MMA (256 x 256 x 32) reads each CTA's
+// activation half and both weight halves, so an SM takes in 32 KB from L2
+// per 128 x 256 x 128 slab of work instead of 48 KB. Both CTAs' copies
+// complete on the first CTA's stage barrier; its MMA thread commits to the
+// empty and slab barriers of both CTAs (multicast); each CTA's 16 promotion
+// warps (64 columns each) read their own TMEM lanes and release the buffer
+// on the first CTA's barrier. With two slab buffers, every slab's MMA waits
+// for the promotion of the slab two back in both CTAs, and that cross-SM
+// round trip costs more than the L2 traffic saves: on the KDA-like linears
+// it reaches about 41% of the FP8 peak where the one-CTA kernel reaches 47%.
+//
+// Every mbarrier wait is bounded; a wait that runs out records SWS_E_TIMEOUT
+// and the CTA (or pair) finishes with TMEM released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -38,21 +55,43 @@
 namespace sws {
 namespace {
 
-constexpr int kBM = 128;          // activation rows per tile (MMA M)
-constexpr int kBN = 256;          // weight rows per tile (MMA N)
-constexpr int kBK = 128;          // K per slab = one scale block
+constexpr int kBK = 128;  // K per slab = one scale block
+
+// One CTA per 128 x 256 tile: A = 128 activation rows, B = 256 weight rows,
+// two TMEM slab buffers of 256 columns, 8 promotion warps x 128 columns.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK;  // 16 KB
 constexpr int kBBytes = kBN * kBK;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr int kTmemCols = 512;  // two slab buffers of kBN columns
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+
+// A CTA pair per 256 x 256 tile: each CTA loads 128 activation rows and 128
+// weight rows per slab (32 KB); two TMEM slab buffers of 256 columns; 16
+// promotion warps x 64 columns per CTA.
+constexpr int kPairM = 256, kPairN = 256;
+constexpr int kPairStages = 6;
+constexpr int kPairABytes = (kPairM / 2) * kBK;         // 16 KB
+constexpr int kPairBBytes = (kPairN / 2) * kBK;         // 8 KB
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairEpiWarps = 16;
+constexpr int kPairThreads = (2 + kPairEpiWarps) * 32;
+
+constexpr int kTmemCols = 512;
+
+// Scale-factor ring: each promotion thread fetches ex[m, kb] (and lane 0 of
+// each warp s_w[nb, kb]) kScaleDepth slabs ahead with cp.async into shared
+// memory, so no register waits on a global load.
+constexpr int kScaleDepth = 8;
+__host__ __device__ constexpr int scale_ring_bytes(int epi_warps) { return kScaleDepth * (epi_warps * 32 + epi_warps) * 4; }
+constexpr int kSmemBytes = kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + 1024;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + scale_ring_bytes(kPairEpiWarps) + 1024;
 
 struct PrefillParams {
-  CUtensorMap tmap_x;  // xq [M, K] u8, box {128, 128}
-  CUtensorMap tmap_w;  // wq [N, K] u8, box {128, 256}
+  CUtensorMap tmap_x;  // xq [M, K] u8
+  CUtensorMap tmap_w;  // wq [N, K] u8
   const float* ex;     // [M, K/128]
   const float* sw;     // [ceil(N/128), K/128]
   uint16_t* y;         // bf16 [M, N]
@@ -105,19 +144,29 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 lanes x 16 consecutive fp32 columns: thread (lane i) gets row i's values.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 32 lanes x 16 consecutive fp32 columns (thread = lane = row), without
+// waiting (tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 32 consecutive fp32 columns, without waiting (tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
                                             uint64_t* bar) {
@@ -128,9 +177,170 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// ---- CTA-pair helpers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs arrives; memory before it is visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (a shared variable of this CTA) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(dev::smem_addr(p)), "r"(rank));
+  return r;
+}
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier that may sit in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dev::smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// Arrives once on `bar` in both CTAs of the pair when the pair's previously
+// issued MMAs finish.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  const uint16_t both = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          dev::smem_addr(bar)),
+      "h"(both)
+      : "memory");
+}
+
 __device__ __forceinline__ void set_abort(const PrefillParams& p, volatile int* s_abort) {
   dev::set_status(p.status, SWS_E_TIMEOUT);
   *s_abort = 1;
+}
+
+// 4-byte asynchronous global -> shared copy (completion per thread through
+// cp.async groups).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dev::smem_addr(dst)), "l"(src) : "memory");
+}
+
+// One promotion thread's share of a tile: output row m, columns
+// n0 .. n0+kCols-1 (TMEM lane and column `lane_base` within each slab buffer,
+// buffers kBufCols columns apart, kNBuf of them used in turn). For each slab
+// it waits for the slab buffer, adds it into acc with the factor
+// ex[m, kb] * s_w[n0/128, kb], and releases the buffer (once per warp) on
+// `release[buf]` (this CTA's barrier, or the first CTA's for a pair).
+// TMEM is read kLd (16 or 32) columns per load. Returns false if a wait ran out.
+template <bool kPair, int kEpiW, int kCols, int kNBuf, int kBufCols, int kLd>
+__device__ __forceinline__ bool promote_tile(const PrefillParams& p, float (&acc)[kCols], int64_t m, int64_t n0,
+                                             uint32_t lane_base, uint64_t* tfull, const uint32_t (&release)[kNBuf],
+                                             float* ring_ex, float* ring_sw, int64_t& it, int lane,
+                                             volatile int* s_abort) {
+  const int G = p.kslabs;
+  const int64_t sw_rows = (p.N + 127) / 128, nb = n0 / 128;
+  const float* exr = p.ex + (m < p.M ? m : 0) * G;
+  const float* swr = p.sw + (nb < sw_rows ? nb : 0) * G;
+  const bool nb_live = nb < sw_rows, live = m < p.M && nb_live;
+  // ring_ex[d * stride] / ring_sw[d] hold slab kb's factors for d = kb % kScaleDepth
+  // (ring_sw is the warp's: all its lanes share nb, lane 0 fetches it).
+  constexpr int kStride = kEpiW * 32;
+  auto fetch = [&](int kb) {
+    if (kb < G) {
+      const int d = kb % kScaleDepth;
+      if (live) cp_async4(ring_ex + d * kStride, exr + kb);
+      if (lane == 0 && nb_live) cp_async4(ring_sw + d, swr + kb);
+    }
+    dev::cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+  for (int d = 0; d < kScaleDepth; ++d) fetch(d);
+  bool ok = true;
+  for (int kb = 0; kb < G && ok; ++kb) {
+    const int buf = (int)(it % kNBuf);
+    ok = dev::mbar_wait(&tfull[buf], (uint32_t)((it / kNBuf) & 1), kWaitLimitNs);
+    if (!ok) {
+      set_abort(p, s_abort);
+      break;
+    }
+    tc_fence_after();
+    dev::cp_async_wait<kScaleDepth - 1>();  // slab kb's factors have landed
+    __syncwarp();
+    const int d = kb % kScaleDepth;
+    const float fk = live ? ring_ex[d * kStride] * ring_sw[d] : 0.f;
+    __syncwarp();  // every lane has read slot d before lane 0 refills it
+    fetch(kb + kScaleDepth);
+#pragma unroll
+    for (int c = 0; c < kCols / kLd; ++c) {
+      uint32_t v[kLd];
+      if constexpr (kLd == 32)
+        tmem_ld32(lane_base + buf * kBufCols + c * kLd, v);
+      else
+        tmem_ld16(lane_base + buf * kBufCols + c * kLd, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < kLd; ++i) acc[c * kLd + i] = fmaf(fk, __uint_as_float(v[i]), acc[c * kLd + i]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (kPair)  // the first CTA's barrier, through its cluster address
+        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(release[buf]) : "memory");
+      else
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(release[buf]) : "memory");
+    }
+    ++it;
+  }
+  dev::cp_async_wait<0>();  // no copy into the ring outlives the tile
+  return ok;
+}
+
+// Row m, columns n0 .. n0+kCols-1 of Y as bf16 (round to nearest even).
+template <int kCols>
+__device__ __forceinline__ void store_row(const PrefillParams& p, const float (&acc)[kCols], int64_t m, int64_t n0) {
+  if (m >= p.M || n0 >= p.N) return;
+  uint16_t* yrow = p.y + m * p.N + n0;
+  const int64_t ncols = p.N - n0 < kCols ? p.N - n0 : kCols;
+  if (ncols == kCols && (p.N & 7) == 0) {
+#pragma unroll
+    for (int i = 0; i < kCols; i += 8) {
+      uint4 o;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i + 2 * t], acc[i + 2 * t + 1]);
+        w[t] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(yrow + i) = o;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kCols; ++i)
+      if (i < ncols) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(acc[i]);
+        yrow[i] = *reinterpret_cast<const uint16_t*>(&b);
+      }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -225,90 +435,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
     }
   } else {
-    // ---- promotion and output -------------------------------------------------
+    // ---- promotion and output: 8 warps, thread = tile row, 128 columns -------
+    constexpr int kCols = kBN / (kEpiWarps / 4);
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;   // which 128 of the tile's 256 columns
+    const int g = (warp - 2) >> 2;   // which kCols of the tile's kBN columns
     const int row = q * 32 + lane;   // tile row = TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
-    const int64_t sw_rows = (p.N + 127) / 128;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + g * kCols;
+    const uint32_t release[2] = {dev::smem_addr(&tempty[0]), dev::smem_addr(&tempty[1])};
+    float* ring = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    float* ring_ex = ring + (threadIdx.x - 64);
+    float* ring_sw = ring + kScaleDepth * kEpiWarps * 32 + (warp - 2) * kScaleDepth;
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x) {
       const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
       const int64_t m = (int64_t)mt * kBM + row;
-      const int64_t n0 = (int64_t)nt * kBN + h * 128, nb = n0 / 128;
-      const float* exr = p.ex + (m < p.M ? m : 0) * G;
-      const float* swr = p.sw + (nb < sw_rows ? nb : 0) * G;
-      const bool live = m < p.M && nb < sw_rows;
-      // Raw scale loads, multiplied only when used: a product taken at load
-      // time would make the thread wait for both loads right away.
-      auto load_ex = [&](int kb) -> float { return (live && kb < G) ? __ldg(exr + kb) : 0.f; };
-      auto load_sw = [&](int kb) -> float { return (live && kb < G) ? __ldg(swr + kb) : 0.f; };
-      float acc[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      // Scale factors are fetched four slabs ahead (rings fe[d], fw[d] hold slab kb0 + d).
-      float fe[4], fw[4];
-#pragma unroll
-      for (int d = 0; d < 4; ++d) {
-        fe[d] = load_ex(d);
-        fw[d] = load_sw(d);
-      }
-      bool ok = true;
-      for (int kb0 = 0; kb0 < G && ok; kb0 += 4) {
-#pragma unroll
-        for (int d = 0; d < 4; ++d) {
-          const int kb = kb0 + d;
-          if (kb < G && ok) {
-            const int buf = (int)(it & 1);
-            ok = dev::mbar_wait(&tfull[buf], (uint32_t)((it >> 1) & 1), kWaitLimitNs);
-            if (!ok) {
-              set_abort(p, &s_abort);
-            } else {
-              tc_fence_after();
-              const float fk = fe[d] * fw[d];
-              fe[d] = load_ex(kb + 4);
-              fw[d] = load_sw(kb + 4);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                float v[16];
-                tmem_ld16(lane_base + buf * kBN + c * 16, v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(fk, v[i], acc[c * 16 + i]);
-              }
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) dev::mbar_arrive(&tempty[buf]);
-              ++it;
-            }
-          }
-        }
-      }
-      if (!ok) break;
-      // ---- the tile row: bf16, 128 columns -------------------------------------
-      if (m < p.M) {
-        uint16_t* yrow = p.y + m * p.N + n0;
-        const int64_t ncols = p.N - n0 < 128 ? p.N - n0 : 128;
-        if (ncols == 128 && (p.N & 7) == 0) {
-#pragma unroll
-          for (int i = 0; i < 128; i += 8) {
-            uint4 o;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i + 2 * t], acc[i + 2 * t + 1]);
-              w[t] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            *reinterpret_cast<uint4*>(yrow + i) = o;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i < ncols) {
-              const __nv_bfloat16 b = __float2bfloat16_rn(acc[i]);
-              yrow[i] = *reinterpret_cast<const uint16_t*>(&b);
-            }
-        }
-      }
+      const int64_t n0 = (int64_t)nt * kBN + g * kCols;
+      float acc[kCols];
+      if (!promote_tile<false, kEpiWarps, kCols, 2, kBN, 16>(p, acc, m, n0, lane_base, tfull, release, ring_ex,
+                                                             ring_sw, it, lane, &s_abort))
+        break;
+      store_row<kCols>(p, acc, m, n0);
     }
   }
   __syncthreads();
@@ -322,7 +468,191 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
+// ---- CTA-pair kernel ------------------------------------------------------------
+// Cluster rank 0 of each pair holds the stage "full" barriers that count both
+// CTAs' copies and the slab-buffer "empty" barriers that count both CTAs'
+// promotion warps, and its MMA thread issues the pair's MMAs. Tiles of
+// 256 x 256 outputs go to clusters round-robin; CTA r of a pair owns
+// activation rows mt*256 + r*128 .. +127 (its TMEM lanes) and loads weight
+// rows nt*256 + r*128 .. +127 (the pair's MMA reads both weight halves).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr int kNBuf = kTmemCols / kPairN;  // 2 slab buffers
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[kNBuf], tempty[kNBuf], mdone;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int64_t first = cluster_index(), stride = cluster_count();
+  const int G = p.kslabs;
+
+  if (threadIdx.x == 0) {
+    dev::trace_start(p.trace);
+    for (int s = 0; s < kPairStages; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kNBuf; ++b) {
+      dev::mbar_init(&tfull[b], 1);
+      dev::mbar_init(&tempty[b], 2 * kPairEpiWarps);
+    }
+    dev::mbar_init(&mdone, 1);
+    dev::fence_mbar_init();
+    s_abort = 0;
+  }
+  // Both CTAs' barriers are initialised, and both CTAs are running, before any
+  // arrival crosses the pair and before the paired TMEM allocation.
+  cluster_sync();
+  if (warp == 1) {  // the same 512 columns in both CTAs' TMEM
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dev::smem_addr(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---- TMA producer (both CTAs) ----------------------------------------
+    if (lane == 0) {
+      int64_t it = 0;
+      for (int64_t tile = first; tile < tiles && !s_abort; tile += stride) {
+        const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+        const int32_t ya = mt * kPairM + (int32_t)rank * (kPairM / 2);
+        const int32_t yb = nt * kPairN + (int32_t)rank * (kPairN / 2);
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          const int s = (int)(it % kPairStages);
+          if (!dev::mbar_wait(&empty[s], (uint32_t)(((it / kPairStages) & 1) ^ 1), kWaitLimitNs)) {
+            set_abort(p, &s_abort);
+            break;
+          }
+          if (rank == 0) dev::mbar_arrive_expect_tx(&full[s], 2 * kPairStageBytes);
+          const uint32_t bar = cluster_addr(&full[s], 0);
+          uint8_t* st = smem + s * kPairStageBytes;
+          tma_load_2d_pair(st, &p.tmap_x, kb * kBK, ya, bar);
+          tma_load_2d_pair(st + kPairABytes, &p.tmap_w, kb * kBK, yb, bar);
+        }
+      }
+      // Rank 0 sees every stage land (both halves) before the pair may exit.
+      if (rank == 0)
+        for (int64_t k = it - kPairStages; k < it; ++k)
+          if (k >= 0) dev::mbar_wait(&full[(int)(k % kPairStages)], (uint32_t)((k / kPairStages) & 1), kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer (rank 0 only) ------------------------------------------
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_f8(kPairM, kPairN);
+      int64_t it = 0;
+      bool issued = false;
+      for (int64_t tile = first; tile < tiles && !s_abort; tile += stride) {
+        for (int kb = 0; kb < G && !s_abort; ++kb, ++it) {
+          const int s = (int)(it % kPairStages), buf = (int)(it % kNBuf);
+          if (!dev::mbar_wait(&tempty[buf], (uint32_t)(((it / kNBuf) & 1) ^ 1), kWaitLimitNs)) {
+            set_abort(p, &s_abort);
+            break;
+          }
+          tc_fence_after();
+          if (!dev::mbar_wait(&full[s], (uint32_t)((it / kPairStages) & 1), kWaitLimitNs)) {
+            set_abort(p, &s_abort);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = dev::smem_addr(smem + s * kPairStageBytes), b = a + kPairABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8_pair(tmem + buf * kPairN, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
+                        kk > 0);
+          mma_commit_pair(&empty[s]);
+          mma_commit_pair(&tfull[buf]);
+          issued = true;
+        }
+      }
+      if (issued) {  // the pair's MMAs complete before either CTA releases TMEM
+        mma_commit_pair(&mdone);
+        dev::mbar_wait(&mdone, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ---- promotion and output (both CTAs): 16 warps, 64 columns each ------------
+    constexpr int kCols = kPairN / (kPairEpiWarps / 4);
+    const int q = warp & 3;
+    const int g = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + g * kCols;
+    uint32_t release[kNBuf];
+#pragma unroll
+    for (int b = 0; b < kNBuf; ++b) release[b] = cluster_addr(&tempty[b], 0);
+    float* ring = reinterpret_cast<float*>(smem + kPairStages * kPairStageBytes);
+    float* ring_ex = ring + (threadIdx.x - 64);
+    float* ring_sw = ring + kScaleDepth * kPairEpiWarps * 32 + (warp - 2) * kScaleDepth;
+    int64_t it = 0;
+    for (int64_t tile = first; tile < tiles && !s_abort; tile += stride) {
+      const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+      const int64_t m = (int64_t)mt * kPairM + (int64_t)rank * (kPairM / 2) + row;
+      const int64_t n0 = (int64_t)nt * kPairN + g * kCols;
+      float acc[kCols];
+      if (!promote_tile<true, kPairEpiWarps, kCols, kNBuf, kPairN, 16>(p, acc, m, n0, lane_base, tfull, release,
+                                                                       ring_ex, ring_sw, it, lane, &s_abort))
+        break;
+      store_row<kCols>(p, acc, m, n0);
+    }
+  }
+  __syncthreads();
+  if (s_abort && threadIdx.x == 0) {
+    // After a timeout this CTA may have copies in flight whose barrier is the
+    // peer's: give them a millisecond to land before the memory is released.
+    const uint64_t t0 = dev::globaltimer();
+    while (dev::globaltimer() - t0 < 1000000ull) {
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs are done with TMEM and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    dev::trace_end(p.trace, p.tag);
+  }
+}
+
+int g_prefill_kernel = kPrefillAuto;
+
+// Clusters of two prefill_pair_kernel CTAs that fit on the current device at
+// once (0 if none; cached per device).
+int pair_cluster_capacity() {
+  static int cache[64];
+  static bool known[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    int n = 0;
+    if (cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (unsigned)device_sm_count(), 1, 1);
+      cfg.blockDim = dim3(kPairThreads, 1, 1);
+      cfg.dynamicSmemBytes = kPairSmemBytes;
+      if (cudaOccupancyMaxActiveClusters(&n, prefill_pair_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // a failed query leaves no sticky error
+    cache[dev] = n;
+    known[dev] = true;
+  }
+  return cache[dev];
+}
+
 }  // namespace
+
+void set_prefill_kernel(int k) { g_prefill_kernel = k; }
 
 int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   if (a.m <= 0 || a.rows <= 0) return SWS_OK;
@@ -330,10 +660,15 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     return fail(SWS_E_UNSUPPORTED, "prefill: cols=%lld is not a positive multiple of 128", (long long)a.cols);
   if (!aligned16(a.w) || !aligned16(a.xq) || !aligned16(a.y) || !aligned16(a.ex) || !aligned16(a.scales))
     return fail(SWS_E_ALIGN, "prefill: pointer not 16-byte aligned");
+  const int choice = g_prefill_kernel;
+  const int clusters = choice == kPrefillPair ? pair_cluster_capacity() : 0;
+  if (choice == kPrefillPair && clusters <= 0)
+    return fail(SWS_E_UNSUPPORTED, "prefill: no cluster of two CTAs fits on this device");
+  const bool pair = clusters > 0 && choice == kPrefillPair;
   PrefillParams p;
-  int rc = encode_u8_tile_map(&p.tmap_x, a.xq, a.m, a.cols, kBM);
+  int rc = encode_u8_tile_map(&p.tmap_x, a.xq, a.m, a.cols, pair ? kPairM / 2 : kBM);
   if (rc != SWS_OK) return rc;
-  rc = encode_u8_tile_map(&p.tmap_w, a.w, a.rows, a.cols, kBN);
+  rc = encode_u8_tile_map(&p.tmap_w, a.w, a.rows, a.cols, pair ? kPairN / 2 : kBN);
   if (rc != SWS_OK) return rc;
   p.ex = a.ex;
   p.sw = a.scales;
@@ -342,22 +677,27 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   p.N = a.rows;
   p.K = a.cols;
   p.kslabs = (int32_t)(a.cols / kBK);
-  p.m_tiles = (int32_t)cdiv(a.m, kBM);
-  p.n_tiles = (int32_t)cdiv(a.rows, kBN);
+  p.m_tiles = (int32_t)cdiv(a.m, pair ? kPairM : kBM);
+  p.n_tiles = (int32_t)cdiv(a.rows, pair ? kPairN : kBN);
   p.status = a.status;
   p.trace = a.trace;
-  p.tag = a.tag;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute");
+  p.tag = pair ? (a.tag & ~(0xFFull << 48)) | (kTracePrefillPair << 48) : a.tag;
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-  const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-  prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+  if (pair) {
+    const int64_t n_clusters = std::min<int64_t>(tiles, clusters);
+    prefill_pair_kernel<<<(unsigned)(2 * n_clusters), kPairThreads, kPairSmemBytes, s>>>(p);
+  } else {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+      attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute");
+    const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
+    prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+  }
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill kernel launch");
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, pair ? "prefill pair kernel launch" : "prefill kernel launch");
 }
 
 }  // namespace sws

@@ -55,7 +55,8 @@ constexpr int64_t kMaxCounters = 1 << 16;
 // Kinds written into trace tags.
 constexpr uint64_t kTraceGather = 1, kTraceLinear = 2;
 // Kernel of a linear launch, in bits 48..55 of its trace tag.
-constexpr uint64_t kTraceMma = 1, kTraceMmaFused = 2, kTraceTc = 3, kTraceTcFused = 4, kTracePrefill = 5;
+constexpr uint64_t kTraceMma = 1, kTraceMmaFused = 2, kTraceTc = 3, kTraceTcFused = 4, kTracePrefill = 5,
+                   kTracePrefillPair = 6;
 
 // Device-side wait limit for mbarrier / TMA waits, in nanoseconds of
 // %globaltimer. A wait that runs out sets the status word and the kernel exits.
@@ -140,6 +141,8 @@ struct PrefillLaunch {
   uint64_t* trace;
   uint64_t tag;
 };
+enum PrefillKernel { kPrefillAuto = 0, kPrefillSingle = 1, kPrefillPair = 2 };
+void set_prefill_kernel(int k);
 int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);

@@ -42,9 +42,36 @@ def _rand_layer(rng, shapes):
     return LayerData(codes, scales)
 
 
+KERNEL_PREFILL, KERNEL_PREFILL_PAIR = 5, 6
+
+
+@pytest.fixture(params=["single", "pair"])
+def kernel(S, request):
+    """Forces one prefill kernel for the test, then restores the default."""
+    S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_SINGLE if request.param == "single" else S.PREFILL_PAIR)
+    yield KERNEL_PREFILL if request.param == "single" else KERNEL_PREFILL_PAIR
+    S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_AUTO)
+
+
+def _linear_traced(st, j, src, x, m):
+    """Runs one linear with tracing on; returns y and the kernel id of its record."""
+    rec = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
+    st.ctx.trace_begin(rec.data_ptr(), 4, 0)
+    _, _, rows, _ = st.entries[j]
+    y = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st.ctx.linear(j, src, x.data_ptr(), m, y.data_ptr(), 0)
+    torch.cuda.synchronize()
+    n = st.ctx.trace_count()
+    st.ctx.trace_begin(0, 0, 0)
+    tags = [int(t) for t in rec.view(4, 4)[:n, 0].tolist()]
+    return y, [(t >> 48) & 0xFF for t in tags if (t >> 48) & 0xFF in (KERNEL_PREFILL, KERNEL_PREFILL_PAIR)]
+
+
 @pytest.mark.parametrize("m", [65, 128, 300, 1000])
-def test_prefill_ragged_tiles(S, m):
-    # rows not multiples of the 256-row tile (nor of 128), several K slabs.
+def test_prefill_ragged_tiles(S, kernel, m):
+    # rows not multiples of the 256-row weight tile (nor of 128), several K
+    # slabs; with the pair kernel, m = 65 and 128 leave the second CTA's
+    # activation rows, and rows = 256 its weight rows, entirely past the edge.
     shapes = [(0, 4 * 64, 128), (0, 4 * 97, 512), (0, 4 * 250, 1152)]
     rng = np.random.default_rng(40 + m)
     ld = _rand_layer(rng, shapes)
@@ -52,15 +79,36 @@ def test_prefill_ragged_tiles(S, m):
     st.ctx.gather_to_slot(0, 0, 0)
     for j, (_, r, c) in enumerate(shapes):
         x = WL.draw_x(60, j, m, c)
-        y = torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda")
-        st.ctx.linear(j, S.SRC_SLOT0, x.cuda().data_ptr(), m, y.data_ptr(), 0)
-        torch.cuda.synchronize()
+        y, kerns = _linear_traced(st, j, S.SRC_SLOT0, x.cuda(), m)
+        assert kerns == [kernel]
         ref, _ = _ref_quantised(x, ld.codes[j], ld.scales[j])
         assert_close(bf16_tensor_to_f64(y), ref, f"entry {j} m {m}")
     assert st.ctx.status() == 0
 
 
-def test_prefill_special_cases(S):
+@pytest.mark.parametrize("m", [300, 1000])
+def test_prefill_pair_and_single_agree_bitwise(S, m):
+    # Both kernels add the same per-slab MMA results in the same slab order.
+    shapes = [(0, 4 * 97, 512), (0, 4 * 250, 1152)]
+    rng = np.random.default_rng(70 + m)
+    ld = _rand_layer(rng, shapes)
+    st = build_stack(S, shapes, 4, [ld], max_m=m)
+    st.ctx.gather_to_slot(0, 0, 0)
+    try:
+        for j, (_, r, c) in enumerate(shapes):
+            x = WL.draw_x(61, j, m, c).cuda()
+            S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_SINGLE)
+            y1, k1 = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+            S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_PAIR)
+            y2, k2 = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+            assert (k1, k2) == ([KERNEL_PREFILL], [KERNEL_PREFILL_PAIR])
+            assert torch.equal(y1, y2), f"entry {j}: max diff {(y1.float() - y2.float()).abs().max().item()}"
+    finally:
+        S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_AUTO)
+    assert st.ctx.status() == 0
+
+
+def test_prefill_special_cases(S, kernel):
     rng = np.random.default_rng(3)
     r, c, m = 384, 256, 200
     q = rng.integers(0, 0x7E, size=(r, c), dtype=np.uint8)
@@ -112,7 +160,7 @@ def test_prefill_kda_layer_small(S):
 
 
 @pytest.mark.parametrize("m", [2048])
-def test_prefill_full_size_sampled_rows(S, m):
+def test_prefill_full_size_sampled_rows(S, kernel, m):
     # The prefill workload's weights (KDA-like layer, N = 8), full sizes; the
     # oracle computes 48 sampled token rows of every linear.
     w = WL.PREFILL
