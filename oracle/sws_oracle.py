@@ -27,6 +27,8 @@ Readings taken where the pages are silent (each also listed in the design notes)
   * row shard r of an [out, in] weight holds rows [r*out/N, (r+1)*out/N);
   * Y = X W^T with W [out, in]; block scale s[o // 128, i // 128] multiplies the
     decoded code; partial edge blocks use ceil(./128) indexing;
+  * BF16 weights: the same linear with W decoded from bfloat16 patterns and
+    no scales; ModelOpt FP8: one float32 scale for the whole weight;
   * prefill activations: per (row, 128-column group) scale e = 2^k with k the
     smallest integer such that amax <= 448 * 2^k (amax = 0 gives e = 1), and
     codes xq = e4m3_rne(x / e), ties to even, saturating to +-448.
@@ -238,6 +240,37 @@ def dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
 def linear(x: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """Y = X W^T in float64 with W the dequantized weight."""
     return np.asarray(x, dtype=np.float64) @ dequant(codes, scales).T
+
+
+# Weight variants ([WS "加载：行 shard 先行，finalize 再重排", "量化变体"]): BF16
+# weights go through the same flat layout; ModelOpt FP8 keeps its per-tensor
+# scale replicated, outside T.
+
+
+def bf16_decode(bits: np.ndarray) -> np.ndarray:
+    """Value of each 16-bit bfloat16 pattern in float64: sign bit, 8 exponent
+    bits (bias 127), 7 fraction bits; exponent 0 is subnormal (f * 2^-133),
+    exponent 255 is infinity (f = 0) or NaN."""
+    b = np.asarray(bits, dtype=np.int64)
+    sign = np.where(b & 0x8000, -1.0, 1.0)
+    e = (b >> 7) & 0xFF
+    f = (b & 0x7F).astype(np.float64)
+    normal = np.ldexp(1.0 + f / 128.0, (e - 127).astype(np.int64))
+    sub = np.ldexp(f, -133)
+    v = np.where(e == 0, sub, normal)
+    v = np.where(e == 255, np.where(f == 0, np.inf, np.nan), v)
+    return sign * v
+
+
+def linear_bf16(x: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """Y = X W^T in float64 with W [out, in] given as bfloat16 bit patterns."""
+    return np.asarray(x, dtype=np.float64) @ bf16_decode(w_bits).T
+
+
+def linear_per_tensor(x: np.ndarray, codes: np.ndarray, scale: float) -> np.ndarray:
+    """Y = X W^T with W[o, i] = e4m3(q[o, i]) * s, one scale for the whole
+    weight (ModelOpt FP8), in float64."""
+    return np.asarray(x, dtype=np.float64) @ (e4m3_decode(codes) * float(np.float32(scale))).T
 
 
 def quantize_x(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:

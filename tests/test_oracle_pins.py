@@ -339,6 +339,67 @@ def test_linear_transposition_and_block_index_are_pinned():
 
 
 # ---------------------------------------------------------------------------
+# weight variants: BF16 weights, per-tensor FP8 scale
+# ---------------------------------------------------------------------------
+
+
+def test_bf16_decode_closed_forms():
+    # 1.0, -2.0, 0.5, largest finite, smallest normal, smallest subnormal, zeros
+    cases = {0x3F80: 1.0, 0xC000: -2.0, 0x3F00: 0.5, 0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127,
+             0x0080: 2.0 ** -126, 0x0001: 2.0 ** -133, 0x0000: 0.0, 0x8000: -0.0, 0x4049: 3.140625}
+    for bits, want in cases.items():
+        got = O.bf16_decode(np.array([bits]))[0]
+        assert got == want and np.signbit(got) == np.signbit(want), hex(bits)
+    assert np.isinf(O.bf16_decode(np.array([0x7F80]))[0]) and np.isnan(O.bf16_decode(np.array([0x7FC0]))[0])
+
+
+def test_bf16_decode_matches_torch_for_every_pattern():
+    bits = np.arange(1 << 16, dtype=np.int64)
+    t = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    o = O.bf16_decode(bits)
+    same = (o == t) | (np.isnan(o) & np.isnan(t))
+    assert same.all()
+
+
+def _rand_bf16_bits(rng, shape):
+    v = torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * 0.05).to(torch.bfloat16)
+    return v.view(torch.int16).numpy().astype(np.uint16)
+
+
+def test_linear_bf16_matches_exact_rational_dot_products():
+    rng = np.random.default_rng(31)
+    for (m, out, inn) in [(1, 3, 5), (2, 17, 64), (3, 5, 130)]:
+        w = _rand_bf16_bits(rng, (out, inn))
+        x = _bf16_values(rng, (m, inn))
+        y = O.linear_bf16(x, w)
+        wv = O.bf16_decode(w)
+        for a in range(m):
+            for o in range(out):
+                exact = sum(Fraction(float(x[a, i])) * Fraction(float(wv[o, i])) for i in range(inn))
+                assert abs(Fraction(float(y[a, o])) - exact) <= Fraction(1, 10**12) * (1 + abs(exact))
+
+
+def test_linear_bf16_one_hot_and_transposition():
+    rng = np.random.default_rng(32)
+    w = _rand_bf16_bits(rng, (40, 24))  # non-square: a transposed operand fails
+    for i in (0, 7, 23):
+        x = np.zeros((1, 24))
+        x[0, i] = 1.0
+        assert np.array_equal(O.linear_bf16(x, w)[0], O.bf16_decode(w[:, i]))
+
+
+def test_linear_per_tensor_is_block_linear_with_a_constant_grid():
+    rng = np.random.default_rng(33)
+    q = rng.integers(0, 0x7E, size=(300, 260), dtype=np.uint8)
+    x = _bf16_values(rng, (4, 260))
+    s = np.float32(0.0371)
+    grid = np.full((3, 3), s, np.float32)
+    assert np.array_equal(O.linear_per_tensor(x, q, s), O.linear(x, q, grid))
+    # and it scales linearly in s (powers of two are exact)
+    assert np.array_equal(O.linear_per_tensor(x, q, 0.25), 0.25 * O.linear_per_tensor(x, q, 1.0))
+
+
+# ---------------------------------------------------------------------------
 # prefill activation quantiser
 # ---------------------------------------------------------------------------
 
