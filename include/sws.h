@@ -160,28 +160,34 @@ void sws_ctx_destroy(sws_ctx* ctx);
  * in issue order). */
 int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 
-/* Y = X W_j^T for entry j (blog section "核心抽象": the GEMM sees the full W):
- *   Y[m, o] = bf16_rne( sum_i x[m, i] * e4m3(q[o, i]) * s[o/128, i/128] ),
- * fp32 accumulation. W_j is the view slot + o_j (src = SWS_SRC_SLOT0/1; the
- * slot's tag must equal the entry's layer, else SWS_E_STATE), the chunks
- * themselves (SWS_SRC_FUSED), or the replicated buffer for entries outside T
- * (src ignored). x: bf16 [m, cols] row-major; y: bf16 [m, rows] row-major.
- * m in [0, 2^31): m <= 64 runs the split-K decode kernel (tensor-core MMA on
- * f16 operands: W is converted exactly, x is rounded to f16, which is exact
- * for |x| in [2^-24, 65504]); m > 64 runs the prefill path (x quantised by
- * sws_quantize_x into the workspace, then the tcgen05 block-scaled FP8 GEMM).
- * Requires E4M3 weights, cols % 16 == 0, and, for m > 64, cols % 128 == 0.
- * Linears that share a context must not overlap on the GPU (they share the
- * workspace). */
+/* Y = X W_j^T for entry j (blog section "核心抽象": the GEMM sees the full W),
+ * fp32 accumulation, Y rounded to bf16 (nearest even):
+ *   E4M3 entries: Y[m, o] = sum_i x[m, i] * e4m3(q[o, i]) * s[o/128, i/128];
+ *   BF16 entries: Y[m, o] = sum_i x[m, i] * w[o, i]  (no scales; the blog's
+ *                 unquantised variant goes through the same flat layout).
+ * W_j is the view slot + o_j (src = SWS_SRC_SLOT0/1; the slot's tag must equal
+ * the entry's layer, else SWS_E_STATE), the chunks themselves
+ * (SWS_SRC_FUSED), or the replicated buffer for entries outside T (src
+ * ignored). x: bf16 [m, cols] row-major; y: bf16 [m, rows] row-major.
+ * m in [0, 2^31). m <= 64 runs a split-K decode launch: for E4M3 by default
+ * the tcgen05 kernel (x split exactly into two e4m3 terms, see
+ * SWS_OPT_DECODE_KERNEL), for BF16 the mma.sync kernel on bf16 operands.
+ * m > 64 runs the prefill path: E4M3 quantises x (sws_quantize_x into the
+ * workspace) and runs the tcgen05 block-scaled FP8 GEMM; BF16 runs a tcgen05
+ * bf16 GEMM on x directly. Requires E4M3 or BF16 weights (else
+ * SWS_E_UNSUPPORTED), cols % 16 == 0, and, for E4M3 with m > 64,
+ * cols % 128 == 0; E4M3 entries need their scales. Linears that share a
+ * context must not overlap on the GPU (they share the workspace). */
 int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t m, void* y,
                sws_stream_t stream);
 
 /* Every linear of one layer (declaration order, replicated entries included),
  * with io->x[k] / io->y[k] for its k-th entry and a common m: the decode-sized
- * ones (m <= 64) run as grouped launches, up to 8 linears per launch - one for
- * the views (slot src, or replicated buffers) and one for chunk-map reads
- * (SWS_SRC_FUSED) - so a layer pays one launch instead of one per weight.
- * Same results and rules as sws_linear for each entry. */
+ * ones (m <= 64) run as grouped launches, up to 8 linears per launch, one
+ * group per weight source (views: slot src or replicated buffers; chunk-map
+ * reads: SWS_SRC_FUSED) and weight type (E4M3, BF16), so a layer pays one
+ * launch instead of one per weight. Same results and rules as sws_linear for
+ * each entry. */
 int sws_layer_linears(sws_ctx* ctx, int32_t layer, int32_t src, const sws_layer_io* io, sws_stream_t stream);
 
 /* Decode linear that allocates nothing. The paper has no counterpart to this

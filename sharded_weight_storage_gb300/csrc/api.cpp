@@ -115,12 +115,13 @@ int check_linear_args(sws_ctx* c, int32_t j, const void* x, int64_t m, void* y) 
   const sws_plan* p = c->plan;
   if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "linear: entry %d", j);
   const EntryPlan& e = p->entries[j];
-  if (e.dtype != SWS_E4M3) return fail(SWS_E_UNSUPPORTED, "linear: entry %d is not E4M3", j);
+  if (e.dtype != SWS_E4M3 && e.dtype != SWS_BF16)
+    return fail(SWS_E_UNSUPPORTED, "linear: entry %d is neither E4M3 nor BF16", j);
   if (m < 0 || m >= ((int64_t)1 << 31)) return fail(SWS_E_INVALID, "linear: m=%lld", (long long)m);
   if (m == 0 || e.rows == 0) return SWS_OK;
   if (!x || !y) return fail(SWS_E_INVALID, "linear: x or y is NULL");
   if (!aligned16(x) || !aligned16(y)) return fail(SWS_E_ALIGN, "linear: x or y is not 16-byte aligned");
-  if (!c->scales[j]) return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
+  if (e.dtype == SWS_E4M3 && !c->scales[j]) return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
   if (e.cols % 16 != 0) return fail(SWS_E_UNSUPPORTED, "linear: cols=%lld is not a multiple of 16", (long long)e.cols);
   return SWS_OK;
 }
@@ -182,8 +183,28 @@ int prefill_gemm(sws_ctx* c, int32_t j, const uint8_t* w, const PrefillBuf& q, i
   return launch_prefill(pl, s);
 }
 
+// BF16 weights at prefill sizes: no quantiser, the bf16 activations feed the
+// tensor cores directly.
+int prefill_linear_bf16(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+  const EntryPlan& e = c->plan->entries[j];
+  PrefillLaunch pl;
+  pl.w = w;
+  pl.scales = nullptr;
+  pl.xq = static_cast<const uint8_t*>(x);
+  pl.ex = nullptr;
+  pl.y = static_cast<uint16_t*>(y);
+  pl.m = m;
+  pl.rows = e.rows;
+  pl.cols = e.cols;
+  pl.status = status_word(c);
+  pl.trace = next_trace(c);
+  pl.tag = (kTraceLinear << 56) | (kTracePrefill << 48) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
+  return launch_prefill_bf16(pl, s);
+}
+
 int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
+  if (e.dtype == SWS_BF16) return prefill_linear_bf16(c, j, w, x, m, y, s);
   if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
   const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
   if (c->ws_bytes < need)
@@ -197,18 +218,23 @@ int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64
 
 int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s);
 
-// A prefill layer: linear k's activations are quantised on the context's side
-// stream into buffer k % 2 while GEMM k - 1 runs on `s`; GEMM k waits for its
-// quantiser, and quantiser k waits for GEMM k - 2, the last reader of its
-// buffer. Without room for two buffers the linears run one after another.
+// A prefill layer: the q-th E4M3 linear's activations are quantised on the
+// context's side stream into buffer q % 2 while the previous GEMM runs on `s`;
+// GEMM q waits for its quantiser, and quantiser q waits for GEMM q - 2, the
+// last reader of its buffer. BF16 linears need no quantiser and run on `s` in
+// order. Without room for two buffers the linears run one after another.
 int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_io& io, cudaStream_t s) {
   const int64_t m = io.m;
   int64_t per_buf = 0;
+  int n_fp8 = 0;
   for (int32_t j : lp.all) {
-    if (c->plan->entries[j].cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
-    per_buf = std::max(per_buf, prefill_bytes(m, c->plan->entries[j].cols));
+    const EntryPlan& e = c->plan->entries[j];
+    if (e.dtype != SWS_E4M3) continue;
+    if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+    per_buf = std::max(per_buf, prefill_bytes(m, e.cols));
+    ++n_fp8;
   }
-  if (lp.all.size() < 2 || c->ws_bytes < c->ws_decode + 2 * per_buf) {
+  if (n_fp8 < 2 || c->ws_bytes < c->ws_decode + 2 * per_buf) {
     for (size_t k = 0; k < lp.all.size(); ++k) {
       int rc = linear_impl(c, lp.all[k], src, io.x[k], m, io.y[k], s);
       if (rc != SWS_OK) return rc;
@@ -218,6 +244,7 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
   cudaError_t ce = cudaEventRecord(c->call_start, s);  // the activations are ready in s's order
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(c->qstream, c->call_start, 0);
   if (ce != cudaSuccess) return cuda_fail(ce, "prefill layer: stream order");
+  int qi = 0;  // E4M3 linears so far
   for (size_t k = 0; k < lp.all.size(); ++k) {
     const int32_t j = lp.all[k];
     int rc = check_linear_args(c, j, io.x[k], m, io.y[k]);
@@ -229,10 +256,16 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
     rc = weight_source(c, j, src, &w, &fused);
     if (rc != SWS_OK) return rc;
     if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
-    const int b = (int)(k & 1);
+    if (e.dtype == SWS_BF16) {
+      rc = prefill_linear_bf16(c, j, w, io.x[k], m, io.y[k], s);
+      if (rc != SWS_OK) return rc;
+      continue;
+    }
+    const int b = qi & 1;
     const PrefillBuf q = prefill_buf(c, b, per_buf, m, e.cols);
-    if (k >= 2 && (ce = cudaStreamWaitEvent(c->qstream, c->g_done[b], 0)) != cudaSuccess)
+    if (qi >= 2 && (ce = cudaStreamWaitEvent(c->qstream, c->g_done[b], 0)) != cudaSuccess)
       return cuda_fail(ce, "prefill layer: wait");
+    ++qi;
     rc = launch_quantize_x(static_cast<const uint16_t*>(io.x[k]), m, e.cols, q.xq, q.ex, c->qstream);
     if (rc != SWS_OK) return rc;
     if ((ce = cudaEventRecord(c->q_done[b], c->qstream)) != cudaSuccess ||
@@ -260,23 +293,27 @@ int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, vo
   }
   DecodeGroup g;
   init_group(c, g, e.layer, m, fused);
+  g.bf16_w = e.dtype == SWS_BF16;
   g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), e.rows,
                              e.cols, e.offset};
   return launch_group(c, g, e.layer, j, s);
 }
 
-// All linears of a layer: decode-sized ones go out as at most two grouped
-// launches (views by TMA, chunk-map reads), up to kMaxDecodeGroup per launch.
+// All linears of a layer: decode-sized ones go out as grouped launches, one
+// group per (views by TMA or chunk-map reads) x (E4M3 or BF16 weights), up to
+// kMaxDecodeGroup per launch.
 int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io, cudaStream_t s) {
   const LayerPlan& lp = c->plan->layers[layer];
   if (lp.all.empty()) return SWS_OK;
   if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
   const int64_t m = io.m;
   if (m > 64) return prefill_layer(c, lp, src, io, s);
-  DecodeGroup gv, gf;
-  init_group(c, gv, layer, m, false);
-  init_group(c, gf, layer, m, true);
-  int32_t first_v = -1, first_f = -1;
+  DecodeGroup grp[4];  // index: fused * 2 + bf16
+  int32_t first[4] = {-1, -1, -1, -1};
+  for (int q = 0; q < 4; ++q) {
+    init_group(c, grp[q], layer, m, q >= 2);
+    grp[q].bf16_w = (q & 1) != 0;
+  }
   for (size_t k = 0; k < lp.all.size(); ++k) {
     const int32_t j = lp.all[k];
     int rc = check_linear_args(c, j, io.x[k], m, io.y[k]);
@@ -287,19 +324,21 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
     bool fused = false;
     rc = weight_source(c, j, src, &w, &fused);
     if (rc != SWS_OK) return rc;
-    DecodeGroup& g = fused ? gf : gv;
-    int32_t& first = fused ? first_f : first_v;
+    const int q = (fused ? 2 : 0) + (e.dtype == SWS_BF16 ? 1 : 0);
+    DecodeGroup& g = grp[q];
     if (g.n == kMaxDecodeGroup) {
-      rc = launch_group(c, g, layer, first, s);
+      rc = launch_group(c, g, layer, first[q], s);
       if (rc != SWS_OK) return rc;
     }
-    if (g.n == 0) first = j;
+    if (g.n == 0) first[q] = j;
     g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(io.x[k]), static_cast<uint16_t*>(io.y[k]),
                                e.rows, e.cols, e.offset};
   }
-  int rc = launch_group(c, gv, layer, first_v, s);
-  if (rc != SWS_OK) return rc;
-  return launch_group(c, gf, layer, first_f, s);
+  for (int q = 0; q < 4; ++q) {
+    int rc = launch_group(c, grp[q], layer, first[q], s);
+    if (rc != SWS_OK) return rc;
+  }
+  return SWS_OK;
 }
 
 // Activation split region of the tcgen05 decode path: enough for the largest
@@ -324,7 +363,8 @@ int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   int64_t dec = 0;
   if (decode_workspace_bytes(mm, &dec) != SWS_OK) return -1;
   int64_t pre = 0;
-  for (const EntryPlan& e : p->entries) pre = std::max(pre, prefill_bytes(max_m, e.cols));
+  for (const EntryPlan& e : p->entries)
+    if (e.dtype == SWS_E4M3) pre = std::max(pre, prefill_bytes(max_m, e.cols));
   return dec + split_region_bytes(p, mm) + 2 * pre;  // two buffers: quantiser k + 1 beside GEMM k
 }
 

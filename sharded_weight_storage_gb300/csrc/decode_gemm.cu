@@ -55,10 +55,23 @@ using namespace dec;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
-// Position of 16-byte activation unit u (8 f16 of k) in row m of a staged
-// slab: spreads the 4 units a thread reads, and neighbouring rows, over all
-// 32 banks.
-__device__ __forceinline__ int xpos(int u, int m) { return u ^ (((u >> 3) & 1) << 1) ^ (m & 1); }
+// Weight element types: WB = false for e4m3 codes (128 K per 128-byte slab
+// row, block scales), WB = true for bf16 weights (64 K per slab row, no
+// scales). Either way a slab row is 128 bytes, so the staging, the swizzle and
+// the TMA boxes are the same.
+template <bool WB>
+__host__ __device__ constexpr int slab_elems() { return WB ? 64 : 128; }
+
+// Position of 16-byte activation unit u (8 elements of k) in row m of a staged
+// slab: spreads the units a quarter-warp reads, and neighbouring rows, over all
+// 32 banks. e4m3 slabs have 16 units per row, bf16 slabs 8.
+template <bool WB>
+__device__ __forceinline__ int xpos(int u, int m) {
+  if constexpr (WB)
+    return u ^ (m & 7);
+  else
+    return u ^ (((u >> 3) & 1) << 1) ^ (m & 1);
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -68,11 +81,21 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-// ---- activation staging: bf16 global -> f16 shared, one 128-K slab --------
-template <int NT>
+// ---- activation staging: one slab of bf16 X -> shared (as f16 for e4m3
+// weights, as bf16 for bf16 weights) ------------------------------------------
+template <int NT, bool WB>
 struct XStage {
-  static constexpr int kUnits = NT * 8 * 16;  // 16-byte units per slab
+  static constexpr int kRowUnits = slab_elems<WB>() / 8;  // 16-byte units per row
+  static constexpr int kUnits = NT * 8 * kRowUnits;         // 16-byte units per slab
   static constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
   uint4 r[kPer];
 
@@ -80,8 +103,8 @@ struct XStage {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int v = tid + i * kThreads;
-      const int mrow = v >> 4, q = v & 15;
-      const int64_t k = kb * kSlabK + q * 8;
+      const int mrow = v / kRowUnits, q = v % kRowUnits;
+      const int64_t k = kb * slab_elems<WB>() + q * 8;
       uint4 val = make_uint4(0, 0, 0, 0);
       if (v < kUnits && mrow < m && k < e.cols)
         val = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)mrow * e.cols + k));
@@ -93,13 +116,15 @@ struct XStage {
     for (int i = 0; i < kPer; ++i) {
       const int v = tid + i * kThreads;
       if (v < kUnits) {
-        const int mrow = v >> 4, q = v & 15;
-        uint4 h;
-        h.x = bf16x2_to_f16x2(r[i].x);
-        h.y = bf16x2_to_f16x2(r[i].y);
-        h.z = bf16x2_to_f16x2(r[i].z);
-        h.w = bf16x2_to_f16x2(r[i].w);
-        xs[mrow * 16 + xpos(q, mrow)] = h;
+        const int mrow = v / kRowUnits, q = v % kRowUnits;
+        uint4 h = r[i];
+        if constexpr (!WB) {
+          h.x = bf16x2_to_f16x2(r[i].x);
+          h.y = bf16x2_to_f16x2(r[i].y);
+          h.z = bf16x2_to_f16x2(r[i].z);
+          h.w = bf16x2_to_f16x2(r[i].w);
+        }
+        xs[mrow * kRowUnits + xpos<WB>(q, mrow)] = h;
       }
     }
   }
@@ -110,8 +135,8 @@ struct XStage {
 // k = 32*tig + 16*l + [0, 16); the activation fragments come from units
 // 4*tig + 2*l and 4*tig + 2*l + 1 of each n-tile row.
 template <int NT, int R>
-__device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
-                                         int g, int tig) {
+__device__ __forceinline__ void mma_half_e4m3(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
+                                              int g, int tig) {
   uint32_t a[R][2][8];
 #pragma unroll
   for (int rt = 0; rt < R; ++rt)
@@ -131,8 +156,8 @@ __device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&w
   for (int nt = 0; nt < NT; ++nt) {
     const int mrow = nt * 8 + g;
     const int u = 4 * tig + 2 * l;
-    const uint4 b0 = xb[mrow * 16 + xpos(u, mrow)];
-    const uint4 b1 = xb[mrow * 16 + xpos(u + 1, mrow)];
+    const uint4 b0 = xb[mrow * 16 + xpos<false>(u, mrow)];
+    const uint4 b1 = xb[mrow * 16 + xpos<false>(u + 1, mrow)];
     const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
@@ -141,6 +166,32 @@ __device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&w
         mma16816(acc[rt][nt], a[rt][0][2 * kk], a[rt][1][2 * kk], a[rt][0][2 * kk + 1], a[rt][1][2 * kk + 1],
                  bw[2 * kk], bw[2 * kk + 1]);
   }
+}
+
+// bf16 weights: wq[rt][h] holds the 8 weights of row (g + 8h) of row tile rt
+// at k = 16*tig + 8*l + [0, 8); the activations come from unit 2*tig + l.
+template <int NT, int R>
+__device__ __forceinline__ void mma_half_bf16(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
+                                              int g, int tig) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int mrow = nt * 8 + g;
+    const uint4 b = xb[mrow * 8 + xpos<true>(2 * tig + l, mrow)];
+#pragma unroll
+    for (int rt = 0; rt < R; ++rt) {
+      mma16816_bf16(acc[rt][nt], wq[rt][0].x, wq[rt][1].x, wq[rt][0].y, wq[rt][1].y, b.x, b.y);
+      mma16816_bf16(acc[rt][nt], wq[rt][0].z, wq[rt][1].z, wq[rt][0].w, wq[rt][1].w, b.z, b.w);
+    }
+  }
+}
+
+template <int NT, int R, bool WB>
+__device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
+                                         int g, int tig) {
+  if constexpr (WB)
+    mma_half_bf16<NT, R>(acc, wq, xb, l, g, tig);
+  else
+    mma_half_e4m3<NT, R>(acc, wq, xb, l, g, tig);
 }
 
 template <int NT, int R>
@@ -289,14 +340,16 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
 // FUSED = false: weight slabs come from the views by TMA (thread 0 issues).
 // FUSED = true:  every thread copies 16-byte pieces straight from the chunks
 //                with cp.async into the same swizzled layout.
-template <int NT, int R, int S, bool FUSED>
+// WB: bf16 weights (no scales) instead of e4m3 codes with block scales.
+template <int NT, int R, int S, bool FUSED, bool WB>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kRowsWarp = 16 * R;
   constexpr int kRowsCta = kWarps * kRowsWarp;
   constexpr int kStage = kRowsCta * kSlabK;  // bytes of one staged weight slab
   constexpr int kBoxRows = kRowsCta > 256 ? 256 : kRowsCta;
   constexpr int kBoxes = kRowsCta / kBoxRows;
-  using XS = XStage<NT>;
+  using XS = XStage<NT, WB>;
+  constexpr int kElem = WB ? 2 : 1;  // bytes per weight
 
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(16) uint4 xs[2][XS::kUnits];
@@ -333,16 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // thread -> 16-byte column piece cu of rows rr, rr + 32, ...; byte
       // g = t_offset + o * cols + k of T lives in chunk g / C at g % C.
       const int cu = tid & 7;
+      const int64_t rowb = e.cols * kElem;  // bytes per weight row
       const int64_t k = up.kb * kSlabK + 16 * cu;
       const int64_t C = p.chunk_bytes;
-      int64_t gb = e.t_offset + (up.rbl * kRowsCta + (tid >> 3)) * e.cols + k;
+      int64_t gb = e.t_offset + (up.rbl * kRowsCta + (tid >> 3)) * rowb + k;
       int64_t ci = gb / C, off = gb - ci * C;
-      const int64_t step = 32 * e.cols;
+      const int64_t step = 32 * rowb;
 #pragma unroll 4
       for (int jr = 0; jr < kRowsCta / 32; ++jr) {
         const int rr = (tid >> 3) + 32 * jr;
         const int64_t o = up.rbl * kRowsCta + rr;
-        const bool valid = o < e.rows && k < e.cols;
+        const bool valid = o < e.rows && k < rowb;
         const uint8_t* src = p.chunks[valid ? ci : 0] + (valid ? off : 0);
         dev::cp_async16(dst + rr * kSlabK + ((cu ^ (rr & 7)) << 4), src, valid ? 16u : 0u);
         off += step;
@@ -377,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const UnitPos up = unit_pos(p, u0 + i);
     const DecodeEntry& e = p.e[up.j];
     const int64_t row0 = up.rbl * kRowsCta + warp * kRowsWarp;
+    if (WB) return row0 < e.rows ? 1.f : 0.f;
     return row0 < e.rows ? __ldg(e.scales + (row0 >> 7) * e.scale_cols + up.kb) : 0.f;
   };
   float sc_cur = scale_of(lane), sc_next = scale_of(32 + lane);
@@ -434,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             const int r = warp * kRowsWarp + rt * 16 + g + 8 * h;
             wq[rt][h] = *reinterpret_cast<const uint4*>(wb + r * kSlabK + (((2 * tig + l) ^ g) << 4));
           }
-        mma_half<NT, R>(acc, wq, xs[i & 1], l, g, tig);
+        mma_half<NT, R, WB>(acc, wq, xs[i & 1], l, g, tig);
       }
     }
     if (i + 1 < n) cx.store(xs[(i + 1) & 1], tid);
@@ -467,13 +522,13 @@ int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
 int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
-template <int NT, bool FUSED>
+template <int NT, bool FUSED, bool WB>
 cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int R = rows_per_warp_tiles<NT>();
   constexpr int S = stages_for<NT>();
   constexpr int kRowsCta = kWarps * 16 * R;
   constexpr int kSmem = S * kRowsCta * kSlabK + 1024;
-  auto kern = decode_kernel<NT, R, S, FUSED>;
+  auto kern = decode_kernel<NT, R, S, FUSED, WB>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
@@ -483,13 +538,17 @@ cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, int64_t grid_cap, cudaStream_t s) {
+template <bool WB>
+cudaError_t dispatch_w(const DecodeParams& p, int nt, bool fused, int64_t grid_cap, cudaStream_t s) {
   switch (nt) {
-    case 1: return fused ? launch_nt<1, true>(p, grid_cap, s) : launch_nt<1, false>(p, grid_cap, s);
-    case 2: return fused ? launch_nt<2, true>(p, grid_cap, s) : launch_nt<2, false>(p, grid_cap, s);
-    case 4: return fused ? launch_nt<4, true>(p, grid_cap, s) : launch_nt<4, false>(p, grid_cap, s);
-    default: return fused ? launch_nt<8, true>(p, grid_cap, s) : launch_nt<8, false>(p, grid_cap, s);
+    case 1: return fused ? launch_nt<1, true, WB>(p, grid_cap, s) : launch_nt<1, false, WB>(p, grid_cap, s);
+    case 2: return fused ? launch_nt<2, true, WB>(p, grid_cap, s) : launch_nt<2, false, WB>(p, grid_cap, s);
+    case 4: return fused ? launch_nt<4, true, WB>(p, grid_cap, s) : launch_nt<4, false, WB>(p, grid_cap, s);
+    default: return fused ? launch_nt<8, true, WB>(p, grid_cap, s) : launch_nt<8, false, WB>(p, grid_cap, s);
   }
+}
+cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s) {
+  return bf16_w ? dispatch_w<true>(p, nt, fused, grid_cap, s) : dispatch_w<false>(p, nt, fused, grid_cap, s);
 }
 
 // Validates a group and fills the kernel parameters, except the scratch
@@ -520,8 +579,9 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
       continue;
     }
     DecodeEntry& e = p.e[p.n_entries++];
-    if (!g.fused) {
-      int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols, std::min(256, rows_cta));
+    const int64_t elem = g.bf16_w ? 2 : 1;
+    if (!g.fused) {  // the weight as bytes: one 128-byte slab row is 128 e4m3 or 64 bf16 weights
+      int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols * elem, std::min(256, rows_cta));
       if (rc != SWS_OK) return rc;
     }
     e.xs = nullptr;
@@ -540,7 +600,7 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
     e.cols = it.cols;
     e.t_offset = it.t_offset;
     e.scale_cols = cdiv(it.cols, 128);
-    e.slabs = (int32_t)cdiv(it.cols, kSlabK);
+    e.slabs = (int32_t)cdiv(it.cols * elem, kSlabK);
     e.unit_begin = p.units;
     e.rb_begin = rb;
     const int64_t nrb = cdiv(it.rows, rows_cta);
@@ -656,7 +716,7 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   int64_t slabs = 0;
   for (int i = 0; i < g.n; ++i) slabs += cdiv(g.item[i].cols, kSlabK);
   const int64_t split = decode_split_bytes(g.m, slabs);  // the activation split region follows the partial sums
-  bool tc = decode_kernel_for(g.m) == kDecodeTc;
+  bool tc = !g.bf16_w && decode_kernel_for(g.m) == kDecodeTc;  // the tcgen05 kernel takes e4m3 weights
   const int64_t need = dec + (tc ? split : 0);
   if (g.workspace_bytes < need)
     return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);
@@ -681,7 +741,8 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   p.status = reinterpret_cast<int32_t*>(g.workspace);
   p.trace = g.trace;
   p.tag = g.tag | ((tc ? (g.fused ? kTraceTcFused : kTraceTc) : (g.fused ? kTraceMmaFused : kTraceMma)) << 48);
-  cudaError_t e = tc ? launch_decode_tc(p, g.fused, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, kMaxGrid, s);
+  cudaError_t e =
+      tc ? launch_decode_tc(p, g.fused, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, g.bf16_w, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 
@@ -783,6 +844,6 @@ extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t ro
   p.tag = 0;
   // Two partial slots per CTA must fit in the fixed array.
   const int64_t grid_cap = kNoAllocPartialBytes / (2 * slot_bytes_for(nt));
-  e = dispatch(p, nt, false, grid_cap, s);
+  e = dispatch(p, nt, false, false, grid_cap, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
 }

@@ -622,6 +622,180 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   }
 }
 
+// ---- BF16 weights --------------------------------------------------------------
+// Y = X W^T with bf16 X [M, K] and bf16 W [N, K], no scales: the whole K of a
+// tile accumulates in TMEM (tcgen05.mma kind::f16, 128 x 256 x 16), and the
+// tile is read out once. One CTA per 128 x 256 tile; a slab is 64 K (one
+// 128-byte row of each operand), 4 stages of 48 KB; the two TMEM buffers hold
+// consecutive tiles, so the read-out of tile t overlaps the MMAs of tile t+1.
+// 8 read-out warps: thread = tile row (TMEM lane), 128 columns each.
+constexpr int kBf16SlabK = 64;
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4)                     // D format: f32
+         | (1u << 7) | (1u << 10)      // A, B format: bf16
+         | ((uint32_t)(n >> 3) << 17)  // N / 8
+         | ((uint32_t)(m >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_bf16_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mdone;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int G = p.kslabs;  // 64-K slabs
+
+  if (threadIdx.x == 0) {
+    dev::trace_start(p.trace);
+    for (int s = 0; s < kStages; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      dev::mbar_init(&tfull[b], 1);
+      dev::mbar_init(&tempty[b], kEpiWarps);
+    }
+    dev::mbar_init(&mdone, 1);
+    dev::fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dev::smem_addr(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---- TMA producer ----------------------------------------------------
+    if (lane == 0) {
+      int64_t it = 0;
+      for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x) {
+        const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          const int s = (int)(it % kStages);
+          if (!dev::mbar_wait(&empty[s], (uint32_t)(((it / kStages) & 1) ^ 1), kWaitLimitNs)) {
+            set_abort(p, &s_abort);
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          dev::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          // x coordinates are in bytes of the [rows, 2K] byte view: 128 per slab
+          tma_load_2d(st, &p.tmap_x, kb * 128, mt * kBM, &full[s]);
+          tma_load_2d(st + kABytes, &p.tmap_w, kb * 128, nt * kBN, &full[s]);
+        }
+      }
+      for (int64_t k = it - kStages; k < it; ++k)
+        if (k >= 0) dev::mbar_wait(&full[(int)(k % kStages)], (uint32_t)((k / kStages) & 1), kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: a tile's slabs accumulate into TMEM buffer t % 2 -------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+      int64_t it = 0, t = 0;
+      bool issued = false;
+      for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x, ++t) {
+        const int buf = (int)(t & 1);
+        if (!dev::mbar_wait(&tempty[buf], (uint32_t)(((t >> 1) & 1) ^ 1), kWaitLimitNs)) {
+          set_abort(p, &s_abort);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < G && !s_abort; ++kb, ++it) {
+          const int s = (int)(it % kStages);
+          if (!dev::mbar_wait(&full[s], (uint32_t)((it / kStages) & 1), kWaitLimitNs)) {
+            set_abort(p, &s_abort);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = dev::smem_addr(smem + s * kStageBytes), b = a + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBf16SlabK / 16; ++kk)  // 16 K = 32 bytes per MMA
+            mma_bf16(tmem + buf * kBN, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
+                     (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+          issued = true;
+        }
+        if (s_abort) break;
+        mma_commit(&tfull[buf]);
+      }
+      if (issued) {
+        mma_commit(&mdone);
+        dev::mbar_wait(&mdone, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ---- read-out: thread = tile row, 128 columns ----------------------------
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
+    int64_t t = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x, ++t) {
+      const int buf = (int)(t & 1);
+      if (!dev::mbar_wait(&tfull[buf], (uint32_t)((t >> 1) & 1), kWaitLimitNs)) {
+        set_abort(p, &s_abort);
+        break;
+      }
+      tc_fence_after();
+      const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+      const int64_t m = (int64_t)mt * kBM + row;
+      const int64_t n0 = (int64_t)nt * kBN + h * 128;
+      const bool vec = (p.N & 7) == 0;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + buf * kBN + c * 16, v);
+        tmem_wait_ld();
+        const int64_t nc = n0 + c * 16;
+        if (m < p.M && nc < p.N) {
+          uint16_t* yp = p.y + m * p.N + nc;
+          uint32_t w[8];
+#pragma unroll
+          for (int t2 = 0; t2 < 8; ++t2) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * t2]), __uint_as_float(v[2 * t2 + 1]));
+            w[t2] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if (vec && nc + 16 <= p.N) {
+            reinterpret_cast<uint4*>(yp)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(yp)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            for (int i = 0; i < 16 && nc + i < p.N; ++i) yp[i] = (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&tempty[buf]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    dev::trace_end(p.trace, p.tag);
+  }
+}
+
 int g_prefill_kernel = kPrefillAuto;
 
 // Clusters of two prefill_pair_kernel CTAs that fit on the current device at
@@ -698,6 +872,43 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, pair ? "prefill pair kernel launch" : "prefill kernel launch");
+}
+
+int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s) {
+  if (a.m <= 0 || a.rows <= 0) return SWS_OK;
+  if (a.cols <= 0 || a.cols % 8 != 0)
+    return fail(SWS_E_UNSUPPORTED, "prefill: bf16 cols=%lld is not a positive multiple of 8", (long long)a.cols);
+  if (!aligned16(a.w) || !aligned16(a.xq) || !aligned16(a.y))
+    return fail(SWS_E_ALIGN, "prefill: pointer not 16-byte aligned");
+  PrefillParams p;
+  // bf16 rows as bytes: 128-byte boxes (64 K) of [rows, 2K] byte tensors
+  int rc = encode_u8_tile_map(&p.tmap_x, a.xq, a.m, 2 * a.cols, kBM);
+  if (rc != SWS_OK) return rc;
+  rc = encode_u8_tile_map(&p.tmap_w, a.w, a.rows, 2 * a.cols, kBN);
+  if (rc != SWS_OK) return rc;
+  p.ex = nullptr;
+  p.sw = nullptr;
+  p.y = a.y;
+  p.M = a.m;
+  p.N = a.rows;
+  p.K = a.cols;
+  p.kslabs = (int32_t)cdiv(a.cols, kBf16SlabK);
+  p.m_tiles = (int32_t)cdiv(a.m, kBM);
+  p.n_tiles = (int32_t)cdiv(a.rows, kBN);
+  p.status = a.status;
+  p.trace = a.trace;
+  p.tag = a.tag;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (bf16)");
+  const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+  const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
+  prefill_bf16_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill bf16 kernel launch");
 }
 
 }  // namespace sws

@@ -108,6 +108,7 @@ struct DecodeGroup {
   int32_t n = 0;
   int64_t m = 0;
   bool fused = false;
+  bool bf16_w = false;  // every item's weight is bf16 (no scales) instead of e4m3 codes
   const uint8_t* chunks[256];
   int32_t n_chunks = 0;
   int64_t chunk_bytes = 0;
@@ -144,6 +145,9 @@ struct PrefillLaunch {
 enum PrefillKernel { kPrefillAuto = 0, kPrefillSingle = 1, kPrefillPair = 2 };
 void set_prefill_kernel(int k);
 int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
+// bf16 weights: `xq` is the bf16 activation X [m, cols] itself, `w` bf16
+// [rows, cols]; ex and scales are unused.
+int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s);
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);
 

@@ -46,14 +46,25 @@ class ShardedStack:
                    stream: Optional[torch.cuda.Stream] = None):
         """codes[j]: full weight bytes of entry j (host or device, uint8 [rows,
         cols*elem]); they are cut into the loader's 1/N row shards on the device
-        and relaid into this layer's chunks by the relayout kernel."""
+        and relaid into this layer's chunks by the relayout kernel.
+        scales[j]: float32 block scales [ceil(rows/128), ceil(cols/128)] of an
+        E4M3 entry, or one number - a per-tensor scale (ModelOpt FP8), kept
+        replicated outside T and stored as that grid filled with it; absent for
+        BF16 entries."""
         n = self.n_shards
         shard_ptrs, keep = [], []
         for j in self.layer_entries(layer):
             off, nbytes, sharded = self.entry_info[j]
             w = codes[j].to(self.device, non_blocking=False).contiguous()
-            if scales.get(j) is not None:
-                self.scales[j] = scales[j].to(self.device, dtype=torch.float32).contiguous()
+            sc = scales.get(j)
+            if sc is not None:
+                _, _, rows, cols = self.entries[j]
+                grid = (-(-rows // 128), -(-cols // 128))
+                if not torch.is_tensor(sc):
+                    sc = torch.tensor(sc, dtype=torch.float32)
+                if sc.numel() == 1 and tuple(sc.shape) != grid:
+                    sc = torch.full(grid, float(sc.reshape(-1)[0]), dtype=torch.float32)
+                self.scales[j] = sc.to(self.device, dtype=torch.float32).contiguous()
             if not sharded:
                 self.replicated[j] = w
                 continue

@@ -1,0 +1,198 @@
+"""Weight variants of the blog's quantisation section (section "加载：行 shard
+先行，finalize 再重排", the variants list): BF16 weights go through the same flat
+layout and are used without scales; ModelOpt FP8 keeps one per-tensor scale,
+replicated outside T. Checked against the CPU oracle (linear_bf16,
+linear_per_tensor) on decode (m <= 64, slot and chunk-map reads) and prefill
+sizes, with the kernel that ran read from the trace tag (bits 48..55)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as WL
+from helpers import assert_close, bf16_tensor_to_f64
+
+pytestmark = pytest.mark.gpu
+
+KERNEL_MMA, KERNEL_MMA_FUSED, KERNEL_PREFILL = 1, 2, 5
+
+
+@pytest.fixture(scope="module")
+def S(swslib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return swslib
+
+
+def _as_bytes(bits):
+    """bf16 bit patterns [rows, cols] -> the weight's bytes [rows, 2 * cols]."""
+    return np.ascontiguousarray(bits).view(np.uint8).reshape(bits.shape[0], -1)
+
+
+def _stack(S, shapes, n, weights, scales=None, max_m=64):
+    """shapes: (layer, dtype, rows, cols); weights[j]: uint8 bytes [rows, cols * elem]."""
+    from sharded_weight_storage_gb300.storage import ShardedStack
+    st = ShardedStack(shapes, n, max_m=max_m)
+    for l in sorted({s[0] for s in shapes}):
+        js = [j for j, s in enumerate(shapes) if s[0] == l]
+        st.load_layer(l, {j: torch.from_numpy(weights[j]) for j in js},
+                      {j: scales[j] for j in js if scales and j in scales})
+    st.make_ctx()
+    return st
+
+
+def _linear_traced(st, j, src, x, m):
+    rec = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
+    st.ctx.trace_begin(rec.data_ptr(), 4, 0)
+    _, _, rows, _ = st.entries[j]
+    y = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st.ctx.linear(j, src, x.data_ptr(), m, y.data_ptr(), 0)
+    torch.cuda.synchronize()
+    n = st.ctx.trace_count()
+    st.ctx.trace_begin(0, 0, 0)
+    tags = [int(t) for t in rec.view(4, 4)[:n, 0].tolist()]
+    kinds = [(t >> 48) & 0xFF for t in tags if (t >> 56) == 2]
+    return y, kinds
+
+
+def _x64(x):
+    return WL.bf16_to_f64(WL.bf16_bits(x.cpu()))
+
+
+# N = 4. Entry 0 (333 rows) is replicated (333 % 4 != 0); chunk boundaries fall
+# inside rows of entries 1 and 2; cols 208 leaves a partial 64-K slab.
+SHAPES = [(0, 1, 333, 208), (0, 1, 1000, 1040), (0, 1, 256, 64), (0, 1, 512, 208)]
+
+
+@pytest.fixture(scope="module")
+def bf16_stack(S):
+    assert S.BF16 == 1
+    bits = [WL.draw_weight_bf16(61, 0, j, r, c) for j, (_, _, r, c) in enumerate(SHAPES)]
+    st = _stack(S, SHAPES, 4, [_as_bytes(b) for b in bits], max_m=1000)
+    st.ctx.gather_to_slot(0, 0, 0)
+    return st, bits
+
+
+@pytest.mark.parametrize("m", [1, 8, 17, 40, 64])
+def test_bf16_decode_matches_oracle(S, bf16_stack, m):
+    st, bits = bf16_stack
+    for j, (_, _, r, c) in enumerate(SHAPES):
+        x = WL.draw_x(62, j, m, c).cuda()
+        y, kinds = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+        assert kinds == [KERNEL_MMA]
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m}")
+    assert st.ctx.status() == 0
+
+
+@pytest.mark.parametrize("m", [1, 33])
+def test_bf16_decode_through_the_chunk_map(S, bf16_stack, m):
+    st, bits = bf16_stack
+    for j in (1, 2, 3):  # sharded entries
+        _, _, r, c = SHAPES[j]
+        x = WL.draw_x(63, j, m, c).cuda()
+        y, kinds = _linear_traced(st, j, S.SRC_FUSED, x, m)
+        assert kinds == [KERNEL_MMA_FUSED]
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m} (fused)")
+
+
+@pytest.mark.parametrize("m", [3, 200])
+def test_bf16_one_hot_gives_the_weight_exactly(S, bf16_stack, m):
+    # x = e_i picks column i of W: one product, exact in fp32, then rounded to
+    # bf16, which the bf16 weight already is.
+    st, bits = bf16_stack
+    rng = np.random.default_rng(m)
+    for j in (1, 3):
+        _, _, r, c = SHAPES[j]
+        cols = rng.integers(0, c, size=m)
+        xo = torch.zeros((m, c), dtype=torch.bfloat16)
+        xo[np.arange(m), torch.from_numpy(cols)] = 1.0
+        y, _ = _linear_traced(st, j, S.SRC_SLOT0, xo.cuda(), m)
+        want = bits[j][:, cols].T.astype(np.uint16)
+        assert np.array_equal(WL.bf16_bits(y.cpu()), want), f"entry {j}"
+
+
+@pytest.mark.parametrize("m", [65, 300, 1000])
+def test_bf16_prefill_matches_oracle(S, bf16_stack, m):
+    st, bits = bf16_stack
+    for j, (_, _, r, c) in enumerate(SHAPES):
+        x = WL.draw_x(64, j, m, c).cuda()
+        y, kinds = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+        assert kinds == [KERNEL_PREFILL]
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m}")
+    assert st.ctx.status() == 0
+
+
+@pytest.mark.parametrize("m", [8, 200])
+def test_mixed_layer_linears(S, m):
+    # One layer with E4M3 and BF16 linears: the grouped decode launches (one
+    # per weight type) and the prefill layer (quantiser only for E4M3).
+    shapes = [(0, S.E4M3, 512, 256), (0, S.BF16, 256, 512), (0, S.E4M3, 256, 384), (0, S.BF16, 384, 128)]
+    rng = np.random.default_rng(7 + m)
+    weights, scales, ref_w = {}, {}, {}
+    for j, (_, dt, r, c) in enumerate(shapes):
+        if dt == S.E4M3:
+            q, sc = WL.draw_weight(65, 0, j, r, c)
+            weights[j], scales[j] = q, torch.from_numpy(sc)
+            ref_w[j] = (q, sc)
+        else:
+            b = WL.draw_weight_bf16(65, 0, j, r, c)
+            weights[j], ref_w[j] = _as_bytes(b), b
+    st = _stack(S, shapes, 4, weights, scales, max_m=max(m, 64))
+    st.ctx.gather_to_slot(0, 1, 0)
+    xs = [WL.draw_x(66, j, m, c).cuda() for j, (_, _, r, c) in enumerate(shapes)]
+    ys = [torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda") for (_, _, r, c) in shapes]
+    st.ctx.layer_linears(0, S.SRC_SLOT1, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
+    torch.cuda.synchronize()
+    for j, (_, dt, r, c) in enumerate(shapes):
+        xf = _x64(xs[j])
+        if dt == S.E4M3:
+            if m > 64:
+                xq, ex = O.quantize_x(xf)
+                ref = O.dequant_x(xq, ex) @ O.dequant(*ref_w[j]).T
+            else:
+                ref = O.linear(xf, *ref_w[j])
+        else:
+            ref = O.linear_bf16(xf, ref_w[j])
+        assert_close(bf16_tensor_to_f64(ys[j]), ref, f"entry {j} m {m}")
+    assert st.ctx.status() == 0
+
+
+def test_bf16_run_layers(S):
+    shapes = [(l, S.BF16, r, c) for l in range(3) for (r, c) in ((512, 256), (256, 512))]
+    bits = [WL.draw_weight_bf16(67, l, j, r, c) for j, (l, _, r, c) in enumerate(shapes)]
+    st = _stack(S, shapes, 4, [_as_bytes(b) for b in bits])
+    m = 8
+    xs = {j: WL.draw_x(68, j, m, c).cuda() for j, (_, _, r, c) in enumerate(shapes)}
+    ys = {j: torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda")
+          for j, (_, _, r, c) in enumerate(shapes)}
+    io = [([xs[j].data_ptr() for j in st.layer_entries(l)], [ys[j].data_ptr() for j in st.layer_entries(l)], m)
+          for l in range(3)]
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    for flags in (0, S.RUN_FUSED):
+        st.ctx.run_layers(0, 2, io, flags, main.cuda_stream, side.cuda_stream)
+        main.synchronize()
+        for j in ys:
+            assert_close(bf16_tensor_to_f64(ys[j]), O.linear_bf16(_x64(xs[j]), bits[j]), f"entry {j} flags {flags}")
+    assert st.ctx.status() == 0
+
+
+@pytest.mark.parametrize("m", [8, 100])
+def test_per_tensor_fp8_scale(S, m):
+    # ModelOpt FP8: one float32 scale for the whole weight, replicated outside T.
+    shapes = [(0, S.E4M3, 384, 256), (0, S.E4M3, 256, 384)]
+    rng = np.random.default_rng(69)
+    codes = [rng.integers(0, 0x7E, size=(r, c), dtype=np.uint8) | (rng.integers(0, 2, size=(r, c), dtype=np.uint8) << 7)
+             for (_, _, r, c) in shapes]
+    sc = [0.0123, 0.5]
+    st = _stack(S, shapes, 4, codes, {0: sc[0], 1: torch.tensor([sc[1]])}, max_m=max(m, 64))
+    st.ctx.gather_to_slot(0, 0, 0)
+    for j, (_, _, r, c) in enumerate(shapes):
+        x = WL.draw_x(70, j, m, c).cuda()
+        y, _ = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+        xf = _x64(x)
+        if m > 64:
+            xq, ex = O.quantize_x(xf)
+            ref = O.linear_per_tensor(O.dequant_x(xq, ex), codes[j], sc[j])
+        else:
+            ref = O.linear_per_tensor(xf, codes[j], sc[j])
+        assert_close(bf16_tensor_to_f64(y), ref, f"entry {j} m {m}")
