@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--prefill-layers", type=int, default=8, help="layers of the prefill run (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the KDA-layer and tiny-layer decode sections")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-weight section")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
     ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill"],
@@ -613,6 +614,102 @@ def run_decode_config(args, dist, w, relayout: bool):
     return out
 
 
+def run_bf16(args, dist):
+    """BF16 weights (the unquantised variant): the shared-expert layer's two
+    linears as bf16 (|T| = 528 MB, N = 16): gather, decode linears (slot and
+    chunk-map) at each m, weight GB/s against the HBM peak; and the prefill
+    GEMM on one KDA-like [12288, 7168] bf16 linear at m = 8192 against the
+    bf16 tensor peak. Weights are drawn on the device (seeded)."""
+    import torch
+
+    import sharded_weight_storage_gb300 as S
+    import sharded_weight_storage_gb300._lib as L
+    import workloads as WL
+    from sharded_weight_storage_gb300.storage import ShardedStack
+
+    dev = torch.device("cuda", dist.local)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20260)
+
+    def weight(rows, cols):
+        w = torch.randn((rows, cols), generator=gen, device=dev, dtype=torch.float32).mul_(0.02)
+        return w.to(torch.bfloat16).view(torch.uint8)
+
+    w = WL.SHARED_EXPERT
+    ents = [(0, e.rows, e.cols) for e in w.entries]
+    st = ShardedStack([(0, S.BF16, r, c) for (_, r, c) in ents], w.n_shards, max_m=64, device=str(dev))
+    st.load_layer(0, {j: weight(r, c) for j, (_, r, c) in enumerate(ents)}, {})
+    ctx = st.make_ctx()
+    total = st.layout[0][0]
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty(1024, dtype=torch.float32, device=dev)
+    hbm, _ = peaks()
+
+    def timed(fn, reps=20, flush=True):
+        out = []
+        for _ in range(reps):
+            if flush:
+                torch.amax(scratch.view(1024, -1), dim=1, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            out.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) for a, b in out])
+
+    out = {"workload": f"shared_expert_layer with bf16 weights: |T| = {total} B, N = {w.n_shards}",
+           "kernel": "decode_kernel (mma.sync, bf16 operands)", "per_m": {}}
+    with torch.cuda.stream(stream):
+        ctx.gather_to_slot(0, 0, sp)
+        g_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp))
+        out["gather"] = {"us": g_ms * 1e3, "GBps": 2 * total / g_ms / 1e6}
+        for m in (1, 8, 32, 64):
+            xs = [WL.draw_x(w.key, j, m, c).to(dev) for j, (_, r, c) in enumerate(ents)]
+            ys = [torch.empty((m, r), dtype=torch.bfloat16, device=dev) for (_, r, c) in ents]
+            lins = lambda src: ctx.layer_linears(0, src, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys],
+                                                 m, sp)
+            for _ in range(3):
+                lins(S.SRC_SLOT0)
+                lins(S.SRC_FUSED)
+            wb = sum(2 * r * c for (_, r, c) in ents)
+            lb = wb + sum(2 * m * (r + c) for (_, r, c) in ents)
+            slot_ms = timed(lambda: lins(S.SRC_SLOT0))
+            fused_ms = timed(lambda: lins(S.SRC_FUSED))
+            out["per_m"][m] = {
+                "slot_linears_us": slot_ms * 1e3, "slot_linears_GBps": lb / slot_ms / 1e6,
+                "slot_frac_of_hbm": lb / slot_ms / 1e6 / hbm,
+                "fused_linears_us": fused_ms * 1e3, "fused_linears_GBps": lb / fused_ms / 1e6,
+            }
+    assert ctx.status() == 0
+    del st, ctx
+    torch.cuda.empty_cache()
+    # prefill
+    rows, cols, m = 12288, 7168, 8192
+    st = ShardedStack([(0, S.BF16, rows, cols)], 8, max_m=m, device=str(dev))
+    st.load_layer(0, {0: weight(rows, cols)}, {})
+    ctx = st.make_ctx()
+    bf16_burst = fp8_peak()[0] / 2
+    with torch.cuda.stream(stream):
+        ctx.gather_to_slot(0, 0, sp)
+        x = torch.randn((m, cols), generator=gen, device=dev).to(torch.bfloat16)
+        y = torch.empty((m, rows), dtype=torch.bfloat16, device=dev)
+        call = lambda: ctx.linear(0, S.SRC_SLOT0, x.data_ptr(), m, y.data_ptr(), sp)
+        call()
+        t = timed(call, reps=5)
+    fl = 2.0 * m * rows * cols
+    out["prefill"] = {"linear": f"[{rows}, {cols}] bf16 at m = {m}", "kernel": "prefill_bf16_kernel (tcgen05 kind::f16)",
+                      "us": t * 1e3, "TFLOPS": fl / t / 1e9, "frac_of_bf16_peak": fl / t / 1e9 / bf16_burst,
+                      "bf16_peak_tflops": bf16_burst}
+    assert ctx.status() == 0
+    del st, ctx, x, y
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill(args, dist, n_layers):
     """Prefill on the KDA-layer weights (N = 8): per-linear tcgen05 GEMM
     throughput at M = 2048 and 8192, whole-layer time, and lookahead over
@@ -880,6 +977,7 @@ def main():
         configs = {"attn_kda_layer": run_decode_config(args, dist, WL.ATTN_KDA, relayout=True),
                    "tiny_flat_layer": run_decode_config(args, dist, WL.TINY, relayout=True)}
     prefill = run_prefill(args, dist, args.prefill_layers) if args.prefill_layers > 0 else None
+    bf16 = run_bf16(args, dist) if not args.no_bf16 else None
     if dist.rank != 0:
         dist.close()
         return
@@ -921,6 +1019,7 @@ def main():
         "lookahead_stack": stack,
         "decode_configs": configs,
         "prefill": prefill,
+        "bf16_weights": bf16,
         "weight_GBps_step": total / ms_step / 1e6,
     }
     if dist.world == 1 and not args.no_cpu_baseline:
