@@ -278,6 +278,11 @@ int32_t sws_trace_count(const sws_ctx* ctx);
 #define SWS_PREFILL_SINGLE 1     /* one CTA per 128 x 256 output tile */
 #define SWS_PREFILL_PAIR 2       /* a cluster of two CTAs (tcgen05 .cta_group::2) per 256 x 256 tile;
                                     SWS_E_UNSUPPORTED at launch if no such cluster fits */
+#define SWS_OPT_GATHER_ENGINE 3 /* what copies the chunks into a slot (sws_gather_to_slot, run_layers) */
+#define SWS_GATHER_TMA 0        /* default: the TMA bulk-copy kernel (uses SMs, writes a trace record) */
+#define SWS_GATHER_COPY_ENGINE 1 /* N cudaMemcpyAsync device-to-device copies of C bytes on the stream:
+                                    the copy engines move the bytes and no SM is used (the pages'
+                                    all-gather runs on copy engines too); no trace record */
 /* Process-wide options, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance; chunk-map (fused) reads
  * always use the mma.sync kernel. A tcgen05 launch is three kernels on the

@@ -273,6 +273,39 @@ def linear_per_tensor(x: np.ndarray, codes: np.ndarray, scale: float) -> np.ndar
     return np.asarray(x, dtype=np.float64) @ (e4m3_decode(codes) * float(np.float32(scale))).T
 
 
+# Shared-expert chain (the second workload shape): gate_up -> SiLU(gate) * up
+# -> down, with bf16 tensors between the steps.
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Nearest bfloat16 value of each float64 (8 significant bits), ties to the
+    even significand; results beyond the largest finite bf16 become infinity."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros_like(v)
+    fin = np.isfinite(v) & (v != 0)
+    f, p = np.frexp(np.abs(v[fin]))          # |v| = f * 2^p, f in [0.5, 1)
+    p = np.maximum(p, -125)                  # below 2^-126 the spacing stays 2^-133
+    scaled = np.ldexp(np.abs(v[fin]), 8 - p)  # the significand as a number in [128, 256)
+    r = np.floor(scaled)
+    frac = scaled - r
+    up = (frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1))
+    r = r + up
+    mag = np.ldexp(r, p - 8)
+    mag = np.where(mag > (2 - 2.0 ** -7) * 2.0 ** 127, np.inf, mag)
+    out[fin] = np.sign(v[fin]) * mag
+    out[~np.isfinite(v)] = v[~np.isfinite(v)]
+    return out
+
+
+def silu_mul(gu: np.ndarray) -> np.ndarray:
+    """act[m, j] = silu(g[m, j]) * u[m, j] with gu = [g | u] ([m, 2F], the gate
+    half first) and silu(g) = g / (1 + e^-g), in float64."""
+    gu = np.asarray(gu, dtype=np.float64)
+    f = gu.shape[1] // 2
+    g, u = gu[:, :f], gu[:, f:]
+    return g / (1.0 + np.exp(-g)) * u
+
+
 def quantize_x(x: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     """Prefill activation quantiser: for each row and each 128-column group,
     e = 2^k with k the smallest integer such that amax <= 448 * 2^k (e = 1 when

@@ -69,6 +69,8 @@ int ensure_events(sws_ctx* c, size_t n) {
   return SWS_OK;
 }
 
+int g_gather_engine = SWS_GATHER_TMA;
+
 int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   const sws_plan* p = c->plan;
   const LayerPlan& lp = p->layers[layer];
@@ -82,6 +84,14 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   }
   g.chunk_bytes = lp.chunk;
   g.dst = c->slot[slot];
+  if (g_gather_engine == SWS_GATHER_COPY_ENGINE) {  // slot[i*C : (i+1)*C] = chunk i, by the copy engines
+    for (int i = 0; i < g.n; ++i) {
+      cudaError_t e = cudaMemcpyAsync(g.dst + (int64_t)i * lp.chunk, g.chunks[i], (size_t)lp.chunk,
+                                      cudaMemcpyDeviceToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, "gather: cudaMemcpyAsync");
+    }
+    return SWS_OK;
+  }
   g.status = status_word(c);
   g.trace = next_trace(c);
   g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
@@ -611,6 +621,11 @@ int sws_set_option(int32_t option, int64_t value) {
       if (value < SWS_PREFILL_AUTO || value > SWS_PREFILL_PAIR)
         return fail(SWS_E_INVALID, "set_option: prefill kernel %lld", (long long)value);
       set_prefill_kernel((int)value);
+      return SWS_OK;
+    case SWS_OPT_GATHER_ENGINE:
+      if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE)
+        return fail(SWS_E_INVALID, "set_option: gather engine %lld", (long long)value);
+      g_gather_engine = (int)value;
       return SWS_OK;
     default:
       return fail(SWS_E_INVALID, "set_option: unknown option %d", option);

@@ -400,6 +400,42 @@ def test_linear_per_tensor_is_block_linear_with_a_constant_grid():
 
 
 # ---------------------------------------------------------------------------
+# shared-expert chain: bf16 rounding, SiLU * up
+# ---------------------------------------------------------------------------
+
+
+def test_bf16_round_closed_forms():
+    cases = {1.0: 1.0, 1 + 2.0 ** -8: 1.0, 1 + 3 * 2.0 ** -8: 1 + 2.0 ** -6, 1 + 2.0 ** -8 + 2.0 ** -30: 1 + 2.0 ** -7,
+             -(1 + 2.0 ** -7 + 2.0 ** -8): -(1 + 2.0 ** -6), 2.0 ** -133: 2.0 ** -133, 2.0 ** -135: 0.0,
+             3 * 2.0 ** -135: 2.0 ** -133, 0.0: 0.0, 3.38e38: (2 - 2.0 ** -7) * 2.0 ** 127}
+    for v, want in cases.items():
+        assert O.bf16_round(np.array([v]))[0] == want, v
+    assert np.isinf(O.bf16_round(np.array([3.4e38 * 1.01]))[0])
+
+
+def test_bf16_round_matches_torch_on_float32_values():
+    rng = np.random.default_rng(41)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        rng.standard_normal(2000) * 1e-39]).astype(np.float32)
+    t = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(v.astype(np.float64)), t)
+
+
+def test_silu_mul_closed_forms_and_half_order():
+    ln3 = np.log(3.0)
+    gu = np.array([[0.0, ln3, -ln3, 40.0, -40.0, 2.0, 2.0, 2.0, 2.0, 1.5]])  # g | u, F = 5
+    a = O.silu_mul(gu)[0]
+    assert a[0] == 0.0                                   # silu(0) = 0 whatever u is
+    assert abs(a[1] - 0.75 * ln3 * 2.0) < 1e-15          # sigmoid(ln 3) = 3/4
+    assert abs(a[2] - (-0.25 * ln3) * 2.0) < 1e-15       # sigmoid(-ln 3) = 1/4
+    assert abs(a[3] - 40.0 * 2.0) < 1e-12                # silu(x) -> x
+    assert abs(a[4]) < 1e-15                             # silu(-x) -> 0
+    # swapping the halves (silu on the up half) would give silu(2) * 0 = 0 for column 0
+    assert O.silu_mul(np.array([[1.0, 0.0]]))[0, 0] == 0.0 and O.silu_mul(np.array([[0.0, 1.0]]))[0, 0] == 0.0
+    assert abs(O.silu_mul(np.array([[1.0, 1.0]]))[0, 0] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-16
+
+
+# ---------------------------------------------------------------------------
 # prefill activation quantiser
 # ---------------------------------------------------------------------------
 
