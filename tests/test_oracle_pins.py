@@ -407,7 +407,7 @@ def test_linear_per_tensor_is_block_linear_with_a_constant_grid():
 def test_bf16_round_closed_forms():
     cases = {1.0: 1.0, 1 + 2.0 ** -8: 1.0, 1 + 3 * 2.0 ** -8: 1 + 2.0 ** -6, 1 + 2.0 ** -8 + 2.0 ** -30: 1 + 2.0 ** -7,
              -(1 + 2.0 ** -7 + 2.0 ** -8): -(1 + 2.0 ** -6), 2.0 ** -133: 2.0 ** -133, 2.0 ** -135: 0.0,
-             3 * 2.0 ** -135: 2.0 ** -133, 0.0: 0.0, 3.38e38: (2 - 2.0 ** -7) * 2.0 ** 127}
+             3 * 2.0 ** -135: 2.0 ** -133, 0.0: 0.0, 3.39e38: (2 - 2.0 ** -7) * 2.0 ** 127}
     for v, want in cases.items():
         assert O.bf16_round(np.array([v]))[0] == want, v
     assert np.isinf(O.bf16_round(np.array([3.4e38 * 1.01]))[0])
