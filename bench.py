@@ -362,6 +362,35 @@ def run_ours(args, dist):
             ctx.gather_to_slot(0, 0, sp)
         g_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp), reps)
         results["gather_alone"] = {"us": g_ms * 1e3, "GBps": 2 * total / g_ms / 1e6}
+        # the same gather by the copy engines (N cudaMemcpyAsync, no SMs)
+        S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_COPY_ENGINE)
+        for _ in range(3):
+            ctx.gather_to_slot(0, 0, sp)
+        ce_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp), reps)
+        S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
+        results["gather_copy_engine"] = {"us": ce_ms * 1e3, "GBps": 2 * total / ce_ms / 1e6}
+        # shared-expert chain: gate_up -> SiLU(gate) * up -> down at each m
+        f = ents[0][1] // 2
+        chain = {}
+        for m in w.m_values:
+            gu = torch.empty((m, ents[0][1]), dtype=torch.bfloat16, device=dev)
+            act = torch.empty((m, f), dtype=torch.bfloat16, device=dev)
+            yd = torch.empty((m, ents[1][1]), dtype=torch.bfloat16, device=dev)
+
+            def run_chain(src, m=m, gu=gu, act=act, yd=yd):
+                ctx.linear(0, src, xs[m][0].data_ptr(), m, gu.data_ptr(), sp)
+                S.silu_mul(gu.data_ptr(), m, f, act.data_ptr(), sp)
+                ctx.linear(1, src, act.data_ptr(), m, yd.data_ptr(), sp)
+
+            for _ in range(3):
+                run_chain(S.SRC_SLOT0)
+                run_chain(S.SRC_FUSED)
+            c_ms = timed(lambda: run_chain(S.SRC_SLOT0), reps)
+            cf_ms = timed(lambda: run_chain(S.SRC_FUSED), reps)
+            a_ms = timed(lambda: S.silu_mul(gu.data_ptr(), m, f, act.data_ptr(), sp), reps)
+            chain[m] = {"slot_us": c_ms * 1e3, "fused_us": cf_ms * 1e3, "silu_mul_us": a_ms * 1e3,
+                        "silu_mul_GBps": 8 * m * f / a_ms / 1e6, "weight_GBps_slot": total / c_ms / 1e6}
+        results["shared_expert_chain"] = chain
         for m in w.m_values:
             wb, scb, actb = layer_bytes(ents, m)
             lin_bytes = wb + scb + actb
@@ -501,6 +530,17 @@ def run_stack(args, dist, n_layers):
     fused_ms = dist.max(steps(k, S.RUN_FUSED))
     graph_ms = dist.max(graph_steps(k, 0))
     graph_fused_ms = dist.max(graph_steps(k, S.RUN_FUSED))
+    # the lookahead with the gather on the copy engines (no SMs taken from the linears)
+    S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_COPY_ENGINE)
+    steps(1, 0)
+    ce_ms = dist.max(steps(k, 0))
+    ce_exposed = []
+    for _ in range(3):
+        ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
+        ce_exposed.append(ctx.run_timing(n_layers)[0])
+    torch.cuda.synchronize()
+    S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
+    ce_ex = [statistics.median(v[l] for v in ce_exposed) for l in range(n_layers)]
     exposed, layer_ms = [], []
     for _ in range(3):
         ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
@@ -519,6 +559,8 @@ def run_stack(args, dist, n_layers):
         "step_ms": slot_ms, "per_layer_us": slot_ms * 1e3 / n_layers,
         "fused_step_ms": fused_ms, "fused_per_layer_us": fused_ms * 1e3 / n_layers,
         "graph_step_ms": graph_ms, "graph_per_layer_us": graph_ms * 1e3 / n_layers,
+        "copy_engine_gather_step_ms": ce_ms, "copy_engine_gather_per_layer_us": ce_ms * 1e3 / n_layers,
+        "copy_engine_exposed_gather_us_per_layer": 1e3 * statistics.mean(ce_ex[1:]) if n_layers > 1 else 1e3 * ce_ex[0],
         "graph_fused_step_ms": graph_fused_ms, "graph_fused_per_layer_us": graph_fused_ms * 1e3 / n_layers,
         "exposed_gather_us_per_layer": 1e3 * statistics.mean(ex[1:]) if n_layers > 1 else 1e3 * ex[0],
         "exposed_gather_first_layer_us": 1e3 * ex[0],
@@ -1015,6 +1057,8 @@ def main():
         "exposed_gather_us_per_layer": stack["exposed_gather_us_per_layer"] if stack else None,
         "kernels": kernels,
         "gather_alone": r["gather_alone"],
+        "gather_copy_engine": r["gather_copy_engine"],
+        "shared_expert_chain": r["shared_expert_chain"],
         "per_m": r["per_m"],
         "lookahead_stack": stack,
         "decode_configs": configs,

@@ -156,8 +156,9 @@ void sws_ctx_destroy(sws_ctx* ctx);
 
 /* One layer's gather (blog "flat layout" step 3, all_gather_into_tensor):
  * slot[i*C : (i+1)*C] = chunk(layer, i) for i in [0, N), a pure byte copy on
- * `stream` by a TMA bulk-copy kernel. Tags the slot with `layer` (host-side,
- * in issue order). */
+ * `stream`, by the TMA bulk-copy kernel or, with SWS_OPT_GATHER_ENGINE =
+ * SWS_GATHER_COPY_ENGINE, by N cudaMemcpyAsync copies. Tags the slot with
+ * `layer` (host-side, in issue order). */
 int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 
 /* Y = X W_j^T for entry j (blog section "核心抽象": the GEMM sees the full W),
@@ -247,6 +248,14 @@ int sws_run_timing(sws_ctx* ctx, float* exposed_ms, float* layer_ms, int32_t n);
  * (ties to even, saturating). x bf16 [m, k] row-major, xq u8 [m, k],
  * ex float32 [m, ceil(k/128)]; k % 16 == 0. */
 int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws_stream_t stream);
+
+/* SiLU(gate) * up, the step between a shared expert's two linears (gate_up ->
+ * SiLU * up -> down; the blog's shared-expert layer, the second workload):
+ *   act[m, j] = bf16_rne( g / (1 + e^-g) * u ),  g = gu[m, j], u = gu[m, f + j],
+ * computed in fp32. gu bf16 [m, 2f] row-major with the gate half first (the
+ * gate_up linear's output), act bf16 [m, f]; f % 8 == 0, both 16-byte aligned
+ * (else SWS_E_UNSUPPORTED / SWS_E_ALIGN). Runs on `stream`. */
+int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t stream);
 
 /* Device-side status of a context: 0, or the SWS_E_* code a kernel recorded
  * (e.g. SWS_E_TIMEOUT when a wait on a TMA completion gave up). Synchronises

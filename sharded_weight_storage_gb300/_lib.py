@@ -67,6 +67,7 @@ _PROTOS = [
                                  C.c_void_p]),
     ("sws_run_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32]),
     ("sws_quantize_x", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
+    ("sws_silu_mul", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
     ("sws_trace_count", C.c_int32, [C.c_void_p]),
@@ -174,6 +175,11 @@ def set_option(option: int, value: int):
 def quantize_x(x: int, m: int, k: int, xq: int, ex: int, stream: int = 0):
     check(lib().sws_quantize_x(C.c_void_p(x), m, k, C.c_void_p(xq), C.c_void_p(ex), C.c_void_p(stream or None)),
           "quantize_x")
+
+
+def silu_mul(gu: int, m: int, f: int, act: int, stream: int = 0):
+    """act[m, f] = SiLU(gu[:, :f]) * gu[:, f:] (bf16 in and out, device pointers)."""
+    check(lib().sws_silu_mul(C.c_void_p(gu), m, f, C.c_void_p(act), C.c_void_p(stream or None)), "silu_mul")
 
 
 class Ctx:

@@ -1,0 +1,62 @@
+// SiLU(gate) * up between the two linears of a shared expert (the second
+// workload shape: gate_up -> SiLU * up -> down, bf16 tensors in between).
+//
+//   act[m, j] = bf16_rne( g / (1 + e^-g) * u ),  g = gu[m, j], u = gu[m, F + j]
+//
+// computed in fp32. HBM-bound: 6 bytes in and 2 out per output element; each
+// thread handles 8 consecutive columns with 16-byte loads and stores, over a
+// grid-stride loop sized to the SM count.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sws_internal.h"
+
+namespace sws {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t silu_mul2(uint32_t g, uint32_t u) {
+  const float g0 = bf16_lo(g), g1 = bf16_hi(g), u0 = bf16_lo(u), u1 = bf16_hi(u);
+  const float a0 = g0 / (1.0f + expf(-g0)) * u0;
+  const float a1 = g1 / (1.0f + expf(-g1)) * u1;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a0, a1);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restrict__ gu, int64_t m, int64_t f,
+                                                        uint16_t* __restrict__ act) {
+  const int64_t per_row = f / 8;  // 8-column groups per row
+  const int64_t n = m * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row, c = (i - r * per_row) * 8;
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * f + c));
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(gu + r * 2 * f + f + c));
+    uint4 o;
+    o.x = silu_mul2(g.x, u.x);
+    o.y = silu_mul2(g.y, u.y);
+    o.z = silu_mul2(g.z, u.z);
+    o.w = silu_mul2(g.w, u.w);
+    *reinterpret_cast<uint4*>(act + r * f + c) = o;
+  }
+}
+
+}  // namespace
+
+int launch_silu_mul(const uint16_t* gu, int64_t m, int64_t f, uint16_t* act, cudaStream_t s) {
+  if (m < 0 || f < 0) return fail(SWS_E_INVALID, "silu_mul: m=%lld f=%lld", (long long)m, (long long)f);
+  if (f % 8 != 0) return fail(SWS_E_UNSUPPORTED, "silu_mul: f=%lld is not a multiple of 8", (long long)f);
+  if (m == 0 || f == 0) return SWS_OK;
+  if (!gu || !act) return fail(SWS_E_INVALID, "silu_mul: NULL pointer");
+  if (!aligned16(gu) || !aligned16(act)) return fail(SWS_E_ALIGN, "silu_mul: pointer not 16-byte aligned");
+  const int64_t groups = m * (f / 8);
+  const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), (int64_t)device_sm_count() * 8);
+  silu_mul_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, m, f, act);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "silu_mul kernel launch");
+}
+
+}  // namespace sws

@@ -586,6 +586,10 @@ int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws
                            (cudaStream_t)stream);
 }
 
+int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t stream) {
+  return launch_silu_mul(static_cast<const uint16_t*>(gu), m, f, static_cast<uint16_t*>(act), (cudaStream_t)stream);
+}
+
 int sws_ctx_status(sws_ctx* c, int32_t clear) {
   if (!c) return fail(SWS_E_INVALID, "ctx_status: ctx is NULL");
   int32_t v = 0;

@@ -130,6 +130,7 @@ void set_decode_kernel(int k);
 int decode_kernel_for(int64_t m);
 
 int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, float* ex, cudaStream_t s);
+int launch_silu_mul(const uint16_t* gu, int64_t m, int64_t f, uint16_t* act, cudaStream_t s);
 
 struct PrefillLaunch {
   const uint8_t* w;      // fp8 [rows, cols] (slot view or replicated buffer)

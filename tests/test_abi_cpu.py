@@ -134,3 +134,27 @@ def test_relayout_validates_before_any_launch(swslib):
     assert ei.value.code == S.E_ALIGN
     with pytest.raises(S.SwsError):
         S.relayout(plan, 1, [16] * 4, [16, 32, 48, 64])
+
+
+def test_silu_mul_validates_before_any_launch(swslib):
+    S = swslib
+    S.silu_mul(0, 0, 16, 0)  # m = 0: nothing to do, no device touched
+    with pytest.raises(S.SwsError) as ei:
+        S.silu_mul(4096, 2, 12, 8192)
+    assert ei.value.code == S.E_UNSUPPORTED  # f % 8 != 0
+    with pytest.raises(S.SwsError) as ei:
+        S.silu_mul(4096, -1, 16, 8192)
+    assert ei.value.code == S.E_INVALID
+    with pytest.raises(S.SwsError) as ei:
+        S.silu_mul(4097, 2, 16, 8192)
+    assert ei.value.code == S.E_ALIGN
+
+
+def test_options_reject_unknown_values(swslib):
+    S = swslib
+    for opt, bad in ((S.OPT_DECODE_KERNEL, 3), (S.OPT_PREFILL_KERNEL, 3), (S.OPT_GATHER_ENGINE, 2), (99, 0)):
+        with pytest.raises(S.SwsError) as ei:
+            S.set_option(opt, bad)
+        assert ei.value.code == S.E_INVALID
+    S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
+    S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_AUTO)
