@@ -43,6 +43,7 @@ extern "C" {
  * section "只 shard 真正 replicated 的权重": such weights are skipped with a
  * warning). The plan is still created. */
 #define SWS_W_SKIPPED 1
+#define SWS_W_COLD 2 /* sws_wait_prefetch: nothing was prefetched, the gather ran inline */
 #define SWS_E_INVALID (-1)     /* bad argument: N, shape, index, size, layout */
 #define SWS_E_ALIGN (-2)       /* a device pointer is not 16-byte aligned */
 #define SWS_E_STATE (-3)       /* slot holds another layer, or calls out of order */
@@ -65,6 +66,8 @@ extern "C" {
 /* ---- run_layers flags -------------------------------------------------- */
 #define SWS_RUN_FUSED 1u  /* no gather: every linear reads the chunks directly */
 #define SWS_RUN_TIMING 2u /* record per-layer CUDA events (see sws_run_timing) */
+#define SWS_RUN_FIRST_PREFETCHED 4u /* the first layer was prefetched into slot 0 (sws_prefetch_layer):
+                                       wait for it instead of gathering it (cold start: gather) */
 
 typedef struct CUstream_st* sws_stream_t;
 typedef struct sws_plan sws_plan;
@@ -233,6 +236,23 @@ int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t
  * timing events and is not capturable (SWS_E_INVALID while capturing). */
 int sws_run_layers(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
                    sws_stream_t main, sws_stream_t side);
+
+/* Draft-model first-layer prefetch (blog "CUDA graph 与 draft 模型": the draft
+ * model's layer 0 has no previous layer to hide its gather behind, so the
+ * gather is taken out of the graph and issued early on a dedicated stream;
+ * a shared side stream would queue it behind the target model's gathers).
+ * sws_prefetch_layer: `stream` waits for the last reader of `slot` in this
+ * context (its done event), gathers `layer` into `slot` and records an event;
+ * the slot is marked as holding a prefetched `layer`.
+ * sws_wait_prefetch: `stream` waits once for that gather if `layer` is the
+ * prefetched one (returns SWS_OK); otherwise - a cold start, or another gather
+ * into the slot since - `stream` waits for the slot's last reader and gathers
+ * `layer` inline (returns SWS_W_COLD). run_layers with
+ * SWS_RUN_FIRST_PREFETCHED does the same for its first layer (slot 0) on the
+ * side stream. Host-side bookkeeping in issue order; meant for eager launches
+ * outside a captured graph, as the blog does. */
+int sws_prefetch_layer(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
+int sws_wait_prefetch(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 
 /* After a run with SWS_RUN_TIMING: synchronises on the recorded events and
  * writes, per layer of that run (n values each, n = last - first + 1):

@@ -11,11 +11,11 @@ from typing import Optional, Sequence
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsws.so")
 
-OK, W_SKIPPED = 0, 1
+OK, W_SKIPPED, W_COLD = 0, 1, 2
 E_INVALID, E_ALIGN, E_STATE, E_CUDA, E_TIMEOUT, E_UNSUPPORTED, E_WORKSPACE = -1, -2, -3, -4, -5, -6, -7
 E4M3, BF16, F32, U8 = 0, 1, 2, 3
 SRC_SLOT0, SRC_SLOT1, SRC_FUSED = 0, 1, 2
-RUN_FUSED, RUN_TIMING = 1, 2
+RUN_FUSED, RUN_TIMING, RUN_FIRST_PREFETCHED = 1, 2, 4
 OPT_DECODE_KERNEL = 1
 DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05 = 0, 1, 2
 OPT_PREFILL_KERNEL = 2
@@ -23,7 +23,7 @@ PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
 OPT_GATHER_ENGINE = 3
 GATHER_TMA, GATHER_COPY_ENGINE = 0, 1
 
-_NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
+_NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", 2: "SWS_W_COLD", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}
 
 
@@ -68,6 +68,8 @@ _PROTOS = [
     ("sws_run_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32]),
     ("sws_quantize_x", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("sws_silu_mul", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
+    ("sws_prefetch_layer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
+    ("sws_wait_prefetch", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
     ("sws_trace_count", C.c_int32, [C.c_void_p]),
@@ -226,6 +228,16 @@ class Ctx:
             arr[i] = _LayerIO(C.cast(xa, C.POINTER(C.c_void_p)), C.cast(ya, C.POINTER(C.c_void_p)), m)
         check(lib().sws_run_layers(self.handle, first, last, arr, flags, C.c_void_p(main or None),
                                    C.c_void_p(side or None)), "run_layers")
+
+    def prefetch_layer(self, layer: int, slot: int, stream: int = 0):
+        """Gathers `layer` into `slot` on `stream` ahead of use (draft-model layer 0)."""
+        check(lib().sws_prefetch_layer(self.handle, layer, slot, C.c_void_p(stream or None)), "prefetch_layer")
+
+    def wait_prefetch(self, layer: int, slot: int, stream: int = 0) -> bool:
+        """`stream` waits for the prefetch of `layer`; returns True on a cold
+        start, when the gather had to run inline on `stream`."""
+        return check(lib().sws_wait_prefetch(self.handle, layer, slot, C.c_void_p(stream or None)),
+                     "wait_prefetch") == W_COLD
 
     def run_timing(self, n: int):
         a = (C.c_float * n)()

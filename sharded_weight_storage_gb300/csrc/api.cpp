@@ -40,6 +40,10 @@ struct sws_ctx {
   // while the current GEMM runs (two workspace buffers)
   cudaStream_t qstream = nullptr;
   cudaEvent_t q_done[2] = {nullptr, nullptr}, g_done[2] = {nullptr, nullptr};
+  // layer prefetched into each slot by sws_prefetch_layer and not consumed
+  // yet (-1: none), and the event its gather recorded
+  int32_t prefetch_layer[2] = {-1, -1};
+  cudaEvent_t prefetched[2] = {nullptr, nullptr};
 };
 
 namespace {
@@ -75,6 +79,7 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   const sws_plan* p = c->plan;
   const LayerPlan& lp = p->layers[layer];
   c->slot_tag[slot] = layer;
+  c->prefetch_layer[slot] = -1;  // whatever was prefetched into this slot is overwritten
   if (lp.total == 0) return SWS_OK;
   GatherLaunch g;
   g.n = p->n_shards;
@@ -97,6 +102,21 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
   cudaError_t e = launch_gather(g, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
+}
+
+// Layer `layer` in slot `slot` for work on `s`: if sws_prefetch_layer left it
+// there, `s` waits for that gather once; otherwise (cold start) `s` waits for
+// the slot's last reader and gathers inline. *cold tells which.
+int take_prefetch(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s, bool* cold) {
+  if (c->prefetch_layer[slot] == layer) {
+    *cold = false;
+    c->prefetch_layer[slot] = -1;
+    SWS_CUDA_TRY(cudaStreamWaitEvent(s, c->prefetched[slot], 0));
+    return SWS_OK;
+  }
+  *cold = true;
+  SWS_CUDA_TRY(cudaStreamWaitEvent(s, c->done[slot], 0));
+  return gather_impl(c, layer, slot, s);
 }
 
 // Where entry j's weight lives for source `src`: a view (slot or replicated
@@ -443,7 +463,9 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
     }
   }
   if ((e = cudaEventCreateWithFlags(&c->call_start, cudaEventDisableTiming)) != cudaSuccess ||
-      (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess) {
+      (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&c->prefetched[0], cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&c->prefetched[1], cudaEventDisableTiming)) != cudaSuccess) {
     sws_ctx_destroy(c);
     return cuda_fail(e, "ctx_create: cudaEventCreate");
   }
@@ -469,6 +491,8 @@ void sws_ctx_destroy(sws_ctx* c) {
   }
   if (c->call_start) cudaEventDestroy(c->call_start);
   if (c->join) cudaEventDestroy(c->join);
+  for (int s = 0; s < 2; ++s)
+    if (c->prefetched[s]) cudaEventDestroy(c->prefetched[s]);
   for (int b = 0; b < 2; ++b) {
     if (c->q_done[b]) cudaEventDestroy(c->q_done[b]);
     if (c->g_done[b]) cudaEventDestroy(c->g_done[b]);
@@ -509,7 +533,10 @@ int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* 
   if (last < first) return SWS_OK;
   if (first < 0 || last >= L) return fail(SWS_E_INVALID, "run_layers: range [%d, %d] outside [0, %d)", first, last, L);
   if (!io) return fail(SWS_E_INVALID, "run_layers: io is NULL");
-  if (flags & ~(SWS_RUN_FUSED | SWS_RUN_TIMING)) return fail(SWS_E_INVALID, "run_layers: flags 0x%x", flags);
+  if (flags & ~(SWS_RUN_FUSED | SWS_RUN_TIMING | SWS_RUN_FIRST_PREFETCHED))
+    return fail(SWS_E_INVALID, "run_layers: flags 0x%x", flags);
+  if ((flags & SWS_RUN_FUSED) && (flags & SWS_RUN_FIRST_PREFETCHED))
+    return fail(SWS_E_INVALID, "run_layers: SWS_RUN_FIRST_PREFETCHED needs the slot path");
   cudaStream_t ms = (cudaStream_t)main_s, ss = (cudaStream_t)side_s;
   const bool timing = (flags & SWS_RUN_TIMING) != 0;
   const int32_t n = last - first + 1;
@@ -542,7 +569,13 @@ int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* 
   SWS_CUDA_TRY(cudaEventRecord(c->call_start, ms));
   if (timing) SWS_CUDA_TRY(cudaEventRecord(c->t_wait[0], ms));
   SWS_CUDA_TRY(cudaStreamWaitEvent(ss, c->call_start, 0));
-  int rc = gather_impl(c, first, slot_of(first), ss);
+  int rc = SWS_OK;
+  if (flags & SWS_RUN_FIRST_PREFETCHED) {  // blog "CUDA graph 与 draft 模型": the first layer was prefetched
+    bool cold = false;
+    rc = take_prefetch(c, first, slot_of(first), ss, &cold);
+  } else {
+    rc = gather_impl(c, first, slot_of(first), ss);
+  }
   if (rc != SWS_OK) return rc;
   SWS_CUDA_TRY(cudaEventRecord(c->ready[slot_of(first)], ss));
   for (int32_t l = first; l <= last; ++l) {
@@ -584,6 +617,31 @@ int sws_run_timing(sws_ctx* c, float* exposed_ms, float* layer_ms, int32_t n) {
 int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws_stream_t stream) {
   return launch_quantize_x(static_cast<const uint16_t*>(x), m, k, static_cast<uint8_t*>(xq), ex,
                            (cudaStream_t)stream);
+}
+
+int sws_prefetch_layer(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "prefetch_layer: ctx is NULL");
+  if (layer < 0 || layer >= (int32_t)c->plan->layers.size())
+    return fail(SWS_E_INVALID, "prefetch_layer: layer %d", layer);
+  if (slot != 0 && slot != 1) return fail(SWS_E_INVALID, "prefetch_layer: slot %d", slot);
+  cudaStream_t s = (cudaStream_t)stream;
+  SWS_CUDA_TRY(cudaStreamWaitEvent(s, c->done[slot], 0));  // the slot's last reader in this context
+  int rc = gather_impl(c, layer, slot, s);
+  if (rc != SWS_OK) return rc;
+  SWS_CUDA_TRY(cudaEventRecord(c->prefetched[slot], s));
+  c->prefetch_layer[slot] = layer;
+  return SWS_OK;
+}
+
+int sws_wait_prefetch(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "wait_prefetch: ctx is NULL");
+  if (layer < 0 || layer >= (int32_t)c->plan->layers.size())
+    return fail(SWS_E_INVALID, "wait_prefetch: layer %d", layer);
+  if (slot != 0 && slot != 1) return fail(SWS_E_INVALID, "wait_prefetch: slot %d", slot);
+  bool cold = false;
+  int rc = take_prefetch(c, layer, slot, (cudaStream_t)stream, &cold);
+  if (rc != SWS_OK) return rc;
+  return cold ? SWS_W_COLD : SWS_OK;
 }
 
 int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t stream) {
