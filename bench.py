@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the KDA-layer and tiny-layer decode sections")
     ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-weight section")
+    ap.add_argument("--no-prefetch", action="store_true", help="skip the draft-model prefetch section")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
     ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill"],
@@ -752,6 +753,68 @@ def run_bf16(args, dist):
     return out
 
 
+def run_prefetch(args, dist, n_target=16, reps=10):
+    """Draft-model layer-0 prefetch: a target stack of n_target shared-expert
+    layers runs its lookahead, then (after an optional host-side window that
+    stands for the work between the two models) a one-layer draft context runs
+    its first layer. The exposed part of the draft's first gather (time its
+    compute stream waits for the layer) is measured for: a cold start (gather
+    inline), a prefetch on a dedicated stream issued before the target, and a
+    prefetch on the target's side stream issued after the target's layers."""
+    import torch
+
+    import sharded_weight_storage_gb300 as S
+    import workloads as WL
+    from sharded_weight_storage_gb300.storage import ShardedStack
+
+    dev = torch.device("cuda", dist.local)
+    w = WL.SHARED_EXPERT
+    base = WL.base_layer(w, 0)
+    codes = [torch.from_numpy(c).to(dev) for c in base.codes]
+    scales = [torch.from_numpy(s_).to(dev) for s_ in base.scales]
+    ne = len(w.entries)
+    tst = ShardedStack([(l, S.E4M3, e.rows, e.cols) for l in range(n_target) for e in w.entries], w.n_shards,
+                       max_m=64, device=str(dev))
+    for l in range(n_target):
+        tst.load_layer(l, {l * ne + j: codes[j] for j in range(ne)}, {l * ne + j: scales[j] for j in range(ne)})
+    dst = ShardedStack([(0, S.E4M3, e.rows, e.cols) for e in w.entries], w.n_shards, max_m=64, device=str(dev))
+    dst.load_layer(0, {j: codes[j] for j in range(ne)}, {j: scales[j] for j in range(ne)})
+    tctx, dctx = tst.make_ctx(), dst.make_ctx()
+    m = HEADLINE_M
+    xs = [WL.draw_x(w.key, j, m, e.cols).to(dev) for j, e in enumerate(w.entries)]
+    ys = [torch.empty((m, e.rows), dtype=torch.bfloat16, device=dev) for e in w.entries]
+    tio = [([x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m) for _ in range(n_target)]
+    dio = [([x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m)]
+    main, side, dside, pre = (torch.cuda.Stream(device=dev) for _ in range(4))
+
+    def step(variant, window_s):
+        if variant == "dedicated":
+            dctx.prefetch_layer(0, 0, pre.cuda_stream)
+        tctx.run_layers(0, n_target - 1, tio, 0, main.cuda_stream, side.cuda_stream)
+        if variant == "shared_side":
+            dctx.prefetch_layer(0, 0, side.cuda_stream)
+        if window_s > 0:
+            time.sleep(window_s)
+        flags = S.RUN_TIMING | (0 if variant == "cold" else S.RUN_FIRST_PREFETCHED)
+        dctx.run_layers(0, 0, dio, flags, main.cuda_stream, dside.cuda_stream)
+        exposed, _ = dctx.run_timing(1)
+        return exposed[0]
+
+    out = {"workload": f"target: {n_target} shared-expert layers (N=16, M={m}); draft: one shared-expert layer",
+           "gather_bytes": dst.layout[0][0], "exposed_draft_gather_us": {}}
+    for window_ms in (0.0, 4.0):
+        res = {}
+        for variant in ("cold", "dedicated", "shared_side"):
+            step(variant, window_ms / 1e3)
+            vals = [step(variant, window_ms / 1e3) for _ in range(reps)]
+            res[variant] = 1e3 * statistics.median(vals)
+        out["exposed_draft_gather_us"][f"host_window_{window_ms:g}ms"] = res
+    torch.cuda.synchronize()
+    del tst, dst, tctx, dctx, codes, scales
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill(args, dist, n_layers):
     """Prefill on the KDA-layer weights (N = 8): per-linear tcgen05 GEMM
     throughput at M = 2048 and 8192, whole-layer time, and lookahead over
@@ -1020,6 +1083,7 @@ def main():
                    "tiny_flat_layer": run_decode_config(args, dist, WL.TINY, relayout=True)}
     prefill = run_prefill(args, dist, args.prefill_layers) if args.prefill_layers > 0 else None
     bf16 = run_bf16(args, dist) if not args.no_bf16 else None
+    prefetch = run_prefetch(args, dist) if not args.no_prefetch else None
     if dist.rank != 0:
         dist.close()
         return
@@ -1064,6 +1128,7 @@ def main():
         "decode_configs": configs,
         "prefill": prefill,
         "bf16_weights": bf16,
+        "draft_prefetch": prefetch,
         "weight_GBps_step": total / ms_step / 1e6,
     }
     if dist.world == 1 and not args.no_cpu_baseline:
