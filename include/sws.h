@@ -226,7 +226,10 @@ int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t
  * records done(l). At most two layers' full weights are resident. With
  * SWS_RUN_FUSED no gather runs and the linears read the chunks directly.
  * io[l - first] gives layer l's activations and outputs. On return `main`
- * carries all the work (side-stream work is joined into it).
+ * carries all the work (side-stream work is joined into it). The linears'
+ * kernels are launched with the device's highest stream priority and the
+ * gather with the default one, so that the block scheduler gives the SMs to
+ * the linears first when both wait for them.
  * Stream capture: without SWS_RUN_TIMING the call only enqueues kernels and
  * event record/wait pairs (no synchronisation, no allocation, no query), so
  * it records into a CUDA graph when `main` is capturing: the fork to `side`

@@ -54,8 +54,7 @@ int launch_silu_mul(const uint16_t* gu, int64_t m, int64_t f, uint16_t* act, cud
   if (!aligned16(gu) || !aligned16(act)) return fail(SWS_E_ALIGN, "silu_mul: pointer not 16-byte aligned");
   const int64_t groups = m * (f / 8);
   const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), (int64_t)device_sm_count() * 8);
-  silu_mul_kernel<<<(unsigned)blocks, 256, 0, s>>>(gu, m, f, act);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_high(silu_mul_kernel, dim3((unsigned)blocks), dim3(256), 0, s, gu, m, f, act);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "silu_mul kernel launch");
 }
 

@@ -534,8 +534,7 @@ cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
   if (attr != cudaSuccess) return attr;
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
-  kern<<<(unsigned)grid, kThreads, kSmem, s>>>(p);
-  return cudaGetLastError();
+  return launch_high(kern, dim3((unsigned)grid), dim3(kThreads), kSmem, s, p);
 }
 
 template <bool WB>

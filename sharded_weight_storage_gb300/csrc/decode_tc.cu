@@ -715,21 +715,25 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   int64_t threads = 0;
   for (int j = 0; j < p.n_entries; ++j)
     if (p.e[j].split_owner) threads += (int64_t)p.e[j].slabs * N * 8;
-  split_x_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, N);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributePriority;
+  at[0].val.priority = high_priority();
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;  // priority only
+  cudaError_t e = cudaLaunchKernelEx(&cfg, split_x_kernel, p, (int)N);
   if (e != cudaSuccess) return e;
   // 2. the GEMM, as a programmatic dependent launch of (1)
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;  // priority + programmatic stream serialization
   e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
   // 3. the split-K settle (and the straddling rows of a chunk-map launch), as
   //    a programmatic dependent launch of (2)

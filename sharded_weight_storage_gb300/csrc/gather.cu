@@ -37,6 +37,24 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// The highest stream priority of the current device (the numerically smallest
+// value; cached per device). The linears' kernels are launched with it so that,
+// when a gather on another stream competes for SMs, the block scheduler
+// places the linears' CTAs first; the gather keeps the default priority.
+int high_priority() {
+  static int cache[64];
+  static bool known[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!known[dev]) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) greatest = 0;
+    cache[dev] = greatest;
+    known[dev] = true;
+  }
+  return cache[dev];
+}
+
 int check_device() {
   int dev = 0, major = 0, minor = 0;
   cudaError_t e = cudaGetDevice(&dev);

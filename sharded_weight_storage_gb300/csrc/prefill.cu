@@ -106,8 +106,7 @@ int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, floa
   if (tasks == 0) return SWS_OK;
   if (!aligned16(x) || !aligned16(xq) || !aligned16(ex)) return fail(SWS_E_ALIGN, "quantize_x: pointer not 16-byte aligned");
   const int64_t blocks = std::min<int64_t>(cdiv(tasks, 32), (int64_t)device_sm_count() * 8);
-  quantize_x_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, m, k, groups, xq, ex);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_high(quantize_x_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, m, k, groups, xq, ex);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "quantize_x kernel launch");
 }
 

@@ -859,7 +859,9 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   if (pair) {
     const int64_t n_clusters = std::min<int64_t>(tiles, clusters);
-    prefill_pair_kernel<<<(unsigned)(2 * n_clusters), kPairThreads, kPairSmemBytes, s>>>(p);
+    cudaError_t le = launch_high(prefill_pair_kernel, dim3((unsigned)(2 * n_clusters)), dim3(kPairThreads),
+                                 kPairSmemBytes, s, p);
+    if (le != cudaSuccess) return cuda_fail(le, "prefill pair kernel launch");
   } else {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
@@ -868,10 +870,10 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     });
     if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute");
     const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-    prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
+    cudaError_t le = launch_high(prefill_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
+    if (le != cudaSuccess) return cuda_fail(le, "prefill kernel launch");
   }
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SWS_OK : cuda_fail(e, pair ? "prefill pair kernel launch" : "prefill kernel launch");
+  return SWS_OK;
 }
 
 int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s) {
@@ -906,8 +908,7 @@ int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s) {
   if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (bf16)");
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-  prefill_bf16_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_high(prefill_bf16_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill bf16 kernel launch");
 }
 

@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 #include <string>
@@ -70,6 +72,24 @@ int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t c
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
+int high_priority();  // launch priority of the linears' kernels (see gather.cu)
+
+// Launch with the high priority (kernels of the linears and their helpers).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_high(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        Args&&... args) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributePriority;
+  at[0].val.priority = high_priority();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 int check_device();  // SWS_OK if the current device is sm_103, else an error code
 
 struct GatherLaunch {
