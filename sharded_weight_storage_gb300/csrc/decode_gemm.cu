@@ -584,9 +584,9 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
       if (rc != SWS_OK) return rc;
     }
     e.xs = nullptr;
-    if (tc) {  // the entry's activation split blocks, one per K slab
+    if (tc) {  // the entry's activation blocks, one per K slab: (hi, lo, e) for e4m3 weights, x for bf16
       e.xs = tc_split;
-      tc_split += cdiv(it.cols, kSlabK) * tc_split_block_bytes(tc_n_pad(g.m));
+      tc_split += cdiv(it.cols * elem, kSlabK) * tc_x_block_bytes(tc_n_pad(g.m), g.bf16_w);
     }
     e.scales = it.scales;
     e.x = it.x;
@@ -712,10 +712,11 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   int64_t dec = 0;
   int rc = decode_workspace_bytes(g.m, &dec);
   if (rc != SWS_OK) return rc;
-  int64_t slabs = 0;
-  for (int i = 0; i < g.n; ++i) slabs += cdiv(g.item[i].cols, kSlabK);
-  const int64_t split = decode_split_bytes(g.m, slabs);  // the activation split region follows the partial sums
-  bool tc = !g.bf16_w && decode_kernel_for(g.m) == kDecodeTc;  // the tcgen05 kernel takes e4m3 weights
+  int64_t split = 0;  // the activation split region follows the partial sums
+  for (int i = 0; i < g.n; ++i)
+    split += cdiv(g.item[i].cols * (g.bf16_w ? 2 : 1), kSlabK) * tc_x_block_bytes(tc_n_pad(std::max<int64_t>(g.m, 1)), g.bf16_w);
+  // bf16 weights through the chunk map go to the mma.sync kernel
+  bool tc = decode_kernel_for(g.m) == kDecodeTc && !(g.bf16_w && g.fused);
   const int64_t need = dec + (tc ? split : 0);
   if (g.workspace_bytes < need)
     return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);
@@ -741,7 +742,7 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   p.trace = g.trace;
   p.tag = g.tag | ((tc ? (g.fused ? kTraceTcFused : kTraceTc) : (g.fused ? kTraceMmaFused : kTraceMma)) << 48);
   cudaError_t e =
-      tc ? launch_decode_tc(p, g.fused, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, g.bf16_w, kMaxGrid, s);
+      tc ? launch_decode_tc(p, g.fused, g.bf16_w, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, g.bf16_w, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 

@@ -1,6 +1,8 @@
 // Split-K FP8 decode GEMM (m <= 64) on tcgen05 tensor cores: the same linear
 // and the same split-K partition as decode_gemm.cu (see there), for the m where
-// the warp-level mma.sync path cannot keep up with HBM.
+// the warp-level mma.sync path cannot keep up with HBM. A bf16-weight variant
+// (WB) shares everything but the operands: x itself is the B operand
+// (split_x_bf16_kernel), the MMAs are kind::f16 and no scales apply.
 //
 //   Y[m, o] = bf16_rne( sum_kb s[o/128, kb] * sum_{i in kb} x[m, i] * e4m3(q[o, i]) )
 //
@@ -70,17 +72,21 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return r;
 }
 
-template <int N>
+// WB = false: e4m3 weights, activations split into two e4m3 terms (hi, lo)
+// and a scale per row; WB = true: bf16 weights (64 K per 128-byte slab row)
+// and the bf16 activations themselves as the one B operand, no scales.
+template <int N, bool WB = false>
 struct TcCfg {
-  static constexpr int kWBytes = kTcRows * kSlabK;              // e4m3 weight slab, 128-byte swizzle
-  static constexpr int kTermBytes = N * kSlabK;                 // one e4m3 B operand [N][128]
-  static constexpr int kXBytes = (int)tc_split_block_bytes(N);  // hi, lo, e
-  static constexpr int kSwOff = kWBytes + kXBytes;              // four fp32 weight scales
+  static constexpr int kWBytes = kTcRows * kSlabK;  // weight slab, 128-byte swizzle
+  static constexpr int kTermBytes = N * kSlabK;     // one B operand [N][128 bytes]
+  static constexpr int kXBytes = WB ? kTermBytes : (int)tc_split_block_bytes(N);  // (hi, lo, e) or x
+  static constexpr int kSwOff = kWBytes + kXBytes;  // four fp32 weight scales
   static constexpr int kStageBytes = (kSwOff + 16 + 1023) / 1024 * 1024;
   static constexpr int kStages = N <= 16 ? 6 : N <= 32 ? 5 : 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024;
-  static constexpr int kDBufs = N <= 32 ? 4 : 2;  // TMEM accumulator buffers of 2 tiles x 2N columns
-  static constexpr int kTmemCols = pow2_at_least(kDBufs * 4 * N);
+  static constexpr int kDCols = WB ? 2 * N : 4 * N;  // one TMEM accumulator buffer: 2 tiles x (2N or N) columns
+  static constexpr int kDBufs = N <= 32 ? 4 : 2;
+  static constexpr int kTmemCols = pow2_at_least(kDBufs * kDCols);
   static constexpr int kSlotFloats = kTcRows * N;  // partial-sum slot of one CTA
 };
 static_assert(TcCfg<16>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
@@ -103,6 +109,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f8(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+// kind::f16 instruction descriptor: A, B bf16, D f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 
 // D (TMEM) (+)= A (shared memory) x B (shared memory).
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -111,6 +121,15 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
@@ -235,6 +254,33 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ De
   if (g == 0) reinterpret_cast<float*>(blk + 2 * n_pad * 128)[r] = es;
 }
 
+// bf16 weights: the B operand of a (entry, 64-K slab) block is the bf16
+// activations themselves, [n_pad rows][128 bytes] in the 128-byte swizzled
+// order, zero past m and past cols. Eight threads per (entry, slab, row), one
+// 16-byte piece each.
+__global__ void __launch_bounds__(256) split_x_bf16_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) dev::trace_start(p.trace);
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = (int)(tid & 7);
+  int64_t task = tid >> 3;
+  int j = 0;
+  for (; j < p.n_entries; ++j) {
+    if (!p.e[j].split_owner) continue;
+    const int64_t t = (int64_t)p.e[j].slabs * n_pad;
+    if (task < t) break;
+    task -= t;
+  }
+  if (j >= p.n_entries) return;
+  const DecodeEntry& e = p.e[j];
+  const int64_t kb = task / n_pad;
+  const int r = (int)(task - kb * n_pad);
+  const int64_t col = kb * 64 + g * 8;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (r < p.m && col < e.cols) v = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col));
+  *reinterpret_cast<uint4*>(e.xs + kb * (int64_t)n_pad * 128 + r * 128 + ((g ^ (r & 7)) << 4)) = v;
+}
+
 // ---- 2. GEMM ---------------------------------------------------------------------
 
 // Walks a CTA's consecutive units like an odometer (K slab, then row block,
@@ -308,9 +354,9 @@ __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& 
   for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
 }
 
-template <int N>
+template <int N, bool WB>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
-  using Cf = TcCfg<N>;
+  using Cf = TcCfg<N, WB>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t dsm[];
   constexpr int kDBufs = Cf::kDBufs;
@@ -389,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int64_t lr0 = cur.rbl * kTcRows + t * 128;  // first row of the tile in the entry
-          const bool in = lr0 < cur.rows;
+          const bool in = !WB && lr0 < cur.rows;  // bf16 weights have no scales
           const int64_t g0 = cur.row_base + lr0;
           const int64_t g1 = cur.row_base + (lr0 + 127 < cur.rows ? lr0 + 127 : cur.rows - 1);
           cp_async4(sw + 2 * t, cur.scales + (in ? (g0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
@@ -412,7 +458,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     if (lane == 0) {
       // B is the split block's hi and lo operands as one 2N-row operand, so
       // each weight tile is read once: D[:, 0:N] = A hi^T, D[:, N:2N] = A lo^T.
-      constexpr uint32_t idesc = idesc_f8(128, 2 * N);
+      // bf16: B is x itself, D[:, 0:N] = A x^T, 16 K per MMA.
+      constexpr uint32_t idesc = WB ? idesc_bf16(128, N) : idesc_f8(128, 2 * N);
       bool issued = false;
       for (int64_t i = 0; i < n && !s_abort; ++i) {
         const int s = (int)(i % S), b = (int)(i % kDBufs);
@@ -428,9 +475,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int k = 0; k < kSlabK / 32; ++k)
-            mma_f8(tmem + b * 4 * N + t * 2 * N, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32),
-                   smem_desc_sw128(xb + k * 32), idesc, k != 0);
+          for (int k = 0; k < kSlabK / 32; ++k) {  // 32 bytes of K per MMA
+            const uint32_t d = tmem + b * Cf::kDCols + t * (Cf::kDCols / 2);
+            if constexpr (WB)
+              mma_bf16(d, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32), smem_desc_sw128(xb + k * 32), idesc,
+                       k != 0);
+            else
+              mma_f8(d, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32), smem_desc_sw128(xb + k * 32), idesc,
+                     k != 0);
+          }
         mma_commit(&sempty[s]);
         mma_commit(&dfull[b]);
         issued = true;
@@ -459,21 +512,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       if (fail) break;
       tc_fence_after();
       const uint8_t* st = smem + s * Cf::kStageBytes;
-      const float* ex = reinterpret_cast<const float*>(st + Cf::kWBytes + 2 * Cf::kTermBytes);
-      // this row's 128-row scale block: the tile's first or last one
-      const float* swt = reinterpret_cast<const float*>(st + Cf::kSwOff) + 2 * t;
-      const int64_t g0 = cur.row_base + cur.rbl * kTcRows + t * 128;
-      const float sw = ((g0 + row) >> 7) == (g0 >> 7) ? swt[0] : swt[1];
-      const uint32_t dcol = tmem + lane_off + b * 4 * N + t * 2 * N;  // hi columns; lo N further
+      const uint32_t dcol = tmem + lane_off + b * Cf::kDCols + t * (Cf::kDCols / 2);
+      if constexpr (WB) {  // no scales: the slab's products add straight in
 #pragma unroll
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t rh[16], rl[16];
-        tmem_ld16_nowait(dcol + c0, rh);
-        tmem_ld16_nowait(dcol + N + c0, rl);
-        tmem_wait_ld();
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          uint32_t rh[16];
+          tmem_ld16_nowait(dcol + c0, rh);
+          tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          acc[c0 + k] = fmaf(sw * ex[c0 + k], __uint_as_float(rh[k]) + __uint_as_float(rl[k]), acc[c0 + k]);
+          for (int k = 0; k < 16; ++k) acc[c0 + k] += __uint_as_float(rh[k]);
+        }
+      } else {
+        const float* ex = reinterpret_cast<const float*>(st + Cf::kWBytes + 2 * Cf::kTermBytes);
+        // this row's 128-row scale block: the tile's first or last one
+        const float* swt = reinterpret_cast<const float*>(st + Cf::kSwOff) + 2 * t;
+        const int64_t g0 = cur.row_base + cur.rbl * kTcRows + t * 128;
+        const float sw = ((g0 + row) >> 7) == (g0 >> 7) ? swt[0] : swt[1];
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 16) {  // hi columns; lo N further
+          uint32_t rh[16], rl[16];
+          tmem_ld16_nowait(dcol + c0, rh);
+          tmem_ld16_nowait(dcol + N + c0, rl);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            acc[c0 + k] = fmaf(sw * ex[c0 + k], __uint_as_float(rh[k]) + __uint_as_float(rl[k]), acc[c0 + k]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -702,13 +766,13 @@ void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
   }
 }
 
-template <int N, bool FUSED>
+template <int N, bool FUSED, bool WB>
 cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
-  constexpr int kSmem = TcCfg<N>::kSmem;
+  constexpr int kSmem = TcCfg<N, WB>::kSmem;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(decode_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    attr = cudaFuncSetAttribute(decode_tc_kernel<N, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr != cudaSuccess) return attr;
   // 1. split the activations of every entry
@@ -726,7 +790,7 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;  // priority only
-  cudaError_t e = cudaLaunchKernelEx(&cfg, split_x_kernel, p, (int)N);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, WB ? split_x_bf16_kernel : split_x_kernel, p, (int)N);
   if (e != cudaSuccess) return e;
   // 2. the GEMM, as a programmatic dependent launch of (1)
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
@@ -734,7 +798,7 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.numAttrs = 2;  // priority + programmatic stream serialization
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N>, p);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N, WB>, p);
   // 3. the split-K settle (and the straddling rows of a chunk-map launch), as
   //    a programmatic dependent launch of (2)
   if (e != cudaSuccess) return e;
@@ -748,21 +812,22 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED>, p, sp);
 }
 
-template <bool FUSED>
+template <bool FUSED, bool WB>
 cudaError_t launch_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   switch ((int)tc_n_pad(p.m)) {
-    case 16: return launch_tc_n<16, FUSED>(p, grid_cap, s);
-    case 32: return launch_tc_n<32, FUSED>(p, grid_cap, s);
-    case 48: return launch_tc_n<48, FUSED>(p, grid_cap, s);
-    default: return launch_tc_n<64, FUSED>(p, grid_cap, s);
+    case 16: return launch_tc_n<16, FUSED, WB>(p, grid_cap, s);
+    case 32: return launch_tc_n<32, FUSED, WB>(p, grid_cap, s);
+    case 48: return launch_tc_n<48, FUSED, WB>(p, grid_cap, s);
+    default: return launch_tc_n<64, FUSED, WB>(p, grid_cap, s);
   }
 }
 
 }  // namespace
 
 namespace dec {
-cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int64_t grid_cap, cudaStream_t s) {
-  return fused ? launch_tc<true>(p, grid_cap, s) : launch_tc<false>(p, grid_cap, s);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s) {
+  if (bf16_w) return launch_tc<false, true>(p, grid_cap, s);  // views only: chunk-map bf16 reads use mma.sync
+  return fused ? launch_tc<true, false>(p, grid_cap, s) : launch_tc<false, false>(p, grid_cap, s);
 }
 int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }
 }  // namespace dec

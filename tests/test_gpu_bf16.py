@@ -14,7 +14,7 @@ from helpers import assert_close, bf16_tensor_to_f64
 
 pytestmark = pytest.mark.gpu
 
-KERNEL_MMA, KERNEL_MMA_FUSED, KERNEL_PREFILL = 1, 2, 5
+KERNEL_MMA, KERNEL_MMA_FUSED, KERNEL_TC, KERNEL_PREFILL = 1, 2, 3, 5
 
 
 @pytest.fixture(scope="module")
@@ -73,13 +73,21 @@ def bf16_stack(S):
     return st, bits
 
 
+@pytest.fixture(params=["tcgen05", "mma"])
+def decode_kernel(S, request):
+    """The default (tcgen05 kind::f16) or the mma.sync decode kernel on views."""
+    S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_AUTO if request.param == "tcgen05" else S.DECODE_MMA)
+    yield KERNEL_TC if request.param == "tcgen05" else KERNEL_MMA
+    S.set_option(S.OPT_DECODE_KERNEL, S.DECODE_AUTO)
+
+
 @pytest.mark.parametrize("m", [1, 8, 17, 40, 64])
-def test_bf16_decode_matches_oracle(S, bf16_stack, m):
+def test_bf16_decode_matches_oracle(S, bf16_stack, decode_kernel, m):
     st, bits = bf16_stack
     for j, (_, _, r, c) in enumerate(SHAPES):
         x = WL.draw_x(62, j, m, c).cuda()
         y, kinds = _linear_traced(st, j, S.SRC_SLOT0, x, m)
-        assert kinds == [KERNEL_MMA]
+        assert kinds == [decode_kernel]
         assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m}")
     assert st.ctx.status() == 0
 
@@ -95,7 +103,7 @@ def test_bf16_decode_through_the_chunk_map(S, bf16_stack, m):
         assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m} (fused)")
 
 
-@pytest.mark.parametrize("m", [3, 200])
+@pytest.mark.parametrize("m", [3, 40, 200])
 def test_bf16_one_hot_gives_the_weight_exactly(S, bf16_stack, m):
     # x = e_i picks column i of W: one product, exact in fp32, then rounded to
     # bf16, which the bf16 weight already is.
