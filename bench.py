@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-prefetch", action="store_true", help="skip the draft-model prefetch section")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
-    ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill"],
+    ap.add_argument("--only", choices=["gather", "decode", "layer", "fused", "step", "noalloc", "prefill", "bf16layer"],
                     default=None,
                     help="profiling driver: build the shared-expert layer and run one kernel --reps times")
     ap.add_argument("--m", type=int, default=HEADLINE_M)
@@ -1016,6 +1016,25 @@ def run_only(args, dist):
 
     set_decode_kernel(S, args.decode_kernel)
     set_prefill_kernel(S, args.prefill_kernel)
+    if args.only == "bf16layer":  # the shared-expert layer's linears with bf16 weights at m = --m
+        w = WL.SHARED_EXPERT
+        ents = [(0, e.rows, e.cols) for e in w.entries]
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(20260)
+        st = ShardedStack([(0, S.BF16, r, c) for (_, r, c) in ents], w.n_shards, max_m=64)
+        st.load_layer(0, {j: torch.randn((r, c), generator=gen, device="cuda").mul_(0.02).to(torch.bfloat16)
+                          .view(torch.uint8) for j, (_, r, c) in enumerate(ents)}, {})
+        ctx = st.make_ctx()
+        ctx.gather_to_slot(0, 0, 0)
+        m = args.m
+        xs = [WL.draw_x(w.key, j, m, c).cuda() for j, (_, r, c) in enumerate(ents)]
+        ys = [torch.empty((m, r), dtype=torch.bfloat16, device="cuda") for (_, r, c) in ents]
+        for _ in range(args.reps):
+            ctx.layer_linears(0, S.SRC_SLOT0, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        print(f"only=bf16layer m={m} reps={args.reps}: ok")
+        return
     if args.only == "prefill":  # one KDA-layer linear (entry --entry) at m = --m tokens
         w = WL.PREFILL
         ents = [(0, e.rows, e.cols) for e in w.entries]
