@@ -175,8 +175,8 @@ int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t s
  * ignored). x: bf16 [m, cols] row-major; y: bf16 [m, rows] row-major.
  * m in [0, 2^31). m <= 64 runs a split-K decode launch, by default on the
  * tcgen05 kernel (SWS_OPT_DECODE_KERNEL): for E4M3 with x split exactly into
- * two e4m3 terms (kind::f8f6f4), for BF16 on bf16 operands (kind::f16);
- * chunk-map (SWS_SRC_FUSED) reads of BF16 weights use the mma.sync kernel.
+ * two e4m3 terms (kind::f8f6f4), for BF16 on bf16 operands (kind::f16),
+ * from views or through the chunk map (SWS_SRC_FUSED).
  * m > 64 runs the prefill path: E4M3 quantises x (sws_quantize_x into the
  * workspace) and runs the tcgen05 block-scaled FP8 GEMM; BF16 runs a tcgen05
  * bf16 GEMM on x directly. Requires E4M3 or BF16 weights (else

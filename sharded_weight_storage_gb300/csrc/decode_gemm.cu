@@ -659,7 +659,8 @@ int build_fused_segments(DecodeParams& p, const DecodeParams& lin, const DecodeG
   int64_t rb = 0;
   for (int j = 0; j < lin.n_entries; ++j) {
     const DecodeEntry& L = lin.e[j];
-    const int64_t o = L.t_offset, cols = L.cols, rows = L.rows, end = o + rows * cols;
+    // byte arithmetic: `cols` here is the row length in bytes
+    const int64_t o = L.t_offset, cols = L.cols * (g.bf16_w ? 2 : 1), rows = L.rows, end = o + rows * cols;
     const int64_t c0 = o / C, c1 = (end - 1) / C;
     bool owner = true;
     for (int64_t c = c0; c <= c1; ++c) {
@@ -715,8 +716,7 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   int64_t split = 0;  // the activation split region follows the partial sums
   for (int i = 0; i < g.n; ++i)
     split += cdiv(g.item[i].cols * (g.bf16_w ? 2 : 1), kSlabK) * tc_x_block_bytes(tc_n_pad(std::max<int64_t>(g.m, 1)), g.bf16_w);
-  // bf16 weights through the chunk map go to the mma.sync kernel
-  bool tc = decode_kernel_for(g.m) == kDecodeTc && !(g.bf16_w && g.fused);
+  bool tc = decode_kernel_for(g.m) == kDecodeTc;
   const int64_t need = dec + (tc ? split : 0);
   if (g.workspace_bytes < need)
     return fail(SWS_E_WORKSPACE, "decode: workspace %lld < %lld bytes", (long long)g.workspace_bytes, (long long)need);

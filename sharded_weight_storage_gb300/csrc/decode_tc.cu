@@ -432,16 +432,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         // Block scales of each 128-row tile's first and last row (a segment's
         // tile may cross a 128-row scale block of its linear).
         float* sw = reinterpret_cast<float*>(st + Cf::kSwOff);
+        if constexpr (!WB) {  // bf16 weights have no scales
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int64_t lr0 = cur.rbl * kTcRows + t * 128;  // first row of the tile in the entry
-          const bool in = !WB && lr0 < cur.rows;  // bf16 weights have no scales
-          const int64_t g0 = cur.row_base + lr0;
-          const int64_t g1 = cur.row_base + (lr0 + 127 < cur.rows ? lr0 + 127 : cur.rows - 1);
-          cp_async4(sw + 2 * t, cur.scales + (in ? (g0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
-          cp_async4(sw + 2 * t + 1, cur.scales + (in ? (g1 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+          for (int t = 0; t < 2; ++t) {
+            const int64_t lr0 = cur.rbl * kTcRows + t * 128;  // first row of the tile in the entry
+            const bool in = lr0 < cur.rows;
+            const int64_t g0 = cur.row_base + lr0;
+            const int64_t g1 = cur.row_base + (lr0 + 127 < cur.rows ? lr0 + 127 : cur.rows - 1);
+            cp_async4(sw + 2 * t, cur.scales + (in ? (g0 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+            cp_async4(sw + 2 * t + 1, cur.scales + (in ? (g1 >> 7) * cur.scale_cols + cur.kb : 0), in ? 4u : 0u);
+          }
         }
-        cp_async_arrive_noinc(&sfull[s]);
+        cp_async_arrive_noinc(&sfull[s]);  // (with no copies pending it arrives at once)
         const uint8_t* src = cur.xs + cur.kb * Cf::kXBytes;
         if (split_ready)
           dev::bulk_g2s(st + Cf::kWBytes, src, Cf::kXBytes, &sfull[s]);
@@ -587,15 +589,15 @@ struct SettlePlan {
 // Chunk-map launches add one block per straddling row and 16-column group
 // (blockIdx.x >= sp.n): that row is in no segment, so the block computes it
 // directly from the chunks (straddle_row).
-template <int N>
+template <int N, bool WB>
 __device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
 
-template <int N, bool FUSED>
+template <int N, bool FUSED, bool WB>
 __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p,
                                                          const __grid_constant__ SettlePlan sp) {
   grid_dependency_wait();  // the GEMM's results are complete and visible
   if (FUSED && (int32_t)blockIdx.x >= sp.n) {
-    straddle_row<N>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
+    straddle_row<N, WB>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
     return;
   }
   const SettleTask tk = sp.task[blockIdx.x];
@@ -659,56 +661,77 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
 
 // Row st.row of a linear, read through the chunk map (a chunk boundary falls
 // inside it), for outputs m = c0 .. c0 + 15. The block stages the row in 4 KB
-// windows (32 slabs; 16-byte pieces never straddle a boundary, which is a
-// multiple of 16), so each window costs one memory round trip. Warp w takes
-// slabs w, w + 8, ... of a window and each lane four weights of a slab; a lane
-// accumulates s[kb] * x * w over its slabs for every m, and the warps' sums are
+// windows (32 slabs of 128 bytes; 16-byte pieces never straddle a boundary,
+// which is a multiple of 16), so each window costs one memory round trip. Warp
+// w takes slabs w, w + 8, ... of a window and each lane four weights of a slab
+// (e4m3: 4 bytes, times the slab's block scale; bf16: 8 bytes, no scale); a
+// lane accumulates x * w over its slabs for every m, and the warps' sums are
 // added once at the end, warp by warp in a fixed order.
-template <int N>
+template <int N, bool WB>
 __device__ void straddle_row(const DecodeParams& p, int sidx, int c0) {
   constexpr int kWin = 32 * kSlabK;  // bytes per window
   constexpr int kWarps = kTcRows / 32;
+  constexpr int kElem = WB ? 2 : 1;
   __shared__ __align__(16) uint8_t wbuf[kWin];
   __shared__ float sbuf[32];
   __shared__ float part[kWarps][16];
   const DecodeEntry& e = p.e[p.st.entry[sidx]];  // a segment of the linear: its pointers
   const int64_t r = p.st.row[sidx];                // row of the linear
-  const int64_t cols = e.cols, rows = e.y_rows, C = p.chunk_bytes, t0 = e.t_offset + r * cols;
-  const float* srow = e.scales + (r >> 7) * e.scale_cols;
+  const int64_t cols = e.cols, rowb = cols * kElem, rows = e.y_rows, C = p.chunk_bytes;
+  const int64_t t0 = e.t_offset + r * rowb;
+  const float* srow = WB ? nullptr : e.scales + (r >> 7) * e.scale_cols;
   uint16_t* const y = e.y;
   const int slabs = e.slabs, m = p.m;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float acc[16];
 #pragma unroll
   for (int h = 0; h < 16; ++h) acc[h] = 0.f;
-  for (int64_t w0 = 0; w0 < cols; w0 += kWin) {
+  for (int64_t w0 = 0; w0 < rowb; w0 += kWin) {
     __syncthreads();  // the previous window is consumed
     for (int t = threadIdx.x; t < kWin / 16; t += blockDim.x) {
       const int64_t k = w0 + 16 * t;
-      if (k < cols) {
+      if (k < rowb) {
         const int64_t g = t0 + k;
         *reinterpret_cast<uint4*>(wbuf + 16 * t) = *reinterpret_cast<const uint4*>(p.chunks[g / C] + g % C);
       }
     }
     const int kb0 = (int)(w0 / kSlabK);
-    if (threadIdx.x < 32) sbuf[threadIdx.x] = kb0 + (int)threadIdx.x < slabs ? __ldg(srow + kb0 + threadIdx.x) : 0.f;
+    if (!WB && threadIdx.x < 32)
+      sbuf[threadIdx.x] = kb0 + (int)threadIdx.x < slabs ? __ldg(srow + kb0 + threadIdx.x) : 0.f;
     __syncthreads();
     for (int sl = warp; sl < 32; sl += kWarps) {
-      const int64_t k = w0 + sl * kSlabK + lane * 4;
-      if (k >= cols) break;  // cols % 16 == 0: four weights are all in or all out
-      const uint32_t w4 = *reinterpret_cast<const uint32_t*>(wbuf + sl * kSlabK + lane * 4);
-      const float2 w01 = e4m3x2_to_f32x2(w4), w23 = e4m3x2_to_f32x2(w4 >> 16);
-      const float sc = sbuf[sl];
-      const float a0 = sc * w01.x, a1 = sc * w01.y, a2 = sc * w23.x, a3 = sc * w23.y;
+      if constexpr (WB) {
+        // 64 bf16 weights per slab: lane takes weights 2*lane, 2*lane + 1 (one
+        // 4-byte word), k = (w0 + sl*128)/2 + 2*lane
+        const int64_t kb = w0 + sl * kSlabK + lane * 4;  // byte offset in the row
+        if (kb >= rowb) break;
+        const int64_t k = kb / 2;
+        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wbuf + sl * kSlabK + lane * 4);
+        const float a0 = __uint_as_float(w2 << 16), a1 = __uint_as_float(w2 & 0xffff0000u);
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        if (c0 + h < m) {
-          const uint2 x4 = *reinterpret_cast<const uint2*>(e.x + (int64_t)(c0 + h) * cols + k);
-          float v = acc[h];
-          v = fmaf(__uint_as_float(x4.x << 16), a0, v);
-          v = fmaf(__uint_as_float(x4.x & 0xffff0000u), a1, v);
-          v = fmaf(__uint_as_float(x4.y << 16), a2, v);
-          acc[h] = fmaf(__uint_as_float(x4.y & 0xffff0000u), a3, v);
+        for (int h = 0; h < 16; ++h) {
+          if (c0 + h < m) {
+            const uint32_t x2 = *reinterpret_cast<const uint32_t*>(e.x + (int64_t)(c0 + h) * cols + k);
+            acc[h] = fmaf(__uint_as_float(x2 & 0xffff0000u), a1, fmaf(__uint_as_float(x2 << 16), a0, acc[h]));
+          }
+        }
+      } else {
+        const int64_t k = w0 + sl * kSlabK + lane * 4;
+        if (k >= cols) break;  // cols % 16 == 0: four weights are all in or all out
+        const uint32_t w4 = *reinterpret_cast<const uint32_t*>(wbuf + sl * kSlabK + lane * 4);
+        const float2 w01 = e4m3x2_to_f32x2(w4), w23 = e4m3x2_to_f32x2(w4 >> 16);
+        const float sc = sbuf[sl];
+        const float a0 = sc * w01.x, a1 = sc * w01.y, a2 = sc * w23.x, a3 = sc * w23.y;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          if (c0 + h < m) {
+            const uint2 x4 = *reinterpret_cast<const uint2*>(e.x + (int64_t)(c0 + h) * cols + k);
+            float v = acc[h];
+            v = fmaf(__uint_as_float(x4.x << 16), a0, v);
+            v = fmaf(__uint_as_float(x4.x & 0xffff0000u), a1, v);
+            v = fmaf(__uint_as_float(x4.y << 16), a2, v);
+            acc[h] = fmaf(__uint_as_float(x4.y & 0xffff0000u), a3, v);
+          }
         }
       }
     }
@@ -809,7 +832,7 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.gridDim = dim3((unsigned)blocks, N / 16);
   cfg.blockDim = dim3(kTcRows);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED>, p, sp);
+  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED, WB>, p, sp);
 }
 
 template <bool FUSED, bool WB>
@@ -826,7 +849,7 @@ cudaError_t launch_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
 
 namespace dec {
 cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s) {
-  if (bf16_w) return launch_tc<false, true>(p, grid_cap, s);  // views only: chunk-map bf16 reads use mma.sync
+  if (bf16_w) return fused ? launch_tc<true, true>(p, grid_cap, s) : launch_tc<false, true>(p, grid_cap, s);
   return fused ? launch_tc<true, false>(p, grid_cap, s) : launch_tc<false, false>(p, grid_cap, s);
 }
 int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }

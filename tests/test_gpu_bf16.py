@@ -14,7 +14,7 @@ from helpers import assert_close, bf16_tensor_to_f64
 
 pytestmark = pytest.mark.gpu
 
-KERNEL_MMA, KERNEL_MMA_FUSED, KERNEL_TC, KERNEL_PREFILL = 1, 2, 3, 5
+KERNEL_MMA, KERNEL_MMA_FUSED, KERNEL_TC, KERNEL_TC_FUSED, KERNEL_PREFILL = 1, 2, 3, 4, 5
 
 
 @pytest.fixture(scope="module")
@@ -99,8 +99,36 @@ def test_bf16_decode_through_the_chunk_map(S, bf16_stack, m):
         _, _, r, c = SHAPES[j]
         x = WL.draw_x(63, j, m, c).cuda()
         y, kinds = _linear_traced(st, j, S.SRC_FUSED, x, m)
-        assert kinds == [KERNEL_MMA_FUSED]
+        assert kinds == [KERNEL_TC_FUSED]
         assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m} (fused)")
+
+
+def test_bf16_straddling_rows_one_hot(S, bf16_stack):
+    # Rows that a chunk boundary splits are computed by the settle kernel from
+    # the chunks: with one-hot x they give the bf16 weight exactly.
+    st, bits = bf16_stack
+    plan = O.plan_layout([(l, r, c, 2) for (l, _, r, c) in SHAPES], 4)
+    lay = plan.layers[0]
+    straddling = []
+    for j, (_, _, r, c) in enumerate(SHAPES):
+        if not plan.sharded[j]:
+            continue
+        o = lay.offsets[j]
+        for i in range(1, 4):
+            b = i * lay.chunk
+            if o < b < o + r * c * 2 and (b - o) % (2 * c):
+                straddling.append((j, (b - o) // (2 * c)))
+    assert straddling
+    rng = np.random.default_rng(5)
+    m = 8
+    for j, row in straddling:
+        _, _, r, c = SHAPES[j]
+        cols = rng.integers(0, c, size=m)
+        xo = torch.zeros((m, c), dtype=torch.bfloat16)
+        xo[np.arange(m), torch.from_numpy(cols)] = 1.0
+        y, kinds = _linear_traced(st, j, S.SRC_FUSED, xo.cuda(), m)
+        assert kinds == [KERNEL_TC_FUSED]
+        assert np.array_equal(WL.bf16_bits(y[:, row].cpu()), bits[j][row, cols].astype(np.uint16)), f"entry {j} row {row}"
 
 
 @pytest.mark.parametrize("m", [3, 40, 200])
