@@ -325,6 +325,13 @@ int32_t sws_trace_count(const sws_ctx* ctx);
  * SWS_E_INVALID for an unknown option or value. */
 int sws_set_option(int32_t option, int64_t value);
 
+/* Failure-detection check: one kernel waits, with the bounded wait every
+ * kernel of the library uses, on a barrier that nothing arrives at; after
+ * limit_ns (0..1e8) it records SWS_E_TIMEOUT in the context's status word (as
+ * a kernel whose TMA copy never landed would) and returns. The context stays
+ * usable; sws_ctx_status reports and clears the code. */
+int sws_test_bounded_wait(sws_ctx* ctx, int64_t limit_ns, sws_stream_t stream);
+
 /* ---- misc --------------------------------------------------------------- */
 const char* sws_last_error(void);
 /* Library version as major*10000 + minor*100 + patch. */

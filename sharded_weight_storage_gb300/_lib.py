@@ -69,6 +69,7 @@ _PROTOS = [
     ("sws_quantize_x", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("sws_silu_mul", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
     ("sws_prefetch_layer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
+    ("sws_test_bounded_wait", C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
     ("sws_wait_prefetch", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
@@ -238,6 +239,9 @@ class Ctx:
         start, when the gather had to run inline on `stream`."""
         return check(lib().sws_wait_prefetch(self.handle, layer, slot, C.c_void_p(stream or None)),
                      "wait_prefetch") == W_COLD
+
+    def test_bounded_wait(self, limit_ns: int, stream: int = 0):
+        check(lib().sws_test_bounded_wait(self.handle, limit_ns, C.c_void_p(stream or None)), "test_bounded_wait")
 
     def run_timing(self, n: int):
         a = (C.c_float * n)()

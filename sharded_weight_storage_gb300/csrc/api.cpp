@@ -644,6 +644,13 @@ int sws_wait_prefetch(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t stre
   return cold ? SWS_W_COLD : SWS_OK;
 }
 
+int sws_test_bounded_wait(sws_ctx* c, int64_t limit_ns, sws_stream_t stream) {
+  if (!c) return fail(SWS_E_INVALID, "test_bounded_wait: ctx is NULL");
+  if (limit_ns < 0 || limit_ns > 100000000) return fail(SWS_E_INVALID, "test_bounded_wait: limit %lld ns", (long long)limit_ns);
+  cudaError_t e = launch_bounded_wait(status_word(c), (uint64_t)limit_ns, (cudaStream_t)stream);
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "test_bounded_wait: launch");
+}
+
 int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t stream) {
   return launch_silu_mul(static_cast<const uint16_t*>(gu), m, f, static_cast<uint16_t*>(act), (cudaStream_t)stream);
 }

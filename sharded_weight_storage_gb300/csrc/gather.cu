@@ -261,7 +261,22 @@ __global__ void trace_reset_kernel(uint64_t* rec, int32_t n) {
     rec[4 * i + 3] = 0;
   }
 }
+// A wait on an mbarrier that nothing arrives at, with the same bounded wait
+// every kernel of the library uses: it gives up after limit_ns and records
+// SWS_E_TIMEOUT in the status word, then the kernel returns normally.
+__global__ void bounded_wait_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  dev::mbar_init(&bar, 1);
+  dev::fence_mbar_init();
+  if (!dev::mbar_wait(&bar, 0, limit_ns)) dev::set_status(status, SWS_E_TIMEOUT);
+}
 }  // namespace
+
+cudaError_t launch_bounded_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s) {
+  bounded_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;

@@ -171,6 +171,7 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s);
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);
+cudaError_t launch_bounded_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace sws
 

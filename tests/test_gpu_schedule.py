@@ -196,3 +196,56 @@ def test_run_layers_captures_into_a_cuda_graph(S, stack, m):
             want = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[l].codes[j], layers[l].scales[j])
             assert_close(bf16_tensor_to_f64(ys[j]), want, f"replay 2, layer {l} entry {j}")
     assert st.ctx.status() == 0
+
+
+def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable(S, stack):
+    # Failure detection without a fault: a kernel waits (the library's bounded
+    # wait) on a barrier nothing arrives at, gives up after 2 ms and records
+    # SWS_E_TIMEOUT; the host reads it and the next launches run normally.
+    st, layers = stack
+    assert st.ctx.status(clear=True) == 0
+    st.ctx.test_bounded_wait(2_000_000)
+    assert st.ctx.status(clear=True) == S.E_TIMEOUT
+    assert st.ctx.status() == 0
+    m = 4
+    xs, ys, io = _io(st, 2, 2, m)
+    st.ctx.gather_to_slot(2, 0, 0)
+    for j in st.layer_entries(2):
+        st.ctx.linear(j, S.SRC_SLOT0, xs[j].data_ptr(), m, ys[j].data_ptr(), 0)
+    torch.cuda.synchronize()
+    for j in st.layer_entries(2):
+        want = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[2].codes[j], layers[2].scales[j])
+        assert_close(bf16_tensor_to_f64(ys[j]), want, f"entry {j} after the timeout")
+    assert st.ctx.status() == 0
+
+
+def test_prefill_layers_record_into_a_cuda_graph(S):
+    # m > 64: each layer's linears quantise their activations on the
+    # context's own stream, forked from and joined into `main`; that fork and
+    # join record into the graph as well.
+    w = WL.scaled_workload(WL.ATTN_KDA, rows_div=8, cols_div=8, n_layers=2, name="kda2_div8")
+    ents = workload_entries(w)
+    layers = draw_layers(w)
+    m = 130
+    st = build_stack(S, ents, w.n_shards, layers, max_m=m)
+    xs, ys, io = _io(st, 0, 1, m, key=w.key)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    st.ctx.run_layers(0, 1, io, 0, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    ref = {j: y.clone() for j, y in ys.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        st.ctx.run_layers(0, 1, io, 0, main.cuda_stream, side.cuda_stream)
+    for y in ys.values():
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for j in ys:
+        assert torch.equal(ys[j], ref[j]), f"entry {j}: graph replay differs from the eager run"
+    for l in range(2):
+        for j in st.layer_entries(l):
+            xf = WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu()))
+            xq, ex = O.quantize_x(xf)
+            want = O.dequant_x(xq, ex) @ O.dequant(layers[l].codes[j], layers[l].scales[j]).T
+            assert_close(bf16_tensor_to_f64(ys[j]), want, f"layer {l} entry {j}")
+    assert st.ctx.status() == 0
