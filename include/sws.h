@@ -317,9 +317,11 @@ int32_t sws_trace_count(const sws_ctx* ctx);
                                     the copy engines move the bytes and no SM is used (the pages'
                                     all-gather runs on copy engines too); no trace record */
 /* Process-wide options, read at each launch. Both decode kernels compute the
- * same linear (sws_linear) within the same tolerance; chunk-map (fused) reads
- * always use the mma.sync kernel. A tcgen05 launch is three kernels on the
- * stream (activation split, GEMM, split-K settle); an mma.sync launch is one.
+ * same linear (sws_linear) within the same tolerance, from views and through
+ * the chunk map (a chunk-map launch whose segments or split rows exceed the
+ * tcgen05 launch's tables runs on the mma.sync kernel). A tcgen05 launch is
+ * three kernels on the stream (activation split, GEMM, split-K settle); an
+ * mma.sync launch is one.
  * Both prefill kernels compute the same sums in the same slab order per output
  * element and give bit-identical results.
  * SWS_E_INVALID for an unknown option or value. */

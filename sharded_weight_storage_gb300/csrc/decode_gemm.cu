@@ -1,6 +1,9 @@
-// Split-K FP8 skinny decode GEMM (m <= 64) on zero-copy weight views.
+// Split-K FP8 skinny decode GEMM (m <= 64) on zero-copy weight views, on
+// warp-level mma.sync (the tcgen05 kernel in decode_tc.cu is the default).
 //
 //   Y[m, o] = bf16_rne( sum_kb s[o/128, kb] * sum_{i in kb} x[m, i] * e4m3(q[o, i]) )
+//
+// (bf16 weights, WB: the same without scales, 64 K per 128-byte slab row.)
 //
 // The linear the weight-sharding blog keeps unchanged (section "核心抽象":
 // the GEMM sees the full W; Y = X W^T with W [out, in]); block scales are
@@ -623,7 +626,8 @@ void set_decode_kernel(int k) { g_decode_kernel = k; }
 
 // The tcgen05 kernel streams the weights at the HBM rate for every m <= 64
 // (its MMAs and activation split are small next to the weight bytes); the
-// mma.sync kernel serves the fused path and can be selected for comparison.
+// mma.sync kernel serves chunk-map launches beyond the tcgen05 segment tables
+// and can be selected for comparison.
 int decode_kernel_for(int64_t m) {
   if (g_decode_kernel != kDecodeAuto) return g_decode_kernel;
   (void)m;
