@@ -232,3 +232,26 @@ def test_per_tensor_fp8_scale(S, m):
         else:
             ref = O.linear_per_tensor(xf, codes[j], sc[j])
         assert_close(bf16_tensor_to_f64(y), ref, f"entry {j} m {m}")
+
+
+def test_bf16_shared_expert_full_size_sampled(S):
+    # The shared-expert layer at full size with bf16 weights (528 MB, N = 16):
+    # decode at M = 32 from the slot and through the chunk map, and prefill at
+    # m = 2048, on 40 sampled output rows (all tokens) against the oracle.
+    w = WL.SHARED_EXPERT
+    shapes = [(0, S.BF16, e.rows, e.cols) for e in w.entries]
+    bits = [WL.draw_weight_bf16(71, 0, j, e.rows, e.cols) for j, e in enumerate(w.entries)]
+    st = _stack(S, shapes, w.n_shards, [_as_bytes(b) for b in bits], max_m=2048)
+    st.ctx.gather_to_slot(0, 0, 0)
+    rng = np.random.default_rng(72)
+    for j, e in enumerate(w.entries):
+        rows = np.unique(np.concatenate([[0, e.rows - 1], rng.choice(e.rows, size=38, replace=False)]))
+        wsel = bits[j][rows]
+        for m, src, kind in ((32, S.SRC_SLOT0, KERNEL_TC), (32, S.SRC_FUSED, KERNEL_TC_FUSED),
+                             (2048, S.SRC_SLOT0, KERNEL_PREFILL)):
+            x = WL.draw_x(73, j, m, e.cols).cuda()
+            y, kinds = _linear_traced(st, j, src, x, m)
+            assert kinds == [kind]
+            want = O.linear_bf16(_x64(x), wsel)
+            assert_close(bf16_tensor_to_f64(y)[:, rows], want, f"{e.name} m {m} src {src}")
+    assert st.ctx.status() == 0
