@@ -28,7 +28,8 @@ Readings taken where the pages are silent (each also listed in the design notes)
   * Y = X W^T with W [out, in]; block scale s[o // 128, i // 128] multiplies the
     decoded code; partial edge blocks use ceil(./128) indexing;
   * BF16 weights: the same linear with W decoded from bfloat16 patterns and
-    no scales; ModelOpt FP8: one float32 scale for the whole weight;
+    no scales; FP16 weights: W from binary16 patterns and x rounded to f16 (the
+    f16 tensor-core operand); ModelOpt FP8: one float32 scale for the whole weight;
   * prefill activations: per (row, 128-column group) scale e = 2^k with k the
     smallest integer such that amax <= 448 * 2^k (amax = 0 gives e = 1), and
     codes xq = e4m3_rne(x / e), ties to even, saturating to +-448.
@@ -265,6 +266,48 @@ def bf16_decode(bits: np.ndarray) -> np.ndarray:
 def linear_bf16(x: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
     """Y = X W^T in float64 with W [out, in] given as bfloat16 bit patterns."""
     return np.asarray(x, dtype=np.float64) @ bf16_decode(w_bits).T
+
+
+def f16_decode(bits: np.ndarray) -> np.ndarray:
+    """Value of each 16-bit IEEE binary16 pattern in float64: sign bit, 5
+    exponent bits (bias 15), 10 fraction bits; exponent 0 is subnormal
+    (f * 2^-24), exponent 31 is infinity (f = 0) or NaN."""
+    b = np.asarray(bits, dtype=np.int64)
+    sign = np.where(b & 0x8000, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int64))
+    sub = np.ldexp(f, -24)
+    v = np.where(e == 0, sub, normal)
+    v = np.where(e == 31, np.where(f == 0, np.inf, np.nan), v)
+    return sign * v
+
+
+def f16_round(v: np.ndarray) -> np.ndarray:
+    """Nearest binary16 value of each float64 (11 significant bits, subnormal
+    spacing 2^-24), ties to the even significand; beyond the largest finite
+    value (65504) the result is infinity."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros_like(v)
+    fin = np.isfinite(v) & (v != 0)
+    f, p = np.frexp(np.abs(v[fin]))
+    p = np.maximum(p, -13)                     # below 2^-14 the spacing stays 2^-24
+    scaled = np.ldexp(np.abs(v[fin]), 11 - p)  # significand in [1024, 2048)
+    r = np.floor(scaled)
+    frac = scaled - r
+    r = r + ((frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1)))
+    mag = np.ldexp(r, p - 11)
+    mag = np.where(mag > 65504.0, np.inf, mag)
+    out[fin] = np.sign(v[fin]) * mag
+    out[~np.isfinite(v)] = v[~np.isfinite(v)]
+    return out
+
+
+def linear_f16(x: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """Y = X W^T in float64 with W [out, in] given as binary16 patterns; the
+    activations enter the f16 tensor-core operand, so they are rounded to f16
+    first (exact for bf16 values with |x| in [2^-14, 65504])."""
+    return f16_round(np.asarray(x, dtype=np.float64)) @ f16_decode(w_bits).T
 
 
 def linear_per_tensor(x: np.ndarray, codes: np.ndarray, scale: float) -> np.ndarray:

@@ -388,6 +388,44 @@ def test_linear_bf16_one_hot_and_transposition():
         assert np.array_equal(O.linear_bf16(x, w)[0], O.bf16_decode(w[:, i]))
 
 
+def test_f16_decode_closed_forms_and_every_pattern():
+    cases = {0x3C00: 1.0, 0xC000: -2.0, 0x3800: 0.5, 0x7BFF: 65504.0, 0x0400: 2.0 ** -14, 0x0001: 2.0 ** -24,
+             0x0000: 0.0, 0x3555: 0.333251953125}
+    for bits, want in cases.items():
+        assert O.f16_decode(np.array([bits]))[0] == want, hex(bits)
+    assert np.isinf(O.f16_decode(np.array([0x7C00]))[0]) and np.isnan(O.f16_decode(np.array([0x7E00]))[0])
+    bits = np.arange(1 << 16, dtype=np.int64)
+    ref = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    o = O.f16_decode(bits)
+    assert ((o == ref) | (np.isnan(o) & np.isnan(ref))).all()
+
+
+def test_f16_round_closed_forms_and_numpy():
+    cases = {1 + 2.0 ** -11: 1.0, 1 + 3 * 2.0 ** -11: 1 + 2.0 ** -9, 1 + 2.0 ** -11 + 2.0 ** -30: 1 + 2.0 ** -10,
+             2.0 ** -25: 0.0, 3 * 2.0 ** -26: 2.0 ** -24, 65519.0: 65504.0, 0.0: 0.0}
+    for v, want in cases.items():
+        assert O.f16_round(np.array([v]))[0] == want, v
+    assert np.isinf(O.f16_round(np.array([65520.0]))[0])
+    rng = np.random.default_rng(43)
+    v = rng.standard_normal(50000) * 10.0 ** rng.integers(-9, 5, 50000)
+    assert np.array_equal(O.f16_round(v), v.astype(np.float16).astype(np.float64))
+
+
+def test_linear_f16_exact_rational_and_one_hot():
+    rng = np.random.default_rng(44)
+    w = (rng.standard_normal((7, 40)) * 0.05).astype(np.float16).view(np.uint16)
+    x = _bf16_values(rng, (3, 40))
+    y = O.linear_f16(x, w)
+    wv, xv = O.f16_decode(w), O.f16_round(x)
+    for a in range(3):
+        for o in range(7):
+            exact = sum(Fraction(float(xv[a, i])) * Fraction(float(wv[o, i])) for i in range(40))
+            assert abs(Fraction(float(y[a, o])) - exact) <= Fraction(1, 10**12) * (1 + abs(exact))
+    e = np.zeros((1, 40))
+    e[0, 9] = 1.0
+    assert np.array_equal(O.linear_f16(e, w)[0], O.f16_decode(w[:, 9]))
+
+
 def test_linear_per_tensor_is_block_linear_with_a_constant_grid():
     rng = np.random.default_rng(33)
     q = rng.integers(0, 0x7E, size=(300, 260), dtype=np.uint8)
