@@ -26,7 +26,7 @@
  *   - Streams: sws_stream_t is a cudaStream_t; NULL is the legacy default
  *     stream. All device work is asynchronous with respect to the host.
  *   - Element types: SWS_E4M3 is OCP FP8 E4M3FN (1 byte), SWS_BF16 2 bytes,
- *     SWS_F32 4 bytes, SWS_U8 1 byte.
+ *     SWS_F32 4 bytes, SWS_U8 1 byte, SWS_F16 IEEE binary16 (2 bytes).
  */
 #ifndef SWS_H_
 #define SWS_H_
@@ -57,6 +57,7 @@ extern "C" {
 #define SWS_BF16 1
 #define SWS_F32 2
 #define SWS_U8 3
+#define SWS_F16 4
 
 /* ---- linear weight sources --------------------------------------------- */
 #define SWS_SRC_SLOT0 0 /* view of slot 0 (must hold the entry's layer) */
@@ -77,7 +78,7 @@ typedef struct sws_ctx sws_ctx;
  * one row shards split), cols = in_features; row-major [rows, cols]. */
 typedef struct sws_entry {
   int32_t layer; /* layer id, 0 <= layer < 2^20 */
-  int32_t dtype; /* SWS_E4M3, SWS_BF16, SWS_F32 or SWS_U8 */
+  int32_t dtype; /* SWS_E4M3, SWS_BF16, SWS_F32, SWS_U8 or SWS_F16 */
   int64_t rows;
   int64_t cols;
 } sws_entry;
@@ -168,18 +169,22 @@ int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t s
  * fp32 accumulation, Y rounded to bf16 (nearest even):
  *   E4M3 entries: Y[m, o] = sum_i x[m, i] * e4m3(q[o, i]) * s[o/128, i/128];
  *   BF16 entries: Y[m, o] = sum_i x[m, i] * w[o, i]  (no scales; the blog's
- *                 unquantised variant goes through the same flat layout).
+ *                 unquantised variant goes through the same flat layout);
+ *   F16 entries:  Y[m, o] = sum_i f16(x[m, i]) * w[o, i]  (w IEEE binary16,
+ *                 x rounded to nearest even f16 first, the tensor cores'
+ *                 operands of one MMA sharing one format).
  * W_j is the view slot + o_j (src = SWS_SRC_SLOT0/1; the slot's tag must equal
  * the entry's layer, else SWS_E_STATE), the chunks themselves
  * (SWS_SRC_FUSED), or the replicated buffer for entries outside T (src
  * ignored). x: bf16 [m, cols] row-major; y: bf16 [m, rows] row-major.
  * m in [0, 2^31). m <= 64 runs a split-K decode launch, by default on the
  * tcgen05 kernel (SWS_OPT_DECODE_KERNEL): for E4M3 with x split exactly into
- * two e4m3 terms (kind::f8f6f4), for BF16 on bf16 operands (kind::f16),
- * from views or through the chunk map (SWS_SRC_FUSED).
+ * two e4m3 terms (kind::f8f6f4), for BF16 / F16 on bf16 / f16 operands
+ * (kind::f16), from views or through the chunk map (SWS_SRC_FUSED).
  * m > 64 runs the prefill path: E4M3 quantises x (sws_quantize_x into the
  * workspace) and runs the tcgen05 block-scaled FP8 GEMM; BF16 runs a tcgen05
- * bf16 GEMM on x directly. Requires E4M3 or BF16 weights (else
+ * bf16 GEMM on x directly; F16 rounds x to f16 into the workspace and runs
+ * the same GEMM on f16 operands. Requires E4M3, BF16 or F16 weights (else
  * SWS_E_UNSUPPORTED), cols % 16 == 0, and, for E4M3 with m > 64,
  * cols % 128 == 0; E4M3 entries need their scales. Linears that share a
  * context must not overlap on the GPU (they share the workspace). */
@@ -190,7 +195,7 @@ int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t 
  * with io->x[k] / io->y[k] for its k-th entry and a common m: the decode-sized
  * ones (m <= 64) run as grouped launches, up to 8 linears per launch, one
  * group per weight source (views: slot src or replicated buffers; chunk-map
- * reads: SWS_SRC_FUSED) and weight type (E4M3, BF16), so a layer pays one
+ * reads: SWS_SRC_FUSED) and weight type (E4M3, BF16, F16), so a layer pays one
  * launch instead of one per weight. Same results and rules as sws_linear for
  * each entry. */
 int sws_layer_linears(sws_ctx* ctx, int32_t layer, int32_t src, const sws_layer_io* io, sws_stream_t stream);

@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libsws.so")
 
 OK, W_SKIPPED, W_COLD = 0, 1, 2
 E_INVALID, E_ALIGN, E_STATE, E_CUDA, E_TIMEOUT, E_UNSUPPORTED, E_WORKSPACE = -1, -2, -3, -4, -5, -6, -7
-E4M3, BF16, F32, U8 = 0, 1, 2, 3
+E4M3, BF16, F32, U8, F16 = 0, 1, 2, 3, 4
 SRC_SLOT0, SRC_SLOT1, SRC_FUSED = 0, 1, 2
 RUN_FUSED, RUN_TIMING, RUN_FIRST_PREFETCHED = 1, 2, 4
 OPT_DECODE_KERNEL = 1

@@ -6,7 +6,12 @@
 // computed in fp32. HBM-bound: 6 bytes in and 2 out per output element; each
 // thread handles 8 consecutive columns with 16-byte loads and stores, over a
 // grid-stride loop sized to the SM count.
+//
+// Also here: the bf16 -> f16 rounding of activations that meet f16 weights at
+// prefill sizes (the tensor cores take both operands of one MMA in the same
+// 16-bit format), 2 bytes in and 2 out per element.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -44,7 +49,35 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t* __restric
   }
 }
 
+// Each bf16 value rounded to nearest even f16 (overflow to +-inf).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const __half2 h = __floats2half2_rn(bf16_lo(v), bf16_hi(v));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(256) to_f16_kernel(const uint16_t* __restrict__ x, int64_t n8,
+                                                      uint16_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    uint4 o;
+    o.x = bf16x2_to_f16x2(v.x);
+    o.y = bf16x2_to_f16x2(v.y);
+    o.z = bf16x2_to_f16x2(v.z);
+    o.w = bf16x2_to_f16x2(v.w);
+    reinterpret_cast<uint4*>(out)[i] = o;
+  }
+}
+
 }  // namespace
+
+int launch_to_f16(const uint16_t* x, int64_t n, uint16_t* out, cudaStream_t s) {
+  if (n < 0 || n % 8 != 0) return fail(SWS_E_UNSUPPORTED, "to_f16: n=%lld is not a multiple of 8", (long long)n);
+  if (n == 0) return SWS_OK;
+  if (!aligned16(x) || !aligned16(out)) return fail(SWS_E_ALIGN, "to_f16: pointer not 16-byte aligned");
+  const int64_t blocks = std::min<int64_t>(cdiv(n / 8, 256), (int64_t)device_sm_count() * 8);
+  cudaError_t e = launch_high(to_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, n / 8, out);
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "to_f16 kernel launch");
+}
 
 int launch_silu_mul(const uint16_t* gu, int64_t m, int64_t f, uint16_t* act, cudaStream_t s) {
   if (m < 0 || f < 0) return fail(SWS_E_INVALID, "silu_mul: m=%lld f=%lld", (long long)m, (long long)f);

@@ -55,10 +55,17 @@ uint64_t* next_trace(sws_ctx* c) {
   return c->trace + 4 * (int64_t)(c->trace_next++);
 }
 
-int64_t prefill_bytes(int64_t m, int64_t cols) {
+// Workspace one prefill linear's activations need: E4M3 entries the
+// quantiser's xq and ex, F16 entries x rounded to f16; BF16 entries none.
+int64_t prefill_bytes(int32_t dtype, int64_t m, int64_t cols) {
   if (m <= 64) return 0;
+  if (dtype == SWS_F16) return roundup(2 * m * cols, 256);
+  if (dtype != SWS_E4M3) return 0;
   return roundup(m * cols, 256) + roundup(m * cdiv(cols, 128) * 4, 256);
 }
+
+// Weight type of a decode group: 0 e4m3 codes with block scales, 1 bf16, 2 f16.
+int weight_type(int32_t dtype) { return dtype == SWS_BF16 ? 1 : dtype == SWS_F16 ? 2 : 0; }
 
 int ensure_events(sws_ctx* c, size_t n) {
   while (c->t_wait.size() < n) {
@@ -145,8 +152,8 @@ int check_linear_args(sws_ctx* c, int32_t j, const void* x, int64_t m, void* y) 
   const sws_plan* p = c->plan;
   if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "linear: entry %d", j);
   const EntryPlan& e = p->entries[j];
-  if (e.dtype != SWS_E4M3 && e.dtype != SWS_BF16)
-    return fail(SWS_E_UNSUPPORTED, "linear: entry %d is neither E4M3 nor BF16", j);
+  if (e.dtype != SWS_E4M3 && e.dtype != SWS_BF16 && e.dtype != SWS_F16)
+    return fail(SWS_E_UNSUPPORTED, "linear: entry %d is not E4M3, BF16 or F16", j);
   if (m < 0 || m >= ((int64_t)1 << 31)) return fail(SWS_E_INVALID, "linear: m=%lld", (long long)m);
   if (m == 0 || e.rows == 0) return SWS_OK;
   if (!x || !y) return fail(SWS_E_INVALID, "linear: x or y is NULL");
@@ -184,7 +191,9 @@ int launch_group(sws_ctx* c, DecodeGroup& g, int32_t layer, int32_t first_entry,
   return rc;
 }
 
-// Quantised activations of a prefill linear: xq [m, cols] then ex [m, cols/128].
+// Activations of a prefill linear in the workspace: for E4M3 weights the
+// quantiser's xq [m, cols] then ex [m, cols/128]; for F16 weights x as f16
+// [m, cols] at xq.
 struct PrefillBuf {
   uint8_t* xq;
   float* ex;
@@ -213,9 +222,9 @@ int prefill_gemm(sws_ctx* c, int32_t j, const uint8_t* w, const PrefillBuf& q, i
   return launch_prefill(pl, s);
 }
 
-// BF16 weights at prefill sizes: no quantiser, the bf16 activations feed the
-// tensor cores directly.
-int prefill_linear_bf16(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+// 16-bit weights at prefill sizes: no quantiser, the activations (bf16 as
+// given, or already rounded to f16 for f16 weights) feed the tensor cores.
+int prefill_linear_16(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
   PrefillLaunch pl;
   pl.w = w;
@@ -229,18 +238,24 @@ int prefill_linear_bf16(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, 
   pl.status = status_word(c);
   pl.trace = next_trace(c);
   pl.tag = (kTraceLinear << 56) | (kTracePrefill << 48) | ((uint64_t)e.layer << 32) | (uint64_t)(uint32_t)j;
-  return launch_prefill_bf16(pl, s);
+  return launch_prefill_16(pl, e.dtype == SWS_F16, s);
 }
 
 int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
-  if (e.dtype == SWS_BF16) return prefill_linear_bf16(c, j, w, x, m, y, s);
-  if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
-  const int64_t need = c->ws_decode + prefill_bytes(m, e.cols);
+  if (e.dtype == SWS_BF16) return prefill_linear_16(c, j, w, x, m, y, s);
+  if (e.dtype == SWS_E4M3 && e.cols % 128 != 0)
+    return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+  const int64_t need = c->ws_decode + prefill_bytes(e.dtype, m, e.cols);
   if (c->ws_bytes < need)
     return fail(SWS_E_WORKSPACE, "linear: workspace %lld < %lld bytes for m=%lld", (long long)c->ws_bytes,
                 (long long)need, (long long)m);
   const PrefillBuf q = prefill_buf(c, 0, 0, m, e.cols);
+  if (e.dtype == SWS_F16) {
+    int rc = launch_to_f16(static_cast<const uint16_t*>(x), m * e.cols, reinterpret_cast<uint16_t*>(q.xq), s);
+    if (rc != SWS_OK) return rc;
+    return prefill_linear_16(c, j, w, q.xq, m, y, s);
+  }
   int rc = launch_quantize_x(static_cast<const uint16_t*>(x), m, e.cols, q.xq, q.ex, s);
   if (rc != SWS_OK) return rc;
   return prefill_gemm(c, j, w, q, m, y, s);
@@ -248,23 +263,25 @@ int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64
 
 int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s);
 
-// A prefill layer: the q-th E4M3 linear's activations are quantised on the
-// context's side stream into buffer q % 2 while the previous GEMM runs on `s`;
-// GEMM q waits for its quantiser, and quantiser q waits for GEMM q - 2, the
-// last reader of its buffer. BF16 linears need no quantiser and run on `s` in
-// order. Without room for two buffers the linears run one after another.
+// A prefill layer: the q-th E4M3 linear's activations are quantised (the q-th
+// F16 linear's rounded to f16) on the context's side stream into buffer q % 2
+// while the previous GEMM runs on `s`; GEMM q waits for its quantiser, and
+// quantiser q waits for GEMM q - 2, the last reader of its buffer. BF16
+// linears need neither and run on `s` in order. Without room for two buffers
+// the linears run one after another.
 int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_io& io, cudaStream_t s) {
   const int64_t m = io.m;
   int64_t per_buf = 0;
-  int n_fp8 = 0;
+  int n_q = 0;  // linears whose activations go through the side stream
   for (int32_t j : lp.all) {
     const EntryPlan& e = c->plan->entries[j];
-    if (e.dtype != SWS_E4M3) continue;
-    if (e.cols % 128 != 0) return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
-    per_buf = std::max(per_buf, prefill_bytes(m, e.cols));
-    ++n_fp8;
+    if (e.dtype != SWS_E4M3 && e.dtype != SWS_F16) continue;
+    if (e.dtype == SWS_E4M3 && e.cols % 128 != 0)
+      return fail(SWS_E_UNSUPPORTED, "linear: prefill needs cols %% 128 == 0");
+    per_buf = std::max(per_buf, prefill_bytes(e.dtype, m, e.cols));
+    ++n_q;
   }
-  if (n_fp8 < 2 || c->ws_bytes < c->ws_decode + 2 * per_buf) {
+  if (n_q < 2 || c->ws_bytes < c->ws_decode + 2 * per_buf) {
     for (size_t k = 0; k < lp.all.size(); ++k) {
       int rc = linear_impl(c, lp.all[k], src, io.x[k], m, io.y[k], s);
       if (rc != SWS_OK) return rc;
@@ -274,7 +291,7 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
   cudaError_t ce = cudaEventRecord(c->call_start, s);  // the activations are ready in s's order
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(c->qstream, c->call_start, 0);
   if (ce != cudaSuccess) return cuda_fail(ce, "prefill layer: stream order");
-  int qi = 0;  // E4M3 linears so far
+  int qi = 0;  // E4M3 and F16 linears so far
   for (size_t k = 0; k < lp.all.size(); ++k) {
     const int32_t j = lp.all[k];
     int rc = check_linear_args(c, j, io.x[k], m, io.y[k]);
@@ -287,7 +304,7 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
     if (rc != SWS_OK) return rc;
     if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
     if (e.dtype == SWS_BF16) {
-      rc = prefill_linear_bf16(c, j, w, io.x[k], m, io.y[k], s);
+      rc = prefill_linear_16(c, j, w, io.x[k], m, io.y[k], s);
       if (rc != SWS_OK) return rc;
       continue;
     }
@@ -296,12 +313,15 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
     if (qi >= 2 && (ce = cudaStreamWaitEvent(c->qstream, c->g_done[b], 0)) != cudaSuccess)
       return cuda_fail(ce, "prefill layer: wait");
     ++qi;
-    rc = launch_quantize_x(static_cast<const uint16_t*>(io.x[k]), m, e.cols, q.xq, q.ex, c->qstream);
+    const bool f16 = e.dtype == SWS_F16;
+    rc = f16 ? launch_to_f16(static_cast<const uint16_t*>(io.x[k]), m * e.cols, reinterpret_cast<uint16_t*>(q.xq),
+                             c->qstream)
+             : launch_quantize_x(static_cast<const uint16_t*>(io.x[k]), m, e.cols, q.xq, q.ex, c->qstream);
     if (rc != SWS_OK) return rc;
     if ((ce = cudaEventRecord(c->q_done[b], c->qstream)) != cudaSuccess ||
         (ce = cudaStreamWaitEvent(s, c->q_done[b], 0)) != cudaSuccess)
       return cuda_fail(ce, "prefill layer: quantiser order");
-    rc = prefill_gemm(c, j, w, q, m, io.y[k], s);
+    rc = f16 ? prefill_linear_16(c, j, w, q.xq, m, io.y[k], s) : prefill_gemm(c, j, w, q, m, io.y[k], s);
     if (rc != SWS_OK) return rc;
     if ((ce = cudaEventRecord(c->g_done[b], s)) != cudaSuccess) return cuda_fail(ce, "prefill layer: record");
   }
@@ -323,26 +343,27 @@ int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, vo
   }
   DecodeGroup g;
   init_group(c, g, e.layer, m, fused);
-  g.bf16_w = e.dtype == SWS_BF16;
+  g.wtype = weight_type(e.dtype);
   g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), e.rows,
                              e.cols, e.offset};
   return launch_group(c, g, e.layer, j, s);
 }
 
 // All linears of a layer: decode-sized ones go out as grouped launches, one
-// group per (views by TMA or chunk-map reads) x (E4M3 or BF16 weights), up to
-// kMaxDecodeGroup per launch.
+// group per (views by TMA or chunk-map reads) x (E4M3, BF16 or F16 weights),
+// up to kMaxDecodeGroup per launch.
 int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io, cudaStream_t s) {
   const LayerPlan& lp = c->plan->layers[layer];
   if (lp.all.empty()) return SWS_OK;
   if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
   const int64_t m = io.m;
   if (m > 64) return prefill_layer(c, lp, src, io, s);
-  DecodeGroup grp[4];  // index: fused * 2 + bf16
-  int32_t first[4] = {-1, -1, -1, -1};
-  for (int q = 0; q < 4; ++q) {
-    init_group(c, grp[q], layer, m, q >= 2);
-    grp[q].bf16_w = (q & 1) != 0;
+  constexpr int kGroups = 6;  // index: fused * 3 + weight type
+  DecodeGroup grp[kGroups];
+  int32_t first[kGroups] = {-1, -1, -1, -1, -1, -1};
+  for (int q = 0; q < kGroups; ++q) {
+    init_group(c, grp[q], layer, m, q >= 3);
+    grp[q].wtype = q % 3;
   }
   for (size_t k = 0; k < lp.all.size(); ++k) {
     const int32_t j = lp.all[k];
@@ -354,7 +375,7 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
     bool fused = false;
     rc = weight_source(c, j, src, &w, &fused);
     if (rc != SWS_OK) return rc;
-    const int q = (fused ? 2 : 0) + (e.dtype == SWS_BF16 ? 1 : 0);
+    const int q = (fused ? 3 : 0) + weight_type(e.dtype);
     DecodeGroup& g = grp[q];
     if (g.n == kMaxDecodeGroup) {
       rc = launch_group(c, g, layer, first[q], s);
@@ -364,7 +385,7 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
     g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(io.x[k]), static_cast<uint16_t*>(io.y[k]),
                                e.rows, e.cols, e.offset};
   }
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kGroups; ++q) {
     int rc = launch_group(c, grp[q], layer, first[q], s);
     if (rc != SWS_OK) return rc;
   }
@@ -394,7 +415,7 @@ int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   if (decode_workspace_bytes(mm, &dec) != SWS_OK) return -1;
   int64_t pre = 0;
   for (const EntryPlan& e : p->entries)
-    if (e.dtype == SWS_E4M3) pre = std::max(pre, prefill_bytes(max_m, e.cols));
+    pre = std::max(pre, prefill_bytes(e.dtype, max_m, e.cols));
   return dec + split_region_bytes(p, mm) + 2 * pre;  // two buffers: quantiser k + 1 beside GEMM k
 }
 

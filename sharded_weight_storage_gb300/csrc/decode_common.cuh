@@ -178,7 +178,8 @@ __host__ __device__ constexpr int64_t tc_split_block_bytes(int64_t n_pad) { retu
 __host__ __device__ constexpr int64_t tc_x_block_bytes(int64_t n_pad, bool bf16_w) {
   return bf16_w ? 128 * n_pad : tc_split_block_bytes(n_pad);
 }
-cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s);
+// wtype: 0 e4m3 weights with block scales, 1 bf16 weights, 2 f16 weights.
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int wtype, int64_t grid_cap, cudaStream_t s);
 int64_t tc_slot_bytes(int64_t m);
 
 }  // namespace dec

@@ -3,7 +3,8 @@
 //
 //   Y[m, o] = bf16_rne( sum_kb s[o/128, kb] * sum_{i in kb} x[m, i] * e4m3(q[o, i]) )
 //
-// (bf16 weights, WB: the same without scales, 64 K per 128-byte slab row.)
+// (bf16 or f16 weights, WT = 1 or 2: the same without scales, 64 K per
+// 128-byte slab row; for f16 weights x is rounded to f16.)
 //
 // The linear the weight-sharding blog keeps unchanged (section "核心抽象":
 // the GEMM sees the full W; Y = X W^T with W [out, in]); block scales are
@@ -59,7 +60,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
 // Weight element types: WB = false for e4m3 codes (128 K per 128-byte slab
-// row, block scales), WB = true for bf16 weights (64 K per slab row, no
+// row, block scales), WB = true for 16-bit weights (64 K per slab row, no
 // scales). Either way a slab row is 128 bytes, so the staging, the swizzle and
 // the TMA boxes are the same.
 template <bool WB>
@@ -95,8 +96,9 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32
 
 // ---- activation staging: one slab of bf16 X -> shared (as f16 for e4m3
 // weights, as bf16 for bf16 weights) ------------------------------------------
-template <int NT, bool WB>
+template <int NT, int WT>
 struct XStage {
+  static constexpr bool WB = WT != 0;
   static constexpr int kRowUnits = slab_elems<WB>() / 8;  // 16-byte units per row
   static constexpr int kUnits = NT * 8 * kRowUnits;         // 16-byte units per slab
   static constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
@@ -121,7 +123,7 @@ struct XStage {
       if (v < kUnits) {
         const int mrow = v / kRowUnits, q = v % kRowUnits;
         uint4 h = r[i];
-        if constexpr (!WB) {
+        if constexpr (WT != 1) {  // f16 operands: e4m3 and f16 weights
           h.x = bf16x2_to_f16x2(r[i].x);
           h.y = bf16x2_to_f16x2(r[i].y);
           h.z = bf16x2_to_f16x2(r[i].z);
@@ -171,28 +173,36 @@ __device__ __forceinline__ void mma_half_e4m3(float (&acc)[R][NT][4], const uint
   }
 }
 
-// bf16 weights: wq[rt][h] holds the 8 weights of row (g + 8h) of row tile rt
-// at k = 16*tig + 8*l + [0, 8); the activations come from unit 2*tig + l.
-template <int NT, int R>
-__device__ __forceinline__ void mma_half_bf16(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
-                                              int g, int tig) {
+// 16-bit weights: wq[rt][h] holds the 8 weights of row (g + 8h) of row tile
+// rt at k = 16*tig + 8*l + [0, 8); the activations come from unit 2*tig + l
+// (bf16, or f16 for f16 weights).
+template <int NT, int R, bool F16>
+__device__ __forceinline__ void mma_half_16(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
+                                            int g, int tig) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int mrow = nt * 8 + g;
     const uint4 b = xb[mrow * 8 + xpos<true>(2 * tig + l, mrow)];
 #pragma unroll
     for (int rt = 0; rt < R; ++rt) {
-      mma16816_bf16(acc[rt][nt], wq[rt][0].x, wq[rt][1].x, wq[rt][0].y, wq[rt][1].y, b.x, b.y);
-      mma16816_bf16(acc[rt][nt], wq[rt][0].z, wq[rt][1].z, wq[rt][0].w, wq[rt][1].w, b.z, b.w);
+      if constexpr (F16) {
+        mma16816(acc[rt][nt], wq[rt][0].x, wq[rt][1].x, wq[rt][0].y, wq[rt][1].y, b.x, b.y);
+        mma16816(acc[rt][nt], wq[rt][0].z, wq[rt][1].z, wq[rt][0].w, wq[rt][1].w, b.z, b.w);
+      } else {
+        mma16816_bf16(acc[rt][nt], wq[rt][0].x, wq[rt][1].x, wq[rt][0].y, wq[rt][1].y, b.x, b.y);
+        mma16816_bf16(acc[rt][nt], wq[rt][0].z, wq[rt][1].z, wq[rt][0].w, wq[rt][1].w, b.z, b.w);
+      }
     }
   }
 }
 
-template <int NT, int R, bool WB>
+template <int NT, int R, int WT>
 __device__ __forceinline__ void mma_half(float (&acc)[R][NT][4], const uint4 (&wq)[R][2], const uint4* xb, int l,
                                          int g, int tig) {
-  if constexpr (WB)
-    mma_half_bf16<NT, R>(acc, wq, xb, l, g, tig);
+  if constexpr (WT == 1)
+    mma_half_16<NT, R, false>(acc, wq, xb, l, g, tig);
+  else if constexpr (WT == 2)
+    mma_half_16<NT, R, true>(acc, wq, xb, l, g, tig);
   else
     mma_half_e4m3<NT, R>(acc, wq, xb, l, g, tig);
 }
@@ -343,15 +353,16 @@ __device__ __forceinline__ void settle_partials(const DecodeParams& p, const Run
 // FUSED = false: weight slabs come from the views by TMA (thread 0 issues).
 // FUSED = true:  every thread copies 16-byte pieces straight from the chunks
 //                with cp.async into the same swizzled layout.
-// WB: bf16 weights (no scales) instead of e4m3 codes with block scales.
-template <int NT, int R, int S, bool FUSED, bool WB>
+// WT: 0 e4m3 codes with block scales; 1 bf16, 2 f16 weights (no scales).
+template <int NT, int R, int S, bool FUSED, int WT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int kRowsWarp = 16 * R;
   constexpr int kRowsCta = kWarps * kRowsWarp;
   constexpr int kStage = kRowsCta * kSlabK;  // bytes of one staged weight slab
   constexpr int kBoxRows = kRowsCta > 256 ? 256 : kRowsCta;
   constexpr int kBoxes = kRowsCta / kBoxRows;
-  using XS = XStage<NT, WB>;
+  using XS = XStage<NT, WT>;
+  constexpr bool WB = WT != 0;
   constexpr int kElem = WB ? 2 : 1;  // bytes per weight
 
   extern __shared__ uint8_t dsm[];
@@ -492,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             const int r = warp * kRowsWarp + rt * 16 + g + 8 * h;
             wq[rt][h] = *reinterpret_cast<const uint4*>(wb + r * kSlabK + (((2 * tig + l) ^ g) << 4));
           }
-        mma_half<NT, R, WB>(acc, wq, xs[i & 1], l, g, tig);
+        mma_half<NT, R, WT>(acc, wq, xs[i & 1], l, g, tig);
       }
     }
     if (i + 1 < n) cx.store(xs[(i + 1) & 1], tid);
@@ -525,13 +536,13 @@ int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
 int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
-template <int NT, bool FUSED, bool WB>
+template <int NT, bool FUSED, int WT>
 cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int R = rows_per_warp_tiles<NT>();
   constexpr int S = stages_for<NT>();
   constexpr int kRowsCta = kWarps * 16 * R;
   constexpr int kSmem = S * kRowsCta * kSlabK + 1024;
-  auto kern = decode_kernel<NT, R, S, FUSED, WB>;
+  auto kern = decode_kernel<NT, R, S, FUSED, WT>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
@@ -540,17 +551,21 @@ cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   return launch_high(kern, dim3((unsigned)grid), dim3(kThreads), kSmem, s, p);
 }
 
-template <bool WB>
+template <int WT>
 cudaError_t dispatch_w(const DecodeParams& p, int nt, bool fused, int64_t grid_cap, cudaStream_t s) {
   switch (nt) {
-    case 1: return fused ? launch_nt<1, true, WB>(p, grid_cap, s) : launch_nt<1, false, WB>(p, grid_cap, s);
-    case 2: return fused ? launch_nt<2, true, WB>(p, grid_cap, s) : launch_nt<2, false, WB>(p, grid_cap, s);
-    case 4: return fused ? launch_nt<4, true, WB>(p, grid_cap, s) : launch_nt<4, false, WB>(p, grid_cap, s);
-    default: return fused ? launch_nt<8, true, WB>(p, grid_cap, s) : launch_nt<8, false, WB>(p, grid_cap, s);
+    case 1: return fused ? launch_nt<1, true, WT>(p, grid_cap, s) : launch_nt<1, false, WT>(p, grid_cap, s);
+    case 2: return fused ? launch_nt<2, true, WT>(p, grid_cap, s) : launch_nt<2, false, WT>(p, grid_cap, s);
+    case 4: return fused ? launch_nt<4, true, WT>(p, grid_cap, s) : launch_nt<4, false, WT>(p, grid_cap, s);
+    default: return fused ? launch_nt<8, true, WT>(p, grid_cap, s) : launch_nt<8, false, WT>(p, grid_cap, s);
   }
 }
-cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s) {
-  return bf16_w ? dispatch_w<true>(p, nt, fused, grid_cap, s) : dispatch_w<false>(p, nt, fused, grid_cap, s);
+cudaError_t dispatch(const DecodeParams& p, int nt, bool fused, int wtype, int64_t grid_cap, cudaStream_t s) {
+  switch (wtype) {
+    case 1: return dispatch_w<1>(p, nt, fused, grid_cap, s);
+    case 2: return dispatch_w<2>(p, nt, fused, grid_cap, s);
+    default: return dispatch_w<0>(p, nt, fused, grid_cap, s);
+  }
 }
 
 // Validates a group and fills the kernel parameters, except the scratch
@@ -581,7 +596,7 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
       continue;
     }
     DecodeEntry& e = p.e[p.n_entries++];
-    const int64_t elem = g.bf16_w ? 2 : 1;
+    const int64_t elem = (g.wtype != 0 ? 2 : 1);
     if (!g.fused) {  // the weight as bytes: one 128-byte slab row is 128 e4m3 or 64 bf16 weights
       int rc = encode_u8_tile_map(&e.tmap, it.w, it.rows, it.cols * elem, std::min(256, rows_cta));
       if (rc != SWS_OK) return rc;
@@ -589,7 +604,7 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
     e.xs = nullptr;
     if (tc) {  // the entry's activation blocks, one per K slab: (hi, lo, e) for e4m3 weights, x for bf16
       e.xs = tc_split;
-      tc_split += cdiv(it.cols * elem, kSlabK) * tc_x_block_bytes(tc_n_pad(g.m), g.bf16_w);
+      tc_split += cdiv(it.cols * elem, kSlabK) * tc_x_block_bytes(tc_n_pad(g.m), g.wtype != 0);
     }
     e.scales = it.scales;
     e.x = it.x;
@@ -664,7 +679,7 @@ int build_fused_segments(DecodeParams& p, const DecodeParams& lin, const DecodeG
   for (int j = 0; j < lin.n_entries; ++j) {
     const DecodeEntry& L = lin.e[j];
     // byte arithmetic: `cols` here is the row length in bytes
-    const int64_t o = L.t_offset, cols = L.cols * (g.bf16_w ? 2 : 1), rows = L.rows, end = o + rows * cols;
+    const int64_t o = L.t_offset, cols = L.cols * ((g.wtype != 0 ? 2 : 1)), rows = L.rows, end = o + rows * cols;
     const int64_t c0 = o / C, c1 = (end - 1) / C;
     bool owner = true;
     for (int64_t c = c0; c <= c1; ++c) {
@@ -719,7 +734,7 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   if (rc != SWS_OK) return rc;
   int64_t split = 0;  // the activation split region follows the partial sums
   for (int i = 0; i < g.n; ++i)
-    split += cdiv(g.item[i].cols * (g.bf16_w ? 2 : 1), kSlabK) * tc_x_block_bytes(tc_n_pad(std::max<int64_t>(g.m, 1)), g.bf16_w);
+    split += cdiv(g.item[i].cols * ((g.wtype != 0 ? 2 : 1)), kSlabK) * tc_x_block_bytes(tc_n_pad(std::max<int64_t>(g.m, 1)), g.wtype != 0);
   bool tc = decode_kernel_for(g.m) == kDecodeTc;
   const int64_t need = dec + (tc ? split : 0);
   if (g.workspace_bytes < need)
@@ -746,7 +761,7 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
   p.trace = g.trace;
   p.tag = g.tag | ((tc ? (g.fused ? kTraceTcFused : kTraceTc) : (g.fused ? kTraceMmaFused : kTraceMma)) << 48);
   cudaError_t e =
-      tc ? launch_decode_tc(p, g.fused, g.bf16_w, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, g.bf16_w, kMaxGrid, s);
+      tc ? launch_decode_tc(p, g.fused, g.wtype, kMaxGrid, s) : dispatch(p, nt_for(g.m), g.fused, g.wtype, kMaxGrid, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "decode kernel launch");
 }
 
@@ -848,6 +863,6 @@ extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t ro
   p.tag = 0;
   // Two partial slots per CTA must fit in the fixed array.
   const int64_t grid_cap = kNoAllocPartialBytes / (2 * slot_bytes_for(nt));
-  e = dispatch(p, nt, false, false, grid_cap, s);
+  e = dispatch(p, nt, false, 0, grid_cap, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
 }

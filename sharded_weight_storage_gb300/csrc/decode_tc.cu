@@ -1,8 +1,9 @@
 // Split-K FP8 decode GEMM (m <= 64) on tcgen05 tensor cores: the same linear
 // and the same split-K partition as decode_gemm.cu (see there), for the m where
 // the warp-level mma.sync path cannot keep up with HBM. A bf16-weight variant
-// (WB) shares everything but the operands: x itself is the B operand
-// (split_x_bf16_kernel), the MMAs are kind::f16 and no scales apply.
+// and an fp16-weight variant (WT = 1, 2) share everything but the operands: x
+// itself (as bf16, or rounded to f16) is the B operand (split_x_16_kernel),
+// the MMAs are kind::f16 and no scales apply.
 //
 //   Y[m, o] = bf16_rne( sum_kb s[o/128, kb] * sum_{i in kb} x[m, i] * e4m3(q[o, i]) )
 //
@@ -109,9 +110,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f8(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-// kind::f16 instruction descriptor: A, B bf16, D f32, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// kind::f16 instruction descriptor: A, B bf16 (or f16 when f16 is set), D f32,
+// both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_16(int m, int n, bool f16) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // D (TMEM) (+)= A (shared memory) x B (shared memory).
@@ -124,7 +126,7 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -254,11 +256,12 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ De
   if (g == 0) reinterpret_cast<float*>(blk + 2 * n_pad * 128)[r] = es;
 }
 
-// bf16 weights: the B operand of a (entry, 64-K slab) block is the bf16
-// activations themselves, [n_pad rows][128 bytes] in the 128-byte swizzled
-// order, zero past m and past cols. Eight threads per (entry, slab, row), one
-// 16-byte piece each.
-__global__ void __launch_bounds__(256) split_x_bf16_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad) {
+// 16-bit weights: the B operand of a (entry, 64-K slab) block is the
+// activations themselves - as bf16, or rounded to f16 (to_f16) for f16
+// weights - [n_pad rows][128 bytes] in the 128-byte swizzled order, zero past m
+// and past cols. Eight threads per (entry, slab, row), one 16-byte piece each.
+__global__ void __launch_bounds__(256) split_x_16_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad,
+                                                          int32_t to_f16) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) dev::trace_start(p.trace);
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -278,6 +281,12 @@ __global__ void __launch_bounds__(256) split_x_bf16_kernel(const __grid_constant
   const int64_t col = kb * 64 + g * 8;
   uint4 v = make_uint4(0, 0, 0, 0);
   if (r < p.m && col < e.cols) v = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col));
+  if (to_f16) {
+    v.x = bf16x2_to_f16x2(v.x);
+    v.y = bf16x2_to_f16x2(v.y);
+    v.z = bf16x2_to_f16x2(v.z);
+    v.w = bf16x2_to_f16x2(v.w);
+  }
   *reinterpret_cast<uint4*>(e.xs + kb * (int64_t)n_pad * 128 + r * 128 + ((g ^ (r & 7)) << 4)) = v;
 }
 
@@ -354,8 +363,9 @@ __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& 
   for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
 }
 
-template <int N, bool WB>
+template <int N, int WT>
 __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr bool WB = WT != 0;  // 16-bit weights, no scales
   using Cf = TcCfg<N, WB>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t dsm[];
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       // B is the split block's hi and lo operands as one 2N-row operand, so
       // each weight tile is read once: D[:, 0:N] = A hi^T, D[:, N:2N] = A lo^T.
       // bf16: B is x itself, D[:, 0:N] = A x^T, 16 K per MMA.
-      constexpr uint32_t idesc = WB ? idesc_bf16(128, N) : idesc_f8(128, 2 * N);
+      constexpr uint32_t idesc = WB ? idesc_16(128, N, WT == 2) : idesc_f8(128, 2 * N);
       bool issued = false;
       for (int64_t i = 0; i < n && !s_abort; ++i) {
         const int s = (int)(i % S), b = (int)(i % kDBufs);
@@ -480,8 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
           for (int k = 0; k < kSlabK / 32; ++k) {  // 32 bytes of K per MMA
             const uint32_t d = tmem + b * Cf::kDCols + t * (Cf::kDCols / 2);
             if constexpr (WB)
-              mma_bf16(d, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32), smem_desc_sw128(xb + k * 32), idesc,
-                       k != 0);
+              mma_16(d, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32), smem_desc_sw128(xb + k * 32), idesc,
+                     k != 0);
             else
               mma_f8(d, smem_desc_sw128(wa + t * (128 * kSlabK) + k * 32), smem_desc_sw128(xb + k * 32), idesc,
                      k != 0);
@@ -589,15 +599,15 @@ struct SettlePlan {
 // Chunk-map launches add one block per straddling row and 16-column group
 // (blockIdx.x >= sp.n): that row is in no segment, so the block computes it
 // directly from the chunks (straddle_row).
-template <int N, bool WB>
+template <int N, int WT>
 __device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
 
-template <int N, bool FUSED, bool WB>
+template <int N, bool FUSED, int WT>
 __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p,
                                                          const __grid_constant__ SettlePlan sp) {
   grid_dependency_wait();  // the GEMM's results are complete and visible
   if (FUSED && (int32_t)blockIdx.x >= sp.n) {
-    straddle_row<N, WB>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
+    straddle_row<N, WT>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
     return;
   }
   const SettleTask tk = sp.task[blockIdx.x];
@@ -667,8 +677,9 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
 // (e4m3: 4 bytes, times the slab's block scale; bf16: 8 bytes, no scale); a
 // lane accumulates x * w over its slabs for every m, and the warps' sums are
 // added once at the end, warp by warp in a fixed order.
-template <int N, bool WB>
+template <int N, int WT>
 __device__ void straddle_row(const DecodeParams& p, int sidx, int c0) {
+  constexpr bool WB = WT != 0;
   constexpr int kWin = 32 * kSlabK;  // bytes per window
   constexpr int kWarps = kTcRows / 32;
   constexpr int kElem = WB ? 2 : 1;
@@ -707,12 +718,30 @@ __device__ void straddle_row(const DecodeParams& p, int sidx, int c0) {
         if (kb >= rowb) break;
         const int64_t k = kb / 2;
         const uint32_t w2 = *reinterpret_cast<const uint32_t*>(wbuf + sl * kSlabK + lane * 4);
-        const float a0 = __uint_as_float(w2 << 16), a1 = __uint_as_float(w2 & 0xffff0000u);
+        float a0, a1;
+        if constexpr (WT == 2) {  // f16 weights; x takes the f16 operand's rounding too
+          const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&w2));
+          a0 = wf.x;
+          a1 = wf.y;
+        } else {
+          a0 = __uint_as_float(w2 << 16);
+          a1 = __uint_as_float(w2 & 0xffff0000u);
+        }
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
           if (c0 + h < m) {
-            const uint32_t x2 = *reinterpret_cast<const uint32_t*>(e.x + (int64_t)(c0 + h) * cols + k);
-            acc[h] = fmaf(__uint_as_float(x2 & 0xffff0000u), a1, fmaf(__uint_as_float(x2 << 16), a0, acc[h]));
+            uint32_t x2 = *reinterpret_cast<const uint32_t*>(e.x + (int64_t)(c0 + h) * cols + k);
+            float x0, x1;
+            if constexpr (WT == 2) {
+              x2 = bf16x2_to_f16x2(x2);
+              const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&x2));
+              x0 = xf.x;
+              x1 = xf.y;
+            } else {
+              x0 = __uint_as_float(x2 << 16);
+              x1 = __uint_as_float(x2 & 0xffff0000u);
+            }
+            acc[h] = fmaf(x1, a1, fmaf(x0, a0, acc[h]));
           }
         }
       } else {
@@ -789,13 +818,14 @@ void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
   }
 }
 
-template <int N, bool FUSED, bool WB>
+template <int N, bool FUSED, int WT>
 cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
+  constexpr bool WB = WT != 0;
   constexpr int kSmem = TcCfg<N, WB>::kSmem;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(decode_tc_kernel<N, WB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    attr = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr != cudaSuccess) return attr;
   // 1. split the activations of every entry
@@ -813,7 +843,8 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;  // priority only
-  cudaError_t e = cudaLaunchKernelEx(&cfg, WB ? split_x_bf16_kernel : split_x_kernel, p, (int)N);
+  cudaError_t e = WB ? cudaLaunchKernelEx(&cfg, split_x_16_kernel, p, (int)N, (int)(WT == 2))
+                     : cudaLaunchKernelEx(&cfg, split_x_kernel, p, (int)N);
   if (e != cudaSuccess) return e;
   // 2. the GEMM, as a programmatic dependent launch of (1)
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
@@ -821,7 +852,7 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.numAttrs = 2;  // priority + programmatic stream serialization
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N, WB>, p);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<N, WT>, p);
   // 3. the split-K settle (and the straddling rows of a chunk-map launch), as
   //    a programmatic dependent launch of (2)
   if (e != cudaSuccess) return e;
@@ -832,25 +863,28 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.gridDim = dim3((unsigned)blocks, N / 16);
   cfg.blockDim = dim3(kTcRows);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED, WB>, p, sp);
+  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED, WT>, p, sp);
 }
 
-template <bool FUSED, bool WB>
+template <bool FUSED, int WT>
 cudaError_t launch_tc(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   switch ((int)tc_n_pad(p.m)) {
-    case 16: return launch_tc_n<16, FUSED, WB>(p, grid_cap, s);
-    case 32: return launch_tc_n<32, FUSED, WB>(p, grid_cap, s);
-    case 48: return launch_tc_n<48, FUSED, WB>(p, grid_cap, s);
-    default: return launch_tc_n<64, FUSED, WB>(p, grid_cap, s);
+    case 16: return launch_tc_n<16, FUSED, WT>(p, grid_cap, s);
+    case 32: return launch_tc_n<32, FUSED, WT>(p, grid_cap, s);
+    case 48: return launch_tc_n<48, FUSED, WT>(p, grid_cap, s);
+    default: return launch_tc_n<64, FUSED, WT>(p, grid_cap, s);
   }
 }
 
 }  // namespace
 
 namespace dec {
-cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, bool bf16_w, int64_t grid_cap, cudaStream_t s) {
-  if (bf16_w) return fused ? launch_tc<true, true>(p, grid_cap, s) : launch_tc<false, true>(p, grid_cap, s);
-  return fused ? launch_tc<true, false>(p, grid_cap, s) : launch_tc<false, false>(p, grid_cap, s);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int wtype, int64_t grid_cap, cudaStream_t s) {
+  switch (wtype) {
+    case 1: return fused ? launch_tc<true, 1>(p, grid_cap, s) : launch_tc<false, 1>(p, grid_cap, s);
+    case 2: return fused ? launch_tc<true, 2>(p, grid_cap, s) : launch_tc<false, 2>(p, grid_cap, s);
+    default: return fused ? launch_tc<true, 0>(p, grid_cap, s) : launch_tc<false, 0>(p, grid_cap, s);
+  }
 }
 int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }
 }  // namespace dec

@@ -39,6 +39,7 @@ int elem_bytes(int32_t dtype) {
     case SWS_BF16: return 2;
     case SWS_F32: return 4;
     case SWS_U8: return 1;
+    case SWS_F16: return 2;
     default: return 0;
   }
 }

@@ -622,8 +622,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   }
 }
 
-// ---- BF16 weights --------------------------------------------------------------
-// Y = X W^T with bf16 X [M, K] and bf16 W [N, K], no scales: the whole K of a
+// ---- 16-bit weights -------------------------------------------------------------
+// Y = X W^T with bf16 X [M, K] and bf16 W [N, K] (or both f16), no scales: the whole K of a
 // tile accumulates in TMEM (tcgen05.mma kind::f16, 128 x 256 x 16), and the
 // tile is read out once. One CTA per 128 x 256 tile; a slab is 64 K (one
 // 128-byte row of each operand), 4 stages of 48 KB; the two TMEM buffers hold
@@ -631,14 +631,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 // 8 read-out warps: thread = tile row (TMEM lane), 128 columns each.
 constexpr int kBf16SlabK = 64;
 
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4)                     // D format: f32
-         | (1u << 7) | (1u << 10)      // A, B format: bf16
+__host__ __device__ constexpr uint32_t idesc_16(int m, int n, bool f16) {
+  return (1u << 4)                                      // D format: f32
+         | (f16 ? 0u : (1u << 7) | (1u << 10))          // A, B format: f16 (0) or bf16 (1)
          | ((uint32_t)(n >> 3) << 17)  // N / 8
          | ((uint32_t)(m >> 4) << 24); // M / 16
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void mma_16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -647,6 +647,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) prefill_bf16_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mdone;
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_bf16_kernel(const __grid_
   } else if (warp == 1) {
     // ---- MMA issuer: a tile's slabs accumulate into TMEM buffer t % 2 -------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+      constexpr uint32_t idesc = idesc_16(kBM, kBN, F16);
       int64_t it = 0, t = 0;
       bool issued = false;
       for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x, ++t) {
@@ -727,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_bf16_kernel(const __grid_
           const uint32_t a = dev::smem_addr(smem + s * kStageBytes), b = a + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBf16SlabK / 16; ++kk)  // 16 K = 32 bytes per MMA
-            mma_bf16(tmem + buf * kBN, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
+            mma_16(tmem + buf * kBN, smem_desc_sw128(a + kk * 32), smem_desc_sw128(b + kk * 32), idesc,
                      (kb > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
           issued = true;
@@ -876,14 +877,14 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   return SWS_OK;
 }
 
-int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s) {
+int launch_prefill_16(const PrefillLaunch& a, bool f16, cudaStream_t s) {
   if (a.m <= 0 || a.rows <= 0) return SWS_OK;
   if (a.cols <= 0 || a.cols % 8 != 0)
-    return fail(SWS_E_UNSUPPORTED, "prefill: bf16 cols=%lld is not a positive multiple of 8", (long long)a.cols);
+    return fail(SWS_E_UNSUPPORTED, "prefill: 16-bit cols=%lld is not a positive multiple of 8", (long long)a.cols);
   if (!aligned16(a.w) || !aligned16(a.xq) || !aligned16(a.y))
     return fail(SWS_E_ALIGN, "prefill: pointer not 16-byte aligned");
   PrefillParams p;
-  // bf16 rows as bytes: 128-byte boxes (64 K) of [rows, 2K] byte tensors
+  // 16-bit rows as bytes: 128-byte boxes (64 K) of [rows, 2K] byte tensors
   int rc = encode_u8_tile_map(&p.tmap_x, a.xq, a.m, 2 * a.cols, kBM);
   if (rc != SWS_OK) return rc;
   rc = encode_u8_tile_map(&p.tmap_w, a.w, a.rows, 2 * a.cols, kBN);
@@ -903,13 +904,16 @@ int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr = cudaFuncSetAttribute(prefill_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(prefill_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
-  if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (bf16)");
+  if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (16-bit)");
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-  cudaError_t e = launch_high(prefill_bf16_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
-  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill bf16 kernel launch");
+  cudaError_t e = f16 ? launch_high(prefill_bf16_kernel<true>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p)
+                      : launch_high(prefill_bf16_kernel<false>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill 16-bit kernel launch");
 }
 
 }  // namespace sws

@@ -128,7 +128,7 @@ struct DecodeGroup {
   int32_t n = 0;
   int64_t m = 0;
   bool fused = false;
-  bool bf16_w = false;  // every item's weight is bf16 (no scales) instead of e4m3 codes
+  int wtype = 0;  // every item's weight: 0 e4m3 codes with block scales, 1 bf16, 2 f16 (no scales)
   const uint8_t* chunks[256];
   int32_t n_chunks = 0;
   int64_t chunk_bytes = 0;
@@ -151,6 +151,8 @@ int decode_kernel_for(int64_t m);
 
 int launch_quantize_x(const uint16_t* x, int64_t m, int64_t k, uint8_t* xq, float* ex, cudaStream_t s);
 int launch_silu_mul(const uint16_t* gu, int64_t m, int64_t f, uint16_t* act, cudaStream_t s);
+// bf16 -> f16 (round to nearest even) of n elements, n % 8 == 0.
+int launch_to_f16(const uint16_t* x, int64_t n, uint16_t* out, cudaStream_t s);
 
 struct PrefillLaunch {
   const uint8_t* w;      // fp8 [rows, cols] (slot view or replicated buffer)
@@ -166,9 +168,9 @@ struct PrefillLaunch {
 enum PrefillKernel { kPrefillAuto = 0, kPrefillSingle = 1, kPrefillPair = 2 };
 void set_prefill_kernel(int k);
 int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
-// bf16 weights: `xq` is the bf16 activation X [m, cols] itself, `w` bf16
-// [rows, cols]; ex and scales are unused.
-int launch_prefill_bf16(const PrefillLaunch& a, cudaStream_t s);
+// 16-bit weights: `xq` is the activation X [m, cols] in the weights' format
+// (bf16, or f16 when f16 is set), `w` [rows, cols]; ex and scales are unused.
+int launch_prefill_16(const PrefillLaunch& a, bool f16, cudaStream_t s);
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);
 cudaError_t launch_bounded_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);

@@ -50,7 +50,7 @@ class ShardedStack:
         scales[j]: float32 block scales [ceil(rows/128), ceil(cols/128)] of an
         E4M3 entry, or one number - a per-tensor scale (ModelOpt FP8), kept
         replicated outside T and stored as that grid filled with it; absent for
-        BF16 entries."""
+        BF16 and F16 entries."""
         n = self.n_shards
         shard_ptrs, keep = [], []
         for j in self.layer_entries(layer):

@@ -73,6 +73,44 @@ def build_stack(S, entries, n_shards, layers: List[LayerData], max_m=64):
     return st
 
 
+def weight_bytes(bits: np.ndarray) -> np.ndarray:
+    """16-bit weight bit patterns [rows, cols] -> the weight's bytes [rows, 2 * cols]."""
+    return np.ascontiguousarray(bits).view(np.uint8).reshape(bits.shape[0], -1)
+
+
+def typed_stack(S, shapes, n, weights, scales=None, max_m=64):
+    """shapes: (layer, dtype, rows, cols); weights[j]: uint8 bytes [rows, cols * elem];
+    scales[j]: block scales or one per-tensor scale of an E4M3 entry."""
+    from sharded_weight_storage_gb300.storage import ShardedStack
+    st = ShardedStack(shapes, n, max_m=max_m)
+    for l in sorted({s[0] for s in shapes}):
+        js = [j for j, s in enumerate(shapes) if s[0] == l]
+        st.load_layer(l, {j: torch.from_numpy(weights[j]) for j in js},
+                      {j: scales[j] for j in js if scales and j in scales})
+    st.make_ctx()
+    return st
+
+
+def linear_kinds(st, j, src, x, m):
+    """Runs one linear with tracing on; returns y and the kernel ids (trace tag
+    bits 48..55) of its linear records."""
+    rec = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
+    st.ctx.trace_begin(rec.data_ptr(), 4, 0)
+    _, _, rows, _ = st.entries[j]
+    y = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st.ctx.linear(j, src, x.data_ptr(), m, y.data_ptr(), 0)
+    torch.cuda.synchronize()
+    n = st.ctx.trace_count()
+    st.ctx.trace_begin(0, 0, 0)
+    tags = [int(t) for t in rec.view(4, 4)[:n, 0].tolist()]
+    return y, [(t >> 48) & 0xFF for t in tags if (t >> 56) == 2]
+
+
+def x_f64(x: torch.Tensor) -> np.ndarray:
+    """bf16 tensor (any device) -> float64 array of its exact values."""
+    return WL.bf16_to_f64(WL.bf16_bits(x.cpu()))
+
+
 def oracle_layer_T(entries, n_shards, layer: int, ld: LayerData):
     plan = O.plan_layout([(l, r, c, 1) for (l, r, c) in entries], n_shards)
     shards = {j: WL.row_shards(q, n_shards) for j, q in ld.codes.items() if plan.sharded[j]}

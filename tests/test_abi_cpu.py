@@ -123,6 +123,23 @@ def test_workspace_bytes_grows_with_prefill_m(swslib):
     assert c - b >= 4096 * 512 + 4096 * 4 * 4
 
 
+def test_workspace_bytes_per_weight_type(swslib):
+    # prefill activations in the workspace: E4M3 the quantiser's codes and
+    # scales, F16 x rounded to f16 (2 bytes each), BF16 none (x is used as is);
+    # two buffers of the largest.
+    S = swslib
+    m, cols = 4096, 512
+    base = {}
+    for dt in (S.E4M3, S.BF16, S.F16):
+        plan = S.Plan([(0, dt, 256, cols)], 4)
+        base[dt] = (S.workspace_bytes(plan, 64), S.workspace_bytes(plan, m))
+    assert base[S.BF16][1] == base[S.BF16][0]
+    assert base[S.F16][1] - base[S.F16][0] == 2 * (2 * m * cols)
+    assert base[S.E4M3][1] - base[S.E4M3][0] == 2 * (m * cols + m * (cols // 128) * 4)
+    plan = S.Plan([(0, S.F16, 256, 24)], 4)  # elements of 2 bytes in the layout
+    assert plan.entry(0)[1] == 256 * 24 * 2
+
+
 def test_relayout_validates_before_any_launch(swslib):
     S = swslib
     plan = S.Plan([(0, S.E4M3, 8, 16)], 4)

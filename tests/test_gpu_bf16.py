@@ -10,7 +10,7 @@ import torch
 
 import oracle as O
 import workloads as WL
-from helpers import assert_close, bf16_tensor_to_f64
+from helpers import assert_close, bf16_tensor_to_f64, linear_kinds, typed_stack, weight_bytes, x_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -24,41 +24,6 @@ def S(swslib):
     return swslib
 
 
-def _as_bytes(bits):
-    """bf16 bit patterns [rows, cols] -> the weight's bytes [rows, 2 * cols]."""
-    return np.ascontiguousarray(bits).view(np.uint8).reshape(bits.shape[0], -1)
-
-
-def _stack(S, shapes, n, weights, scales=None, max_m=64):
-    """shapes: (layer, dtype, rows, cols); weights[j]: uint8 bytes [rows, cols * elem]."""
-    from sharded_weight_storage_gb300.storage import ShardedStack
-    st = ShardedStack(shapes, n, max_m=max_m)
-    for l in sorted({s[0] for s in shapes}):
-        js = [j for j, s in enumerate(shapes) if s[0] == l]
-        st.load_layer(l, {j: torch.from_numpy(weights[j]) for j in js},
-                      {j: scales[j] for j in js if scales and j in scales})
-    st.make_ctx()
-    return st
-
-
-def _linear_traced(st, j, src, x, m):
-    rec = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
-    st.ctx.trace_begin(rec.data_ptr(), 4, 0)
-    _, _, rows, _ = st.entries[j]
-    y = torch.full((m, rows), float("nan"), dtype=torch.bfloat16, device="cuda")
-    st.ctx.linear(j, src, x.data_ptr(), m, y.data_ptr(), 0)
-    torch.cuda.synchronize()
-    n = st.ctx.trace_count()
-    st.ctx.trace_begin(0, 0, 0)
-    tags = [int(t) for t in rec.view(4, 4)[:n, 0].tolist()]
-    kinds = [(t >> 48) & 0xFF for t in tags if (t >> 56) == 2]
-    return y, kinds
-
-
-def _x64(x):
-    return WL.bf16_to_f64(WL.bf16_bits(x.cpu()))
-
-
 # N = 4. Entry 0 (333 rows) is replicated (333 % 4 != 0); chunk boundaries fall
 # inside rows of entries 1 and 2; cols 208 leaves a partial 64-K slab.
 SHAPES = [(0, 1, 333, 208), (0, 1, 1000, 1040), (0, 1, 256, 64), (0, 1, 512, 208)]
@@ -68,7 +33,7 @@ SHAPES = [(0, 1, 333, 208), (0, 1, 1000, 1040), (0, 1, 256, 64), (0, 1, 512, 208
 def bf16_stack(S):
     assert S.BF16 == 1
     bits = [WL.draw_weight_bf16(61, 0, j, r, c) for j, (_, _, r, c) in enumerate(SHAPES)]
-    st = _stack(S, SHAPES, 4, [_as_bytes(b) for b in bits], max_m=1000)
+    st = typed_stack(S, SHAPES, 4, [weight_bytes(b) for b in bits], max_m=1000)
     st.ctx.gather_to_slot(0, 0, 0)
     return st, bits
 
@@ -86,9 +51,9 @@ def test_bf16_decode_matches_oracle(S, bf16_stack, decode_kernel, m):
     st, bits = bf16_stack
     for j, (_, _, r, c) in enumerate(SHAPES):
         x = WL.draw_x(62, j, m, c).cuda()
-        y, kinds = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+        y, kinds = linear_kinds(st, j, S.SRC_SLOT0, x, m)
         assert kinds == [decode_kernel]
-        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m}")
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(x_f64(x), bits[j]), f"entry {j} m {m}")
     assert st.ctx.status() == 0
 
 
@@ -98,9 +63,9 @@ def test_bf16_decode_through_the_chunk_map(S, bf16_stack, m):
     for j in (1, 2, 3):  # sharded entries
         _, _, r, c = SHAPES[j]
         x = WL.draw_x(63, j, m, c).cuda()
-        y, kinds = _linear_traced(st, j, S.SRC_FUSED, x, m)
+        y, kinds = linear_kinds(st, j, S.SRC_FUSED, x, m)
         assert kinds == [KERNEL_TC_FUSED]
-        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m} (fused)")
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(x_f64(x), bits[j]), f"entry {j} m {m} (fused)")
 
 
 def test_bf16_straddling_rows_one_hot(S, bf16_stack):
@@ -126,7 +91,7 @@ def test_bf16_straddling_rows_one_hot(S, bf16_stack):
         cols = rng.integers(0, c, size=m)
         xo = torch.zeros((m, c), dtype=torch.bfloat16)
         xo[np.arange(m), torch.from_numpy(cols)] = 1.0
-        y, kinds = _linear_traced(st, j, S.SRC_FUSED, xo.cuda(), m)
+        y, kinds = linear_kinds(st, j, S.SRC_FUSED, xo.cuda(), m)
         assert kinds == [KERNEL_TC_FUSED]
         assert np.array_equal(WL.bf16_bits(y[:, row].cpu()), bits[j][row, cols].astype(np.uint16)), f"entry {j} row {row}"
 
@@ -142,7 +107,7 @@ def test_bf16_one_hot_gives_the_weight_exactly(S, bf16_stack, m):
         cols = rng.integers(0, c, size=m)
         xo = torch.zeros((m, c), dtype=torch.bfloat16)
         xo[np.arange(m), torch.from_numpy(cols)] = 1.0
-        y, _ = _linear_traced(st, j, S.SRC_SLOT0, xo.cuda(), m)
+        y, _ = linear_kinds(st, j, S.SRC_SLOT0, xo.cuda(), m)
         want = bits[j][:, cols].T.astype(np.uint16)
         assert np.array_equal(WL.bf16_bits(y.cpu()), want), f"entry {j}"
 
@@ -152,9 +117,9 @@ def test_bf16_prefill_matches_oracle(S, bf16_stack, m):
     st, bits = bf16_stack
     for j, (_, _, r, c) in enumerate(SHAPES):
         x = WL.draw_x(64, j, m, c).cuda()
-        y, kinds = _linear_traced(st, j, S.SRC_SLOT0, x, m)
+        y, kinds = linear_kinds(st, j, S.SRC_SLOT0, x, m)
         assert kinds == [KERNEL_PREFILL]
-        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(_x64(x), bits[j]), f"entry {j} m {m}")
+        assert_close(bf16_tensor_to_f64(y), O.linear_bf16(x_f64(x), bits[j]), f"entry {j} m {m}")
     assert st.ctx.status() == 0
 
 
@@ -172,15 +137,15 @@ def test_mixed_layer_linears(S, m):
             ref_w[j] = (q, sc)
         else:
             b = WL.draw_weight_bf16(65, 0, j, r, c)
-            weights[j], ref_w[j] = _as_bytes(b), b
-    st = _stack(S, shapes, 4, weights, scales, max_m=max(m, 64))
+            weights[j], ref_w[j] = weight_bytes(b), b
+    st = typed_stack(S, shapes, 4, weights, scales, max_m=max(m, 64))
     st.ctx.gather_to_slot(0, 1, 0)
     xs = [WL.draw_x(66, j, m, c).cuda() for j, (_, _, r, c) in enumerate(shapes)]
     ys = [torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda") for (_, _, r, c) in shapes]
     st.ctx.layer_linears(0, S.SRC_SLOT1, [x.data_ptr() for x in xs], [y.data_ptr() for y in ys], m, 0)
     torch.cuda.synchronize()
     for j, (_, dt, r, c) in enumerate(shapes):
-        xf = _x64(xs[j])
+        xf = x_f64(xs[j])
         if dt == S.E4M3:
             if m > 64:
                 xq, ex = O.quantize_x(xf)
@@ -196,7 +161,7 @@ def test_mixed_layer_linears(S, m):
 def test_bf16_run_layers(S):
     shapes = [(l, S.BF16, r, c) for l in range(3) for (r, c) in ((512, 256), (256, 512))]
     bits = [WL.draw_weight_bf16(67, l, j, r, c) for j, (l, _, r, c) in enumerate(shapes)]
-    st = _stack(S, shapes, 4, [_as_bytes(b) for b in bits])
+    st = typed_stack(S, shapes, 4, [weight_bytes(b) for b in bits])
     m = 8
     xs = {j: WL.draw_x(68, j, m, c).cuda() for j, (_, _, r, c) in enumerate(shapes)}
     ys = {j: torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -208,7 +173,7 @@ def test_bf16_run_layers(S):
         st.ctx.run_layers(0, 2, io, flags, main.cuda_stream, side.cuda_stream)
         main.synchronize()
         for j in ys:
-            assert_close(bf16_tensor_to_f64(ys[j]), O.linear_bf16(_x64(xs[j]), bits[j]), f"entry {j} flags {flags}")
+            assert_close(bf16_tensor_to_f64(ys[j]), O.linear_bf16(x_f64(xs[j]), bits[j]), f"entry {j} flags {flags}")
     assert st.ctx.status() == 0
 
 
@@ -220,12 +185,12 @@ def test_per_tensor_fp8_scale(S, m):
     codes = [rng.integers(0, 0x7E, size=(r, c), dtype=np.uint8) | (rng.integers(0, 2, size=(r, c), dtype=np.uint8) << 7)
              for (_, _, r, c) in shapes]
     sc = [0.0123, 0.5]
-    st = _stack(S, shapes, 4, codes, {0: sc[0], 1: torch.tensor([sc[1]])}, max_m=max(m, 64))
+    st = typed_stack(S, shapes, 4, codes, {0: sc[0], 1: torch.tensor([sc[1]])}, max_m=max(m, 64))
     st.ctx.gather_to_slot(0, 0, 0)
     for j, (_, _, r, c) in enumerate(shapes):
         x = WL.draw_x(70, j, m, c).cuda()
-        y, _ = _linear_traced(st, j, S.SRC_SLOT0, x, m)
-        xf = _x64(x)
+        y, _ = linear_kinds(st, j, S.SRC_SLOT0, x, m)
+        xf = x_f64(x)
         if m > 64:
             xq, ex = O.quantize_x(xf)
             ref = O.linear_per_tensor(O.dequant_x(xq, ex), codes[j], sc[j])
@@ -241,7 +206,7 @@ def test_bf16_shared_expert_full_size_sampled(S):
     w = WL.SHARED_EXPERT
     shapes = [(0, S.BF16, e.rows, e.cols) for e in w.entries]
     bits = [WL.draw_weight_bf16(71, 0, j, e.rows, e.cols) for j, e in enumerate(w.entries)]
-    st = _stack(S, shapes, w.n_shards, [_as_bytes(b) for b in bits], max_m=2048)
+    st = typed_stack(S, shapes, w.n_shards, [weight_bytes(b) for b in bits], max_m=2048)
     st.ctx.gather_to_slot(0, 0, 0)
     rng = np.random.default_rng(72)
     for j, e in enumerate(w.entries):
@@ -250,8 +215,8 @@ def test_bf16_shared_expert_full_size_sampled(S):
         for m, src, kind in ((32, S.SRC_SLOT0, KERNEL_TC), (32, S.SRC_FUSED, KERNEL_TC_FUSED),
                              (2048, S.SRC_SLOT0, KERNEL_PREFILL)):
             x = WL.draw_x(73, j, m, e.cols).cuda()
-            y, kinds = _linear_traced(st, j, src, x, m)
+            y, kinds = linear_kinds(st, j, src, x, m)
             assert kinds == [kind]
-            want = O.linear_bf16(_x64(x), wsel)
+            want = O.linear_bf16(x_f64(x), wsel)
             assert_close(bf16_tensor_to_f64(y)[:, rows], want, f"{e.name} m {m} src {src}")
     assert st.ctx.status() == 0

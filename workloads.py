@@ -140,6 +140,14 @@ def draw_weight_bf16(workload_key: int, layer: int, entry: int, rows: int, cols:
     return torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def draw_weight_f16(workload_key: int, layer: int, entry: int, rows: int, cols: int) -> np.ndarray:
+    """f16 weight [rows, cols] as uint16 bit patterns, w ~ N(0, 0.02) rounded
+    to IEEE binary16 (the unquantised weight variant stored as FP16)."""
+    w = rng_for(workload_key, layer, entry, KIND_W).standard_normal((rows, cols), dtype=np.float32)
+    w *= np.float32(0.02)
+    return w.astype(np.float16).view(np.uint16)
+
+
 def draw_row_signs(workload_key: int, layer: int, entry: int, rows: int) -> np.ndarray:
     """Per-row sign-bit mask (0x00 or 0x80) for layer `layer` of a stack."""
     bits = rng_for(workload_key, layer, entry, KIND_SIGN).integers(0, 2, size=rows, dtype=np.uint8)
