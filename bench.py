@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--prefill-layers", type=int, default=8, help="layers of the prefill run (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the KDA-layer and tiny-layer decode sections")
-    ap.add_argument("--no-bf16", action="store_true", help="skip the bf16-weight section")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the 16-bit (bf16, f16) weight sections")
     ap.add_argument("--no-prefetch", action="store_true", help="skip the draft-model prefetch section")
     ap.add_argument("--clock-soak-s", type=float, default=0.5,
                     help="untimed run of the same step for clock samples when the timed region is too short")
@@ -667,12 +667,14 @@ def run_decode_config(args, dist, w, relayout: bool):
     return out
 
 
-def run_bf16(args, dist):
-    """BF16 weights (the unquantised variant): the shared-expert layer's two
-    linears as bf16 (|T| = 528 MB, N = 16): gather, decode linears (slot and
-    chunk-map) at each m, weight GB/s against the HBM peak; and the prefill
-    GEMM on one KDA-like [12288, 7168] bf16 linear at m = 8192 against the
-    bf16 tensor peak. Weights are drawn on the device (seeded)."""
+def run_16bit(args, dist, f16=False):
+    """16-bit weights (the unquantised variants, bf16 or f16): the
+    shared-expert layer's two linears in that format (|T| = 528 MB, N = 16):
+    gather, decode linears (slot and chunk-map) at each m, weight GB/s against
+    the HBM peak; and the prefill GEMM on one KDA-like [12288, 7168] linear at
+    m = 8192 against the 16-bit tensor peak (f16 and bf16 share it; for f16
+    the time includes the rounding of x to f16). Weights are drawn on the
+    device (seeded)."""
     import torch
 
     import sharded_weight_storage_gb300 as S
@@ -682,15 +684,16 @@ def run_bf16(args, dist):
 
     dev = torch.device("cuda", dist.local)
     gen = torch.Generator(device=dev)
-    gen.manual_seed(20260)
+    gen.manual_seed(20260 + f16)
+    wdt, sdt, name = (torch.float16, S.F16, "f16") if f16 else (torch.bfloat16, S.BF16, "bf16")
 
     def weight(rows, cols):
         w = torch.randn((rows, cols), generator=gen, device=dev, dtype=torch.float32).mul_(0.02)
-        return w.to(torch.bfloat16).view(torch.uint8)
+        return w.to(wdt).view(torch.uint8)
 
     w = WL.SHARED_EXPERT
     ents = [(0, e.rows, e.cols) for e in w.entries]
-    st = ShardedStack([(0, S.BF16, r, c) for (_, r, c) in ents], w.n_shards, max_m=64, device=str(dev))
+    st = ShardedStack([(0, sdt, r, c) for (_, r, c) in ents], w.n_shards, max_m=64, device=str(dev))
     st.load_layer(0, {j: weight(r, c) for j, (_, r, c) in enumerate(ents)}, {})
     ctx = st.make_ctx()
     total = st.layout[0][0]
@@ -714,8 +717,8 @@ def run_bf16(args, dist):
         torch.cuda.synchronize()
         return statistics.median([a.elapsed_time(b) for a, b in out])
 
-    out = {"workload": f"shared_expert_layer with bf16 weights: |T| = {total} B, N = {w.n_shards}",
-           "kernel": "decode_kernel (mma.sync, bf16 operands)", "per_m": {}}
+    out = {"workload": f"shared_expert_layer with {name} weights: |T| = {total} B, N = {w.n_shards}",
+           "kernel": f"decode_tc_kernel (tcgen05 kind::f16, {name} operands)", "per_m": {}}
     with torch.cuda.stream(stream):
         ctx.gather_to_slot(0, 0, sp)
         g_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp))
@@ -742,7 +745,7 @@ def run_bf16(args, dist):
     torch.cuda.empty_cache()
     # prefill
     rows, cols, m = 12288, 7168, 8192
-    st = ShardedStack([(0, S.BF16, rows, cols)], 8, max_m=m, device=str(dev))
+    st = ShardedStack([(0, sdt, rows, cols)], 8, max_m=m, device=str(dev))
     st.load_layer(0, {0: weight(rows, cols)}, {})
     ctx = st.make_ctx()
     bf16_burst = fp8_peak()[0] / 2
@@ -754,7 +757,8 @@ def run_bf16(args, dist):
         call()
         t = timed(call, reps=5)
     fl = 2.0 * m * rows * cols
-    out["prefill"] = {"linear": f"[{rows}, {cols}] bf16 at m = {m}", "kernel": "prefill_bf16_kernel (tcgen05 kind::f16)",
+    kern = "to_f16_kernel + prefill_bf16_kernel<true>" if f16 else "prefill_bf16_kernel<false>"
+    out["prefill"] = {"linear": f"[{rows}, {cols}] {name} at m = {m}", "kernel": f"{kern} (tcgen05 kind::f16)",
                       "us": t * 1e3, "TFLOPS": fl / t / 1e9, "frac_of_bf16_peak": fl / t / 1e9 / bf16_burst,
                       "bf16_peak_tflops": bf16_burst}
     assert ctx.status() == 0
@@ -1111,7 +1115,8 @@ def main():
         configs = {"attn_kda_layer": run_decode_config(args, dist, WL.ATTN_KDA, relayout=True),
                    "tiny_flat_layer": run_decode_config(args, dist, WL.TINY, relayout=True)}
     prefill = run_prefill(args, dist, args.prefill_layers) if args.prefill_layers > 0 else None
-    bf16 = run_bf16(args, dist) if not args.no_bf16 else None
+    bf16 = run_16bit(args, dist) if not args.no_bf16 else None
+    f16 = run_16bit(args, dist, f16=True) if not args.no_bf16 else None
     prefetch = run_prefetch(args, dist) if not args.no_prefetch else None
     if dist.rank != 0:
         dist.close()
@@ -1157,6 +1162,7 @@ def main():
         "decode_configs": configs,
         "prefill": prefill,
         "bf16_weights": bf16,
+        "f16_weights": f16,
         "draft_prefetch": prefetch,
         "weight_GBps_step": total / ms_step / 1e6,
     }
