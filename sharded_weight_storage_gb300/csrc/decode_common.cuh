@@ -174,9 +174,10 @@ __host__ __device__ constexpr int64_t tc_n_pad(int64_t m) { return (m + 15) / 16
 // [hi e4m3 n_pad x 128 | lo e4m3 n_pad x 128 | e fp32 n_pad].
 __host__ __device__ constexpr int64_t tc_split_block_bytes(int64_t n_pad) { return 260 * n_pad; }
 // Activation block of one entry and 128-byte weight slab: the split block for
-// e4m3 weights, the bf16 activations [n_pad][64] (128 bytes a row) for bf16.
-__host__ __device__ constexpr int64_t tc_x_block_bytes(int64_t n_pad, bool bf16_w) {
-  return bf16_w ? 128 * n_pad : tc_split_block_bytes(n_pad);
+// e4m3 weights, the 16-bit activations [n_pad][64] (128 bytes a row) for bf16
+// or f16 weights.
+__host__ __device__ constexpr int64_t tc_x_block_bytes(int64_t n_pad, bool w16) {
+  return w16 ? 128 * n_pad : tc_split_block_bytes(n_pad);
 }
 // wtype: 0 e4m3 weights with block scales, 1 bf16 weights, 2 f16 weights.
 cudaError_t launch_decode_tc(const DecodeParams& p, bool fused, int wtype, int64_t grid_cap, cudaStream_t s);

@@ -74,8 +74,9 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
 }
 
 // WB = false: e4m3 weights, activations split into two e4m3 terms (hi, lo)
-// and a scale per row; WB = true: bf16 weights (64 K per 128-byte slab row)
-// and the bf16 activations themselves as the one B operand, no scales.
+// and a scale per row; WB = true: 16-bit (bf16 or f16) weights (64 K per
+// 128-byte slab row) and the activations themselves, in the weights' format,
+// as the one B operand, no scales.
 template <int N, bool WB = false>
 struct TcCfg {
   static constexpr int kWBytes = kTcRows * kSlabK;  // weight slab, 128-byte swizzle
