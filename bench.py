@@ -368,8 +368,14 @@ def run_ours(args, dist):
         for _ in range(3):
             ctx.gather_to_slot(0, 0, sp)
         ce_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp), reps)
+        # the shared-SM gather kernel (one 48 KB CTA per SM) on its own
+        S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA_SHARED_SM)
+        for _ in range(3):
+            ctx.gather_to_slot(0, 0, sp)
+        sh_ms = timed(lambda: ctx.gather_to_slot(0, 0, sp), reps)
         S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
         results["gather_copy_engine"] = {"us": ce_ms * 1e3, "GBps": 2 * total / ce_ms / 1e6}
+        results["gather_shared_sm_alone"] = {"us": sh_ms * 1e3, "GBps": 2 * total / sh_ms / 1e6}
         # shared-expert chain: gate_up -> SiLU(gate) * up -> down at each m
         f = ents[0][1] // 2
         chain = {}
@@ -549,6 +555,19 @@ def run_stack(args, dist, n_layers):
         ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
         ce_exposed.append(ctx.run_timing(n_layers)[0])
     torch.cuda.synchronize()
+    # the lookahead with the shared-SM gather: one 48 KB gather CTA per SM fits
+    # beside the linears' GEMM CTA, so gather(l+1) and the linears of l run on
+    # the same SMs at once (eager, graph replay, and the stamp-based exposure)
+    S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA_SHARED_SM)
+    steps(1, 0)
+    sh_ms = dist.max(steps(k, 0))
+    sh_graph_ms = dist.max(graph_steps(k, 0))
+    sh_exposed = []
+    for _ in range(3):
+        ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
+        sh_exposed.append(ctx.run_timing(n_layers)[0])
+    torch.cuda.synchronize()
+    sh_ex = [statistics.median(v[l] for v in sh_exposed) for l in range(n_layers)]
     S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
     ce_ex = [statistics.median(v[l] for v in ce_exposed) for l in range(n_layers)]
     exposed, layer_ms = [], []
@@ -573,6 +592,11 @@ def run_stack(args, dist, n_layers):
         "copy_engine_gather_step_ms": ce_ms, "copy_engine_gather_per_layer_us": ce_ms * 1e3 / n_layers,
         "copy_engine_exposed_gather_us_per_layer": 1e3 * statistics.mean(ce_ex[1:]) if n_layers > 1 else 1e3 * ce_ex[0],
         "graph_fused_step_ms": graph_fused_ms, "graph_fused_per_layer_us": graph_fused_ms * 1e3 / n_layers,
+        "shared_sm_gather_per_layer_us": sh_ms * 1e3 / n_layers,
+        "shared_sm_gather_graph_per_layer_us": sh_graph_ms * 1e3 / n_layers,
+        "shared_sm_gather_exposed_us_per_layer": 1e3 * statistics.mean(sh_ex[1:]) if n_layers > 1 else 1e3 * sh_ex[0],
+        "shared_sm_gather_exposed_vs_resident_us_per_layer": (sh_ms - fused_ms) * 1e3 / n_layers,
+        "shared_sm_gather_step_GBps": n_layers * (3 * total + sum(layer_bytes(ents[:ne], m)[1:])) / sh_ms / 1e6,
         "exposed_gather_us_per_layer": 1e3 * statistics.mean(ex[1:]) if n_layers > 1 else 1e3 * ex[0],
         "exposed_gather_first_layer_us": 1e3 * ex[0],
         "exposed_frac_of_step": sum(ex) / sum(lm + ex) if sum(lm + ex) > 0 else 0.0,
@@ -1155,6 +1179,7 @@ def main():
         "exposed_gather_us_per_layer": stack["exposed_gather_us_per_layer"] if stack else None,
         "kernels": kernels,
         "gather_alone": r["gather_alone"],
+        "gather_shared_sm_alone": r["gather_shared_sm_alone"],
         "gather_copy_engine": r["gather_copy_engine"],
         "shared_expert_chain": r["shared_expert_chain"],
         "per_m": r["per_m"],

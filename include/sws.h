@@ -321,6 +321,10 @@ int32_t sws_trace_count(const sws_ctx* ctx);
 #define SWS_GATHER_COPY_ENGINE 1 /* N cudaMemcpyAsync device-to-device copies of C bytes on the stream:
                                     the copy engines move the bytes and no SM is used (the pages'
                                     all-gather runs on copy engines too); no trace record */
+#define SWS_GATHER_TMA_SHARED_SM 2 /* the TMA kernel with one 48 KB CTA per SM, which fits beside a
+                                      decode GEMM CTA (m <= 32): run_layers' lookahead gather then
+                                      shares the SMs with the current layer's linears instead of
+                                      waiting for them; slower than SWS_GATHER_TMA on its own */
 /* Process-wide options, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance, from views and through
  * the chunk map (a chunk-map launch whose segments or split rows exceed the

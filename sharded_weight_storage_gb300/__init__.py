@@ -8,7 +8,8 @@ from ._lib import (BF16, E4M3, F16, E_ALIGN, E_CUDA, E_INVALID, E_STATE, E_TIMEO
                    OK, RUN_FUSED, RUN_TIMING, RUN_FIRST_PREFETCHED, W_COLD, SRC_FUSED, SRC_SLOT0, SRC_SLOT1, U8, W_SKIPPED, Ctx, Plan, SwsError,
                    last_error, lib, plan_create, quantize_x, relayout, workspace_bytes, set_option, silu_mul,
                    OPT_DECODE_KERNEL, DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05, OPT_PREFILL_KERNEL,
-                   PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR, OPT_GATHER_ENGINE, GATHER_TMA, GATHER_COPY_ENGINE)
+                   PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR, OPT_GATHER_ENGINE, GATHER_TMA, GATHER_COPY_ENGINE,
+                   GATHER_TMA_SHARED_SM)
 
 lib()  # load now: no silent fallback when the extension is missing
 
@@ -17,4 +18,4 @@ __all__ = ["Plan", "Ctx", "SwsError", "plan_create", "relayout", "workspace_byte
            "RUN_TIMING", "RUN_FIRST_PREFETCHED", "W_COLD", "OK", "W_SKIPPED", "E_INVALID", "E_ALIGN", "E_STATE", "E_CUDA", "E_TIMEOUT",
            "E_UNSUPPORTED", "E_WORKSPACE", "set_option", "OPT_DECODE_KERNEL", "DECODE_AUTO",
            "DECODE_MMA", "DECODE_TCGEN05", "OPT_PREFILL_KERNEL", "PREFILL_AUTO", "PREFILL_SINGLE",
-           "PREFILL_PAIR", "OPT_GATHER_ENGINE", "GATHER_TMA", "GATHER_COPY_ENGINE"]
+           "PREFILL_PAIR", "OPT_GATHER_ENGINE", "GATHER_TMA", "GATHER_COPY_ENGINE", "GATHER_TMA_SHARED_SM"]

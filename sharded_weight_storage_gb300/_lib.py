@@ -21,7 +21,7 @@ DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05 = 0, 1, 2
 OPT_PREFILL_KERNEL = 2
 PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
 OPT_GATHER_ENGINE = 3
-GATHER_TMA, GATHER_COPY_ENGINE = 0, 1
+GATHER_TMA, GATHER_COPY_ENGINE, GATHER_TMA_SHARED_SM = 0, 1, 2
 
 _NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", 2: "SWS_W_COLD", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}

@@ -107,6 +107,7 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   g.status = status_word(c);
   g.trace = next_trace(c);
   g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
+  g.shared_sm = g_gather_engine == SWS_GATHER_TMA_SHARED_SM;
   cudaError_t e = launch_gather(g, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
 }
@@ -713,7 +714,7 @@ int sws_set_option(int32_t option, int64_t value) {
       set_prefill_kernel((int)value);
       return SWS_OK;
     case SWS_OPT_GATHER_ENGINE:
-      if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE)
+      if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE && value != SWS_GATHER_TMA_SHARED_SM)
         return fail(SWS_E_INVALID, "set_option: gather engine %lld", (long long)value);
       g_gather_engine = (int)value;
       return SWS_OK;

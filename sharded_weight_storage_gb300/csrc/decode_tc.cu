@@ -84,7 +84,9 @@ struct TcCfg {
   static constexpr int kXBytes = WB ? kTermBytes : (int)tc_split_block_bytes(N);  // (hi, lo, e) or x
   static constexpr int kSwOff = kWBytes + kXBytes;  // four fp32 weight scales
   static constexpr int kStageBytes = (kSwOff + 16 + 1023) / 1024 * 1024;
-  static constexpr int kStages = N <= 16 ? 6 : N <= 32 ? 5 : 4;
+  // 4 stages hold 128 KB of weights in flight per SM (measured as fast as 5
+  // or 6) and leave room beside the CTA for a shared-SM gather CTA up to N = 32.
+  static constexpr int kStages = 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024;
   static constexpr int kDCols = WB ? 2 * N : 4 * N;  // one TMEM accumulator buffer: 2 tiles x (2N or N) columns
   static constexpr int kDBufs = N <= 32 ? 4 : 2;
@@ -96,6 +98,9 @@ static_assert(TcCfg<32>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory")
 static_assert(TcCfg<48>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
 static_assert(TcCfg<64>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
 static_assert(TcCfg<64>::kTmemCols <= 512, "decode_tc: TMEM columns");
+// A shared-SM gather CTA (3 x 16 KB stages) fits beside one GEMM CTA up to N = 32
+// (228 KB of shared memory per SM, 1 KB reserved per CTA).
+static_assert(TcCfg<32>::kSmem + 1024 + 3 * 16384 + 1024 <= 228 * 1024, "decode_tc: room for a gather CTA");
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
@@ -827,6 +832,9 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
     attr = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (attr == cudaSuccess)  // an SM running this CTA can still take a gather CTA
+      attr = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared);
   });
   if (attr != cudaSuccess) return attr;
   // 1. split the activations of every entry

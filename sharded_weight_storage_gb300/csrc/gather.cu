@@ -7,7 +7,12 @@
 // issues bulk TMA loads (global -> shared, completion on an mbarrier) and bulk
 // TMA stores (shared -> global) so that several tiles per SM are in flight
 // without occupying registers. Tiles are assigned round-robin over a grid
-// sized to the SM count.
+// sized to the SM count. Two shapes: 2 CTAs per SM with 3 x 32 KB stages (the
+// fastest alone), and 1 CTA per SM with 3 x 16 KB stages, which fits in the
+// shared memory a decode GEMM CTA leaves free, so that a lookahead gather and
+// the current layer's linears run on the same SMs at the same time instead of
+// one after the other. Both ask for the largest shared-memory carveout, so an
+// SM that runs one of them can still take the other's CTAs.
 //
 // relayout: section "加载：行 shard 先行，finalize 再重排", step 2 - the one-time
 // remap of per-weight row shards into flat chunks, expressed by the host as a
@@ -76,6 +81,9 @@ namespace {
 constexpr int kGatherTile = 32 * 1024;  // bytes per stage
 constexpr int kGatherStages = 3;
 constexpr int kGatherCtasPerSm = 2;
+constexpr int kSharedTile = 16 * 1024;  // the shared-SM variant
+constexpr int kSharedStages = 3;
+constexpr int kSharedCtasPerSm = 1;
 
 struct GatherParams {
   const uint8_t* chunks[256];
@@ -153,28 +161,39 @@ __global__ void __launch_bounds__(32) gather_kernel(const __grid_constant__ Gath
   dev::trace_end(p.trace, p.tag);
 }
 
-}  // namespace
-
-cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t stream) {
+template <int TILE, int STAGES, int CTAS_PER_SM>
+cudaError_t launch_gather_shape(const GatherLaunch& a, cudaStream_t stream) {
   GatherParams p;
   for (int i = 0; i < a.n; ++i) p.chunks[i] = a.chunks[i];
   p.chunk_bytes = a.chunk_bytes;
-  p.tiles_per_chunk = cdiv(a.chunk_bytes, kGatherTile);
+  p.tiles_per_chunk = cdiv(a.chunk_bytes, TILE);
   p.total_tiles = p.tiles_per_chunk * a.n;
   p.dst = a.dst;
   p.status = a.status;
   p.trace = a.trace;
   p.tag = a.tag;
   if (p.total_tiles == 0) return cudaSuccess;
-  auto kern = gather_kernel<kGatherTile, kGatherStages>;
-  const int smem = kGatherTile * kGatherStages;
+  auto kern = gather_kernel<TILE, STAGES>;
+  constexpr int smem = TILE * STAGES;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] { attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      (int)cudaSharedmemCarveoutMaxShared);
+  });
   if (attr_err != cudaSuccess) return attr_err;
-  const int64_t grid = std::min<int64_t>(p.total_tiles, (int64_t)device_sm_count() * kGatherCtasPerSm);
+  const int64_t grid = std::min<int64_t>(p.total_tiles, (int64_t)device_sm_count() * CTAS_PER_SM);
   kern<<<(unsigned)grid, 32, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t stream) {
+  return a.shared_sm ? launch_gather_shape<kSharedTile, kSharedStages, kSharedCtasPerSm>(a, stream)
+                     : launch_gather_shape<kGatherTile, kGatherStages, kGatherCtasPerSm>(a, stream);
 }
 
 // ---------------------------------------------------------------------------

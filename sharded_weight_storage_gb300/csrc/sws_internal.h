@@ -100,6 +100,7 @@ struct GatherLaunch {
   int32_t* status;
   uint64_t* trace;  // record (4 x u64) or nullptr
   uint64_t tag;     // written into the record's tag field
+  bool shared_sm = false;  // the small-footprint variant that fits beside a decode GEMM CTA
 };
 cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t s);
 

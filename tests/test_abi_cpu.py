@@ -169,7 +169,7 @@ def test_silu_mul_validates_before_any_launch(swslib):
 
 def test_options_reject_unknown_values(swslib):
     S = swslib
-    for opt, bad in ((S.OPT_DECODE_KERNEL, 3), (S.OPT_PREFILL_KERNEL, 3), (S.OPT_GATHER_ENGINE, 2), (99, 0)):
+    for opt, bad in ((S.OPT_DECODE_KERNEL, 3), (S.OPT_PREFILL_KERNEL, 3), (S.OPT_GATHER_ENGINE, 3), (99, 0)):
         with pytest.raises(S.SwsError) as ei:
             S.set_option(opt, bad)
         assert ei.value.code == S.E_INVALID

@@ -97,7 +97,12 @@ def test_shared_expert_chain(S, m, src_name):
     assert st.ctx.status() == 0
 
 
-def test_copy_engine_gather_matches_oracle_and_kernel(S):
+@pytest.mark.parametrize("engine", ["copy_engine", "tma_shared_sm"])
+def test_other_gather_engines_match_oracle_and_kernel(S, engine):
+    # The copy-engine gather and the shared-SM TMA kernel (one 48 KB CTA per
+    # SM, 16 KB tiles: a different tile split of the same chunks) against the
+    # oracle's T and the default kernel, byte for byte.
+    eng = S.GATHER_COPY_ENGINE if engine == "copy_engine" else S.GATHER_TMA_SHARED_SM
     w = WL.scaled_workload(WL.ATTN_KDA, rows_div=8, cols_div=8, name="kda_div8")
     ents = workload_entries(w, 2)
     layers = draw_layers(w, 2)
@@ -105,7 +110,7 @@ def test_copy_engine_gather_matches_oracle_and_kernel(S):
     try:
         for l in range(2):
             _, _, t_ref = oracle_layer_T(ents, w.n_shards, l, layers[l])
-            S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_COPY_ENGINE)
+            S.set_option(S.OPT_GATHER_ENGINE, eng)
             st.slots[1].fill_(0xAB)
             st.ctx.gather_to_slot(l, 1, 0)
             torch.cuda.synchronize()
@@ -120,7 +125,8 @@ def test_copy_engine_gather_matches_oracle_and_kernel(S):
         S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
 
 
-def test_run_layers_with_copy_engine_gather(S):
+@pytest.mark.parametrize("engine", ["copy_engine", "tma_shared_sm"])
+def test_run_layers_with_other_gather_engines(S, engine):
     w = WL.scaled_workload(WL.STACK92, rows_div=16, cols_div=16, n_layers=5, name="stack5_div16")
     ents = workload_entries(w)
     layers = draw_layers(w)
@@ -135,10 +141,24 @@ def test_run_layers_with_copy_engine_gather(S):
             xs[j], ys[j] = a, b
         io.append(([a.data_ptr() for a in xl], [b.data_ptr() for b in yl], m))
     main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    eng = S.GATHER_COPY_ENGINE if engine == "copy_engine" else S.GATHER_TMA_SHARED_SM
     try:
-        S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_COPY_ENGINE)
+        S.set_option(S.OPT_GATHER_ENGINE, eng)
         st.ctx.run_layers(0, 4, io, 0, main.cuda_stream, side.cuda_stream)
         main.synchronize()
+        if engine == "tma_shared_sm":
+            # captured and replayed: the same outputs, bit for bit
+            first = {j: y.clone() for j, y in ys.items()}
+            for y in ys.values():
+                y.fill_(float("nan"))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                st.ctx.run_layers(0, 4, io, 0, main.cuda_stream, side.cuda_stream)
+            with torch.cuda.stream(main):
+                g.replay()
+            main.synchronize()
+            for j in ys:
+                assert torch.equal(ys[j], first[j]), f"entry {j}: graph replay differs"
     finally:
         S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
     for l in range(5):
