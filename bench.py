@@ -781,7 +781,7 @@ def run_16bit(args, dist, f16=False):
         call()
         t = timed(call, reps=5)
     fl = 2.0 * m * rows * cols
-    kern = "to_f16_kernel + prefill_bf16_kernel<true>" if f16 else "prefill_bf16_kernel<false>"
+    kern = "to_f16_kernel + prefill_16_kernel<true>" if f16 else "prefill_16_kernel<false>"
     out["prefill"] = {"linear": f"[{rows}, {cols}] {name} at m = {m}", "kernel": f"{kern} (tcgen05 kind::f16)",
                       "us": t * 1e3, "TFLOPS": fl / t / 1e9, "frac_of_bf16_peak": fl / t / 1e9 / bf16_burst,
                       "bf16_peak_tflops": bf16_burst}

@@ -648,7 +648,7 @@ __device__ __forceinline__ void mma_16(uint32_t d_tmem, uint64_t a_desc, uint64_
 }
 
 template <bool F16>
-__global__ void __launch_bounds__(kThreads, 1) prefill_bf16_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_16_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mdone;
   __shared__ uint32_t s_tmem;
@@ -904,15 +904,15 @@ int launch_prefill_16(const PrefillLaunch& a, bool f16, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr = cudaFuncSetAttribute(prefill_16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(prefill_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      attr = cudaFuncSetAttribute(prefill_16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (16-bit)");
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
   const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-  cudaError_t e = f16 ? launch_high(prefill_bf16_kernel<true>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p)
-                      : launch_high(prefill_bf16_kernel<false>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
+  cudaError_t e = f16 ? launch_high(prefill_16_kernel<true>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p)
+                      : launch_high(prefill_16_kernel<false>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "prefill 16-bit kernel launch");
 }
 
