@@ -544,6 +544,30 @@ def run_stack(args, dist, n_layers):
     main = main_hi
     steps(1, S.RUN_FUSED)
     fused_ms = dist.max(steps(k, S.RUN_FUSED))
+
+    def prefilled_steps(k):
+        # The same linears with their weights already in a slot (layer 0's,
+        # gathered once, read n_layers times): the baseline of the second
+        # reading of the exposed gather (lookahead step minus this).
+        ctx.gather_to_slot(0, 0, main.cuda_stream)
+        ents0 = st.layer_entries(0)
+        xs0 = [xs[j] for j in range(len(ents0))]
+        ys0 = [ys[j] for j in range(len(ents0))]
+        run = lambda: ctx.layer_linears(0, S.SRC_SLOT0, [x.data_ptr() for x in xs0], [y.data_ptr() for y in ys0], m,
+                                        main.cuda_stream)
+        for _ in range(n_layers):
+            run()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        for _ in range(k):
+            for _ in range(n_layers):
+                run()
+        b.record(main)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / k
+
+    prefilled_ms = dist.max(prefilled_steps(k))
     graph_ms = dist.max(graph_steps(k, 0))
     graph_fused_ms = dist.max(graph_steps(k, S.RUN_FUSED))
     # the lookahead with the gather on the copy engines (no SMs taken from the linears)
@@ -601,6 +625,8 @@ def run_stack(args, dist, n_layers):
         "exposed_gather_first_layer_us": 1e3 * ex[0],
         "exposed_frac_of_step": sum(ex) / sum(lm + ex) if sum(lm + ex) > 0 else 0.0,
         "exposed_vs_resident_us_per_layer": (slot_ms - fused_ms) * 1e3 / n_layers,
+        "prefilled_slot_per_layer_us": prefilled_ms * 1e3 / n_layers,
+        "exposed_vs_prefilled_slot_us_per_layer": (slot_ms - prefilled_ms) * 1e3 / n_layers,
         "layer_linears_us": 1e3 * statistics.mean(lm),
         "step_GBps": n_layers * (3 * total + sum(layer_bytes(ents[:ne], m)[1:])) / slot_ms / 1e6,
         "fused_weight_GBps": n_layers * total / fused_ms / 1e6,
