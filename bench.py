@@ -431,13 +431,34 @@ def run_ours(args, dist):
     hx = [x.cpu().pin_memory() for x in xs[m]]
     hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys[m]]
 
+    # A serving loop's order: the step's activations come in from pinned host
+    # memory and its outputs go back on a copy stream, beside the gather on the
+    # compute stream; events keep every buffer's readers and writers in order
+    # (x is overwritten only after the previous step's linears read it, y only
+    # after its previous copy out finished).
+    cs = torch.cuda.Stream(device=dev)
+    lin_done = torch.cuda.Event()
+    y_free = torch.cuda.Event()
+    x_ready = torch.cuda.Event()
+    lin_done.record(stream)
+    y_free.record(stream)
+
     def e2e_step():
-        for j in range(len(ents)):
-            xs[m][j].copy_(hx[j], non_blocking=True)
+        cs.wait_event(lin_done)
+        with torch.cuda.stream(cs):
+            for j in range(len(ents)):
+                xs[m][j].copy_(hx[j], non_blocking=True)
+        x_ready.record(cs)
         ctx.gather_to_slot(0, 0, sp)
+        stream.wait_event(x_ready)
+        stream.wait_event(y_free)
         ctx.layer_linears(0, 0, [x.data_ptr() for x in xs[m]], [y.data_ptr() for y in ys[m]], m, sp)
-        for j in range(len(ents)):
-            hy[j].copy_(ys[m][j], non_blocking=True)
+        lin_done.record(stream)
+        cs.wait_event(lin_done)
+        with torch.cuda.stream(cs):
+            for j in range(len(ents)):
+                hy[j].copy_(ys[m][j], non_blocking=True)
+        y_free.record(cs)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -448,6 +469,7 @@ def run_ours(args, dist):
         a.record(stream)
         for _ in range(args.steps):
             e2e_step()
+        stream.wait_event(y_free)  # the last step's outputs are back on the host
         b.record(stream)
         torch.cuda.synchronize()
     e2e_ms = dist.max(a.elapsed_time(b)) / args.steps
