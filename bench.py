@@ -556,6 +556,24 @@ def run_stack(args, dist, n_layers):
         del g
         return a.elapsed_time(b) / k
 
+    def lib_graph_steps(k, flags):
+        # The library's own capture (sws_graph_capture), instantiated with
+        # per-node priorities, so the linears keep their launch priority.
+        g = ctx.graph_capture(0, n_layers - 1, io, flags, main.cuda_stream, side.cuda_stream)
+        try:
+            for _ in range(2):
+                g.launch(main.cuda_stream)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for _ in range(k):
+                g.launch(main.cuda_stream)
+            b.record(main)
+            torch.cuda.synchronize()
+        finally:
+            g.close()
+        return a.elapsed_time(b) / k
+
     k = max(3, args.steps // 2)
     steps(max(2, args.warmup // 2), 0)
     slot_ms = dist.max(steps(k, 0))
@@ -592,6 +610,8 @@ def run_stack(args, dist, n_layers):
     prefilled_ms = dist.max(prefilled_steps(k))
     graph_ms = dist.max(graph_steps(k, 0))
     graph_fused_ms = dist.max(graph_steps(k, S.RUN_FUSED))
+    lib_graph_ms = dist.max(lib_graph_steps(k, 0))
+    lib_graph_fused_ms = dist.max(lib_graph_steps(k, S.RUN_FUSED))
     # the lookahead with the gather on the copy engines (no SMs taken from the linears)
     S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_COPY_ENGINE)
     steps(1, 0)
@@ -608,6 +628,7 @@ def run_stack(args, dist, n_layers):
     steps(1, 0)
     sh_ms = dist.max(steps(k, 0))
     sh_graph_ms = dist.max(graph_steps(k, 0))
+    sh_lib_graph_ms = dist.max(lib_graph_steps(k, 0))
     sh_exposed = []
     for _ in range(3):
         ctx.run_layers(0, n_layers - 1, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
@@ -635,11 +656,14 @@ def run_stack(args, dist, n_layers):
         "equal_stream_priority_per_layer_us": slot_equal_prio_ms * 1e3 / n_layers,
         "fused_step_ms": fused_ms, "fused_per_layer_us": fused_ms * 1e3 / n_layers,
         "graph_step_ms": graph_ms, "graph_per_layer_us": graph_ms * 1e3 / n_layers,
+        "library_graph_per_layer_us": lib_graph_ms * 1e3 / n_layers,
+        "library_graph_fused_per_layer_us": lib_graph_fused_ms * 1e3 / n_layers,
         "copy_engine_gather_step_ms": ce_ms, "copy_engine_gather_per_layer_us": ce_ms * 1e3 / n_layers,
         "copy_engine_exposed_gather_us_per_layer": 1e3 * statistics.mean(ce_ex[1:]) if n_layers > 1 else 1e3 * ce_ex[0],
         "graph_fused_step_ms": graph_fused_ms, "graph_fused_per_layer_us": graph_fused_ms * 1e3 / n_layers,
         "shared_sm_gather_per_layer_us": sh_ms * 1e3 / n_layers,
         "shared_sm_gather_graph_per_layer_us": sh_graph_ms * 1e3 / n_layers,
+        "shared_sm_gather_library_graph_per_layer_us": sh_lib_graph_ms * 1e3 / n_layers,
         "shared_sm_gather_exposed_us_per_layer": 1e3 * statistics.mean(sh_ex[1:]) if n_layers > 1 else 1e3 * sh_ex[0],
         "shared_sm_gather_exposed_vs_resident_us_per_layer": (sh_ms - fused_ms) * 1e3 / n_layers,
         "shared_sm_gather_step_GBps": n_layers * (3 * total + sum(layer_bytes(ents[:ne], m)[1:])) / sh_ms / 1e6,

@@ -73,6 +73,7 @@ extern "C" {
 typedef struct CUstream_st* sws_stream_t;
 typedef struct sws_plan sws_plan;
 typedef struct sws_ctx sws_ctx;
+typedef struct sws_graph sws_graph;
 
 /* One weight declared to the planner. rows = out_features (dimension 0, the
  * one row shards split), cols = in_features; row-major [rows, cols]. */
@@ -270,6 +271,26 @@ int sws_wait_prefetch(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t st
  *                   first layer, from the run's start),
  *   layer_ms[l]   - time from the start to the end of layer l's linears. */
 int sws_run_timing(sws_ctx* ctx, float* exposed_ms, float* layer_ms, int32_t n);
+
+/* A lookahead run recorded once as a CUDA graph (blog "CUDA graph 与 draft
+ * 模型": the per-layer schedule is fixed, so it is replayed instead of
+ * re-issued). sws_graph_capture captures sws_run_layers(ctx, first, last, io,
+ * flags, main, side) on `main` (thread-local capture mode; `main` must not be
+ * the legacy default stream nor already capturing, else SWS_E_INVALID /
+ * SWS_E_STATE) and instantiates it with per-node priorities kept
+ * (cudaGraphInstantiateFlagUseNodePriority), so the linears' kernels keep the
+ * higher launch priority they have in eager runs. SWS_RUN_TIMING and
+ * SWS_RUN_FIRST_PREFETCHED are not allowed (SWS_E_INVALID). Nothing runs at
+ * capture; each sws_graph_launch replays the run on `stream` on the pointers
+ * given at capture (refill the activations in place between launches). The
+ * graph uses the context's events, slots and workspace: replays of graphs of
+ * one context, and eager calls on it, must not overlap on the GPU. On error
+ * *out is NULL and any partial capture is discarded. The caller destroys the
+ * graph (sws_graph_destroy, NULL allowed) before the context. */
+int sws_graph_capture(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
+                      sws_stream_t main, sws_stream_t side, sws_graph** out);
+int sws_graph_launch(sws_graph* graph, sws_stream_t stream);
+void sws_graph_destroy(sws_graph* graph);
 
 /* Prefill activation quantiser: for each row m and 128-column group g,
  * ex[m, g] = 2^k with k the smallest integer such that amax <= 448 * 2^k

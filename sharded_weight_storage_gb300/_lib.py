@@ -66,6 +66,10 @@ _PROTOS = [
     ("sws_run_layers", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_uint32, C.c_void_p,
                                  C.c_void_p]),
     ("sws_run_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32]),
+    ("sws_graph_capture", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_uint32, C.c_void_p,
+                                    C.c_void_p, C.POINTER(C.c_void_p)]),
+    ("sws_graph_launch", C.c_int, [C.c_void_p, C.c_void_p]),
+    ("sws_graph_destroy", None, [C.c_void_p]),
     ("sws_quantize_x", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("sws_silu_mul", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
     ("sws_prefetch_layer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
@@ -185,6 +189,27 @@ def silu_mul(gu: int, m: int, f: int, act: int, stream: int = 0):
     check(lib().sws_silu_mul(C.c_void_p(gu), m, f, C.c_void_p(act), C.c_void_p(stream or None)), "silu_mul")
 
 
+class Graph:
+    """A captured lookahead run (sws_graph_capture); destroy it before its context."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def launch(self, stream: int = 0):
+        check(lib().sws_graph_launch(self.handle, C.c_void_p(stream or None)), "graph_launch")
+
+    def close(self):
+        if self.handle:
+            lib().sws_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Ctx:
     """sws_ctx_create and the calls that take a context."""
 
@@ -218,8 +243,8 @@ class Ctx:
         check(lib().sws_layer_linears(self.handle, layer, src, C.byref(io), C.c_void_p(stream or None)),
               "layer_linears")
 
-    def run_layers(self, first: int, last: int, io: Sequence[tuple], flags: int, main: int, side: int):
-        """io[l - first] = (x_ptrs, y_ptrs, m) for layer l."""
+    @staticmethod
+    def _io_array(io: Sequence[tuple]):
         n = max(1, len(io))
         arr = (_LayerIO * n)()
         keep = []
@@ -227,8 +252,22 @@ class Ctx:
             xa, ya = _ptrs(xs), _ptrs(ys)
             keep += [xa, ya]
             arr[i] = _LayerIO(C.cast(xa, C.POINTER(C.c_void_p)), C.cast(ya, C.POINTER(C.c_void_p)), m)
+        return arr, keep
+
+    def run_layers(self, first: int, last: int, io: Sequence[tuple], flags: int, main: int, side: int):
+        """io[l - first] = (x_ptrs, y_ptrs, m) for layer l."""
+        arr, keep = self._io_array(io)
         check(lib().sws_run_layers(self.handle, first, last, arr, flags, C.c_void_p(main or None),
                                    C.c_void_p(side or None)), "run_layers")
+
+    def graph_capture(self, first: int, last: int, io: Sequence[tuple], flags: int, main: int, side: int) -> "Graph":
+        """Records run_layers(first, last, io, flags, main, side) as a CUDA
+        graph instantiated with per-node priorities; replay with Graph.launch."""
+        arr, keep = self._io_array(io)
+        h = C.c_void_p()
+        check(lib().sws_graph_capture(self.handle, first, last, arr, flags, C.c_void_p(main or None),
+                                      C.c_void_p(side or None), C.byref(h)), "graph_capture")
+        return Graph(h.value)
 
     def prefetch_layer(self, layer: int, slot: int, stream: int = 0):
         """Gathers `layer` into `slot` on `stream` ahead of use (draft-model layer 0)."""

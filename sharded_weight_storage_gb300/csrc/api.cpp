@@ -621,6 +621,58 @@ int sws_run_layers(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* 
   return SWS_OK;
 }
 
+int sws_graph_capture(sws_ctx* c, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
+                      sws_stream_t main_s, sws_stream_t side_s, sws_graph** out) {
+  if (!out) return fail(SWS_E_INVALID, "graph_capture: out is NULL");
+  *out = nullptr;
+  if (!c) return fail(SWS_E_INVALID, "graph_capture: ctx is NULL");
+  if (flags & (SWS_RUN_TIMING | SWS_RUN_FIRST_PREFETCHED))
+    return fail(SWS_E_INVALID, "graph_capture: SWS_RUN_TIMING and SWS_RUN_FIRST_PREFETCHED are eager-only");
+  cudaStream_t ms = (cudaStream_t)main_s;
+  if (!ms) return fail(SWS_E_INVALID, "graph_capture: the legacy default stream cannot capture");
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  SWS_CUDA_TRY(cudaStreamIsCapturing(ms, &cap));
+  if (cap != cudaStreamCaptureStatusNone) return fail(SWS_E_STATE, "graph_capture: main is already capturing");
+  SWS_CUDA_TRY(cudaStreamBeginCapture(ms, cudaStreamCaptureModeThreadLocal));
+  const int rc = sws_run_layers(c, first, last, io, flags, main_s, side_s);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ee = cudaStreamEndCapture(ms, &g);  // always ends it, so `main` is usable again
+  if (rc != SWS_OK) {
+    if (g) cudaGraphDestroy(g);
+    return rc;
+  }
+  if (ee != cudaSuccess) return cuda_fail(ee, "graph_capture: cudaStreamEndCapture");
+  cudaGraphExec_t x = nullptr;
+  const cudaError_t ie = cudaGraphInstantiateWithFlags(&x, g, cudaGraphInstantiateFlagUseNodePriority);
+  if (ie != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(ie, "graph_capture: cudaGraphInstantiateWithFlags");
+  }
+  sws_graph* h = new (std::nothrow) sws_graph;
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return fail(SWS_E_INVALID, "graph_capture: out of host memory");
+  }
+  h->graph = g;
+  h->exec = x;
+  *out = h;
+  return SWS_OK;
+}
+
+int sws_graph_launch(sws_graph* g, sws_stream_t stream) {
+  if (!g) return fail(SWS_E_INVALID, "graph_launch: graph is NULL");
+  SWS_CUDA_TRY(cudaGraphLaunch(g->exec, (cudaStream_t)stream));
+  return SWS_OK;
+}
+
+void sws_graph_destroy(sws_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
 int sws_run_timing(sws_ctx* c, float* exposed_ms, float* layer_ms, int32_t n) {
   if (!c) return fail(SWS_E_INVALID, "run_timing: ctx is NULL");
   if (c->timed_n == 0) return fail(SWS_E_STATE, "run_timing: the last run had no SWS_RUN_TIMING");

@@ -178,6 +178,11 @@ cudaError_t launch_bounded_wait(int32_t* status, uint64_t limit_ns, cudaStream_t
 
 }  // namespace sws
 
+struct sws_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
 struct sws_plan {
   int32_t n_shards = 1;
   uint32_t flags = 0;

@@ -167,6 +167,17 @@ def test_silu_mul_validates_before_any_launch(swslib):
     assert ei.value.code == S.E_ALIGN
 
 
+def test_graph_calls_validate_before_any_cuda_call(swslib):
+    import ctypes as C
+    L = swslib.lib()
+    out = C.c_void_p(123)
+    assert L.sws_graph_capture(None, 0, 0, None, 0, None, None, C.byref(out)) == swslib.E_INVALID
+    assert out.value is None  # *out is cleared on error
+    assert L.sws_graph_capture(None, 0, 0, None, 0, None, None, None) == swslib.E_INVALID
+    assert L.sws_graph_launch(None, None) == swslib.E_INVALID
+    L.sws_graph_destroy(None)  # a no-op
+
+
 def test_options_reject_unknown_values(swslib):
     S = swslib
     for opt, bad in ((S.OPT_DECODE_KERNEL, 3), (S.OPT_PREFILL_KERNEL, 3), (S.OPT_GATHER_ENGINE, 3), (99, 0)):

@@ -198,6 +198,54 @@ def test_run_layers_captures_into_a_cuda_graph(S, stack, m):
     assert st.ctx.status() == 0
 
 
+@pytest.mark.parametrize("flags", [0, "fused"])
+def test_library_graph_keeps_the_eager_results(S, stack, flags):
+    # sws_graph_capture records the same run (instantiated with per-node
+    # priorities): a launch gives the eager run's bits, a second launch on new
+    # activations in the same buffers gives their results; bad arguments are
+    # refused before anything is captured.
+    st, layers = stack
+    fl = S.RUN_FUSED if flags == "fused" else 0
+    m = 8
+    xs, ys, io = _io(st, 0, 6, m)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    st.ctx.run_layers(0, 6, io, fl, main.cuda_stream, side.cuda_stream)
+    main.synchronize()
+    ref = {j: y.clone() for j, y in ys.items()}
+    for bad in (S.RUN_TIMING, S.RUN_FIRST_PREFETCHED):
+        with pytest.raises(S.SwsError) as ei:
+            st.ctx.graph_capture(0, 6, io, bad, main.cuda_stream, side.cuda_stream)
+        assert ei.value.code == S.E_INVALID
+    with pytest.raises(S.SwsError) as ei:  # the legacy default stream cannot capture
+        st.ctx.graph_capture(0, 6, io, fl, 0, side.cuda_stream)
+    assert ei.value.code == S.E_INVALID
+    with pytest.raises(S.SwsError):  # a bad range is refused, and main is left usable
+        st.ctx.graph_capture(0, 9, io, fl, main.cuda_stream, side.cuda_stream)
+    g = st.ctx.graph_capture(0, 6, io, fl, main.cuda_stream, side.cuda_stream)
+    try:
+        for y in ys.values():
+            y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.launch(main.cuda_stream)
+        main.synchronize()
+        for j in ys:
+            assert torch.equal(ys[j], ref[j]), f"entry {j}: graph launch differs from the eager run"
+        for x in xs.values():  # new inputs, same buffers
+            x.copy_(torch.flip(x, dims=[1]))
+        torch.cuda.synchronize()
+        g.launch(main.cuda_stream)
+        main.synchronize()
+        for l in range(0, 7):
+            for j in st.layer_entries(l):
+                want = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[l].codes[j], layers[l].scales[j])
+                assert_close(bf16_tensor_to_f64(ys[j]), want, f"launch 2, layer {l} entry {j}")
+    finally:
+        g.close()
+    st.ctx.run_layers(0, 6, io, fl, main.cuda_stream, side.cuda_stream)  # eager still works afterwards
+    main.synchronize()
+    assert st.ctx.status() == 0
+
+
 def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable(S, stack):
     # Failure detection without a fault: a kernel waits (the library's bounded
     # wait) on a barrier nothing arrives at, gives up after 2 ms and records
