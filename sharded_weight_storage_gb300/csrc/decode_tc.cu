@@ -31,6 +31,8 @@
 //   3. settle_kernel, a programmatic dependent of (2): adds the partial sums
 //      of every shared row block in K order and writes Y. Settling in its own
 //      grid keeps the GEMM free of fences, atomics and cold code at its end.
+//      It releases its own dependents at once, so a gather that follows on the
+//      stream (the next step's) overlaps it.
 // decode_tc_kernel (swap-AB: weight rows are the MMA's M = 128 dimension, the
 // activations its N = 16..64 dimension, m rounded up to 16):
 //   * warp 0, one thread: producer. Per unit (256 weight rows x 128 K) one TMA
@@ -612,6 +614,10 @@ template <int N, bool FUSED, int WT>
 __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p,
                                                          const __grid_constant__ SettlePlan sp) {
   grid_dependency_wait();  // the GEMM's results are complete and visible
+  // A gather launched next on the stream (programmatic serialisation) may
+  // start now: it writes a slot, which nothing here reads, and reads chunks,
+  // which nothing here writes; later stream work still waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (FUSED && (int32_t)blockIdx.x >= sp.n) {
     straddle_row<N, WT>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
     return;

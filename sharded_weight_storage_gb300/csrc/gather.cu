@@ -185,8 +185,21 @@ cudaError_t launch_gather_shape(const GatherLaunch& a, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = std::min<int64_t>(p.total_tiles, (int64_t)device_sm_count() * CTAS_PER_SM);
-  kern<<<(unsigned)grid, 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: when the previous kernel on the stream
+  // is a decode launch's settle grid (which releases its dependents at once),
+  // the gather overlaps it; after any other kernel it starts as usual, when
+  // that kernel completes. The gather never waits on its predecessor's data.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
