@@ -163,7 +163,12 @@ void sws_ctx_destroy(sws_ctx* ctx);
  * slot[i*C : (i+1)*C] = chunk(layer, i) for i in [0, N), a pure byte copy on
  * `stream`, by the TMA bulk-copy kernel or, with SWS_OPT_GATHER_ENGINE =
  * SWS_GATHER_COPY_ENGINE, by N cudaMemcpyAsync copies. Tags the slot with
- * `layer` (host-side, in issue order). */
+ * `layer` (host-side, in issue order). The kernel is launched with
+ * programmatic stream serialisation: right after a decode linear of this
+ * library on `stream`, it may start while that launch's last (settle) kernel,
+ * which reads no slot and writes only y, finishes; after any other work it
+ * starts when that work completes, and work queued after it still waits for
+ * everything before it. */
 int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 
 /* Y = X W_j^T for entry j (blog section "核心抽象": the GEMM sees the full W),

@@ -82,7 +82,11 @@ int ensure_events(sws_ctx* c, size_t n) {
 
 int g_gather_engine = SWS_GATHER_TMA;
 
-int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
+// overlap_prev: launch the kernel with programmatic stream serialisation (see
+// launch_gather); only the stand-alone gather call asks for it. Inside
+// run_layers the gathers sit behind event waits on the side stream, where it
+// gains nothing, and a captured programmatic edge there slowed graph replays.
+int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s, bool overlap_prev = false) {
   const sws_plan* p = c->plan;
   const LayerPlan& lp = p->layers[layer];
   c->slot_tag[slot] = layer;
@@ -108,6 +112,7 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s) {
   g.trace = next_trace(c);
   g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
   g.shared_sm = g_gather_engine == SWS_GATHER_TMA_SHARED_SM;
+  g.overlap_prev = overlap_prev;
   cudaError_t e = launch_gather(g, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
 }
@@ -532,7 +537,7 @@ int sws_gather_to_slot(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t str
   if (!c) return fail(SWS_E_INVALID, "gather_to_slot: ctx is NULL");
   if (layer < 0 || layer >= (int32_t)c->plan->layers.size()) return fail(SWS_E_INVALID, "gather_to_slot: layer %d", layer);
   if (slot != 0 && slot != 1) return fail(SWS_E_INVALID, "gather_to_slot: slot %d", slot);
-  return gather_impl(c, layer, slot, (cudaStream_t)stream);
+  return gather_impl(c, layer, slot, (cudaStream_t)stream, /*overlap_prev=*/true);
 }
 
 int sws_linear(sws_ctx* c, int32_t entry, int32_t src, const void* x, int64_t m, void* y, sws_stream_t stream) {

@@ -185,10 +185,11 @@ cudaError_t launch_gather_shape(const GatherLaunch& a, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = std::min<int64_t>(p.total_tiles, (int64_t)device_sm_count() * CTAS_PER_SM);
-  // Programmatic stream serialisation: when the previous kernel on the stream
-  // is a decode launch's settle grid (which releases its dependents at once),
-  // the gather overlaps it; after any other kernel it starts as usual, when
-  // that kernel completes. The gather never waits on its predecessor's data.
+  // With overlap_prev, programmatic stream serialisation: when the previous
+  // kernel on the stream is a decode launch's settle grid (which releases its
+  // dependents at once), the gather overlaps it; after any other kernel it
+  // starts as usual, when that kernel completes. The gather never waits on
+  // its predecessor's data.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(32);
@@ -198,7 +199,7 @@ cudaError_t launch_gather_shape(const GatherLaunch& a, cudaStream_t stream) {
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.overlap_prev ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -101,6 +101,7 @@ struct GatherLaunch {
   uint64_t* trace;  // record (4 x u64) or nullptr
   uint64_t tag;     // written into the record's tag field
   bool shared_sm = false;  // the small-footprint variant that fits beside a decode GEMM CTA
+  bool overlap_prev = false;  // programmatic stream serialisation: may overlap a predecessor that allows it
 };
 cudaError_t launch_gather(const GatherLaunch& a, cudaStream_t s);
 
