@@ -37,7 +37,7 @@
 // activations its N = 16..64 dimension, m rounded up to 16):
 //   * warp 0, one thread: producer. Per unit (256 weight rows x 128 K) one TMA
 //     load of the weight slab, one bulk copy of the slab's split block and two
-//     4-byte async copies of the unit's weight scales, into one of 4-6 stages.
+//     4-byte async copies of the unit's weight scales, into one of 4 stages.
 //   * warp 1: allocates TMEM and issues, per unit, 2 tiles x 4 MMAs
 //     (128 x 2N x 32: the hi and lo operands side by side as one 2N-row B
 //     operand, so each weight byte is read from shared memory once) into one

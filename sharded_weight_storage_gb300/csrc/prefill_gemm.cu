@@ -74,7 +74,7 @@ constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kPairM = 256, kPairN = 256;
 constexpr int kPairStages = 6;
 constexpr int kPairABytes = (kPairM / 2) * kBK;         // 16 KB
-constexpr int kPairBBytes = (kPairN / 2) * kBK;         // 8 KB
+constexpr int kPairBBytes = (kPairN / 2) * kBK;         // 16 KB
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairEpiWarps = 16;
 constexpr int kPairThreads = (2 + kPairEpiWarps) * 32;
