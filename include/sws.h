@@ -290,8 +290,12 @@ int sws_run_timing(sws_ctx* ctx, float* exposed_ms, float* layer_ms, int32_t n);
  * given at capture (refill the activations in place between launches). The
  * graph uses the context's events, slots and workspace: replays of graphs of
  * one context, and eager calls on it, must not overlap on the GPU. On error
- * *out is NULL and any partial capture is discarded. The caller destroys the
- * graph (sws_graph_destroy, NULL allowed) before the context. */
+ * *out is NULL, any partial capture is discarded and the context's host-side
+ * state (slot tags, prefetch marks, trace position) is as before the call. On
+ * success the slots' layer tags become unknown: an eager sws_linear from a
+ * slot needs a sws_gather_to_slot (or a run_layers) first, else SWS_E_STATE.
+ * The caller destroys the graph (sws_graph_destroy, NULL allowed) before the
+ * context. */
 int sws_graph_capture(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io* io, uint32_t flags,
                       sws_stream_t main, sws_stream_t side, sws_graph** out);
 int sws_graph_launch(sws_graph* graph, sws_stream_t stream);

@@ -638,19 +638,34 @@ int sws_graph_capture(sws_ctx* c, int32_t first, int32_t last, const sws_layer_i
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   SWS_CUDA_TRY(cudaStreamIsCapturing(ms, &cap));
   if (cap != cudaStreamCaptureStatusNone) return fail(SWS_E_STATE, "graph_capture: main is already capturing");
+  // Host-side bookkeeping runs in issue order, but nothing captured has run:
+  // on failure it is put back; on success the slots' layers are unknown until
+  // the next gather (a launch of the graph leaves them as the capture did).
+  const int32_t tag0 = c->slot_tag[0], tag1 = c->slot_tag[1];
+  const int32_t pre0 = c->prefetch_layer[0], pre1 = c->prefetch_layer[1];
+  const int32_t trace_next = c->trace_next;
+  auto restore = [&] {
+    c->slot_tag[0] = tag0;
+    c->slot_tag[1] = tag1;
+    c->prefetch_layer[0] = pre0;
+    c->prefetch_layer[1] = pre1;
+    c->trace_next = trace_next;
+  };
   SWS_CUDA_TRY(cudaStreamBeginCapture(ms, cudaStreamCaptureModeThreadLocal));
   const int rc = sws_run_layers(c, first, last, io, flags, main_s, side_s);
   cudaGraph_t g = nullptr;
   const cudaError_t ee = cudaStreamEndCapture(ms, &g);  // always ends it, so `main` is usable again
-  if (rc != SWS_OK) {
+  if (rc != SWS_OK || ee != cudaSuccess) {
     if (g) cudaGraphDestroy(g);
-    return rc;
+    restore();
+    return rc != SWS_OK ? rc : cuda_fail(ee, "graph_capture: cudaStreamEndCapture");
   }
-  if (ee != cudaSuccess) return cuda_fail(ee, "graph_capture: cudaStreamEndCapture");
+  c->slot_tag[0] = c->slot_tag[1] = -1;
   cudaGraphExec_t x = nullptr;
   const cudaError_t ie = cudaGraphInstantiateWithFlags(&x, g, cudaGraphInstantiateFlagUseNodePriority);
   if (ie != cudaSuccess) {
     cudaGraphDestroy(g);
+    restore();
     return cuda_fail(ie, "graph_capture: cudaGraphInstantiateWithFlags");
   }
   sws_graph* h = new (std::nothrow) sws_graph;

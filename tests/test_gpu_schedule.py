@@ -241,6 +241,11 @@ def test_library_graph_keeps_the_eager_results(S, stack, flags):
                 assert_close(bf16_tensor_to_f64(ys[j]), want, f"launch 2, layer {l} entry {j}")
     finally:
         g.close()
+    if not fl:  # after a capture the slots' layers are unknown to the host: an eager slot read is refused
+        j0 = st.layer_entries(6)[0]
+        with pytest.raises(S.SwsError) as ei:
+            st.ctx.linear(j0, S.SRC_SLOT0, xs[j0].data_ptr(), m, ys[j0].data_ptr(), 0)
+        assert ei.value.code == S.E_STATE
     st.ctx.run_layers(0, 6, io, fl, main.cuda_stream, side.cuda_stream)  # eager still works afterwards
     main.synchronize()
     assert st.ctx.status() == 0
