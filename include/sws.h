@@ -135,8 +135,9 @@ int sws_relayout(const sws_plan* plan, int32_t layer, const void* const* row_sha
 
 /* Bytes of workspace a context needs for linears with up to max_m rows of
  * activations (split-K partial sums, counters, the tcgen05 decode path's
- * activation split blocks, two buffers of prefill quantiser output and the
- * device status word). */
+ * activation split blocks, two buffers of prefill activations - the
+ * quantiser's output for E4M3 entries, x rounded to f16 for F16 entries - and
+ * the device status word). */
 int64_t sws_workspace_bytes(const sws_plan* plan, int64_t max_m);
 
 /* Creates a context over caller-owned device memory:
