@@ -97,13 +97,17 @@ def test_shared_expert_chain(S, m, src_name):
     assert st.ctx.status() == 0
 
 
+@pytest.mark.parametrize("wname", ["kda_div8", "tiny"])
 @pytest.mark.parametrize("engine", ["copy_engine", "tma_shared_sm"])
-def test_other_gather_engines_match_oracle_and_kernel(S, engine):
+def test_other_gather_engines_match_oracle_and_kernel(S, engine, wname):
     # The copy-engine gather and the shared-SM TMA kernel (one 48 KB CTA per
     # SM, 16 KB tiles: a different tile split of the same chunks) against the
-    # oracle's T and the default kernel, byte for byte.
+    # oracle's T and the default kernel, byte for byte. kda_div8's chunks are
+    # 21 whole 16 KB tiles (10.5 of the default's 32 KB); the tiny layer's
+    # 90,112-byte chunks end in a partial tile for both shapes.
     eng = S.GATHER_COPY_ENGINE if engine == "copy_engine" else S.GATHER_TMA_SHARED_SM
-    w = WL.scaled_workload(WL.ATTN_KDA, rows_div=8, cols_div=8, name="kda_div8")
+    w = WL.scaled_workload(WL.ATTN_KDA, rows_div=8, cols_div=8, name="kda_div8") if wname == "kda_div8" \
+        else WL.scaled_workload(WL.TINY, n_layers=2)
     ents = workload_entries(w, 2)
     layers = draw_layers(w, 2)
     st = build_stack(S, ents, w.n_shards, layers)
