@@ -159,10 +159,11 @@ def test_prefill_kda_layer_small(S):
         print(f"entry {j}: relative error vs bf16-exact oracle {rel:.3e}")
 
 
-@pytest.mark.parametrize("m", [2048])
+@pytest.mark.parametrize("m", [2048, 8192])
 def test_prefill_full_size_sampled_rows(S, kernel, m):
-    # The prefill workload's weights (KDA-like layer, N = 8), full sizes; the
-    # oracle computes 48 sampled token rows of every linear.
+    # The prefill workload's weights (KDA-like layer, N = 8), full sizes, at
+    # both token counts the benchmark times; the oracle computes 48 sampled
+    # token rows (and the first and last) of every linear.
     w = WL.PREFILL
     ents = workload_entries(w, 1)
     layers = draw_layers(WL.scaled_workload(w, n_layers=1), 1)
