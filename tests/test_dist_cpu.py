@@ -74,3 +74,28 @@ def test_single_rank_has_no_process_group(monkeypatch):
     assert d.world == 1 and d.pg is None and d.max(2.5) == 2.5
     d.barrier()
     d.close()
+
+
+def test_reference_arm_line_on_cpu(monkeypatch):
+    # The reference arm times the CPU oracle on a bounded sample of the
+    # shared-expert step and reports it with the same metric and config as
+    # the GPU arm, plus its cpu_baseline block and a zero-copy e2e.
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    sys.path.insert(0, ROOT)
+    import bench
+
+    d = bench.Dist()
+
+    class Args:
+        steps, warmup, gpus = 1, 0, 1
+
+    try:
+        line = bench.run_reference(Args, d)
+    finally:
+        d.close()
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["dtype"] == "f64"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"] == bench.config_block(1)
