@@ -82,6 +82,8 @@ def test_run_layers_outputs_and_ordering(S, stack, first, last):
             a, b = lin.get(l, (t0, t1))
             lin[l] = (min(a, t0), max(b, t1))
     assert sorted(gathers) == list(range(first, last + 1))
+    # exactly one gather per layer (the pages' one all-gather per layer)
+    assert sum(1 for k, _, _, _ in recs if k == 1) == last - first + 1
     assert sorted(lin) == list(range(first, last + 1))
     for (kb, lb), (ka, la) in O.happens_before(first, last):
         before = gathers[lb] if kb == "gather" else lin[lb]
