@@ -243,6 +243,22 @@ def linear(x: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64) @ dequant(codes, scales).T
 
 
+def dequant_at(codes: np.ndarray, scales: np.ndarray, rows=None, cols=None) -> np.ndarray:
+    """The sub-matrix W[rows][:, cols] of the dequantized weight, computed for
+    the selected rows and columns only: element (o, i) is
+    e4m3(q[o, i]) * s[o // 128, i // 128] in float64 (None selects all)."""
+    r = np.arange(codes.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    c = np.arange(codes.shape[1]) if cols is None else np.asarray(cols, dtype=np.int64)
+    s = np.asarray(scales, dtype=np.float64)[np.ix_(r // 128, c // 128)]
+    return e4m3_decode(np.asarray(codes)[np.ix_(r, c)]) * s
+
+
+def linear_rows(x: np.ndarray, codes: np.ndarray, scales: np.ndarray, rows) -> np.ndarray:
+    """Y[:, rows] of Y = X W^T: the outputs of the selected weight rows, from
+    those rows alone (for checking samples of full-size outputs)."""
+    return np.asarray(x, dtype=np.float64) @ dequant_at(codes, scales, rows=rows).T
+
+
 # Weight variants ([WS "加载：行 shard 先行，finalize 再重排", "量化变体"]): BF16
 # weights go through the same flat layout; ModelOpt FP8 keeps its per-tensor
 # scale replicated, outside T.

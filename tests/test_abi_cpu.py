@@ -61,6 +61,22 @@ def test_planner_matches_oracle_on_workloads(swslib, w):
     _compare_plan(swslib, [(0, e.rows, e.cols, 1) for e in w.entries], w.n_shards)
 
 
+def test_planner_matches_hand_derived_padded_layouts(swslib):
+    # tests/golden/layout_padding.txt: per-entry and tail padding both non-zero,
+    # replicated entries left out of T
+    from test_oracle_pins import read_padding_golden
+    S = swslib
+    dt = {1: S.E4M3, 2: S.BF16, 4: S.F32}
+    for n, ents, total, chunk in read_padding_golden().values():
+        with pytest.warns(RuntimeWarning):
+            plan = S.Plan([(0, dt[e], r, c) for (_, r, c, e, _) in ents], n)
+        assert plan.layer(0) == (total, chunk, len(ents))
+        assert plan.slot_bytes == total
+        for j, (_, r, c, e, off) in enumerate(ents):
+            assert plan.entry(j) == (off, r * c * e, off >= 0)
+        _compare_plan(S, [(0, r, c, e) for (_, r, c, e, _) in ents], n)
+
+
 def test_planner_matches_oracle_on_92_layer_stack(swslib):
     w = WL.STACK92
     _compare_plan(swslib, [(l, e.rows, e.cols, 1) for l in range(w.n_layers) for e in w.entries], w.n_shards)

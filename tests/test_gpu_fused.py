@@ -94,7 +94,7 @@ def test_fused_tc_straddling_rows_one_hot(S):
         xo[np.arange(m), torch.from_numpy(cols)] = 1.0
         y, kern = _linear_traced(S, st, j, S.SRC_FUSED, xo.cuda(), m)
         assert kern == KERNEL_TC_FUSED
-        want = O.e4m3_decode(ld.codes[j][row, cols]) * ld.scales[j][row // 128, cols // 128].astype(np.float64)
+        want = O.dequant_at(ld.codes[j], ld.scales[j], [row], cols)[0]
         got = y[:, row].cpu()
         assert torch.equal(got, torch.from_numpy(want).float().to(torch.bfloat16)), f"entry {j} row {row}"
 

@@ -130,17 +130,22 @@ def _check_linear_full(st, ld, j, src, m, key):
 
 
 def _check_linear_sampled(st, ld, j, src, m, key, n_rows=384, seed=0):
+    """Sampled output rows (n_rows of them, plus the first and last), or every
+    row when n_rows is None, computed by the oracle 4096 rows at a time."""
     layer, _, rows, cols = st.entries[j]
     x = WL.draw_x(key, j, m, cols)
-    y = _run_linear(st, j, src, x.cuda(), m)
+    y = bf16_tensor_to_f64(_run_linear(st, j, src, x.cuda(), m))
+    xf = WL.bf16_to_f64(WL.bf16_bits(x))
+    if n_rows is None:
+        for r0 in range(0, rows, 4096):
+            sel = np.arange(r0, min(rows, r0 + 4096))
+            assert_close(y[:, sel], O.linear_rows(xf, ld.codes[j], ld.scales[j], sel),
+                         f"entry {j} src {src} m {m} rows {r0}..{sel[-1]}")
+        return
     rng = np.random.default_rng(seed + j)
     sel = np.unique(np.concatenate([[0, rows - 1], rng.choice(rows, size=min(n_rows, rows), replace=False)]))
-    # dequantise only the selected rows, each with its own block-row of scales
-    wq = ld.codes[j][sel]
-    sc = ld.scales[j]
-    deq = O.e4m3_decode(wq) * np.repeat(sc[sel // 128].astype(np.float64), 128, axis=1)[:, :cols]
-    ref = WL.bf16_to_f64(WL.bf16_bits(x)) @ deq.T
-    assert_close(bf16_tensor_to_f64(y)[:, sel], ref, f"entry {j} src {src} m {m} (sampled rows)")
+    ref = O.linear_rows(xf, ld.codes[j], ld.scales[j], sel)
+    assert_close(y[:, sel], ref, f"entry {j} src {src} m {m} (sampled rows)")
 
 
 @pytest.mark.parametrize("w", [WL.TINY, SMALL_KDA], ids=lambda w: w.name)
@@ -165,9 +170,12 @@ def test_decode_linear_full_size_sampled_rows(S, w, ms):
     st.ctx.gather_to_slot(0, 0, 0)
     for m in ms:
         for j in range(len(ents)):
-            _check_linear_sampled(st, layers[0], j, S.SRC_SLOT0, m, w.key)
-            if m in (1, 64):
-                _check_linear_sampled(st, layers[0], j, S.SRC_FUSED, m, w.key, seed=7)
+            # the benchmark's decode size (m = 32 on the shared-expert layer): every output row
+            every = w is WL.SHARED_EXPERT and m == 32
+            _check_linear_sampled(st, layers[0], j, S.SRC_SLOT0, m, w.key, n_rows=None if every else 384)
+            if m in (1, 32, 64):
+                _check_linear_sampled(st, layers[0], j, S.SRC_FUSED, m, w.key, seed=7,
+                                      n_rows=None if every else 384)
 
 
 def test_decode_ragged_shapes(S):
@@ -211,7 +219,7 @@ def test_decode_special_cases(S):
         xo = torch.zeros((1, c), dtype=torch.bfloat16)
         xo[0, i] = 1.0
         y = _run_linear(st, 0, S.SRC_SLOT0, xo.cuda(), 1)
-        col = O.e4m3_decode(q[:, i]) * sc[np.arange(r) // 128, i // 128].astype(np.float64)
+        col = O.dequant_at(q, sc, cols=[i])[:, 0]
         want = torch.from_numpy(col).float().to(torch.bfloat16)
         assert torch.equal(y[0].cpu(), want)
     # m = 0 is a no-op
@@ -379,7 +387,7 @@ def test_decode_kernels_ragged_and_special(S, decode_kernel):
         xo = torch.zeros((m, c), dtype=torch.bfloat16)
         xo[np.arange(m), torch.from_numpy(cols)] = 1.0
         y = _run_linear(st, 2, S.SRC_SLOT1, xo.cuda(), m)
-        want = O.e4m3_decode(codes[2][:, cols].T) * scales[2][np.arange(r) // 128][:, cols // 128].T.astype(np.float64)
+        want = O.dequant_at(codes[2], scales[2], cols=cols).T
         if decode_kernel == "tcgen05":
             assert torch.equal(y.cpu(), torch.from_numpy(want).float().to(torch.bfloat16)), f"m {m}"
         else:

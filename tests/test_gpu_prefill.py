@@ -133,7 +133,7 @@ def test_prefill_special_cases(S, kernel):
     xo[np.arange(m), torch.from_numpy(cols)] = 1.0
     st.ctx.linear(0, S.SRC_SLOT1, xo.cuda().data_ptr(), m, y.data_ptr(), 0)
     torch.cuda.synchronize()
-    want = O.e4m3_decode(q[:, cols].T) * sc[np.arange(r) // 128][:, cols // 128].T.astype(np.float64)
+    want = O.dequant_at(q, sc, cols=cols).T
     got = bf16_tensor_to_f64(y)
     assert np.array_equal(got, WL.bf16_to_f64(WL.bf16_bits(torch.from_numpy(want).float().to(torch.bfloat16))))
 

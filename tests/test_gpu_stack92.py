@@ -61,11 +61,9 @@ def test_stack92_lookahead_full_size(S):
         base = bases[l % w.n_base]
         for j, e in enumerate(w.entries):
             rows = np.unique(np.concatenate([[0, e.rows - 1], rng.choice(e.rows, size=38, replace=False)]))
-            signs = WL.draw_row_signs(w.key, l, j, e.rows)[rows]
-            codes = base.codes[j][rows] ^ signs[:, None]
-            # the sampled rows' block scales: row r uses scale row r // 128
-            sc = base.scales[j][rows // 128]
-            want = x_f64(xs[j]) @ (O.e4m3_decode(codes) * np.repeat(sc.astype(np.float64), 128, axis=1)[:, :e.cols]).T
+            # layer l's codes: the base layer's with each row's sign bit flipped by its draw
+            codes = base.codes[j] ^ WL.draw_row_signs(w.key, l, j, e.rows)[:, None]
+            want = O.linear_rows(x_f64(xs[j]), codes, base.scales[j], rows)
             assert_close(bf16_tensor_to_f64(ys[l][j])[:, rows], want, f"layer {l} {e.name}")
     # every layer's slot is the concatenation of its chunks, byte for byte
     for l in range(L):

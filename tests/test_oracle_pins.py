@@ -561,3 +561,227 @@ def test_schedule_gates_each_gather_on_the_slot_previous_user():
     assert O.max_live_layers(0, 9) == 2
     assert O.max_live_layers(5, 5) == 1
     assert O.schedule(4, 3) == []
+
+
+# ---------------------------------------------------------------------------
+# layouts with non-zero padding, the chunk map, the lookahead's edges
+# (hand-typed goldens), each with planted mistakes that must fail them
+# ---------------------------------------------------------------------------
+
+
+def read_padding_golden():
+    """Cases of tests/golden/layout_padding.txt: name -> (N, [(entry name, rows,
+    cols, elem, offset or -1)], |T|, C)."""
+    cases = {}
+    with open(os.path.join(GOLDEN, "layout_padding.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, ents, total, chunk = [p.strip() for p in line.split("|")]
+            name, n = head.split()
+            rows = []
+            for tok in ents.split():
+                nm, rest = tok.split(":")
+                shape, off = rest.split("=")
+                r, c, e = (int(v) for v in shape.split(","))
+                rows.append((nm, r, c, e, int(off)))
+            cases[name] = (int(n), rows, int(total), int(chunk))
+    return cases
+
+
+def _layout_matches_padding_golden(plan_fn) -> bool:
+    for n, ents, total, chunk in read_padding_golden().values():
+        p = plan_fn([(0, r, c, e) for (_, r, c, e, _) in ents], n)
+        ly = p.layers[0]
+        if (ly.total, ly.chunk) != (total, chunk):
+            return False
+        for j, (_, _, _, _, off) in enumerate(ents):
+            if off < 0:
+                if p.sharded[j] or j in ly.offsets:
+                    return False
+            elif ly.offsets.get(j) != off:
+                return False
+    return True
+
+
+def test_layout_with_padding_matches_hand_derived_golden():
+    assert _layout_matches_padding_golden(O.plan_layout)
+
+
+def _mutant_plan(entry_pad, tail_pad):
+    """plan_layout with its two padding rules replaced: a planted mistake."""
+    def plan(entries, n):
+        p = O.plan_layout(entries, n)
+        for ly in p.layers.values():
+            off = 0
+            for j in ly.entries:
+                ly.offsets[j] = off
+                off += entry_pad(ly.sizes[j], n)
+            ly.total = tail_pad(off, n)
+            ly.chunk = ly.total // n
+        return p
+    return plan
+
+
+@pytest.mark.parametrize("entry_pad,tail_pad", [
+    (lambda s, n: O.roundup(s, 16), lambda t, n: O.roundup(t, 16 * n)),      # the rule itself
+    (lambda s, n: O.roundup(s, 32), lambda t, n: O.roundup(t, 16 * n)),      # entries over-padded
+    (lambda s, n: O.roundup(s, 16 * n), lambda t, n: O.roundup(t, 16 * n)),  # each entry to 16N
+    (lambda s, n: O.roundup(s, 16), lambda t, n: O.roundup(t, 16)),          # no 16N tail rule
+    (lambda s, n: s, lambda t, n: O.roundup(t, 16 * n)),                     # no 16-byte entry rule
+], ids=["rule", "entry32", "entry16N", "tail16", "entry1"])
+def test_padding_golden_catches_planted_padding_mistakes(entry_pad, tail_pad, request):
+    ok = _layout_matches_padding_golden(_mutant_plan(entry_pad, tail_pad))
+    assert ok == (request.node.callspec.id == "rule")
+
+
+def test_padded_layouts_pack_chunk_and_relayout():
+    rng = np.random.default_rng(31)
+    for n, ents, total, chunk in read_padding_golden().values():
+        p = O.plan_layout([(0, r, c, e) for (_, r, c, e, _) in ents], n)
+        ly = p.layers[0]
+        data = {j: rng.integers(1, 256, size=(ents[j][1], ents[j][2] * ents[j][3]), dtype=np.uint8)
+                for j in ly.entries}
+        t = O.pack(p, 0, data)
+        assert t.size == total
+        pad = np.ones(total, bool)
+        for j in ly.entries:
+            pad[ly.offsets[j]:ly.offsets[j] + ly.sizes[j]] = False
+            assert np.array_equal(O.view(p, 0, t, j), data[j])
+        # the padding bytes (per entry and at the tail) are the only zeros
+        assert pad.sum() == total - sum(ly.sizes.values()) > 0
+        assert not t[pad].any() and t[~pad].all()
+        ch = O.split_chunks(p, 0, t)
+        assert [c.size for c in ch] == [chunk] * n and np.array_equal(O.gather(ch), t)
+        shards = {j: WL.row_shards(data[j], n) for j in ly.entries}
+        assert all(np.array_equal(a, b) for a, b in zip(O.relayout(p, 0, shards), ch))
+
+
+def test_chunk_map_matches_hand_derived_points():
+    n, ents, _, _ = read_padding_golden()["pad_n7"]
+    layouts = {"tiny_flat_layer": _plan_for(WL.TINY),
+               "pad_n7": O.plan_layout([(0, r, c, e) for (_, r, c, e, _) in ents], n)}
+    seen = 0
+    with open(os.path.join(GOLDEN, "chunk_map_points.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                name, g, ci, off = line.split()
+                assert O.chunk_map(layouts[name], 0, int(g)) == (int(ci), int(off)), line
+                seen += 1
+    assert seen == 8
+
+
+def test_chunk_map_finds_every_byte_of_t_in_its_chunk():
+    # step 2's byte rule: rank i holds T[i*C, (i+1)*C), so byte g is byte g % C of chunk g // C
+    rng = np.random.default_rng(32)
+    plans = [O.plan_layout([(0, r, c, e) for (_, r, c, e, _) in ents], n)
+             for n, ents, _, _ in read_padding_golden().values()]
+    plans.append(_plan_for(WL.TINY))
+    for p in plans:
+        ly = p.layers[0]
+        t = rng.integers(0, 256, size=ly.total, dtype=np.uint8)
+        chunks = [t[i * ly.chunk:(i + 1) * ly.chunk] for i in range(p.n_shards)]
+        hit = np.zeros((p.n_shards, ly.chunk), bool)
+        for g in range(0, ly.total, max(1, ly.total // 4099)):
+            ci, off = O.chunk_map(p, 0, g)
+            assert 0 <= ci < p.n_shards and 0 <= off < ly.chunk
+            assert chunks[ci][off] == t[g]
+            assert not hit[ci, off]
+            hit[ci, off] = True
+
+
+def read_edges_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "lookahead_edges.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, edges = [p.strip() for p in line.split("|")]
+            first, last = (int(v) for v in head.split())
+            cases.append((first, last, set(edges.split())))
+    return cases
+
+
+def _edge_names(edges):
+    short = {"gather": "g", "compute": "c"}
+    return {f"{short[a[0]]}{a[1]}<{short[b[0]]}{b[1]}" for a, b in edges}
+
+
+def _edges_match_golden(fn) -> bool:
+    return all(_edge_names(fn(first, last)) == want for first, last, want in read_edges_golden())
+
+
+def test_happens_before_matches_hand_listed_edges():
+    assert _edges_match_golden(O.happens_before)
+
+
+def test_edges_golden_catches_planted_schedule_mistakes():
+    def no_slot_reuse(first, last):  # the gate on done(l-2) dropped
+        return [e for e in O.happens_before(first, last) if e[0][0] != "compute"]
+
+    def gate_one_back(first, last):  # gated on done(l-1) instead of done(l-2)
+        out = [e for e in O.happens_before(first, last) if e[0][0] != "compute"]
+        return out + [(("compute", l - 1), ("gather", l)) for l in range(first + 1, last + 1)]
+
+    def gate_from_first(first, last):  # the slot-reuse gate also on the second layer
+        return O.happens_before(first, last) + [(("compute", first - 1), ("gather", first + 1))] \
+            if last > first else O.happens_before(first, last)
+
+    for bad in (no_slot_reuse, gate_one_back, gate_from_first):
+        assert not _edges_match_golden(bad), bad.__name__
+
+
+def test_happens_before_follows_from_the_issue_order():
+    """Every listed edge is implied by the schedule's issue order: program
+    order on each stream plus record -> wait pairs of the same event."""
+    for first, last, _ in read_edges_golden():
+        ops = O.schedule(first, last)
+        succ = {i: set() for i in range(len(ops))}
+        prev_on = {}
+        for i, op in enumerate(ops):
+            if op.stream in prev_on:
+                succ[prev_on[op.stream]].add(i)
+            prev_on[op.stream] = i
+        for i, a in enumerate(ops):
+            for k, b in enumerate(ops):
+                if a.layer == b.layer and (a.kind, b.kind) in (("record_ready", "wait_ready"),
+                                                               ("record_done", "wait_done")):
+                    succ[i].add(k)
+
+        def reach(i):
+            seen, todo = set(), [i]
+            while todo:
+                for k in succ[todo.pop()]:
+                    if k not in seen:
+                        seen.add(k)
+                        todo.append(k)
+            return seen
+
+        idx = {(op.kind, op.layer): i for i, op in enumerate(ops) if op.kind in ("gather", "compute")}
+        for a, b in O.happens_before(first, last):
+            assert idx[b] in reach(idx[a]), (first, last, a, b)
+        # the lookahead itself: gather(l + 1) is not ordered after compute(l),
+        # so the two may overlap
+        for l in range(first, last):
+            assert idx[("gather", l + 1)] not in reach(idx[("compute", l)])
+
+
+def test_dequant_at_and_linear_rows_select_from_the_definition():
+    rng = np.random.default_rng(33)
+    rows, cols = 300, 200  # partial 128-blocks in both directions
+    q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x41
+    sc = (2.0 ** rng.uniform(-8, -4, size=(3, 2))).astype(np.float32)
+    rsel, csel = [0, 5, 127, 128, 299], [0, 127, 128, 199]
+    got = O.dequant_at(q, sc, rsel, csel)
+    for a, o in enumerate(rsel):  # element by element from the definition
+        for b, i in enumerate(csel):
+            assert got[a, b] == O.e4m3_code_value(int(q[o, i])) * float(sc[o // 128, i // 128])
+    assert np.array_equal(O.dequant_at(q, sc), O.dequant(q, sc))
+    x = _bf16_values(rng, (3, cols))
+    np.testing.assert_allclose(O.linear_rows(x, q, sc, rsel), O.linear(x, q, sc)[:, rsel], rtol=1e-12, atol=0)
+    onehot = np.zeros((1, cols))
+    onehot[0, 130] = 1.0
+    assert np.array_equal(O.linear_rows(onehot, q, sc, rsel)[0], O.dequant_at(q, sc, rsel, [130])[:, 0])
