@@ -250,7 +250,7 @@ class Timer:
         return [a.elapsed_time(b) for a, b in self.pairs.get(key, [])]
 
 
-KERNEL_EVENT_EVERY = 10  # headline steps between two with per-kernel events
+KERNEL_TIMING_STEPS = 50  # at least this many event-bracketed steps give the per-kernel durations
 
 
 def run_ours(args, dist):
@@ -318,12 +318,11 @@ def run_ours(args, dist):
         with torch.cuda.stream(stream):
             h0 = time.time()
             t0 = tm.ev()
-            # Per-kernel events on every 10th step only: a timing event between
-            # one step's settle kernel and the next step's gather keeps the
-            # gather from starting under the settle, so timing every step would
-            # slow the steps it measures.
+            # No events inside: a timing event between one step's settle
+            # kernel and the next step's gather keeps the gather from starting
+            # under the settle, so per-kernel events would slow the steps.
             for i in range(args.steps):
-                step(HEADLINE_M, tm if i % KERNEL_EVENT_EVERY == 0 else None)
+                step(HEADLINE_M)
             t1 = tm.ev()
             torch.cuda.synchronize()
             h1 = time.time()
@@ -346,8 +345,21 @@ def run_ours(args, dist):
     window_ms = dist.max(window_ms)
     wb, scb, actb = layer_bytes(ents, HEADLINE_M)
     step_bytes = 2 * total + wb + scb + actb
-    per_kernel = {k: statistics.mean(tm.ms(k)) for k in ("gather", "linears")}
-    results["headline"] = dict(window_ms=window_ms, step_bytes=step_bytes, per_kernel_ms=per_kernel)
+    # Per-kernel durations behind `roofline`: the same step, right after the
+    # timed region (clocks and caches as they were there), repeated at least
+    # KERNEL_TIMING_STEPS times with events around each of its two launches.
+    kt = Timer(stream)
+    n_kt = max(KERNEL_TIMING_STEPS, args.steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step(HEADLINE_M)
+        for _ in range(n_kt):
+            step(HEADLINE_M, kt)
+    torch.cuda.synchronize()
+    per_kernel = {k: statistics.mean(kt.ms(k)) for k in ("gather", "linears")}
+    per_kernel_median = {k: statistics.median(kt.ms(k)) for k in ("gather", "linears")}
+    results["headline"] = dict(window_ms=window_ms, step_bytes=step_bytes, per_kernel_ms=per_kernel,
+                               per_kernel_median_ms=per_kernel_median, kernel_timing_steps=n_kt)
 
     # ---- per-M breakdown: step, slot linears, fused linears, gather alone --
     def timed(fn, reps, do_flush=True):
@@ -1107,8 +1119,8 @@ def config_block(world):
             "N_chunks": 16, "M": HEADLINE_M,
             "l2": "inputs larger than L2 (264 MB chunks + 264 MB slot per step); kernel-only timings flush L2 "
                   "by reading 512 MB before each launch",
-            "kernel_events": f"per-kernel CUDA events on every {KERNEL_EVENT_EVERY}th timed step (roofline "
-                             "durations); the step time covers all steps",
+            "kernel_events": f"none inside the timed region; the roofline's per-kernel durations are the mean "
+                             f"of >= {KERNEL_TIMING_STEPS} further steps with events around each launch",
             "parallelism": f"replicas x{world} (no collective)"}
 
 
@@ -1187,9 +1199,10 @@ def run_only(args, dist):
         elif args.only == "fused":
             ctx.linear(j, S.SRC_FUSED, x.data_ptr(), m, y.data_ptr(), 0)
         elif args.only == "noalloc":
-            S.lib().sws_linear_noalloc(C.c_void_p(st.slots[0].data_ptr() + off), C.c_void_p(st.scales[j].data_ptr()),
-                                       ents[j][1], ents[j][2], C.c_void_p(x.data_ptr()), m,
-                                       C.c_void_p(y.data_ptr()), None)
+            rc = S.lib().sws_linear_noalloc(C.c_void_p(st.slots[0].data_ptr() + off),
+                                            C.c_void_p(st.scales[j].data_ptr()), ents[j][1], ents[j][2],
+                                            C.c_void_p(x.data_ptr()), m, C.c_void_p(y.data_ptr()), None)
+            assert rc == 0, f"sws_linear_noalloc: {S.last_error()}"
         else:
             ctx.gather_to_slot(0, 0, 0)
             for jj in range(len(ents)):
@@ -1198,6 +1211,8 @@ def run_only(args, dist):
                 ctx.linear(jj, S.SRC_SLOT0, xx.data_ptr(), m, yy.data_ptr(), 0)
     torch.cuda.synchronize()
     assert ctx.status() == 0
+    if args.only == "noalloc":
+        assert S.noalloc_status() == 0
     print(f"only={args.only} m={m} entry={j} reps={args.reps}: ok")
 
 
@@ -1241,8 +1256,12 @@ def main():
     dom = max(pk, key=lambda k: pk[k])
     achieved = kbytes[dom] / pk[dom] / 1e6
     traffic = ncu_traffic(f"{knames[dom][0]}:{dom}", knames[dom][1])
-    kernels = {k: {"kernel": knames[k][0], "us": pk[k] * 1e3, "GBps": kbytes[k] / pk[k] / 1e6,
-                   "frac_of_hbm": kbytes[k] / pk[k] / 1e6 / hbm, "share_of_step": pk[k] / sum(pk.values())}
+    pkm = h["per_kernel_median_ms"]
+    kernels = {k: {"kernel": knames[k][0], "us": pk[k] * 1e3, "median_us": pkm[k] * 1e3,
+                   "GBps": kbytes[k] / pk[k] / 1e6, "frac_of_hbm": kbytes[k] / pk[k] / 1e6 / hbm,
+                   "share_of_step": pk[k] / sum(pk.values()), "launches_timed": h["kernel_timing_steps"],
+                   "algorithmic_bytes_per_launch": kbytes[k],
+                   "traffic": ncu_traffic(f"{knames[k][0]}:{k}", knames[k][1])}
                for k in pk}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
@@ -1252,7 +1271,9 @@ def main():
         "config": config_block(dist.world),
         "roofline": {"bound": "hbm", "kernel": knames[dom][0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
-                     "algorithmic_bytes_per_launch": kbytes[dom]},
+                     "algorithmic_bytes_per_launch": kbytes[dom], "launches_timed": h["kernel_timing_steps"],
+                     "kernels": {k: {"kernel": v["kernel"], "achieved": v["GBps"], "frac": v["frac_of_hbm"]}
+                                 for k, v in kernels.items()}},
         "e2e": {"value": dist.world * h["step_bytes"] / r["e2e"]["step_ms"] / 1e6, "unit": "GB/s",
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"],
                 "ms_per_step": r["e2e"]["step_ms"]},

@@ -213,23 +213,39 @@ int sws_layer_linears(sws_ctx* ctx, int32_t layer, int32_t src, const sws_layer_
  * weights has no headroom for allocations made later, and a device allocation
  * in the middle of a decode step can stall the whole GPU; such a caller passes
  * only its inputs and outputs here. Same result as sws_linear for m <= 64
- * (within rounding: the split-K partition may differ):
+ * (within rounding: the split-K partition may differ), on the warp-level
+ * mma.sync decode kernel:
  *   w:      E4M3 weight [rows, cols] row-major (e.g. a slot view slot + o_j),
  *   scales: float32 block scales [ceil(rows/128), ceil(cols/128)],
  *   x:      bf16 [m, cols], y: bf16 [m, rows]; all 16-byte aligned.
  * Limits: 0 <= m <= 64, cols % 16 == 0, at most 4096 row blocks (2,097,152
  * rows for m <= 16, 1,048,576 rows for 16 < m <= 64); anything larger is
  * rejected with SWS_E_INVALID / SWS_E_UNSUPPORTED before any launch.
- * Scratch: a fixed 8 MiB + 16 KiB array inside the library's device image
- * (every GPU that loads the library holds it until the process exits). It is
- * shared by all calls on a device and keeps the last call's contents; the
- * arrival counters in it are cleared on `stream` before each launch. Calls
- * whose work overlaps on the GPU race on it, so serialise them (one stream).
+ * Scratch: a fixed array of 32 MiB + 16 KiB + 256 B inside the library's
+ * device image (every GPU that loads the library holds it until the process
+ * exits): split-K partial sums (two 64 KiB slots for each of up to 256 CTAs,
+ * so the grid is the same as sws_linear's), one arrival counter per row block
+ * and one int32 status word. It is shared by all calls on a device and keeps
+ * the last call's contents; the arrival counters are cleared on `stream`
+ * before each launch. Calls whose work overlaps on the GPU race on it, so
+ * serialise them (one stream).
+ * Status: a device-side wait of the kernel that runs out (2 s) records
+ * SWS_E_TIMEOUT in the status word, and the rows it left unwritten stay as
+ * they were; the call itself has already returned SWS_OK by then, so read the
+ * word with sws_noalloc_status. It stays set until cleared there.
  * The first call on a device looks up the array's device address with
- * cudaGetSymbolAddress (with that device current); make that first call
- * before any stream capture. No cudaMalloc / cudaFree is ever called. */
+ * cudaGetSymbolAddress (with that device current) and clears the status word
+ * on `stream`; make that first call before any stream capture. No cudaMalloc /
+ * cudaFree is ever called. */
 int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t cols, const void* x, int64_t m,
                        void* y, sws_stream_t stream);
+/* Status word of sws_linear_noalloc's scratch on the current device: *status
+ * receives 0, or the SWS_E_* code one of its kernels recorded since the last
+ * clear (e.g. SWS_E_TIMEOUT). Waits for the device's queued work first, at
+ * most the host wait limit (SWS_OPT_HOST_WAIT_MS): past it the call returns
+ * SWS_E_TIMEOUT itself and *status is not read. `clear` != 0 resets the word.
+ * Returns SWS_OK when *status was read. Allocates nothing. */
+int sws_noalloc_status(int32_t clear, int32_t* status);
 
 /* Lookahead over layers first..last (blog "提前一层" and "SGLang 中的实现"):
  * gather(first) is issued on `side` after `side` waits for work already
@@ -270,8 +286,10 @@ int sws_run_layers(sws_ctx* ctx, int32_t first, int32_t last, const sws_layer_io
 int sws_prefetch_layer(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 int sws_wait_prefetch(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t stream);
 
-/* After a run with SWS_RUN_TIMING: synchronises on the recorded events and
- * writes, per layer of that run (n values each, n = last - first + 1):
+/* After a run with SWS_RUN_TIMING: waits for the recorded events (polling, at
+ * most the host wait limit SWS_OPT_HOST_WAIT_MS, else SWS_E_TIMEOUT with a
+ * message saying so) and writes, per layer of that run (n values each,
+ * n = last - first + 1):
  *   exposed_ms[l] - time `main` stood waiting for ready(l) (from the end of
  *                   layer l-1's linears to the start of layer l's; for the
  *                   first layer, from the run's start),
@@ -318,8 +336,13 @@ int sws_quantize_x(const void* x, int64_t m, int64_t k, void* xq, float* ex, sws
 int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t stream);
 
 /* Device-side status of a context: 0, or the SWS_E_* code a kernel recorded
- * (e.g. SWS_E_TIMEOUT when a wait on a TMA completion gave up). Synchronises
- * the device. `clear` != 0 resets it. */
+ * (e.g. SWS_E_TIMEOUT when a wait on a TMA completion gave up). Waits for all
+ * work queued on the context's device first, at most the host wait limit
+ * (SWS_OPT_HOST_WAIT_MS): past it the call returns SWS_E_TIMEOUT without
+ * reading the word, the device's work continues, and a later call reads it.
+ * The call empties sws_last_error() first, so after it a non-empty message
+ * means the call itself failed (host wait, CUDA error) and an empty one that
+ * the value is the word. `clear` != 0 resets the word. */
 int sws_ctx_status(sws_ctx* ctx, int32_t clear);
 
 /* ---- tracing ------------------------------------------------------------ */
@@ -356,6 +379,8 @@ int32_t sws_trace_count(const sws_ctx* ctx);
                                       decode GEMM CTA (m <= 32): run_layers' lookahead gather then
                                       shares the SMs with the current layer's linears instead of
                                       waiting for them; slower than SWS_GATHER_TMA on its own */
+#define SWS_OPT_HOST_WAIT_MS 4 /* limit of the host-side waits (sws_run_timing, sws_ctx_status,
+                                  sws_noalloc_status), in ms, 1..3600000; default 10000 */
 /* Process-wide options, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance, from views and through
  * the chunk map (a chunk-map launch whose segments or split rows exceed the
@@ -371,7 +396,9 @@ int sws_set_option(int32_t option, int64_t value);
  * kernel of the library uses, on a barrier that nothing arrives at; after
  * limit_ns (0..1e8) it records SWS_E_TIMEOUT in the context's status word (as
  * a kernel whose TMA copy never landed would) and returns. The context stays
- * usable; sws_ctx_status reports and clears the code. */
+ * usable; sws_ctx_status reports and clears the code. With ctx == NULL the
+ * code goes to the status word of sws_linear_noalloc's scratch on the current
+ * device (read with sws_noalloc_status). */
 int sws_test_bounded_wait(sws_ctx* ctx, int64_t limit_ns, sws_stream_t stream);
 
 /* ---- misc --------------------------------------------------------------- */

@@ -22,6 +22,7 @@ OPT_PREFILL_KERNEL = 2
 PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
 OPT_GATHER_ENGINE = 3
 GATHER_TMA, GATHER_COPY_ENGINE, GATHER_TMA_SHARED_SM = 0, 1, 2
+OPT_HOST_WAIT_MS = 4
 
 _NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", 2: "SWS_W_COLD", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}
@@ -63,6 +64,7 @@ _PROTOS = [
     ("sws_layer_linears", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_void_p]),
     ("sws_linear_noalloc", C.c_int, [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int64,
                                      C.c_void_p, C.c_void_p]),
+    ("sws_noalloc_status", C.c_int, [C.c_int32, C.POINTER(C.c_int32)]),
     ("sws_run_layers", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(_LayerIO), C.c_uint32, C.c_void_p,
                                  C.c_void_p]),
     ("sws_run_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32]),
@@ -179,6 +181,25 @@ def set_option(option: int, value: int):
     check(lib().sws_set_option(option, value), "set_option")
 
 
+def linear_noalloc(w: int, scales: int, rows: int, cols: int, x: int, m: int, y: int, stream: int = 0):
+    """Decode linear with the library's fixed device scratch (no workspace)."""
+    check(lib().sws_linear_noalloc(C.c_void_p(w), C.c_void_p(scales), rows, cols, C.c_void_p(x), m, C.c_void_p(y),
+                                   C.c_void_p(stream or None)), "linear_noalloc")
+
+
+def noalloc_status(clear: bool = False) -> int:
+    """Status word of linear_noalloc's scratch: 0 or an SWS_E_* code. A host
+    wait that ran out, or a CUDA error, raises."""
+    v = C.c_int32()
+    check(lib().sws_noalloc_status(1 if clear else 0, C.byref(v)), "noalloc_status")
+    return v.value
+
+
+def test_bounded_wait_noalloc(limit_ns: int, stream: int = 0):
+    """The bounded-wait check on linear_noalloc's status word."""
+    check(lib().sws_test_bounded_wait(None, limit_ns, C.c_void_p(stream or None)), "test_bounded_wait")
+
+
 def quantize_x(x: int, m: int, k: int, xq: int, ex: int, stream: int = 0):
     check(lib().sws_quantize_x(C.c_void_p(x), m, k, C.c_void_p(xq), C.c_void_p(ex), C.c_void_p(stream or None)),
           "quantize_x")
@@ -289,7 +310,11 @@ class Ctx:
         return list(a), list(b)
 
     def status(self, clear: bool = False) -> int:
+        """The context's device status word (0 or an SWS_E_* code). A host wait
+        that ran out, or a CUDA error, raises (sws_last_error is set)."""
         rc = lib().sws_ctx_status(self.handle, 1 if clear else 0)
+        if rc < 0 and last_error():
+            raise SwsError(rc, "ctx_status: " + last_error())
         return rc
 
     def trace_begin(self, records: int, capacity: int, stream: int = 0):

@@ -11,11 +11,69 @@
 #include <string.h>
 
 #include <algorithm>
+#include <chrono>
+#include <condition_variable>
+#include <memory>
 #include <new>
+#include <thread>
 
 #include "sws_internal.h"
 
 using namespace sws;
+
+namespace sws {
+
+namespace {
+int g_host_wait_ms = 10000;  // SWS_OPT_HOST_WAIT_MS
+}
+
+int host_wait_ms() { return g_host_wait_ms; }
+
+int wait_event_deadline(cudaEvent_t ev, const char* what) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const auto limit = std::chrono::milliseconds(g_host_wait_ms);
+  for (int spin = 0;; ++spin) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return SWS_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(e, what);
+    if (std::chrono::steady_clock::now() - t0 > limit)
+      return fail(SWS_E_TIMEOUT, "%s: the device had not reached the event after %d ms (host wait limit)", what,
+                  g_host_wait_ms);
+    if (spin > 64) std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+int device_sync_deadline(int device, const char* what) {
+  // cudaDeviceSynchronize cannot be polled, so a helper thread makes the call
+  // and this thread waits for it with the limit; after a timeout the helper
+  // returns by itself once the device has finished the work queued before it.
+  struct State {
+    std::mutex mu;
+    std::condition_variable cv;
+    bool done = false;
+    cudaError_t err = cudaSuccess;
+  };
+  auto st = std::make_shared<State>();
+  try {
+    std::thread([st, device] {
+      cudaError_t e = cudaSetDevice(device);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      std::lock_guard<std::mutex> lock(st->mu);
+      st->err = e;
+      st->done = true;
+      st->cv.notify_all();
+    }).detach();
+  } catch (...) {
+    return fail(SWS_E_INVALID, "%s: could not start the wait thread", what);
+  }
+  std::unique_lock<std::mutex> lock(st->mu);
+  if (!st->cv.wait_for(lock, std::chrono::milliseconds(g_host_wait_ms), [&] { return st->done; }))
+    return fail(SWS_E_TIMEOUT, "%s: the device had not finished its queued work after %d ms (host wait limit)", what,
+                g_host_wait_ms);
+  return st->err == cudaSuccess ? SWS_OK : cuda_fail(st->err, what);
+}
+
+}  // namespace sws
 
 struct sws_ctx {
   const sws_plan* plan = nullptr;
@@ -697,7 +755,8 @@ int sws_run_timing(sws_ctx* c, float* exposed_ms, float* layer_ms, int32_t n) {
   if (!c) return fail(SWS_E_INVALID, "run_timing: ctx is NULL");
   if (c->timed_n == 0) return fail(SWS_E_STATE, "run_timing: the last run had no SWS_RUN_TIMING");
   if (n < c->timed_n) return fail(SWS_E_INVALID, "run_timing: n=%d < %d layers", n, c->timed_n);
-  SWS_CUDA_TRY(cudaEventSynchronize(c->t_end[c->timed_n - 1]));
+  const int rc = wait_event_deadline(c->t_end[c->timed_n - 1], "run_timing");
+  if (rc != SWS_OK) return rc;
   for (int32_t i = 0; i < c->timed_n; ++i) {
     float a = 0.f, b = 0.f;
     SWS_CUDA_TRY(cudaEventElapsedTime(&a, c->t_wait[i], c->t_begin[i]));
@@ -739,9 +798,15 @@ int sws_wait_prefetch(sws_ctx* c, int32_t layer, int32_t slot, sws_stream_t stre
 }
 
 int sws_test_bounded_wait(sws_ctx* c, int64_t limit_ns, sws_stream_t stream) {
-  if (!c) return fail(SWS_E_INVALID, "test_bounded_wait: ctx is NULL");
   if (limit_ns < 0 || limit_ns > 100000000) return fail(SWS_E_INVALID, "test_bounded_wait: limit %lld ns", (long long)limit_ns);
-  cudaError_t e = launch_bounded_wait(status_word(c), (uint64_t)limit_ns, (cudaStream_t)stream);
+  int32_t* status = nullptr;
+  if (c) {
+    status = status_word(c);
+  } else {  // the status word of sws_linear_noalloc's fixed scratch on the current device
+    const int rc = noalloc_status_word(&status, (cudaStream_t)stream);
+    if (rc != SWS_OK) return rc;
+  }
+  cudaError_t e = launch_bounded_wait(status, (uint64_t)limit_ns, (cudaStream_t)stream);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "test_bounded_wait: launch");
 }
 
@@ -751,10 +816,15 @@ int sws_silu_mul(const void* gu, int64_t m, int64_t f, void* act, sws_stream_t s
 
 int sws_ctx_status(sws_ctx* c, int32_t clear) {
   if (!c) return fail(SWS_E_INVALID, "ctx_status: ctx is NULL");
+  clear_error();  // a message after this call comes from the call itself, not from the status word
   int32_t v = 0;
-  SWS_CUDA_TRY(cudaDeviceSynchronize());
+  const int rc = device_sync_deadline(c->device, "ctx_status");
+  if (rc != SWS_OK) return rc;
   SWS_CUDA_TRY(cudaMemcpy(&v, c->ws, sizeof v, cudaMemcpyDeviceToHost));
-  if (clear) SWS_CUDA_TRY(cudaMemset(c->ws, 0, sizeof v));
+  if (clear) {
+    SWS_CUDA_TRY(cudaMemset(c->ws, 0, sizeof v));
+    SWS_CUDA_TRY(cudaStreamSynchronize(nullptr));  // cleared before any later launch
+  }
   return v;
 }
 
@@ -784,6 +854,10 @@ int sws_set_option(int32_t option, int64_t value) {
       if (value < SWS_PREFILL_AUTO || value > SWS_PREFILL_PAIR)
         return fail(SWS_E_INVALID, "set_option: prefill kernel %lld", (long long)value);
       set_prefill_kernel((int)value);
+      return SWS_OK;
+    case SWS_OPT_HOST_WAIT_MS:
+      if (value < 1 || value > 3600000) return fail(SWS_E_INVALID, "set_option: host wait %lld ms", (long long)value);
+      g_host_wait_ms = (int)value;
       return SWS_OK;
     case SWS_OPT_GATHER_ENGINE:
       if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE && value != SWS_GATHER_TMA_SHARED_SM)

@@ -534,7 +534,7 @@ constexpr int stages_for() { return NT <= 2 ? 3 : NT == 4 ? 6 : 5; }
 
 int nt_for(int64_t m) { return m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8; }
 int rows_per_cta(int nt) { return kWarps * 16 * (nt <= 2 ? 4 : 2); }
-int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
+constexpr int64_t slot_bytes_for(int nt) { return (int64_t)kWarps * (nt <= 2 ? 4 : 2) * nt * 32 * 4 * 4; }
 
 template <int NT, bool FUSED, int WT>
 cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
@@ -543,9 +543,9 @@ cudaError_t launch_nt(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr int kRowsCta = kWarps * 16 * R;
   constexpr int kSmem = S * kRowsCta * kSlabK + 1024;
   auto kern = decode_kernel<NT, R, S, FUSED, WT>;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
+  static PerDevice once;
+  const cudaError_t attr =
+      once.run([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem); });
   if (attr != cudaSuccess) return attr;
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
   return launch_high(kern, dim3((unsigned)grid), dim3(kThreads), kSmem, s, p);
@@ -775,9 +775,9 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
 // the weights are placed has no headroom for allocations made later, and a
 // cudaMalloc issued in the middle of a decode step can synchronise the whole
 // device. This variant of the split-K decode kernel keeps its scratch (the
-// split-K partial sums and the per-row-block arrival counters) in a fixed
-// array that lives in the library's device image, so a call needs only the
-// caller's inputs and outputs.
+// split-K partial sums, the per-row-block arrival counters and a status word)
+// in a fixed array that lives in the library's device image, so a call needs
+// only the caller's inputs and outputs.
 //
 // The array is shared by every call on a device and keeps the last call's
 // contents; the arrival counters are cleared on the stream before each launch.
@@ -786,21 +786,25 @@ int launch_decode(const DecodeGroup& g, cudaStream_t s) {
 namespace sws {
 namespace {
 
-constexpr int64_t kNoAllocPartialBytes = int64_t(8) << 20;  // 8 MiB of fp32 partial sums
-constexpr int64_t kNoAllocCounters = 4096;                    // row blocks, one int32 each
-constexpr int64_t kNoAllocScratchBytes = kNoAllocPartialBytes + kNoAllocCounters * 4;
+// fp32 partial sums: two slots of the largest size (m > 32) for each of up to
+// kMaxGrid CTAs, so the grid is never narrowed to fit the array.
+constexpr int64_t kNoAllocPartialBytes = 2 * (int64_t)kMaxGrid * slot_bytes_for(8);  // 32 MiB
+static_assert(kNoAllocPartialBytes == (int64_t(32) << 20), "noalloc partial-sum region");
+constexpr int64_t kNoAllocCounters = 4096;  // row blocks, one int32 each
+constexpr int64_t kNoAllocStatusOffset = kNoAllocPartialBytes + kNoAllocCounters * 4;
+// [partial sums | counters | status word (int32) and padding]
+constexpr int64_t kNoAllocScratchBytes = kNoAllocStatusOffset + 256;
 constexpr int kMaxDevices = 64;
 
-// Partial sums first (256-byte aligned), counters after them.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device. The first call on
-// a device resolves it with cudaGetSymbolAddress (with that device current);
-// later calls reuse the cached address.
-int noalloc_scratch(uint8_t** out) {
+// Device address of the scratch array on the current device. The first use on
+// a device resolves it with cudaGetSymbolAddress (with that device current) and
+// clears the status word on `s`; later uses reuse the cached address.
+int noalloc_scratch(uint8_t** out, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaGetDevice");
@@ -810,6 +814,8 @@ int noalloc_scratch(uint8_t** out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaGetSymbolAddress(scratch)");
+    e = cudaMemsetAsync(static_cast<uint8_t*>(p) + kNoAllocStatusOffset, 0, 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaMemsetAsync(status)");
     g_noalloc_addr[dev] = p;
   }
   *out = static_cast<uint8_t*>(g_noalloc_addr[dev]);
@@ -817,6 +823,15 @@ int noalloc_scratch(uint8_t** out) {
 }
 
 }  // namespace
+
+int noalloc_status_word(int32_t** out, cudaStream_t s) {
+  uint8_t* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch, s);
+  if (rc != SWS_OK) return rc;
+  *out = reinterpret_cast<int32_t*>(scratch + kNoAllocStatusOffset);
+  return SWS_OK;
+}
+
 }  // namespace sws
 
 extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t rows, int64_t cols, const void* x,
@@ -851,18 +866,40 @@ extern "C" int sws_linear_noalloc(const void* w, const float* scales, int64_t ro
   rc = build_params(p, g, &nrb, &empty, s);
   if (rc != SWS_OK || empty) return rc;
   uint8_t* scratch = nullptr;
-  rc = noalloc_scratch(&scratch);
+  rc = noalloc_scratch(&scratch, s);
   if (rc != SWS_OK) return rc;
   int32_t* counters = reinterpret_cast<int32_t*>(scratch + kNoAllocPartialBytes);
   cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)(nrb * 4), s);
   if (e != cudaSuccess) return cuda_fail(e, "linear_noalloc: cudaMemsetAsync(counters)");
   p.counters = counters;
   p.partials = reinterpret_cast<float*>(scratch);
-  p.status = nullptr;
+  // A wait that runs out records SWS_E_TIMEOUT here (read by sws_noalloc_status).
+  p.status = reinterpret_cast<int32_t*>(scratch + kNoAllocStatusOffset);
   p.trace = nullptr;
   p.tag = 0;
-  // Two partial slots per CTA must fit in the fixed array.
+  // Two partial slots per CTA fit in the fixed array for every grid up to kMaxGrid.
   const int64_t grid_cap = kNoAllocPartialBytes / (2 * slot_bytes_for(nt));
   e = dispatch(p, nt, false, 0, grid_cap, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "linear_noalloc: kernel launch");
+}
+
+extern "C" int sws_noalloc_status(int32_t clear, int32_t* status) {
+  using namespace sws;
+  if (!status) return fail(SWS_E_INVALID, "noalloc_status: status is NULL");
+  *status = 0;
+  int32_t* word = nullptr;
+  int rc = noalloc_status_word(&word, nullptr);
+  if (rc != SWS_OK) return rc;
+  int dev = 0;
+  SWS_CUDA_TRY(cudaGetDevice(&dev));
+  rc = device_sync_deadline(dev, "noalloc_status");
+  if (rc != SWS_OK) return rc;
+  int32_t v = 0;
+  SWS_CUDA_TRY(cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost));
+  if (clear) {
+    SWS_CUDA_TRY(cudaMemset(word, 0, sizeof v));
+    SWS_CUDA_TRY(cudaStreamSynchronize(nullptr));  // cleared before any later launch
+  }
+  *status = v;
+  return SWS_OK;
 }

@@ -834,13 +834,13 @@ template <int N, bool FUSED, int WT>
 cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s) {
   constexpr bool WB = WT != 0;
   constexpr int kSmem = TcCfg<N, WB>::kSmem;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (attr == cudaSuccess)  // an SM running this CTA can still take a gather CTA
-      attr = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                  (int)cudaSharedmemCarveoutMaxShared);
+  static PerDevice once;
+  const cudaError_t attr = once.run([] {
+    cudaError_t a = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (a == cudaSuccess)  // an SM running this CTA can still take a gather CTA
+      a = cudaFuncSetAttribute(decode_tc_kernel<N, WT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    return a;
   });
   if (attr != cudaSuccess) return attr;
   // 1. split the activations of every entry

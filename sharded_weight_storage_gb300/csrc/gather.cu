@@ -175,13 +175,13 @@ cudaError_t launch_gather_shape(const GatherLaunch& a, cudaStream_t stream) {
   if (p.total_tiles == 0) return cudaSuccess;
   auto kern = gather_kernel<TILE, STAGES>;
   constexpr int smem = TILE * STAGES;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      (int)cudaSharedmemCarveoutMaxShared);
+  static PerDevice once;
+  const cudaError_t attr_err = once.run([&] {
+    cudaError_t a = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (a == cudaSuccess)
+      a = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    return a;
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = std::min<int64_t>(p.total_tiles, (int64_t)device_sm_count() * CTAS_PER_SM);

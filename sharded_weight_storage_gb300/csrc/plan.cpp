@@ -29,6 +29,8 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+void clear_error() { g_last_error.clear(); }
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(SWS_E_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }

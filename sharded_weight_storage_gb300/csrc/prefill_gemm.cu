@@ -864,11 +864,9 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
                                  kPairSmemBytes, s, p);
     if (le != cudaSuccess) return cuda_fail(le, "prefill pair kernel launch");
   } else {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-      attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
+    static PerDevice once;
+    const cudaError_t attr = once.run(
+        [] { return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
     if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute");
     const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
     cudaError_t le = launch_high(prefill_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
@@ -901,12 +899,12 @@ int launch_prefill_16(const PrefillLaunch& a, bool f16, cudaStream_t s) {
   p.status = a.status;
   p.trace = a.trace;
   p.tag = a.tag;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(prefill_16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(prefill_16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static PerDevice once;
+  const cudaError_t attr = once.run([] {
+    cudaError_t a = cudaFuncSetAttribute(prefill_16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (a == cudaSuccess)
+      a = cudaFuncSetAttribute(prefill_16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return a;
   });
   if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute (16-bit)");
   const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <utility>
 #include <stdint.h>
 
@@ -18,6 +19,7 @@ namespace sws {
 // Records a message for sws_last_error() and returns `code`.
 int fail(int code, const char* fmt, ...);
 int cuda_fail(cudaError_t e, const char* what);
+void clear_error();  // empties sws_last_error() on the calling thread
 #define SWS_CUDA_TRY(expr)                                   \
   do {                                                       \
     cudaError_t _e = (expr);                                 \
@@ -69,6 +71,39 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // that width (128- or 64-byte), zero fill outside.
 int encode_u8_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows,
                        int box_cols = 128);
+
+// Runs a set-up step (kernel attributes such as the dynamic shared-memory
+// limit, which the runtime keeps per device) once for each device it is called
+// on - the current one - and returns that device's result on every later call.
+struct PerDevice {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+  cudaError_t err[kMaxDevices] = {};
+  template <typename F>
+  cudaError_t run(F&& f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      err[dev] = f();
+      done[dev] = true;
+    }
+    return err[dev];
+  }
+};
+
+// Host-side waits for the device (sws_run_timing, sws_ctx_status,
+// sws_noalloc_status) give up after this many milliseconds with SWS_E_TIMEOUT
+// (SWS_OPT_HOST_WAIT_MS; the default is well above the device-side limit).
+int host_wait_ms();
+// Polls `ev` (cudaEventQuery) until it has completed or host_wait_ms() passed.
+int wait_event_deadline(cudaEvent_t ev, const char* what);
+// Waits for all work queued on `device` (cudaDeviceSynchronize on a helper
+// thread) for at most host_wait_ms(); SWS_E_TIMEOUT when it did not finish.
+int device_sync_deadline(int device, const char* what);
 
 // ---- kernel launchers (defined in the .cu files) -----------------------------
 int device_sm_count();
@@ -175,6 +210,9 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 int launch_prefill_16(const PrefillLaunch& a, bool f16, cudaStream_t s);
 
 cudaError_t launch_trace_reset(uint64_t* rec, int32_t n, cudaStream_t s);
+// The status word inside sws_linear_noalloc's fixed scratch on the current
+// device (set up on `s` at the first use on that device).
+int noalloc_status_word(int32_t** out, cudaStream_t s);
 cudaError_t launch_bounded_wait(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace sws

@@ -202,3 +202,38 @@ def test_options_reject_unknown_values(swslib):
         assert ei.value.code == S.E_INVALID
     S.set_option(S.OPT_GATHER_ENGINE, S.GATHER_TMA)
     S.set_option(S.OPT_PREFILL_KERNEL, S.PREFILL_AUTO)
+
+
+def test_linear_noalloc_refuses_bad_sizes_before_any_device_call(swslib):
+    # Limits of the fixed scratch and the argument checks run on the host
+    # before the device is touched, so they are checkable without a GPU
+    # (the pointers below are never dereferenced).
+    import ctypes as C
+    S = swslib
+    L = S.lib()
+
+    def call(rows, cols, m, x=4096, w=4096, sc=8192, y=12288):
+        return L.sws_linear_noalloc(C.c_void_p(w), C.c_void_p(sc), rows, cols, C.c_void_p(x), m, C.c_void_p(y), None)
+
+    assert call(4096 * 512 + 1, 16, 16) == S.E_INVALID  # 4097 row blocks of 512 rows (m <= 16)
+    assert "exceeds the limit of 2097152 rows" in S.last_error()
+    assert call(4096 * 256 + 1, 16, 17) == S.E_INVALID  # 4097 row blocks of 256 rows (m > 16)
+    assert "exceeds the limit of 1048576 rows" in S.last_error()
+    assert call(256, 16, 65) == S.E_INVALID and "m=65" in S.last_error()
+    assert call(256, 16, -1) == S.E_INVALID
+    assert call(-1, 16, 4) == S.E_INVALID
+    assert call(256, 24, 4) == S.E_UNSUPPORTED  # cols % 16 != 0
+    assert call(256, 16, 4, x=4097) == S.E_ALIGN
+    assert call(256, 16, 4, w=4104) == S.E_ALIGN
+    assert call(256, 16, 4, x=0) == S.E_INVALID
+    assert call(0, 16, 4) == S.OK and call(256, 16, 0) == S.OK  # nothing to do
+
+
+def test_host_wait_option_range(swslib):
+    S = swslib
+    for bad in (0, -5, 3_600_001):
+        with pytest.raises(S.SwsError) as ei:
+            S.set_option(S.OPT_HOST_WAIT_MS, bad)
+        assert ei.value.code == S.E_INVALID
+    S.set_option(S.OPT_HOST_WAIT_MS, 10000)
+    assert S.lib().sws_noalloc_status(0, None) == S.E_INVALID

@@ -274,6 +274,40 @@ def test_a_wait_that_runs_out_reports_timeout_and_the_context_stays_usable(S, st
     assert st.ctx.status() == 0
 
 
+def test_host_waits_give_up_at_their_deadline(S, stack):
+    # A kernel that stands for 100 ms (the bounded wait, on a barrier nothing
+    # arrives at) is queued ahead of the work a host wait needs. With a 10 ms
+    # host limit, sws_run_timing and sws_ctx_status return SWS_E_TIMEOUT saying
+    # that the host wait ran out; once the kernel has returned both succeed and
+    # the run's outputs match the oracle.
+    st, layers = stack
+    assert st.ctx.status(clear=True) == 0
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    m = 4
+    xs, ys, io = _io(st, 1, 2, m)
+    try:
+        S.set_option(S.OPT_HOST_WAIT_MS, 10)
+        st.ctx.test_bounded_wait(100_000_000, main.cuda_stream)
+        st.ctx.run_layers(1, 2, io, S.RUN_TIMING, main.cuda_stream, side.cuda_stream)
+        with pytest.raises(S.SwsError) as ei:
+            st.ctx.run_timing(2)
+        assert ei.value.code == S.E_TIMEOUT and "host wait" in str(ei.value)
+        with pytest.raises(S.SwsError) as ei:
+            st.ctx.status()
+        assert ei.value.code == S.E_TIMEOUT and "host wait" in str(ei.value)
+    finally:
+        S.set_option(S.OPT_HOST_WAIT_MS, 10000)
+    exposed, layer_ms = st.ctx.run_timing(2)
+    assert all(t > 0 for t in layer_ms) and exposed[0] >= 0
+    assert st.ctx.status(clear=True) == S.E_TIMEOUT  # the bounded wait's own record
+    assert st.ctx.status() == 0
+    main.synchronize()
+    for l in (1, 2):
+        for j in st.layer_entries(l):
+            want = O.linear(WL.bf16_to_f64(WL.bf16_bits(xs[j].cpu())), layers[l].codes[j], layers[l].scales[j])
+            assert_close(bf16_tensor_to_f64(ys[j]), want, f"layer {l} entry {j}")
+
+
 def test_prefill_layers_record_into_a_cuda_graph(S):
     # m > 64: each layer's linears quantise their activations on the
     # context's own stream, forked from and joined into `main`; that fork and
