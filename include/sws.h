@@ -64,6 +64,16 @@ extern "C" {
 #define SWS_SRC_SLOT1 1 /* view of slot 1 (must hold the entry's layer) */
 #define SWS_SRC_FUSED 2 /* read the layer's chunks directly through the chunk map */
 
+/* ---- plan flags -------------------------------------------------------- */
+/* Block scales inside T: each sharded E4M3 entry's fp32 block-scale tensor
+ * [ceil(rows/128), ceil(cols/128)] becomes an entry of T of its own, right
+ * after the weight (16-byte padded like every entry), so the gather restores
+ * the scales with the weights and the linears read them from the slot (or
+ * through the chunk map). Off by default: the blog keeps scales replicated,
+ * outside the flat layout (section "加载：行 shard 先行，finalize 再重排", the
+ * quantisation variants). */
+#define SWS_SCALES_IN_T 1u
+
 /* ---- run_layers flags -------------------------------------------------- */
 #define SWS_RUN_FUSED 1u  /* no gather: every linear reads the chunks directly */
 #define SWS_RUN_TIMING 2u /* record per-layer CUDA events (see sws_run_timing) */
@@ -100,7 +110,9 @@ typedef struct sws_layer_io {
  * multiples of 16 (every entry's byte size is rounded up to 16), |T| is
  * rounded up to a multiple of 16*N, and C = |T|/N. An entry is sharded iff
  * rows % N == 0; otherwise it is replicated and the call returns
- * SWS_W_SKIPPED. n_shards in [1, 256]; rows, cols >= 0; flags must be 0.
+ * SWS_W_SKIPPED. n_shards in [1, 256]; rows, cols >= 0; flags 0 or
+ * SWS_SCALES_IN_T (then each sharded E4M3 entry is followed in T by its
+ * block-scale tensor, 16-byte padded; sws_plan_scales gives where).
  * On success *out receives a plan owned by the caller (sws_plan_destroy). */
 int sws_plan_create(const sws_entry* entries, int32_t n_entries, int32_t n_shards, uint32_t flags,
                     sws_plan** out);
@@ -113,6 +125,11 @@ int sws_plan_layer(const sws_plan* plan, int32_t layer, int64_t* total_bytes, in
 /* Offset o_j of entry j inside its layer's T (-1 if replicated), its size in
  * bytes and whether it is sharded. */
 int sws_plan_entry(const sws_plan* plan, int32_t j, int64_t* offset, int64_t* nbytes, int32_t* sharded);
+/* With SWS_SCALES_IN_T: offset inside its layer's T of entry j's block-scale
+ * tensor (float32 [ceil(rows/128), ceil(cols/128)] row-major, 16-byte
+ * aligned) and its size in bytes; offset -1 and size 0 when the entry's
+ * scales are not in T (flag off, not E4M3, or a replicated entry). */
+int sws_plan_scales(const sws_plan* plan, int32_t j, int64_t* offset, int64_t* nbytes);
 /* max over layers of |T| - the size each of the two slots needs. */
 int64_t sws_plan_slot_bytes(const sws_plan* plan);
 void sws_plan_destroy(sws_plan* plan);
@@ -131,13 +148,27 @@ void sws_plan_destroy(sws_plan* plan);
 int sws_relayout(const sws_plan* plan, int32_t layer, const void* const* row_shards, void* const* chunks,
                  sws_stream_t stream);
 
+/* With SWS_SCALES_IN_T: fills the scale regions of a layer's chunks. Block
+ * FP8 keeps its scales at full shape on every rank (the blog's block-FP8
+ * variant slices at finalize, from the full tensor), so each chunk i receives
+ * the bytes of each scale tensor that fall into its window [i*C, (i+1)*C).
+ *   scales: host array [n entries of the layer, declaration order] of device
+ *           pointers to the full float32 scale tensors; NULL where the entry's
+ *           scales are not in T. Any 4-byte alignment.
+ *   chunks: as for sws_relayout.
+ * sws_relayout writes the scale regions as zeros, so call this after it, on
+ * the same stream. A no-op for plans without the flag. */
+int sws_relayout_scales(const sws_plan* plan, int32_t layer, const float* const* scales, void* const* chunks,
+                        sws_stream_t stream);
+
 /* ---- context: resident chunks, two slots, scales, workspace ------------- */
 
 /* Bytes of workspace a context needs for linears with up to max_m rows of
  * activations (split-K partial sums, counters, the tcgen05 decode path's
- * activation split blocks, two buffers of prefill activations - the
- * quantiser's output for E4M3 entries, x rounded to f16 for F16 entries - and
- * the device status word). */
+ * activation split blocks, with SWS_SCALES_IN_T a staging area for one
+ * layer's scales read through the chunk map, two buffers of prefill
+ * activations - the quantiser's output for E4M3 entries, x rounded to f16 for
+ * F16 entries - and the device status word). */
 int64_t sws_workspace_bytes(const sws_plan* plan, int64_t max_m);
 
 /* Creates a context over caller-owned device memory:
@@ -147,7 +178,10 @@ int64_t sws_workspace_bytes(const sws_plan* plan, int64_t max_m);
  *   slot0/1:    two device buffers of at least sws_plan_slot_bytes() bytes.
  *   scales:     host array [n_entries] of device pointers to float32 block
  *               scales [ceil(rows/128), ceil(cols/128)] row-major for E4M3
- *               entries (NULL for other types).
+ *               entries (NULL for other types). With SWS_SCALES_IN_T the
+ *               linears of sharded E4M3 entries read their scales from T
+ *               (slot + scale offset, or the chunks), and their pointers here
+ *               may be NULL; replicated E4M3 entries still need theirs.
  *   replicated: host array [n_entries] of device pointers to the full weight
  *               of each replicated entry (NULL for sharded ones); may be NULL
  *               when every entry is sharded.
@@ -193,8 +227,11 @@ int sws_gather_to_slot(sws_ctx* ctx, int32_t layer, int32_t slot, sws_stream_t s
  * bf16 GEMM on x directly; F16 rounds x to f16 into the workspace and runs
  * the same GEMM on f16 operands. Requires E4M3, BF16 or F16 weights (else
  * SWS_E_UNSUPPORTED), cols % 16 == 0, and, for E4M3 with m > 64,
- * cols % 128 == 0; E4M3 entries need their scales. Linears that share a
- * context must not overlap on the GPU (they share the workspace). */
+ * cols % 128 == 0; E4M3 entries need their scales. With SWS_SCALES_IN_T a
+ * sharded E4M3 entry's scales come from T: from the same slot as the weight,
+ * or - on the chunk-map source - copied from the chunks into the workspace by
+ * a small copy kernel queued before the linear's kernels. Linears that share
+ * a context must not overlap on the GPU (they share the workspace). */
 int sws_linear(sws_ctx* ctx, int32_t entry, int32_t src, const void* x, int64_t m, void* y,
                sws_stream_t stream);
 

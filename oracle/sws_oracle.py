@@ -103,6 +103,9 @@ class LayerLayout:
     sizes: Dict[int, int]       # entry -> s_j (bytes)
     total: int                  # |T|
     chunk: int                  # C = |T| / N
+    # scales inside T (optional layout): entry -> offset / bytes of its block-scale tensor
+    scale_offsets: Dict[int, int] = dataclasses.field(default_factory=dict)
+    scale_sizes: Dict[int, int] = dataclasses.field(default_factory=dict)
 
 
 @dataclasses.dataclass
@@ -120,23 +123,36 @@ class Plan:
         return max([ly.total for ly in self.layers.values()], default=0)
 
 
-def plan_layout(entries: Sequence[Tuple[int, int, int, int]], n_shards: int) -> Plan:
-    """entries: (layer, rows, cols, elem_bytes) in declaration order.
+def scale_grid(rows: int, cols: int) -> Tuple[int, int]:
+    """Shape of a weight's block-scale tensor: one float32 per 128 x 128 block."""
+    return -(-rows // 128), -(-cols // 128)
+
+
+def plan_layout(entries: Sequence[Tuple], n_shards: int, scales_in_t: bool = False) -> Plan:
+    """entries: (layer, rows, cols, elem_bytes) or (layer, rows, cols,
+    elem_bytes, block_scaled) in declaration order.
 
     An entry is stored sharded when its rows divide by N; otherwise it stays
     replicated and is left out of T ([WS "只 shard 真正 replicated 的权重"]).
     The sharded entries of a layer are concatenated in declaration order, each
     padded to a 16-byte multiple, and T is padded to a multiple of 16*N; the
-    chunk size is C = |T| / N ([WS "flat layout" steps 1-2])."""
+    chunk size is C = |T| / N ([WS "flat layout" steps 1-2]).
+
+    scales_in_t (a layout the pages do not use - they keep scales replicated,
+    outside T): each sharded block-scaled entry is followed by its float32
+    block-scale tensor as an entry of its own, padded to 16 bytes like any
+    entry."""
     if n_shards < 1:
         raise ValueError("N must be >= 1")
     layer_of = [e[0] for e in entries]
     rows = [e[1] for e in entries]
     cols = [e[2] for e in entries]
     eb = [e[3] for e in entries]
+    scaled = [bool(e[4]) if len(e) > 4 else False for e in entries]
     sharded = [r % n_shards == 0 for r in rows]
     layers: Dict[int, LayerLayout] = {}
-    for j, (layer, r, c, b) in enumerate(entries):
+    for j, e in enumerate(entries):
+        layer, r, c, b = e[:4]
         ly = layers.setdefault(layer, LayerLayout(layer, [], {}, {}, 0, 0))
         if not sharded[j]:
             continue
@@ -145,21 +161,32 @@ def plan_layout(entries: Sequence[Tuple[int, int, int, int]], n_shards: int) -> 
         ly.sizes[j] = s
         ly.entries.append(j)
         ly.total += roundup(s, 16)  # each entry padded to 16 B
+        if scales_in_t and scaled[j]:
+            gr, gc = scale_grid(r, c)
+            ly.scale_offsets[j] = ly.total
+            ly.scale_sizes[j] = 4 * gr * gc
+            ly.total += roundup(4 * gr * gc, 16)
     for ly in layers.values():
         ly.total = roundup(ly.total, 16 * n_shards)  # total padded to 16*N
         ly.chunk = ly.total // n_shards
     return Plan(n_shards, rows, cols, eb, layer_of, sharded, layers)
 
 
-def pack(plan: Plan, layer: int, weight_bytes: Dict[int, np.ndarray]) -> np.ndarray:
+def pack(plan: Plan, layer: int, weight_bytes: Dict[int, np.ndarray],
+         scales: Dict[int, np.ndarray] | None = None) -> np.ndarray:
     """T: the layer's entries in order at their offsets, zero padding
-    ([WS "flat layout" step 1])."""
+    ([WS "flat layout" step 1]); with scales in T, each scale tensor's float32
+    bytes at its own offset."""
     ly = plan.layers[layer]
     t = np.zeros(ly.total, dtype=np.uint8)
     for j in ly.entries:
         b = np.ascontiguousarray(weight_bytes[j]).view(np.uint8).reshape(-1)
         assert b.size == ly.sizes[j]
         t[ly.offsets[j]:ly.offsets[j] + ly.sizes[j]] = b
+    for j, o in ly.scale_offsets.items():
+        b = np.ascontiguousarray(np.asarray(scales[j], dtype=np.float32)).view(np.uint8).reshape(-1)
+        assert b.size == ly.scale_sizes[j]
+        t[o:o + b.size] = b
     return t
 
 
@@ -183,23 +210,40 @@ def view(plan: Plan, layer: int, t: np.ndarray, j: int) -> np.ndarray:
     return t[o:o + s].reshape(plan.rows[j], plan.cols[j] * plan.elem_bytes[j])
 
 
-def relayout(plan: Plan, layer: int, shards: Dict[int, Sequence[np.ndarray]]) -> List[np.ndarray]:
+def scales_view(plan: Plan, layer: int, t: np.ndarray, j: int) -> np.ndarray:
+    """Entry j's block scales read from T (scales-in-T layout): the float32
+    tensor [ceil(rows/128), ceil(cols/128)] at its offset."""
+    ly = plan.layers[layer]
+    o, s = ly.scale_offsets[j], ly.scale_sizes[j]
+    return t[o:o + s].copy().view(np.float32).reshape(scale_grid(plan.rows[j], plan.cols[j]))
+
+
+def relayout(plan: Plan, layer: int, shards: Dict[int, Sequence[np.ndarray]],
+             scales: Dict[int, np.ndarray] | None = None) -> List[np.ndarray]:
     """Row shards -> flat chunks, as the finalize step does it: for each weight,
     a temporary AllGather of its N row shards restores the full weight, and each
     rank copies out the bytes that fall into its window [rank*C, (rank+1)*C) of T;
     everything else in the window stays zero
-    ([WS "加载：行 shard 先行，finalize 再重排" step 2])."""
+    ([WS "加载：行 shard 先行，finalize 再重排" step 2]). With scales in T, every
+    rank holds each full scale tensor (replicated, like the block-FP8 variant
+    that keeps full shapes until finalize) and copies out its window the same way."""
     ly = plan.layers[layer]
     n, c = plan.n_shards, ly.chunk
     chunks = [np.zeros(c, dtype=np.uint8) for _ in range(n)]
-    for j in ly.entries:
-        full = gather([np.ascontiguousarray(x).view(np.uint8).reshape(-1) for x in shards[j]])
-        lo, hi = ly.offsets[j], ly.offsets[j] + ly.sizes[j]
+
+    def copy_window(full, lo, hi):
         for rank in range(n):
             w_lo, w_hi = rank * c, (rank + 1) * c
             a, b = max(lo, w_lo), min(hi, w_hi)
             if a < b:
                 chunks[rank][a - w_lo:b - w_lo] = full[a - lo:b - lo]
+
+    for j in ly.entries:
+        full = gather([np.ascontiguousarray(x).view(np.uint8).reshape(-1) for x in shards[j]])
+        copy_window(full, ly.offsets[j], ly.offsets[j] + ly.sizes[j])
+    for j, o in ly.scale_offsets.items():
+        full = np.ascontiguousarray(np.asarray(scales[j], dtype=np.float32)).view(np.uint8).reshape(-1)
+        copy_window(full, o, o + ly.scale_sizes[j])
     return chunks
 
 

@@ -16,6 +16,7 @@ E_INVALID, E_ALIGN, E_STATE, E_CUDA, E_TIMEOUT, E_UNSUPPORTED, E_WORKSPACE = -1,
 E4M3, BF16, F32, U8, F16 = 0, 1, 2, 3, 4
 SRC_SLOT0, SRC_SLOT1, SRC_FUSED = 0, 1, 2
 RUN_FUSED, RUN_TIMING, RUN_FIRST_PREFETCHED = 1, 2, 4
+SCALES_IN_T = 1  # plan flag
 OPT_DECODE_KERNEL = 1
 DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05 = 0, 1, 2
 OPT_PREFILL_KERNEL = 2
@@ -52,9 +53,12 @@ _PROTOS = [
                                  C.POINTER(C.c_int32)]),
     ("sws_plan_entry", C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                  C.POINTER(C.c_int32)]),
+    ("sws_plan_scales", C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     ("sws_plan_slot_bytes", C.c_int64, [C.c_void_p]),
     ("sws_plan_destroy", None, [C.c_void_p]),
     ("sws_relayout", C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.c_void_p]),
+    ("sws_relayout_scales", C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                                       C.c_void_p]),
     ("sws_workspace_bytes", C.c_int64, [C.c_void_p, C.c_int64]),
     ("sws_ctx_create", C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.c_void_p, C.c_void_p, C.POINTER(C.c_void_p),
                                  C.POINTER(C.c_void_p), C.c_void_p, C.c_int64, C.POINTER(C.c_void_p)]),
@@ -156,6 +160,12 @@ class Plan:
         check(lib().sws_plan_entry(self.handle, j, C.byref(o), C.byref(nb), C.byref(sh)), "plan_entry")
         return o.value, nb.value, bool(sh.value)
 
+    def scales(self, j: int):
+        """(offset in T, bytes) of entry j's block scales, (-1, 0) when not in T."""
+        o, nb = C.c_int64(), C.c_int64()
+        check(lib().sws_plan_scales(self.handle, j, C.byref(o), C.byref(nb)), "plan_scales")
+        return o.value, nb.value
+
     @property
     def slot_bytes(self) -> int:
         return lib().sws_plan_slot_bytes(self.handle)
@@ -168,6 +178,12 @@ def plan_create(entries, n_shards, flags=0) -> Plan:
 def relayout(plan: Plan, layer: int, row_shards: Sequence[int], chunks: Sequence[int], stream: int = 0):
     check(lib().sws_relayout(plan.handle, layer, _ptrs(row_shards), _ptrs(chunks), C.c_void_p(stream or None)),
           "relayout")
+
+
+def relayout_scales(plan: Plan, layer: int, scales: Sequence[int], chunks: Sequence[int], stream: int = 0):
+    """scales[k]: device pointer to the full block scales of the layer's k-th entry (0 if not in T)."""
+    check(lib().sws_relayout_scales(plan.handle, layer, _ptrs(scales), _ptrs(chunks), C.c_void_p(stream or None)),
+          "relayout_scales")
 
 
 def workspace_bytes(plan: Plan, max_m: int) -> int:

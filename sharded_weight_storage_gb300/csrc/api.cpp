@@ -86,6 +86,7 @@ struct sws_ctx {
   uint8_t* ws = nullptr;
   int64_t ws_bytes = 0;
   int64_t ws_decode = 0;  // bytes of the decode region at the start of ws
+  int64_t ws_scales = 0;  // SWS_SCALES_IN_T: the scale staging area (the workspace's last bytes)
   cudaEvent_t ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
   cudaEvent_t call_start = nullptr, join = nullptr;
   // timing of the last SWS_RUN_TIMING run
@@ -212,6 +213,36 @@ int weight_source(sws_ctx* c, int32_t j, int32_t src, const uint8_t** w, bool* f
   return SWS_OK;
 }
 
+// Where entry j's block scales live for source `src`: the caller's replicated
+// buffer, or - with SWS_SCALES_IN_T - T itself: the slot that holds the
+// weight, or the workspace copy staged from the chunks (stage_scales) for the
+// chunk-map source.
+const float* scale_source(sws_ctx* c, int32_t j, int32_t src) {
+  const EntryPlan& e = c->plan->entries[j];
+  if (e.scale_offset < 0) return c->scales[j];
+  if (src == SWS_SRC_FUSED) return reinterpret_cast<const float*>(c->ws + c->ws_scales + e.scale_stage);
+  return reinterpret_cast<const float*>(c->slot[src] + e.scale_offset);
+}
+
+// SWS_SCALES_IN_T, chunk-map source: copies the layer's scale regions from its
+// chunks into the workspace staging area, on `s` before the linears that read
+// them (T bytes [o, o + size) of each scale entry, cut at chunk boundaries).
+int stage_scales(sws_ctx* c, int32_t layer, cudaStream_t s) {
+  const sws_plan* p = c->plan;
+  const LayerPlan& lp = p->layers[layer];
+  if (lp.scale_stage_bytes == 0) return SWS_OK;
+  void* const* chunks = reinterpret_cast<void* const*>(&c->chunks[(size_t)layer * p->n_shards]);
+  std::vector<CopySeg> segs;
+  for (int32_t j : lp.sharded) {
+    const EntryPlan& e = p->entries[j];
+    if (e.scale_offset < 0 || e.scale_bytes == 0) continue;
+    chunk_segments(e.scale_offset, e.scale_offset + e.scale_bytes, lp.chunk, chunks, nullptr,
+                   c->ws + c->ws_scales + e.scale_stage, &segs);
+  }
+  const cudaError_t ce = launch_relayout(segs, s);
+  return ce == cudaSuccess ? SWS_OK : cuda_fail(ce, "linear: scale staging kernel");
+}
+
 int check_linear_args(sws_ctx* c, int32_t j, const void* x, int64_t m, void* y) {
   const sws_plan* p = c->plan;
   if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "linear: entry %d", j);
@@ -222,7 +253,8 @@ int check_linear_args(sws_ctx* c, int32_t j, const void* x, int64_t m, void* y) 
   if (m == 0 || e.rows == 0) return SWS_OK;
   if (!x || !y) return fail(SWS_E_INVALID, "linear: x or y is NULL");
   if (!aligned16(x) || !aligned16(y)) return fail(SWS_E_ALIGN, "linear: x or y is not 16-byte aligned");
-  if (e.dtype == SWS_E4M3 && !c->scales[j]) return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
+  if (e.dtype == SWS_E4M3 && !c->scales[j] && e.scale_offset < 0)
+    return fail(SWS_E_INVALID, "linear: entry %d has no scales", j);
   if (e.cols % 16 != 0) return fail(SWS_E_UNSUPPORTED, "linear: cols=%lld is not a multiple of 16", (long long)e.cols);
   return SWS_OK;
 }
@@ -269,11 +301,12 @@ PrefillBuf prefill_buf(sws_ctx* c, int b, int64_t per_buf, int64_t m, int64_t co
   return r;
 }
 
-int prefill_gemm(sws_ctx* c, int32_t j, const uint8_t* w, const PrefillBuf& q, int64_t m, void* y, cudaStream_t s) {
+int prefill_gemm(sws_ctx* c, int32_t j, int32_t src, const uint8_t* w, const PrefillBuf& q, int64_t m, void* y,
+                 cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
   PrefillLaunch pl;
   pl.w = w;
-  pl.scales = c->scales[j];
+  pl.scales = scale_source(c, j, src);
   pl.xq = q.xq;
   pl.ex = q.ex;
   pl.y = static_cast<uint16_t*>(y);
@@ -305,7 +338,8 @@ int prefill_linear_16(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, in
   return launch_prefill_16(pl, e.dtype == SWS_F16, s);
 }
 
-int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64_t m, void* y, cudaStream_t s) {
+int prefill_linear(sws_ctx* c, int32_t j, int32_t src, const uint8_t* w, const void* x, int64_t m, void* y,
+                   cudaStream_t s) {
   const EntryPlan& e = c->plan->entries[j];
   if (e.dtype == SWS_BF16) return prefill_linear_16(c, j, w, x, m, y, s);
   if (e.dtype == SWS_E4M3 && e.cols % 128 != 0)
@@ -322,7 +356,7 @@ int prefill_linear(sws_ctx* c, int32_t j, const uint8_t* w, const void* x, int64
   }
   int rc = launch_quantize_x(static_cast<const uint16_t*>(x), m, e.cols, q.xq, q.ex, s);
   if (rc != SWS_OK) return rc;
-  return prefill_gemm(c, j, w, q, m, y, s);
+  return prefill_gemm(c, j, src, w, q, m, y, s);
 }
 
 int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, void* y, cudaStream_t s);
@@ -385,7 +419,7 @@ int prefill_layer(sws_ctx* c, const LayerPlan& lp, int32_t src, const sws_layer_
     if ((ce = cudaEventRecord(c->q_done[b], c->qstream)) != cudaSuccess ||
         (ce = cudaStreamWaitEvent(s, c->q_done[b], 0)) != cudaSuccess)
       return cuda_fail(ce, "prefill layer: quantiser order");
-    rc = f16 ? prefill_linear_16(c, j, w, q.xq, m, io.y[k], s) : prefill_gemm(c, j, w, q, m, io.y[k], s);
+    rc = f16 ? prefill_linear_16(c, j, w, q.xq, m, io.y[k], s) : prefill_gemm(c, j, src, w, q, m, io.y[k], s);
     if (rc != SWS_OK) return rc;
     if ((ce = cudaEventRecord(c->g_done[b], s)) != cudaSuccess) return cuda_fail(ce, "prefill layer: record");
   }
@@ -403,13 +437,17 @@ int linear_impl(sws_ctx* c, int32_t j, int32_t src, const void* x, int64_t m, vo
   if (rc != SWS_OK) return rc;
   if (m > 64) {
     if (fused) return fail(SWS_E_UNSUPPORTED, "linear: the fused source is for decode (m <= 64)");
-    return prefill_linear(c, j, w, x, m, y, s);
+    return prefill_linear(c, j, src, w, x, m, y, s);
+  }
+  if (fused && e.scale_offset >= 0) {
+    rc = stage_scales(c, e.layer, s);
+    if (rc != SWS_OK) return rc;
   }
   DecodeGroup g;
   init_group(c, g, e.layer, m, fused);
   g.wtype = weight_type(e.dtype);
-  g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), e.rows,
-                             e.cols, e.offset};
+  g.item[g.n++] = DecodeItem{w, scale_source(c, j, src), static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y),
+                             e.rows, e.cols, e.offset};
   return launch_group(c, g, e.layer, j, s);
 }
 
@@ -422,6 +460,10 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
   if (!io.x || !io.y) return fail(SWS_E_INVALID, "run_layers: io of layer %d has NULL arrays", layer);
   const int64_t m = io.m;
   if (m > 64) return prefill_layer(c, lp, src, io, s);
+  if (m > 0 && src == SWS_SRC_FUSED) {  // scales in T read through the chunk map: staged once for the layer
+    int rc = stage_scales(c, layer, s);
+    if (rc != SWS_OK) return rc;
+  }
   constexpr int kGroups = 6;  // index: fused * 3 + weight type
   DecodeGroup grp[kGroups];
   int32_t first[kGroups] = {-1, -1, -1, -1, -1, -1};
@@ -446,8 +488,8 @@ int layer_linears(sws_ctx* c, int32_t layer, int32_t src, const sws_layer_io& io
       if (rc != SWS_OK) return rc;
     }
     if (g.n == 0) first[q] = j;
-    g.item[g.n++] = DecodeItem{w, c->scales[j], static_cast<const uint16_t*>(io.x[k]), static_cast<uint16_t*>(io.y[k]),
-                               e.rows, e.cols, e.offset};
+    g.item[g.n++] = DecodeItem{w, scale_source(c, j, src), static_cast<const uint16_t*>(io.x[k]),
+                               static_cast<uint16_t*>(io.y[k]), e.rows, e.cols, e.offset};
   }
   for (int q = 0; q < kGroups; ++q) {
     int rc = launch_group(c, grp[q], layer, first[q], s);
@@ -468,6 +510,13 @@ int64_t split_region_bytes(const sws_plan* p, int64_t m) {
   return decode_split_bytes(m, most);
 }
 
+// SWS_SCALES_IN_T: staging area for the chunk-map source, the largest layer's.
+int64_t scale_stage_region_bytes(const sws_plan* p) {
+  int64_t most = 0;
+  for (const LayerPlan& l : p->layers) most = std::max(most, l.scale_stage_bytes);
+  return roundup(most, 256);
+}
+
 }  // namespace
 
 extern "C" {
@@ -480,7 +529,9 @@ int64_t sws_workspace_bytes(const sws_plan* p, int64_t max_m) {
   int64_t pre = 0;
   for (const EntryPlan& e : p->entries)
     pre = std::max(pre, prefill_bytes(e.dtype, max_m, e.cols));
-  return dec + split_region_bytes(p, mm) + 2 * pre;  // two buffers: quantiser k + 1 beside GEMM k
+  // two prefill buffers: quantiser k + 1 beside GEMM k; the scale staging
+  // area (chunk-map decode only, never in use beside a prefill linear) last
+  return dec + split_region_bytes(p, mm) + 2 * pre + scale_stage_region_bytes(p);
 }
 
 int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void* slot1, const float* const* scales,
@@ -502,7 +553,7 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
   if (!aligned16(slot0) || !aligned16(slot1)) return fail(SWS_E_ALIGN, "ctx_create: slot not 16-byte aligned");
   if (E > 0 && !scales) return fail(SWS_E_INVALID, "ctx_create: scales is NULL");
   for (int32_t j = 0; j < E; ++j) {
-    if (plan->entries[j].dtype == SWS_E4M3 && !scales[j])
+    if (plan->entries[j].dtype == SWS_E4M3 && !scales[j] && plan->entries[j].scale_offset < 0)
       return fail(SWS_E_INVALID, "ctx_create: E4M3 entry %d has no scales", j);
     if (scales[j] && !aligned16(scales[j])) return fail(SWS_E_ALIGN, "ctx_create: scales of entry %d unaligned", j);
     if (!plan->entries[j].sharded) {
@@ -533,7 +584,10 @@ int sws_ctx_create(const sws_plan* plan, void* const* chunks, void* slot0, void*
   c->ws_bytes = workspace_bytes;
   int64_t dec64 = 0;
   decode_workspace_bytes(64, &dec64);
-  c->ws_decode = std::min(dec64 + split_region_bytes(plan, 64), workspace_bytes);
+  // The scale staging area (SWS_SCALES_IN_T) is the workspace's last bytes:
+  // decode launches for every m the workspace was sized for end before it.
+  c->ws_scales = (workspace_bytes - scale_stage_region_bytes(plan)) & ~int64_t(15);
+  c->ws_decode = std::min(dec64 + split_region_bytes(plan, 64), c->ws_scales);
   // Only the status word and the split-K arrival counters must start at zero.
   cudaError_t e = cudaMemset(workspace, 0, (size_t)(kCtlBytes + kMaxCounters * 4));
   if (e != cudaSuccess) {

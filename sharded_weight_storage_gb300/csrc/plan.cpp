@@ -50,6 +50,25 @@ int elem_bytes(int32_t dtype) {
 
 using namespace sws;
 
+namespace sws {
+void chunk_segments(int64_t g0, int64_t g1, int64_t c, void* const* chunks, const uint8_t* lin_src, uint8_t* lin_dst,
+                    std::vector<CopySeg>* segs) {
+  while (g0 < g1) {
+    const int64_t ci = g0 / c, in_chunk = g0 - ci * c;
+    const int64_t len = std::min(g1 - g0, c - in_chunk);
+    uint8_t* ch = static_cast<uint8_t*>(chunks[ci]) + in_chunk;
+    if (lin_dst) {
+      segs->push_back(CopySeg{ch, lin_dst, len});
+      lin_dst += len;
+    } else {
+      segs->push_back(CopySeg{lin_src, ch, len});
+      if (lin_src) lin_src += len;
+    }
+    g0 += len;
+  }
+}
+}  // namespace sws
+
 extern "C" {
 
 const char* sws_last_error(void) { return g_last_error.c_str(); }
@@ -62,7 +81,7 @@ int sws_plan_create(const sws_entry* entries, int32_t n_entries, int32_t n_shard
   *out = nullptr;
   if (n_entries < 0 || (n_entries > 0 && !entries)) return fail(SWS_E_INVALID, "plan_create: bad entry list");
   if (n_shards < 1 || n_shards > 256) return fail(SWS_E_INVALID, "plan_create: N=%d outside [1, 256]", n_shards);
-  if (flags != 0) return fail(SWS_E_INVALID, "plan_create: unknown flags 0x%x", flags);
+  if (flags & ~SWS_SCALES_IN_T) return fail(SWS_E_INVALID, "plan_create: unknown flags 0x%x", flags);
   sws_plan* p = new (std::nothrow) sws_plan();
   if (!p) return fail(SWS_E_INVALID, "plan_create: out of host memory");
   p->n_shards = n_shards;
@@ -102,6 +121,14 @@ int sws_plan_create(const sws_entry* entries, int32_t n_entries, int32_t n_shard
     ep.offset = lp.total;           // o_j
     lp.total += roundup(ep.bytes, 16);  // each entry padded to 16 B
     lp.sharded.push_back(j);
+    if ((flags & SWS_SCALES_IN_T) && e.dtype == SWS_E4M3) {
+      // the weight's block scales follow it as their own entry, padded to 16 B
+      ep.scale_bytes = cdiv(e.rows, 128) * cdiv(e.cols, 128) * 4;
+      ep.scale_offset = lp.total;
+      lp.total += roundup(ep.scale_bytes, 16);
+      ep.scale_stage = lp.scale_stage_bytes;
+      lp.scale_stage_bytes += roundup(ep.scale_bytes, 16);
+    }
   }
   for (LayerPlan& lp : p->layers) {
     lp.total = roundup(lp.total, 16 * (int64_t)n_shards);  // total padded to 16*N
@@ -144,6 +171,15 @@ int sws_plan_entry(const sws_plan* p, int32_t j, int64_t* offset, int64_t* nbyte
   return SWS_OK;
 }
 
+int sws_plan_scales(const sws_plan* p, int32_t j, int64_t* offset, int64_t* nbytes) {
+  if (!p) return fail(SWS_E_INVALID, "plan_scales: plan is NULL");
+  if (j < 0 || j >= (int32_t)p->entries.size()) return fail(SWS_E_INVALID, "plan_scales: entry %d", j);
+  const EntryPlan& e = p->entries[j];
+  if (offset) *offset = e.scale_offset;
+  if (nbytes) *nbytes = e.scale_offset >= 0 ? e.scale_bytes : 0;
+  return SWS_OK;
+}
+
 int64_t sws_plan_slot_bytes(const sws_plan* p) { return p ? p->slot_bytes : -1; }
 
 void sws_plan_destroy(sws_plan* p) { delete p; }
@@ -166,17 +202,12 @@ int sws_relayout(const sws_plan* p, int32_t layer, const void* const* row_shards
       if (p->entries[lp.sharded[k]].bytes > 0 && !row_shards[k * n + r])
         return fail(SWS_E_INVALID, "relayout: row shard %d of sharded entry %zu is NULL", r, k);
   // Walk T once, cutting it into maximal runs that stay inside one chunk and
-  // one source (a row shard, or padding).
+  // one source (a row shard, or padding; with SWS_SCALES_IN_T the scale
+  // regions are written as zeros here and filled by sws_relayout_scales).
   std::vector<CopySeg> segs;
   const int64_t c = lp.chunk;
   auto emit = [&](int64_t g0, int64_t g1, const uint8_t* src) {  // T bytes [g0, g1)
-    while (g0 < g1) {
-      int64_t ci = g0 / c, in_chunk = g0 - ci * c;
-      int64_t len = std::min(g1 - g0, c - in_chunk);
-      segs.push_back(CopySeg{src, static_cast<uint8_t*>(chunks[ci]) + in_chunk, len});
-      if (src) src += len;
-      g0 += len;
-    }
+    chunk_segments(g0, g1, c, chunks, src, nullptr, &segs);
   };
   int64_t g = 0;
   for (size_t k = 0; k < lp.sharded.size(); ++k) {
@@ -194,6 +225,33 @@ int sws_relayout(const sws_plan* p, int32_t layer, const void* const* row_shards
   cudaError_t e = launch_relayout(segs, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "relayout kernel launch");
   return SWS_OK;
+}
+
+
+int sws_relayout_scales(const sws_plan* p, int32_t layer, const float* const* scales, void* const* chunks,
+                        sws_stream_t stream) {
+  if (!p) return fail(SWS_E_INVALID, "relayout_scales: plan is NULL");
+  if (layer < 0 || layer >= (int32_t)p->layers.size()) return fail(SWS_E_INVALID, "relayout_scales: layer %d", layer);
+  const LayerPlan& lp = p->layers[layer];
+  if (!(p->flags & SWS_SCALES_IN_T) || lp.total == 0) return SWS_OK;
+  if (!chunks || !scales) return fail(SWS_E_INVALID, "relayout_scales: chunks or scales is NULL");
+  for (int32_t i = 0; i < p->n_shards; ++i) {
+    if (!chunks[i]) return fail(SWS_E_INVALID, "relayout_scales: chunk %d is NULL", i);
+    if (!aligned16(chunks[i])) return fail(SWS_E_ALIGN, "relayout_scales: chunk %d is not 16-byte aligned", i);
+  }
+  // Each rank holds the full (replicated) scale tensor and copies out the
+  // bytes that fall into its window [i*C, (i+1)*C) of T.
+  std::vector<CopySeg> segs;
+  for (size_t k = 0; k < lp.all.size(); ++k) {
+    const EntryPlan& e = p->entries[lp.all[k]];
+    if (e.scale_offset < 0 || e.scale_bytes == 0) continue;
+    if (!scales[k]) return fail(SWS_E_INVALID, "relayout_scales: entry %zu of layer %d has no scales", k, layer);
+    chunk_segments(e.scale_offset, e.scale_offset + e.scale_bytes, lp.chunk, chunks,
+                   reinterpret_cast<const uint8_t*>(scales[k]), nullptr, &segs);
+  }
+  if (segs.empty()) return SWS_OK;
+  cudaError_t e = launch_relayout(segs, (cudaStream_t)stream);
+  return e == cudaSuccess ? SWS_OK : cuda_fail(e, "relayout_scales kernel launch");
 }
 
 }  // extern "C"

@@ -38,12 +38,18 @@ struct EntryPlan {
   bool sharded = false;
   int64_t offset = -1;       // o_j inside the layer's T, -1 if replicated
   int32_t index_in_layer = 0; // position among all entries of the layer
+  // SWS_SCALES_IN_T: the entry's fp32 block scales [ceil(rows/128),
+  // ceil(cols/128)] as their own entry of T right after the weight (-1 when
+  // the scales are not in T), their size, and where the chunk-map path stages
+  // them in the workspace (offset inside the layer's staging area).
+  int64_t scale_offset = -1, scale_bytes = 0, scale_stage = 0;
 };
 
 struct LayerPlan {
   std::vector<int32_t> sharded;  // entry ids packed into T, in order
   std::vector<int32_t> all;      // every entry id of the layer, in order
   int64_t total = 0, chunk = 0;
+  int64_t scale_stage_bytes = 0;  // SWS_SCALES_IN_T: staging area of the layer's scales (chunk-map path)
 };
 
 // ---- device status word and trace records (inside the workspace) -----------
@@ -146,6 +152,12 @@ struct CopySeg {
   int64_t len;
 };
 cudaError_t launch_relayout(const std::vector<CopySeg>& segs, cudaStream_t s);
+// Appends the copy segments that move T bytes [g0, g1) of a layer with chunk
+// size c between the chunks and a linear buffer `lin` (lin holds byte g0 at
+// its start): to_chunks copies lin -> chunks, else chunks -> lin; lin ==
+// nullptr with to_chunks fills the chunk bytes with zeros.
+void chunk_segments(int64_t g0, int64_t g1, int64_t c, void* const* chunks, const uint8_t* lin_src, uint8_t* lin_dst,
+                    std::vector<CopySeg>* segs);
 
 // Decode linears (m <= 64): a group of up to kMaxDecodeGroup linears that
 // share m runs as one launch. Slot path: each item's weight is a view `w`

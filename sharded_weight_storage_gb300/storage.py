@@ -19,13 +19,18 @@ class ShardedStack:
     """Resident storage for a plan: chunk (l, i) is its own device buffer,
     standing in for rank i's shard of layer l."""
 
-    def __init__(self, entries: Sequence[tuple], n_shards: int, max_m: int = 64, device: str = "cuda"):
-        self.plan = L.Plan(entries, n_shards)
+    def __init__(self, entries: Sequence[tuple], n_shards: int, max_m: int = 64, device: str = "cuda",
+                 flags: int = 0):
+        """flags: plan flags (L.SCALES_IN_T puts each sharded E4M3 entry's
+        block scales into T right after the weight)."""
+        self.plan = L.Plan(entries, n_shards, flags)
+        self.flags = flags
         self.entries = list(entries)
         self.n_layers, self.n_shards, self.n_entries = self.plan.info()
         self.device = torch.device(device)
         self.layout = [self.plan.layer(l) for l in range(self.n_layers)]
         self.entry_info = [self.plan.entry(j) for j in range(self.n_entries)]
+        self.scale_info = [self.plan.scales(j) for j in range(self.n_entries)]  # (offset in T or -1, bytes)
         self.chunks: List[List[Optional[torch.Tensor]]] = []
         for total, chunk, _ in self.layout:
             self.chunks.append([torch.empty(chunk, dtype=torch.uint8, device=self.device) if total else None
@@ -74,7 +79,12 @@ class ShardedStack:
             shard_ptrs += [p.data_ptr() for p in parts]
         if self.layout[layer][0] == 0:
             return
-        L.relayout(self.plan, layer, shard_ptrs, [c.data_ptr() for c in self.chunks[layer]], _stream_ptr(stream))
+        chunk_ptrs = [c.data_ptr() for c in self.chunks[layer]]
+        L.relayout(self.plan, layer, shard_ptrs, chunk_ptrs, _stream_ptr(stream))
+        if any(self.scale_info[j][0] >= 0 for j in self.layer_entries(layer)):
+            # scales in T: each chunk takes its window of the full scale tensors
+            L.relayout_scales(self.plan, layer, [self.scales[j].data_ptr() if self.scale_info[j][0] >= 0 else 0
+                                                 for j in self.layer_entries(layer)], chunk_ptrs, _stream_ptr(stream))
         (stream or torch.cuda.current_stream()).synchronize()
         del keep
 
@@ -89,6 +99,12 @@ class ShardedStack:
     # -- accounting -------------------------------------------------------------
     def resident_chunk_bytes(self) -> int:
         return sum(c.numel() for row in self.chunks for c in row if c is not None)
+
+    def slot_scales(self, slot: int, j: int) -> torch.Tensor:
+        """Entry j's block scales inside a slot (scales-in-T layout)."""
+        off, nbytes = self.scale_info[j]
+        _, _, rows, cols = self.entries[j]
+        return self.slots[slot][off:off + nbytes].view(torch.float32).view(-(-rows // 128), -(-cols // 128))
 
     def slot_view(self, slot: int, j: int) -> torch.Tensor:
         off, nbytes, sharded = self.entry_info[j]

@@ -77,6 +77,77 @@ def test_planner_matches_hand_derived_padded_layouts(swslib):
         _compare_plan(S, [(0, r, c, e) for (_, r, c, e, _) in ents], n)
 
 
+def test_planner_with_scales_in_t_matches_hand_derived_layouts(swslib):
+    # tests/golden/layout_scales_in_t.txt: every sharded E4M3 entry followed by
+    # its block-scale tensor, 16-byte padded; replicated and non-E4M3 entries
+    # have none
+    from test_oracle_pins import read_scales_golden
+    S = swslib
+    for n, ents, total, chunk in read_scales_golden().values():
+        dts = [S.E4M3 if s else {1: S.U8, 2: S.BF16, 4: S.F32}[e] for (_, _, _, e, s, _, _) in ents]
+        import warnings
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            plan = S.Plan([(0, dt, r, c) for dt, (_, r, c, _, _, _, _) in zip(dts, ents)], n, S.SCALES_IN_T)
+        assert plan.layer(0) == (total, chunk, len(ents))
+        for j, (_, r, c, e, s, off, soff) in enumerate(ents):
+            assert plan.entry(j)[0] == off
+            assert plan.scales(j) == ((soff, 4 * (-(-r // 128)) * (-(-c // 128))) if soff >= 0 else (-1, 0))
+        plain = S.Plan([(0, dt, r, c) for dt, (_, r, c, _, _, _, _) in zip(dts, ents)], n) \
+            if all(r % n == 0 for (_, r, _, _, _, _, _) in ents) else None
+        if plain is not None:
+            assert all(plain.scales(j) == (-1, 0) for j in range(len(ents)))
+
+
+@pytest.mark.parametrize("n", [1, 3, 8, 16])
+def test_planner_with_scales_in_t_matches_oracle_random(swslib, n):
+    S = swslib
+    rng = np.random.default_rng(2000 + n)
+    import warnings
+    for _ in range(25):
+        ents = []
+        for _ in range(int(rng.integers(1, 9))):
+            rows = int(rng.integers(0, 6)) * n * 64 if rng.random() < 0.75 else int(rng.integers(1, 500))
+            dt = int(rng.choice([S.E4M3, S.E4M3, S.BF16, S.F32]))
+            ents.append((int(rng.integers(0, 3)), dt, rows, int(rng.integers(0, 700))))
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            plan = S.Plan(ents, n, S.SCALES_IN_T)
+        eb = {S.E4M3: 1, S.BF16: 2, S.F32: 4}
+        ref = O.plan_layout([(l, r, c, eb[dt], dt == S.E4M3) for (l, dt, r, c) in ents], n, scales_in_t=True)
+        for l in range(plan.info()[0]):
+            ly = ref.layers.get(l)
+            assert plan.layer(l)[:2] == ((ly.total, ly.chunk) if ly else (0, 0))
+        for j, (l, dt, r, c) in enumerate(ents):
+            ly = ref.layers[l]
+            assert plan.entry(j)[0] == ly.offsets.get(j, -1)
+            assert plan.scales(j) == (ly.scale_offsets.get(j, -1), ly.scale_sizes.get(j, 0))
+        assert plan.slot_bytes == ref.slot_bytes
+
+
+def test_relayout_scales_validates_before_any_launch(swslib):
+    S = swslib
+    plan = S.Plan([(0, S.E4M3, 8, 16)], 4, S.SCALES_IN_T)
+    assert plan.scales(0) == (128, 4)
+    assert plan.layer(0) == (192, 48, 1)
+    with pytest.raises(S.SwsError) as ei:
+        S.relayout_scales(plan, 0, [0], [16, 32, 48, 64])
+    assert ei.value.code == S.E_INVALID  # the entry's scales are missing
+    with pytest.raises(S.SwsError) as ei:
+        S.relayout_scales(plan, 0, [4096], [17, 32, 48, 64])
+    assert ei.value.code == S.E_ALIGN
+    S.relayout_scales(S.Plan([(0, S.E4M3, 8, 16)], 4), 0, [4096], [16, 32, 48, 64])  # no flag: nothing to do
+
+
+def test_workspace_grows_by_the_scale_staging_area(swslib):
+    S = swslib
+    ents = [(0, S.E4M3, 1024, 4096), (0, S.E4M3, 512, 1024), (1, S.E4M3, 256, 256)]
+    a = S.workspace_bytes(S.Plan(ents, 4), 64)
+    b = S.workspace_bytes(S.Plan(ents, 4, S.SCALES_IN_T), 64)
+    # the larger layer's scales, each padded to 16 B: 8*32*4 = 1024 and 4*8*4 = 128, rounded to 256
+    assert b - a == 1280
+
+
 def test_planner_matches_oracle_on_92_layer_stack(swslib):
     w = WL.STACK92
     _compare_plan(swslib, [(l, e.rows, e.cols, 1) for l in range(w.n_layers) for e in w.entries], w.n_shards)
@@ -107,7 +178,7 @@ def test_skipped_entries_warn_and_stay_out_of_T(swslib):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(n=0), dict(n=257), dict(rows=-1), dict(cols=-5), dict(dtype=9), dict(layer=-1), dict(flags=1),
+    dict(n=0), dict(n=257), dict(rows=-1), dict(cols=-5), dict(dtype=9), dict(layer=-1), dict(flags=2),
 ])
 def test_plan_create_rejects_bad_arguments(swslib, bad):
     S = swslib

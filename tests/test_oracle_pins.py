@@ -785,3 +785,109 @@ def test_dequant_at_and_linear_rows_select_from_the_definition():
     onehot = np.zeros((1, cols))
     onehot[0, 130] = 1.0
     assert np.array_equal(O.linear_rows(onehot, q, sc, rsel)[0], O.dequant_at(q, sc, rsel, [130])[:, 0])
+
+
+# ---------------------------------------------------------------------------
+# block scales inside T (optional layout), hand-typed golden
+# ---------------------------------------------------------------------------
+
+
+def read_scales_golden():
+    """Cases of tests/golden/layout_scales_in_t.txt: name -> (N, [(entry name,
+    rows, cols, elem, block_scaled, offset, scale offset)], |T|, C)."""
+    cases = {}
+    with open(os.path.join(GOLDEN, "layout_scales_in_t.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, ents, total, chunk = [p.strip() for p in line.split("|")]
+            name, n = head.split()
+            rows = []
+            for tok in ents.split():
+                nm, rest = tok.split(":")
+                shape, offs = rest.split("=")
+                r, c, e, s = (int(v) for v in shape.split(","))
+                o, so = (int(v) for v in offs.split("/"))
+                rows.append((nm, r, c, e, bool(s), o, so))
+            cases[name] = (int(n), rows, int(total), int(chunk))
+    return cases
+
+
+def _scales_layout_matches_golden(plan_fn) -> bool:
+    for n, ents, total, chunk in read_scales_golden().values():
+        p = plan_fn([(0, r, c, e, s) for (_, r, c, e, s, _, _) in ents], n)
+        ly = p.layers[0]
+        if (ly.total, ly.chunk) != (total, chunk):
+            return False
+        for j, (_, r, c, _, _, off, soff) in enumerate(ents):
+            if ly.offsets.get(j, -1) != off or ly.scale_offsets.get(j, -1) != soff:
+                return False
+            if soff >= 0 and ly.scale_sizes[j] != 4 * (-(-r // 128)) * (-(-c // 128)):
+                return False
+    return True
+
+
+def test_scales_in_t_layout_matches_hand_derived_golden():
+    assert _scales_layout_matches_golden(lambda e, n: O.plan_layout(e, n, scales_in_t=True))
+    # without the flag the same entries give the plain layout: no scale entries
+    n, ents, _, _ = read_scales_golden()["scales_tiny"]
+    assert O.plan_layout([(0, r, c, e, s) for (_, r, c, e, s, _, _) in ents], n).layers[0].total == 360448
+
+
+def _mutant_scales_plan(kind):
+    """plan_layout with the scales placed by a planted wrong rule."""
+    def plan(entries, n):
+        p = O.plan_layout(entries, n, scales_in_t=True)
+        ly = p.layers[0]
+        off = 0
+        grids = {j: 4 * (-(-entries[j][1] // 128)) * (-(-entries[j][2] // 128)) for j in ly.scale_offsets}
+        tail = []
+        for j in ly.entries:
+            if kind == "before" and j in grids:  # scales ahead of their weight
+                ly.scale_offsets[j] = off
+                off += O.roundup(grids[j], 16)
+            ly.offsets[j] = off
+            off += O.roundup(ly.sizes[j], 16)
+            if kind in ("unpadded", "rule") and j in grids:
+                ly.scale_offsets[j] = off
+                off += grids[j] if kind == "unpadded" else O.roundup(grids[j], 16)
+            if kind == "at_end" and j in grids:
+                tail.append(j)
+        for j in tail:  # all scales after all weights
+            ly.scale_offsets[j] = off
+            off += O.roundup(grids[j], 16)
+        ly.total = O.roundup(off, 16 * n)
+        ly.chunk = ly.total // n
+        return p
+    return plan
+
+
+@pytest.mark.parametrize("kind", ["rule", "before", "unpadded", "at_end"])
+def test_scales_golden_catches_planted_placement_mistakes(kind):
+    assert _scales_layout_matches_golden(_mutant_scales_plan(kind)) == (kind == "rule")
+
+
+def test_scales_in_t_pack_view_and_relayout():
+    rng = np.random.default_rng(34)
+    for n, ents, total, chunk in read_scales_golden().values():
+        p = O.plan_layout([(0, r, c, e, s) for (_, r, c, e, s, _, _) in ents], n, scales_in_t=True)
+        ly = p.layers[0]
+        data = {j: rng.integers(1, 256, size=(ents[j][1], ents[j][2] * ents[j][3]), dtype=np.uint8)
+                for j in ly.entries}
+        scales = {j: (2.0 ** rng.uniform(-8, -4, size=O.scale_grid(ents[j][1], ents[j][2]))).astype(np.float32)
+                  for j in range(len(ents)) if ents[j][4]}
+        t = O.pack(p, 0, data, scales)
+        assert t.size == total
+        for j in ly.entries:
+            assert np.array_equal(O.view(p, 0, t, j), data[j])
+        for j in ly.scale_offsets:
+            assert np.array_equal(O.scales_view(p, 0, t, j), scales[j])
+            # the float32 bytes as they are in memory
+            o = ly.scale_offsets[j]
+            assert t[o:o + 4].tobytes() == scales[j].reshape(-1)[:1].tobytes()
+        ch = O.split_chunks(p, 0, t)
+        assert [c.size for c in ch] == [chunk] * n
+        shards = {j: WL.row_shards(data[j], n) for j in ly.entries}
+        got = O.relayout(p, 0, shards, scales)
+        assert all(np.array_equal(a, b) for a, b in zip(got, ch))
