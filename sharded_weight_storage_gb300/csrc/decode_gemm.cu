@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     settle_partials<NT, R, kRowsCta, kRowsWarp>(p, geo, unit_pos(p, u0).rbg, unit_pos(p, u1 - 1).rbg, warp, lane,
                                                 &s_last);
   if (FUSED) dev::cp_async_wait<0>();
-  if (tid == 0) {
+  if (p.trace && tid == 0) {  // the record's end stamp after this kernel's writes
     __threadfence();
     dev::trace_end(p.trace, p.tag);
   }

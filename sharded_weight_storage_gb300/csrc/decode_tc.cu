@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Cf::kTmemCols)
                  : "memory");
   }
-  if (tid == 0) {
+  if (p.trace && tid == 0) {  // the record's end stamp after this kernel's writes
     __threadfence();
     dev::trace_end(p.trace, p.tag);
   }
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__
     }
   }
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
+  if (p.trace && (threadIdx.x & 31) == 0) {  // the record's end stamp after this kernel's writes
     __threadfence();
     dev::trace_end(p.trace, p.tag);
   }
