@@ -357,6 +357,19 @@ def run_ours(args, dist):
             step(HEADLINE_M, kt)
     torch.cuda.synchronize()
     per_kernel = {k: statistics.mean(kt.ms(k)) for k in ("gather", "linears")}
+    # The same step on the chunk-map source: the linears read the chunks
+    # directly, no gather and no slot (back to back, no events inside).
+    with torch.cuda.stream(stream):
+        fused = lambda: ctx.layer_linears(0, S.SRC_FUSED, [x.data_ptr() for x in xs[HEADLINE_M]],
+                                          [y.data_ptr() for y in ys[HEADLINE_M]], HEADLINE_M, sp)
+        for _ in range(args.warmup):
+            fused()
+        f0 = tm.ev()
+        for _ in range(args.steps):
+            fused()
+        f1 = tm.ev()
+    torch.cuda.synchronize()
+    results["fused_step_ms"] = dist.max(f0.elapsed_time(f1)) / args.steps
     per_kernel_median = {k: statistics.median(kt.ms(k)) for k in ("gather", "linears")}
     results["headline"] = dict(window_ms=window_ms, step_bytes=step_bytes, per_kernel_ms=per_kernel,
                                per_kernel_median_ms=per_kernel_median, kernel_timing_steps=n_kt)
@@ -1293,6 +1306,11 @@ def main():
         "f16_weights": f16,
         "draft_prefetch": prefetch,
         "weight_GBps_step": total / ms_step / 1e6,
+        # the chunk-map step: the same linears reading the chunks (no gather, no slot)
+        "fused_step": {"ms_per_step": r["fused_step_ms"],
+                       "GBps": dist.world * (h["step_bytes"] - 2 * total) / r["fused_step_ms"] / 1e6,
+                       "weight_GBps": dist.world * total / r["fused_step_ms"] / 1e6,
+                       "frac_of_hbm": (h["step_bytes"] - 2 * total) / r["fused_step_ms"] / 1e6 / hbm},
     }
     if dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
