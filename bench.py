@@ -456,6 +456,23 @@ def run_ours(args, dist):
                 "fused_linears_us": fused_ms * 1e3, "fused_linears_GBps": lin_bytes / fused_ms / 1e6,
                 "per_entry_slot": per_entry,
             }
+        # the decode linear that allocates nothing (fixed scratch in the
+        # library, warp-level mma.sync kernel) on gate_up from slot 0, beside
+        # sws_linear of the same entry (default tcgen05 kernel)
+        off0, _, _ = st.entry_info[0]
+        rows0, cols0 = ents[0][1], ents[0][2]
+        noalloc = {}
+        for m in w.m_values:
+            def na(m=m):
+                S.linear_noalloc(st.slots[0].data_ptr() + off0, st.scales[0].data_ptr(), rows0, cols0,
+                                 xs[m][0].data_ptr(), m, ys[m][0].data_ptr(), sp)
+            na()
+            assert S.noalloc_status() == 0
+            na_ms = timed(na, reps)
+            nb = sum(layer_bytes([ents[0]], m))
+            noalloc[m] = {"us": na_ms * 1e3, "GBps": nb / na_ms / 1e6,
+                          "sws_linear_GBps": results["per_m"][m]["per_entry_slot"]["gate_up"]["GBps"]}
+        results["noalloc_gate_up"] = noalloc
     torch.cuda.synchronize()
 
     # ---- end to end through the C ABI with host buffers (M = 32) -----------
@@ -1305,6 +1322,7 @@ def main():
         "bf16_weights": bf16,
         "f16_weights": f16,
         "draft_prefetch": prefetch,
+        "noalloc_gate_up": r["noalloc_gate_up"],
         "weight_GBps_step": total / ms_step / 1e6,
         # the chunk-map step: the same linears reading the chunks (no gather, no slot)
         "fused_step": {"ms_per_step": r["fused_step_ms"],

@@ -176,6 +176,22 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Two fp32 lanes per instruction (packed .f32x2 arithmetic, each lane rounded
+// as the scalar instruction would): a += (s * e) * (h + l) for a pair of
+// columns, the same three roundings in the same order as the scalar form.
+__device__ __forceinline__ void promote2(float& a0, float& a1, uint64_t ss, float e0, float e1, uint32_t h0,
+                                         uint32_t h1, uint32_t l0, uint32_t l1) {
+  uint64_t acc, ee, hh, ll;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ee) : "f"(e0), "f"(e1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(hh) : "r"(h0), "r"(h1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ll) : "r"(l0), "r"(l1));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(ee) : "l"(ss));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(hh) : "l"(ll));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(ee), "l"(hh));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
 // Every lane waits; the warp fails if any lane ran out of time.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   const bool ok = dev::mbar_wait(bar, parity, kWaitLimitNs);
@@ -548,6 +564,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
         const float* swt = reinterpret_cast<const float*>(st + Cf::kSwOff) + 2 * t;
         const int64_t g0 = cur.row_base + cur.rbl * kTcRows + t * 128;
         const float sw = ((g0 + row) >> 7) == (g0 >> 7) ? swt[0] : swt[1];
+        uint64_t ss;  // (sw, sw) for the packed multiply
+        asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(sw));
 #pragma unroll
         for (int c0 = 0; c0 < N; c0 += 16) {  // hi columns; lo N further
           uint32_t rh[16], rl[16];
@@ -555,8 +573,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
           tmem_ld16_nowait(dcol + N + c0, rl);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            acc[c0 + k] = fmaf(sw * ex[c0 + k], __uint_as_float(rh[k]) + __uint_as_float(rl[k]), acc[c0 + k]);
+          for (int k = 0; k < 16; k += 2)
+            promote2(acc[c0 + k], acc[c0 + k + 1], ss, ex[c0 + k], ex[c0 + k + 1], rh[k], rh[k + 1], rl[k], rl[k + 1]);
         }
       }
       tc_fence_before();

@@ -162,7 +162,7 @@ def test_prefill_kda_layer_small(S):
 @pytest.mark.parametrize("m", [2048, 8192])
 def test_prefill_full_size_sampled_rows(S, kernel, m):
     # The prefill workload's weights (KDA-like layer, N = 8), full sizes, at
-    # both token counts the benchmark times; the oracle computes 48 sampled
+    # both token counts the benchmark times; the oracle computes 192 sampled
     # token rows (and the first and last) of every linear.
     w = WL.PREFILL
     ents = workload_entries(w, 1)
@@ -175,7 +175,7 @@ def test_prefill_full_size_sampled_rows(S, kernel, m):
         y = torch.empty((m, r), dtype=torch.bfloat16, device="cuda")
         st.ctx.linear(j, S.SRC_SLOT1, x.cuda().data_ptr(), m, y.data_ptr(), 0)
         torch.cuda.synchronize()
-        sel = np.unique(np.concatenate([[0, m - 1], rng.choice(m, size=48, replace=False)]))
+        sel = np.unique(np.concatenate([[0, m - 1], rng.choice(m, size=192, replace=False)]))
         ref, _ = _ref_quantised(x, layers[0].codes[j], layers[0].scales[j], rows=sel)
         assert_close(bf16_tensor_to_f64(y)[sel], ref, f"entry {j} (sampled rows)")
     assert st.ctx.status() == 0
