@@ -93,7 +93,10 @@ struct TcCfg {
   static constexpr int kDCols = WB ? 2 * N : 4 * N;  // one TMEM accumulator buffer: 2 tiles x (2N or N) columns
   static constexpr int kDBufs = N <= 32 ? 4 : 2;
   static constexpr int kTmemCols = pow2_at_least(kDBufs * kDCols);
-  static constexpr int kSlotFloats = kTcRows * N;  // partial-sum slot of one CTA
+  // Partial-sum slot of one CTA run: the sums of its 256 rows x N columns as
+  // float4 groups, group q of row r at q * 256 + r, so a warp's 32 rows are
+  // 512 contiguous bytes for both the GEMM's stores and the settle's loads.
+  static constexpr int kSlotFloats = kTcRows * N;
 };
 static_assert(TcCfg<16>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
 static_assert(TcCfg<32>::kSmem + 1024 <= 227 * 1024, "decode_tc: shared memory");
@@ -212,29 +215,52 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
 
 // ---- 1. activation split ---------------------------------------------------------
 
+// What the split kernels read: the linears whose activations they split, with
+// the first thread of each (a few hundred bytes of launch parameters instead
+// of the GEMM's tensor maps).
+struct SplitLinear {
+  const uint16_t* x;  // bf16 [m, cols]
+  uint8_t* xs;        // its split blocks, one per K slab
+  int64_t cols;
+  int64_t thread_end;  // one past the last thread of this linear
+};
+struct SplitParams {
+  SplitLinear l[kMaxDecodeGroup];
+  int32_t n;  // linears
+  int32_t m;
+  uint64_t* trace;
+};
+// The linear of thread `tid`, or -1 past the last one; `first` receives its first thread.
+__device__ __forceinline__ int split_linear_of(const SplitParams& sp, int64_t tid, int64_t* first) {
+  int64_t b = 0;
+  for (int j = 0; j < sp.n; ++j) {
+    if (tid < sp.l[j].thread_end) {
+      *first = b;
+      return j;
+    }
+    b = sp.l[j].thread_end;
+  }
+  return -1;
+}
+
 // Eight consecutive threads per (entry, K slab, row), 16 activations each. The
 // thread count is a multiple of 128, so whole warps are either in or out.
-__global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad) {
+__global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ SplitParams sp, int32_t n_pad) {
   // Let the GEMM launch now: it waits for this grid's results before it reads them.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) dev::trace_start(p.trace);  // the linear's trace spans all three kernels
+  if (threadIdx.x == 0) dev::trace_start(sp.trace);  // the linear's trace spans all three kernels
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int g = (int)(tid & 7);
-  int64_t task = tid >> 3;  // (entry, slab, row)
-  int j = 0;
-  for (; j < p.n_entries; ++j) {
-    if (!p.e[j].split_owner) continue;  // another segment of the same linear splits it
-    const int64_t t = (int64_t)p.e[j].slabs * n_pad;
-    if (task < t) break;
-    task -= t;
-  }
-  if (j >= p.n_entries) return;
-  const DecodeEntry& e = p.e[j];
+  int64_t first = 0;
+  const int j = split_linear_of(sp, tid, &first);
+  if (j < 0) return;
+  const SplitLinear& e = sp.l[j];
+  const int64_t task = (tid - first) >> 3;  // (slab, row) of the linear
   const int64_t kb = task / n_pad;
   const int r = (int)(task - kb * n_pad);
   const int64_t col = kb * kSlabK + g * 16;
   float v[16];
-  if (r < p.m && col < e.cols) {  // cols is a multiple of 16: a group is all in or all out
+  if (r < sp.m && col < e.cols) {  // cols is a multiple of 16: a group is all in or all out
     const uint4* src = reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col);
     const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
     const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
@@ -284,27 +310,22 @@ __global__ void __launch_bounds__(256) split_x_kernel(const __grid_constant__ De
 // activations themselves - as bf16, or rounded to f16 (to_f16) for f16
 // weights - [n_pad rows][128 bytes] in the 128-byte swizzled order, zero past m
 // and past cols. Eight threads per (entry, slab, row), one 16-byte piece each.
-__global__ void __launch_bounds__(256) split_x_16_kernel(const __grid_constant__ DecodeParams p, int32_t n_pad,
+__global__ void __launch_bounds__(256) split_x_16_kernel(const __grid_constant__ SplitParams sp, int32_t n_pad,
                                                           int32_t to_f16) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) dev::trace_start(p.trace);
+  if (threadIdx.x == 0) dev::trace_start(sp.trace);
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int g = (int)(tid & 7);
-  int64_t task = tid >> 3;
-  int j = 0;
-  for (; j < p.n_entries; ++j) {
-    if (!p.e[j].split_owner) continue;
-    const int64_t t = (int64_t)p.e[j].slabs * n_pad;
-    if (task < t) break;
-    task -= t;
-  }
-  if (j >= p.n_entries) return;
-  const DecodeEntry& e = p.e[j];
+  int64_t first = 0;
+  const int j = split_linear_of(sp, tid, &first);
+  if (j < 0) return;
+  const SplitLinear& e = sp.l[j];
+  const int64_t task = (tid - first) >> 3;
   const int64_t kb = task / n_pad;
   const int r = (int)(task - kb * n_pad);
   const int64_t col = kb * 64 + g * 8;
   uint4 v = make_uint4(0, 0, 0, 0);
-  if (r < p.m && col < e.cols) v = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col));
+  if (r < sp.m && col < e.cols) v = __ldg(reinterpret_cast<const uint4*>(e.x + (int64_t)r * e.cols + col));
   if (to_f16) {
     v.x = bf16x2_to_f16x2(v.x);
     v.y = bf16x2_to_f16x2(v.y);
@@ -379,9 +400,10 @@ __device__ __forceinline__ void tc_end_run(float (&acc)[N], const DecodeParams& 
     }
   } else {
     const int64_t slot = 2 * geo.c + (cur.rb_begin + cur.rbl == first_rbg ? 0 : 1);
-    float4* d = reinterpret_cast<float4*>(p.partials + slot * (int64_t)TcCfg<N>::kSlotFloats + (t * 128 + row) * N);
+    float4* d = reinterpret_cast<float4*>(p.partials + slot * (int64_t)TcCfg<N>::kSlotFloats) + (t * 128 + row);
 #pragma unroll
-    for (int q = 0; q < N / 4; ++q) d[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    for (int q = 0; q < N / 4; ++q)
+      d[q * kTcRows] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
   }
 #pragma unroll
   for (int mm = 0; mm < N; ++mm) acc[mm] = 0.f;
@@ -604,99 +626,113 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
 
 // ---- 3. split-K settle ------------------------------------------------------------
 
-// Which row blocks the GEMM's partition split between CTAs, worked out on the
-// host from the same partition (so the kernel does no unit arithmetic).
+// A row block that the GEMM's partition split between CTAs, worked out on the
+// host from the same partition, with everything its settle block needs: the
+// block's one read of its task is all the launch-parameter traffic it makes.
 struct SettleTask {
-  int32_t j;       // entry
-  int32_t rbl;     // row block in the entry
-  int32_t cf, cl;  // the CTAs that share it, in K order
+  uint16_t* y;      // Y[0, first row of the row block] (bf16, rows `ystride` apart in m)
+  int32_t ystride;  // rows of the linear
+  int32_t rows;     // rows of the row block inside its entry (<= 256)
+  int32_t cf, cl;   // the CTAs that share it, in K order
+  int32_t cf_slot;  // partial slot of CTA cf (its first or its second run); a later CTA's is its first, 2c
+  int32_t pad;
 };
 struct SettlePlan {
-  int32_t n;                           // tasks
-  int32_t cta_first_rbg[kMaxGrid];     // each CTA's first row block (its partial slot 0)
+  int32_t n;  // tasks
+  int32_t m;
+  const float* partials;
+  uint64_t* trace;
+  uint64_t tag;
   SettleTask task[kMaxGrid];
 };
 
-// One block per settle task (a row block the GEMM's partition split between
-// CTAs cf..cl) and 16-column group (blockIdx.y): the block adds the partial
-// sums of those CTAs in K (CTA) order, so the result does not depend on
-// timing, and writes those 16 columns of Y. Thread r owns row r of the row
-// block; it issues the loads of up to four contributions before adding them.
-// Chunk-map launches add one block per straddling row and 16-column group
-// (blockIdx.x >= sp.n): that row is in no segment, so the block computes it
-// directly from the chunks (straddle_row).
-template <int N, int WT>
-__device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
+// Adds the partial sums of one settle task in K (CTA) order, so the result does
+// not depend on timing, and writes Y for columns [c0, c0 + C). Thread r owns row
+// r of the row block; it issues the loads of up to KB contributions before
+// adding them.
+template <int N, int C>
+__device__ __forceinline__ void settle_task(const SettleTask& tk, const float* partials, int m, int c0) {
+  constexpr int KB = C <= 16 ? 4 : C <= 32 ? 2 : 1;  // contributions loaded at once: 12-16 float4 a thread
+  constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
+  const int row = threadIdx.x;
+  if (row >= tk.rows) return;  // past the entry (segment); straddling rows are in none
+  float4 acc[C / 4];
+#pragma unroll
+  for (int q = 0; q < C / 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int32_t cb = tk.cf; cb <= tk.cl; cb += KB) {
+    float4 v[KB][C / 4];
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+      if (cb + k <= tk.cl) {
+        const int64_t slot = cb + k == tk.cf ? tk.cf_slot : 2 * (int64_t)(cb + k);
+        const float4* s4 = reinterpret_cast<const float4*>(partials + slot * kSlot) + (c0 / 4) * kTcRows + row;
+#pragma unroll
+        for (int q = 0; q < C / 4; ++q) v[k][q] = __ldcg(s4 + q * kTcRows);
+      }
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+      if (cb + k <= tk.cl) {
+#pragma unroll
+        for (int q = 0; q < C / 4; ++q) {
+          acc[q].x += v[k][q].x;
+          acc[q].y += v[k][q].y;
+          acc[q].z += v[k][q].z;
+          acc[q].w += v[k][q].w;
+        }
+      }
+  }
+#pragma unroll
+  for (int q = 0; q < C / 4; ++q) {
+    const float a[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int mm = c0 + 4 * q + k;
+      if (mm < m) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
+        tk.y[(int64_t)mm * tk.ystride + row] = *reinterpret_cast<const uint16_t*>(&b);
+      }
+    }
+  }
+}
 
-template <int N, bool FUSED, int WT>
-__global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ DecodeParams p,
-                                                         const __grid_constant__ SettlePlan sp) {
+__device__ __forceinline__ void settle_trace_end(const SettlePlan& sp) {
+  __syncwarp();
+  if (sp.trace && (threadIdx.x & 31) == 0) {  // the record's end stamp after this kernel's writes
+    __threadfence();
+    dev::trace_end(sp.trace, sp.tag);
+  }
+}
+
+// Slot path: one block per settle task, all N columns (a launch has fewer
+// tasks than CTAs, so the grid is one wave).
+template <int N>
+__global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ SettlePlan sp) {
   grid_dependency_wait();  // the GEMM's results are complete and visible
   // A gather launched next on the stream (programmatic serialisation) may
   // start now: it writes a slot, which nothing here reads, and reads chunks,
   // which nothing here writes; later stream work still waits for this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (FUSED && (int32_t)blockIdx.x >= sp.n) {
-    straddle_row<N, WT>(p, (int)blockIdx.x - sp.n, (int)blockIdx.y * 16);
-    return;
-  }
-  const SettleTask tk = sp.task[blockIdx.x];
-  UnitPos up;
-  up.j = tk.j;
-  up.rbl = tk.rbl;
-  up.rbg = p.e[tk.j].rb_begin + tk.rbl;
-  const int64_t cf = tk.cf, cl = tk.cl;
-  const DecodeEntry& e = p.e[up.j];
-  uint16_t* const y = e.y;
-  const int64_t rows = e.rows, ystride = e.y_rows, base = e.row_base;
-  const int m = p.m;
-  const int row = threadIdx.x, c0 = blockIdx.y * 16;
-  const int64_t o = up.rbl * kTcRows + row;  // row of the entry (segment); straddling rows are in none
-  if (o < rows) {
-    constexpr int64_t kSlot = TcCfg<N>::kSlotFloats;
-    float4 acc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t cb = cf; cb <= cl; cb += 4) {
-      float4 v[4][4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (cb + k <= cl) {
-          const float4* s4 =
-              reinterpret_cast<const float4*>(p.partials + (2 * (cb + k) + (up.rbg == sp.cta_first_rbg[cb + k] ? 0 : 1)) * kSlot + row * N + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v[k][q] = __ldcg(s4 + q);
-        }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (cb + k <= cl) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[q].x += v[k][q].x;
-            acc[q].y += v[k][q].y;
-            acc[q].z += v[k][q].z;
-            acc[q].w += v[k][q].w;
-          }
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float a[4] = {acc[q].x, acc[q].y, acc[q].z, acc[q].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int mm = c0 + 4 * q + k;
-        if (mm < m) {
-          const __nv_bfloat16 b = __float2bfloat16_rn(a[k]);
-          y[(int64_t)mm * ystride + base + o] = *reinterpret_cast<const uint16_t*>(&b);
-        }
-      }
-    }
-  }
-  __syncwarp();
-  if (p.trace && (threadIdx.x & 31) == 0) {  // the record's end stamp after this kernel's writes
-    __threadfence();
-    dev::trace_end(p.trace, p.tag);
-  }
+  settle_task<N, N>(sp.task[blockIdx.x], sp.partials, sp.m, 0);
+  settle_trace_end(sp);
+}
+
+// Chunk-map path: the settle tasks as above, then one block per straddling row
+// and 16-column group: that row is in no segment, so the block computes it
+// directly from the chunks (straddle_row).
+template <int N, int WT>
+__device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
+
+template <int N, int WT>
+__global__ void __launch_bounds__(kTcRows) settle_fused_kernel(const __grid_constant__ DecodeParams p,
+                                                               const __grid_constant__ SettlePlan sp) {
+  grid_dependency_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int b = (int)blockIdx.x;
+  if (b < sp.n)
+    settle_task<N, N>(sp.task[b], sp.partials, sp.m, 0);
+  else
+    straddle_row<N, WT>(p, (b - sp.n) / (N / 16), (b - sp.n) % (N / 16) * 16);
+  settle_trace_end(sp);
 }
 
 // Row st.row of a linear, read through the chunk map (a chunk boundary falls
@@ -830,7 +866,10 @@ void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
   };
   auto cta = [&](int64_t u) { return ((u + 1) * G - 1) / U; };
   sp->n = 0;
-  for (int64_t c = 0; c < G; ++c) sp->cta_first_rbg[c] = (int32_t)pos(c * U / G).rbg;
+  sp->m = p.m;
+  sp->partials = p.partials;
+  sp->trace = p.trace;
+  sp->tag = p.tag;
   for (int64_t c = 1; c < G; ++c) {
     const UnitPos up = pos(c * U / G);
     if (up.kb == 0) continue;  // the boundary is a row-block start: nothing is split here
@@ -841,11 +880,37 @@ void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
     const DecodeEntry& e = p.e[up.j];
     const int64_t fu = e.unit_begin + up.rbl * e.slabs;
     SettleTask& t = sp->task[sp->n++];
-    t.j = up.j;
-    t.rbl = (int32_t)up.rbl;
+    t.y = e.y + e.row_base + up.rbl * kTcRows;
+    t.ystride = (int32_t)e.y_rows;
+    t.rows = (int32_t)std::min<int64_t>(kTcRows, e.rows - up.rbl * kTcRows);
     t.cf = (int32_t)cta(fu);
     t.cl = (int32_t)cta(fu + e.slabs - 1);
+    // CTA cf holds the row block's first units: its first run if its range
+    // starts inside the row block, else its last (second) run.
+    t.cf_slot = 2 * t.cf + (pos(t.cf * U / G).rbg == up.rbg ? 0 : 1);
+    t.pad = 0;
   }
+}
+
+// The split kernels' parameters: the linears whose activations a launch splits
+// (the owner entry of each; chunk-map segments of one linear share its blocks).
+SplitParams split_params(const DecodeParams& p, int64_t n_pad, bool w16) {
+  SplitParams sp = {};
+  sp.m = p.m;
+  sp.trace = p.trace;
+  int64_t end = 0;
+  for (int j = 0; j < p.n_entries; ++j) {
+    if (!p.e[j].split_owner) continue;
+    SplitLinear& l = sp.l[sp.n++];
+    l.x = p.e[j].x;
+    l.xs = p.e[j].xs;
+    l.cols = p.e[j].cols;
+    // one thread per 16 (e4m3 split) or 8 (16-bit copy) activations of a slab row
+    end += (int64_t)p.e[j].slabs * n_pad * 8;
+    l.thread_end = end;
+  }
+  (void)w16;
+  return sp;
 }
 
 template <int N, bool FUSED, int WT>
@@ -861,10 +926,10 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
     return a;
   });
   if (attr != cudaSuccess) return attr;
-  // 1. split the activations of every entry
-  int64_t threads = 0;
-  for (int j = 0; j < p.n_entries; ++j)
-    if (p.e[j].split_owner) threads += (int64_t)p.e[j].slabs * N * 8;
+  // 1. split the activations of every linear
+  const SplitParams spl = split_params(p, N, WB);
+  if (spl.n < 1 || spl.n > kMaxDecodeGroup) return cudaErrorInvalidValue;
+  const int64_t threads = spl.l[spl.n - 1].thread_end;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributePriority;
   at[0].val.priority = high_priority();
@@ -876,8 +941,8 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;  // priority only
-  cudaError_t e = WB ? cudaLaunchKernelEx(&cfg, split_x_16_kernel, p, (int)N, (int)(WT == 2))
-                     : cudaLaunchKernelEx(&cfg, split_x_kernel, p, (int)N);
+  cudaError_t e = WB ? cudaLaunchKernelEx(&cfg, split_x_16_kernel, spl, (int)N, (int)(WT == 2))
+                     : cudaLaunchKernelEx(&cfg, split_x_kernel, spl, (int)N);
   if (e != cudaSuccess) return e;
   // 2. the GEMM, as a programmatic dependent launch of (1)
   const int64_t grid = std::min<int64_t>({p.units, (int64_t)device_sm_count(), (int64_t)kMaxGrid, grid_cap});
@@ -891,12 +956,15 @@ cudaError_t launch_tc_n(const DecodeParams& p, int64_t grid_cap, cudaStream_t s)
   if (e != cudaSuccess) return e;
   SettlePlan sp;
   settle_plan(p, grid, &sp);
-  const int64_t blocks = sp.n + (FUSED ? p.st.n : 0);
+  const int64_t blocks = sp.n + (FUSED ? (int64_t)p.st.n * (N / 16) : 0);
   if (blocks < 1) return cudaSuccess;
-  cfg.gridDim = dim3((unsigned)blocks, N / 16);
+  cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kTcRows);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, settle_kernel<N, FUSED, WT>, p, sp);
+  if constexpr (FUSED)
+    return cudaLaunchKernelEx(&cfg, settle_fused_kernel<N, WT>, p, sp);
+  else
+    return cudaLaunchKernelEx(&cfg, settle_kernel<N>, sp);
 }
 
 template <bool FUSED, int WT>
