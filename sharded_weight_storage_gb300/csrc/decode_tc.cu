@@ -31,8 +31,9 @@
 //   3. settle_kernel, a programmatic dependent of (2): adds the partial sums
 //      of every shared row block in K order and writes Y. Settling in its own
 //      grid keeps the GEMM free of fences, atomics and cold code at its end.
-//      It releases its own dependents at once, so a gather that follows on the
-//      stream (the next step's) overlaps it.
+//      The GEMM releases it once every CTA has read all its weights, and it
+//      releases its own dependents at once, so a gather that follows on the
+//      stream (the next step's) overlaps the GEMM's tail and the settle.
 // decode_tc_kernel (swap-AB: weight rows are the MMA's M = 128 dimension, the
 // activations its N = 16..64 dimension, m rounded up to 16):
 //   * warp 0, one thread: producer. Per unit (256 weight rows x 128 K) one TMA
@@ -448,9 +449,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
   }
   __syncthreads();
   tc_fence_after();
-  // No early launch_dependents here: settle blocks that launch early and wait
-  // beside the GEMM's CTAs slow the GEMM down more than the settle's launch
-  // latency costs.
   const uint32_t tmem = s_tmem;
   const RunGeom geo{G, U, c};
 
@@ -510,6 +508,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
       // Before the CTA may exit, every issued stage must have landed.
       for (int64_t k = i - S; k < i; ++k)
         if (k >= 0) dev::mbar_wait(&sfull[(int)(k % S)], (uint32_t)((k / S) & 1), kWaitLimitNs / 4);
+      // This CTA reads nothing more from the weights: once every CTA is here,
+      // the settle grid may launch (it waits for this grid's results), and
+      // with it a gather that follows on the stream may overwrite the slot.
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----------------------------------------------------------
@@ -707,11 +709,13 @@ __device__ __forceinline__ void settle_trace_end(const SettlePlan& sp) {
 // tasks than CTAs, so the grid is one wave).
 template <int N>
 __global__ void __launch_bounds__(kTcRows) settle_kernel(const __grid_constant__ SettlePlan sp) {
-  grid_dependency_wait();  // the GEMM's results are complete and visible
   // A gather launched next on the stream (programmatic serialisation) may
-  // start now: it writes a slot, which nothing here reads, and reads chunks,
-  // which nothing here writes; later stream work still waits for this grid.
+  // start now: this grid launched once every GEMM CTA had read all its
+  // weights, the gather writes a slot, which nothing here reads, and reads
+  // chunks, which nothing here writes; later stream work still waits for
+  // this grid.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_dependency_wait();  // the GEMM's results are complete and visible
   settle_task<N, N>(sp.task[blockIdx.x], sp.partials, sp.m, 0);
   settle_trace_end(sp);
 }
@@ -725,8 +729,8 @@ __device__ void straddle_row(const DecodeParams& p, int sidx, int c0);
 template <int N, int WT>
 __global__ void __launch_bounds__(kTcRows) settle_fused_kernel(const __grid_constant__ DecodeParams p,
                                                                const __grid_constant__ SettlePlan sp) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in settle_kernel
   grid_dependency_wait();
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = (int)blockIdx.x;
   if (b < sp.n)
     settle_task<N, N>(sp.task[b], sp.partials, sp.m, 0);
