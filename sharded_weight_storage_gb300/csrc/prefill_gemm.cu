@@ -86,7 +86,11 @@ constexpr int kTmemCols = 512;
 // memory, so no register waits on a global load.
 constexpr int kScaleDepth = 8;
 __host__ __device__ constexpr int scale_ring_bytes(int epi_warps) { return kScaleDepth * (epi_warps * 32 + epi_warps) * 4; }
-constexpr int kSmemBytes = kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + 1024;
+// Output staging of the one-CTA kernel: per promotion warp, 32 rows x 32 bf16
+// columns (64 bytes a row) at a time.
+constexpr int kOutChunk = 32;
+constexpr int kOutWarpBytes = 32 * kOutChunk * 2;
+constexpr int kSmemBytes = kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + kEpiWarps * kOutWarpBytes + 1024;
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + scale_ring_bytes(kPairEpiWarps) + 1024;
 
 struct PrefillParams {
@@ -355,6 +359,51 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&
   }
 }
 
+// The warp's 32 rows m0 .. m0+31 (row m0 + lane in this lane's acc), columns
+// n0 .. n0+kCols-1 of Y as bf16, through `stage` (kOutWarpBytes): each chunk of
+// 32 columns is written to shared memory row by row (16-byte piece i of row r
+// at slot i ^ ((r >> 1) & 3), so neither the writes nor the reads below
+// conflict on banks) and read back so that one store instruction covers 8
+// rows x 64 contiguous bytes instead of 32 rows x 16 bytes. Falls back to
+// store_row where the columns are ragged.
+template <int kCols>
+__device__ __forceinline__ void store_rows_staged(const PrefillParams& p, const float (&acc)[kCols], int64_t m0,
+                                                  int64_t n0, int lane, uint8_t* stage) {
+  if (n0 + kCols > p.N || (p.N & 7) != 0) {
+    store_row<kCols>(p, acc, m0 + lane, n0);
+    return;
+  }
+  const uint32_t sbase = dev::smem_addr(stage);
+#pragma unroll
+  for (int c = 0; c < kCols / kOutChunk; ++c) {
+    __syncwarp();  // the previous chunk has been read back
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // this lane's row: 4 pieces of 8 columns
+      uint32_t w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const __nv_bfloat162 b2 =
+            __floats2bfloat162_rn(acc[c * kOutChunk + i * 8 + 2 * t], acc[c * kOutChunk + i * 8 + 2 * t + 1]);
+        w[t] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      const uint32_t a = sbase + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                   : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // rows 8j .. 8j+7, four lanes a row
+      const int r = j * 8 + (lane >> 2), i = lane & 3;
+      const uint32_t a = sbase + r * 64 + ((i ^ ((r >> 1) & 3)) << 4);
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                   : "memory");
+      const int64_t m = m0 + r;
+      if (m < p.M) *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + c * kOutChunk + i * 8) = v;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mdone;
@@ -457,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     float* ring = reinterpret_cast<float*>(smem + kStages * kStageBytes);
     float* ring_ex = ring + (threadIdx.x - 64);
     float* ring_sw = ring + kScaleDepth * kEpiWarps * 32 + (warp - 2) * kScaleDepth;
+    uint8_t* stage = smem + kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + (warp - 2) * kOutWarpBytes;
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x) {
       const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
@@ -466,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (!promote_tile<false, kEpiWarps, kCols, 2, kBN, 16>(p, acc, m, n0, lane_base, tfull, release, ring_ex,
                                                              ring_sw, it, lane, &s_abort))
         break;
-      store_row<kCols>(p, acc, m, n0);
+      store_rows_staged<kCols>(p, acc, m - lane, n0, lane, stage);
     }
   }
   __syncthreads();
