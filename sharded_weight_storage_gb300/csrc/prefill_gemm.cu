@@ -366,6 +366,37 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&
 // conflict on banks) and read back so that one store instruction covers 8
 // rows x 64 contiguous bytes instead of 32 rows x 16 bytes. Falls back to
 // store_row where the columns are ragged.
+// One 32-column chunk of the warp's 32 rows (this lane's row as 16 bf16-pair
+// words, columns nc .. nc+31, all inside Y) through `stage`: written row by
+// row (16-byte piece i of row r at slot i ^ ((r >> 1) & 3), so neither the
+// writes nor the reads conflict on banks), read back so that one store
+// instruction covers 8 rows x 64 contiguous bytes instead of 32 rows x 16.
+__device__ __forceinline__ void store_chunk_staged(const PrefillParams& p, const uint32_t (&w)[16], int64_t m0,
+                                                   int64_t nc, int lane, uint32_t sbase) {
+  __syncwarp();  // the previous chunk has been read back
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = sbase + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * i]), "r"(w[4 * i + 1]),
+                 "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
+                 : "memory");
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // rows 8j .. 8j+7, four lanes a row
+    const int r = j * 8 + (lane >> 2), i = lane & 3;
+    const uint32_t a = sbase + r * 64 + ((i ^ ((r >> 1) & 3)) << 4);
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    const int64_t m = m0 + r;
+    if (m < p.M) *reinterpret_cast<uint4*>(p.y + m * p.N + nc + i * 8) = v;
+  }
+}
+
+// The warp's 32 rows m0 .. m0+31 (row m0 + lane in this lane's acc), columns
+// n0 .. n0+kCols-1 of Y as bf16, 32 columns at a time through `stage`
+// (kOutWarpBytes); store_row where the columns are ragged.
 template <int kCols>
 __device__ __forceinline__ void store_rows_staged(const PrefillParams& p, const float (&acc)[kCols], int64_t m0,
                                                   int64_t n0, int lane, uint8_t* stage) {
@@ -376,31 +407,13 @@ __device__ __forceinline__ void store_rows_staged(const PrefillParams& p, const 
   const uint32_t sbase = dev::smem_addr(stage);
 #pragma unroll
   for (int c = 0; c < kCols / kOutChunk; ++c) {
-    __syncwarp();  // the previous chunk has been read back
+    uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {  // this lane's row: 4 pieces of 8 columns
-      uint32_t w[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const __nv_bfloat162 b2 =
-            __floats2bfloat162_rn(acc[c * kOutChunk + i * 8 + 2 * t], acc[c * kOutChunk + i * 8 + 2 * t + 1]);
-        w[t] = *reinterpret_cast<const uint32_t*>(&b2);
-      }
-      const uint32_t a = sbase + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                   : "memory");
+    for (int t = 0; t < 16; ++t) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c * kOutChunk + 2 * t], acc[c * kOutChunk + 2 * t + 1]);
+      w[t] = *reinterpret_cast<const uint32_t*>(&b2);
     }
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {  // rows 8j .. 8j+7, four lanes a row
-      const int r = j * 8 + (lane >> 2), i = lane & 3;
-      const uint32_t a = sbase + r * 64 + ((i ^ ((r >> 1) & 3)) << 4);
-      uint4 v;
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
-                   : "memory");
-      const int64_t m = m0 + r;
-      if (m < p.M) *reinterpret_cast<uint4*>(p.y + m * p.N + n0 + c * kOutChunk + i * 8) = v;
-    }
+    store_chunk_staged(p, w, m0, n0 + c * kOutChunk, lane, sbase);
   }
 }
 
@@ -809,6 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_16_kernel(const __grid_co
     const int h = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
+    const uint32_t stage_addr =
+        dev::smem_addr(smem + kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + (warp - 2) * kOutWarpBytes);
     int64_t t = 0;
     for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x, ++t) {
       const int buf = (int)(t & 1);
@@ -821,6 +836,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_16_kernel(const __grid_co
       const int64_t m = (int64_t)mt * kBM + row;
       const int64_t n0 = (int64_t)nt * kBN + h * 128;
       const bool vec = (p.N & 7) == 0;
+      if (vec && n0 + 128 <= p.N) {  // whole columns: through shared memory, 8 rows x 64 bytes a store
+#pragma unroll 1
+        for (int c = 0; c < 128 / kOutChunk; ++c) {
+          uint32_t v[32], w[16];
+          tmem_ld16(lane_base + buf * kBN + c * kOutChunk, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(lane_base + buf * kBN + c * kOutChunk + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            w[t] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          store_chunk_staged(p, w, m - lane, n0 + c * kOutChunk, lane, stage_addr);
+        }
+      } else {
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[16];
@@ -842,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_16_kernel(const __grid_co
             for (int i = 0; i < 16 && nc + i < p.N; ++i) yp[i] = (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
           }
         }
+      }
       }
       tc_fence_before();
       __syncwarp();
