@@ -359,13 +359,6 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&
   }
 }
 
-// The warp's 32 rows m0 .. m0+31 (row m0 + lane in this lane's acc), columns
-// n0 .. n0+kCols-1 of Y as bf16, through `stage` (kOutWarpBytes): each chunk of
-// 32 columns is written to shared memory row by row (16-byte piece i of row r
-// at slot i ^ ((r >> 1) & 3), so neither the writes nor the reads below
-// conflict on banks) and read back so that one store instruction covers 8
-// rows x 64 contiguous bytes instead of 32 rows x 16 bytes. Falls back to
-// store_row where the columns are ragged.
 // One 32-column chunk of the warp's 32 rows (this lane's row as 16 bf16-pair
 // words, columns nc .. nc+31, all inside Y) through `stage`: written row by
 // row (16-byte piece i of row r at slot i ^ ((r >> 1) & 3), so neither the
