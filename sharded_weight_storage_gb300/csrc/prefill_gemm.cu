@@ -67,6 +67,8 @@ constexpr int kBBytes = kBN * kBK;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
+// The FP8 kernel adds one warp that loads the scale factors.
+constexpr int kFp8Threads = (3 + kEpiWarps) * 32;
 
 // A CTA pair per 256 x 256 tile: each CTA loads 128 activation rows and 128
 // weight rows per slab (32 KB); two TMEM slab buffers of 256 columns; 16
@@ -86,6 +88,12 @@ constexpr int kTmemCols = 512;
 // memory, so no register waits on a global load.
 constexpr int kScaleDepth = 8;
 __host__ __device__ constexpr int scale_ring_bytes(int epi_warps) { return kScaleDepth * (epi_warps * 32 + epi_warps) * 4; }
+// Factor ring of the one-CTA FP8 kernel, filled by its scale warp: per slab
+// (kScaleDepth of them in flight, across tiles) ex[m, kb] of the tile's 128
+// rows and s_w[nb, kb] of its two 128-column blocks.
+constexpr int kFactorSlot = kBM + 2;  // floats
+constexpr int kFactorRingBytes = kScaleDepth * kFactorSlot * 4;
+static_assert(kFactorRingBytes <= scale_ring_bytes(kEpiWarps), "factor ring fits the scale ring's space");
 // Output staging of the one-CTA kernel: per promotion warp, 32 rows x 32 bf16
 // columns (64 bytes a row) at a time.
 constexpr int kOutChunk = 32;
@@ -359,6 +367,49 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&
   }
 }
 
+// One promotion thread's share of a tile in the one-CTA kernel: as
+// promote_tile, with each slab's two factors taken from the factor ring that
+// the scale warp fills (slot it % kScaleDepth: fslot_full says it is filled,
+// fslot_empty takes one arrival per promotion warp once read). `g` selects the
+// tile's 128-column block (its weight-scale row).
+template <int kCols>
+__device__ __forceinline__ bool promote_tile_ring(const PrefillParams& p, float (&acc)[kCols], int row, int g,
+                                                  uint32_t lane_base, uint64_t* tfull, uint64_t* tempty,
+                                                  const float* ring, uint64_t* fslot_full, uint64_t* fslot_empty,
+                                                  int64_t& it, int lane, volatile int* s_abort) {
+  const int G = p.kslabs;
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
+  for (int kb = 0; kb < G; ++kb) {
+    const int buf = (int)(it & 1), d = (int)(it % kScaleDepth);
+    if (!dev::mbar_wait(&fslot_full[d], (uint32_t)((it / kScaleDepth) & 1), kWaitLimitNs) ||
+        !dev::mbar_wait(&tfull[buf], (uint32_t)((it >> 1) & 1), kWaitLimitNs)) {
+      set_abort(p, s_abort);
+      return false;
+    }
+    tc_fence_after();
+    const float* slot = ring + d * kFactorSlot;
+    const float fk = slot[row] * slot[kBM + g];
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(&fslot_empty[d]);
+    uint64_t ff;  // (fk, fk) for the packed FMAs
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ff) : "f"(fk));
+#pragma unroll
+    for (int c = 0; c < kCols / 16; ++c) {
+      uint32_t v[16];
+      tmem_ld16(lane_base + buf * kBN + c * 16, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) fma2(acc[c * 16 + i], acc[c * 16 + i + 1], ff, v[i], v[i + 1]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(&tempty[buf]);
+    ++it;
+  }
+  return true;
+}
+
 // One 32-column chunk of the warp's 32 rows (this lane's row as 16 bf16-pair
 // words, columns nc .. nc+31, all inside Y) through `stage`: written row by
 // row (16-byte piece i of row r at slot i ^ ((r >> 1) & 3), so neither the
@@ -410,9 +461,10 @@ __device__ __forceinline__ void store_rows_staged(const PrefillParams& p, const 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kFp8Threads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mdone;
+  __shared__ __align__(8) uint64_t ffull[kScaleDepth], fempty[kScaleDepth];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   // 128-byte swizzled TMA tiles need a 1024-byte aligned destination.
@@ -430,6 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int b = 0; b < 2; ++b) {
       dev::mbar_init(&tfull[b], 1);
       dev::mbar_init(&tempty[b], kEpiWarps);
+    }
+    for (int d = 0; d < kScaleDepth; ++d) {
+      dev::mbar_init(&ffull[d], 32);  // every lane of the scale warp
+      dev::mbar_init(&fempty[d], kEpiWarps);
     }
     dev::mbar_init(&mdone, 1);
     dev::fence_mbar_init();
@@ -501,6 +557,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         dev::mbar_wait(&mdone, 0, kWaitLimitNs);
       }
     }
+  } else if (warp == 2 + kEpiWarps) {
+    // ---- scale warp: each slab's factors into the ring, kScaleDepth ahead ---
+    float* ring = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    const int64_t sw_rows = (p.N + 127) / 128;
+    int64_t it = 0;
+    for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x) {
+      const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+      const int64_t m0 = (int64_t)mt * kBM + lane * 4, nb0 = (int64_t)nt * (kBN / 128);
+      bool ok = true;
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const int d = (int)(it % kScaleDepth);
+        if (!dev::mbar_wait(&fempty[d], (uint32_t)(((it / kScaleDepth) & 1) ^ 1), kWaitLimitNs)) {
+          set_abort(p, &s_abort);
+          ok = false;
+          break;
+        }
+        float* slot = ring + d * kFactorSlot;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) slot[lane * 4 + r] = m0 + r < p.M ? __ldg(p.ex + (m0 + r) * G + kb) : 0.f;
+        if (lane < 2) slot[kBM + lane] = nb0 + lane < sw_rows ? __ldg(p.sw + (nb0 + lane) * G + kb) : 0.f;
+        dev::mbar_arrive(&ffull[d]);  // each lane, after its own stores
+      }
+      if (!ok) break;
+    }
   } else {
     // ---- promotion and output: 8 warps, thread = tile row, 128 columns -------
     constexpr int kCols = kBN / (kEpiWarps / 4);
@@ -508,10 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int g = (warp - 2) >> 2;   // which kCols of the tile's kBN columns
     const int row = q * 32 + lane;   // tile row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + g * kCols;
-    const uint32_t release[2] = {dev::smem_addr(&tempty[0]), dev::smem_addr(&tempty[1])};
-    float* ring = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    float* ring_ex = ring + (threadIdx.x - 64);
-    float* ring_sw = ring + kScaleDepth * kEpiWarps * 32 + (warp - 2) * kScaleDepth;
+    const float* ring = reinterpret_cast<const float*>(smem + kStages * kStageBytes);
     uint8_t* stage = smem + kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + (warp - 2) * kOutWarpBytes;
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < tiles && !s_abort; tile += gridDim.x) {
@@ -519,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int64_t m = (int64_t)mt * kBM + row;
       const int64_t n0 = (int64_t)nt * kBN + g * kCols;
       float acc[kCols];
-      if (!promote_tile<false, kEpiWarps, kCols, 2, kBN, 16>(p, acc, m, n0, lane_base, tfull, release, ring_ex,
-                                                             ring_sw, it, lane, &s_abort))
+      if (!promote_tile_ring<kCols>(p, acc, row, g, lane_base, tfull, tempty, ring, ffull, fempty, it, lane,
+                                    &s_abort))
         break;
       store_rows_staged<kCols>(p, acc, m - lane, n0, lane, stage);
     }
@@ -955,7 +1032,7 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
         [] { return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
     if (attr != cudaSuccess) return cuda_fail(attr, "prefill: cudaFuncSetAttribute");
     const int64_t grid = std::min<int64_t>(tiles, device_sm_count());
-    cudaError_t le = launch_high(prefill_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p);
+    cudaError_t le = launch_high(prefill_kernel, dim3((unsigned)grid), dim3(kFp8Threads), kSmemBytes, s, p);
     if (le != cudaSuccess) return cuda_fail(le, "prefill kernel launch");
   }
   return SWS_OK;
