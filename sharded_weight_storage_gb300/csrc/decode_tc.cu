@@ -898,6 +898,7 @@ void settle_plan(const DecodeParams& p, int64_t G, SettlePlan* sp) {
 
 // The split kernels' parameters: the linears whose activations a launch splits
 // (the owner entry of each; chunk-map segments of one linear share its blocks).
+// A group has at most kMaxDecodeGroup linears; more owners leave sp.n at -1.
 SplitParams split_params(const DecodeParams& p, int64_t n_pad, bool w16) {
   SplitParams sp = {};
   sp.m = p.m;
@@ -905,6 +906,10 @@ SplitParams split_params(const DecodeParams& p, int64_t n_pad, bool w16) {
   int64_t end = 0;
   for (int j = 0; j < p.n_entries; ++j) {
     if (!p.e[j].split_owner) continue;
+    if (sp.n == kMaxDecodeGroup) {
+      sp.n = -1;
+      return sp;
+    }
     SplitLinear& l = sp.l[sp.n++];
     l.x = p.e[j].x;
     l.xs = p.e[j].xs;
