@@ -418,6 +418,14 @@ int32_t sws_trace_count(const sws_ctx* ctx);
                                       waiting for them; slower than SWS_GATHER_TMA on its own */
 #define SWS_OPT_HOST_WAIT_MS 4 /* limit of the host-side waits (sws_run_timing, sws_ctx_status,
                                   sws_noalloc_status), in ms, 1..3600000; default 10000 */
+#define SWS_OPT_CHECK_BOUNDS 5 /* 0 (default) or 1: a self-check of the library's copy plans.
+                                  Before sws_relayout, sws_relayout_scales, the scale staging of
+                                  a chunk-map linear and a gather launch anything, every copy
+                                  segment is checked against the buffer it reads (a row shard, a
+                                  scale tensor, a chunk of C bytes) and the one it writes (a
+                                  chunk, the slot, the workspace's staging area); a segment that
+                                  leaves one fails the call with SWS_E_INVALID (the message names
+                                  it) and nothing is launched. For debugging; it costs host time. */
 /* Process-wide options, read at each launch. Both decode kernels compute the
  * same linear (sws_linear) within the same tolerance, from views and through
  * the chunk map (a chunk-map launch whose segments or split rows exceed the
@@ -428,6 +436,13 @@ int32_t sws_trace_count(const sws_ctx* ctx);
  * element and give bit-identical results.
  * SWS_E_INVALID for an unknown option or value. */
 int sws_set_option(int32_t option, int64_t value);
+
+/* Test hook of SWS_OPT_CHECK_BOUNDS (host only, no device memory): builds the
+ * copy segments sws_relayout would launch for `layer`, with stand-in
+ * addresses for the row shards and for N chunks of `chunk_bytes` bytes each,
+ * and checks them as that option does. SWS_OK when every segment stays inside
+ * its buffers (chunk_bytes >= the plan's C), SWS_E_INVALID otherwise. */
+int sws_test_check_relayout(const sws_plan* plan, int32_t layer, int64_t chunk_bytes);
 
 /* Failure-detection check: one kernel waits, with the bounded wait every
  * kernel of the library uses, on a barrier that nothing arrives at; after

@@ -10,7 +10,8 @@ from ._lib import (BF16, E4M3, F16, E_ALIGN, E_CUDA, E_INVALID, E_STATE, E_TIMEO
                    last_error, lib, plan_create, quantize_x, relayout, workspace_bytes, set_option, silu_mul,
                    OPT_DECODE_KERNEL, DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05, OPT_PREFILL_KERNEL,
                    PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR, OPT_GATHER_ENGINE, GATHER_TMA, GATHER_COPY_ENGINE,
-                   GATHER_TMA_SHARED_SM, OPT_HOST_WAIT_MS, SCALES_IN_T, relayout_scales, linear_noalloc, noalloc_status, test_bounded_wait_noalloc)
+                   GATHER_TMA_SHARED_SM, OPT_HOST_WAIT_MS, OPT_CHECK_BOUNDS, SCALES_IN_T, relayout_scales, linear_noalloc,
+                   noalloc_status, test_bounded_wait_noalloc, test_check_relayout)
 
 lib()  # load now: no silent fallback when the extension is missing
 
@@ -20,4 +21,5 @@ __all__ = ["Plan", "Ctx", "Graph", "SwsError", "plan_create", "relayout", "works
            "E_UNSUPPORTED", "E_WORKSPACE", "set_option", "OPT_DECODE_KERNEL", "DECODE_AUTO",
            "DECODE_MMA", "DECODE_TCGEN05", "OPT_PREFILL_KERNEL", "PREFILL_AUTO", "PREFILL_SINGLE",
            "PREFILL_PAIR", "OPT_GATHER_ENGINE", "GATHER_TMA", "GATHER_COPY_ENGINE", "GATHER_TMA_SHARED_SM",
-           "OPT_HOST_WAIT_MS", "SCALES_IN_T", "relayout_scales", "linear_noalloc", "noalloc_status", "test_bounded_wait_noalloc"]
+           "OPT_HOST_WAIT_MS", "OPT_CHECK_BOUNDS", "SCALES_IN_T", "relayout_scales", "linear_noalloc", "noalloc_status",
+           "test_bounded_wait_noalloc", "test_check_relayout"]

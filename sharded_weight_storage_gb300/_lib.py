@@ -24,6 +24,7 @@ PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR = 0, 1, 2
 OPT_GATHER_ENGINE = 3
 GATHER_TMA, GATHER_COPY_ENGINE, GATHER_TMA_SHARED_SM = 0, 1, 2
 OPT_HOST_WAIT_MS = 4
+OPT_CHECK_BOUNDS = 5
 
 _NAMES = {0: "SWS_OK", 1: "SWS_W_SKIPPED", 2: "SWS_W_COLD", -1: "SWS_E_INVALID", -2: "SWS_E_ALIGN", -3: "SWS_E_STATE",
           -4: "SWS_E_CUDA", -5: "SWS_E_TIMEOUT", -6: "SWS_E_UNSUPPORTED", -7: "SWS_E_WORKSPACE"}
@@ -80,6 +81,7 @@ _PROTOS = [
     ("sws_silu_mul", C.c_int, [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p]),
     ("sws_prefetch_layer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_test_bounded_wait", C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
+    ("sws_test_check_relayout", C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
     ("sws_wait_prefetch", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
@@ -201,6 +203,12 @@ def linear_noalloc(w: int, scales: int, rows: int, cols: int, x: int, m: int, y:
     """Decode linear with the library's fixed device scratch (no workspace)."""
     check(lib().sws_linear_noalloc(C.c_void_p(w), C.c_void_p(scales), rows, cols, C.c_void_p(x), m, C.c_void_p(y),
                                    C.c_void_p(stream or None)), "linear_noalloc")
+
+
+def test_check_relayout(plan: "Plan", layer: int, chunk_bytes: int) -> int:
+    """sws_test_check_relayout: the SWS_OPT_CHECK_BOUNDS check of the relayout's
+    copy segments against chunks of `chunk_bytes` (host only). Returns the code."""
+    return lib().sws_test_check_relayout(plan.handle, layer, chunk_bytes)
 
 
 def noalloc_status(clear: bool = False) -> int:

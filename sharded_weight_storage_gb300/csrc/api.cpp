@@ -159,6 +159,14 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s, bool ov
   }
   g.chunk_bytes = lp.chunk;
   g.dst = c->slot[slot];
+  if (check_bounds()) {  // slot[i*C : (i+1)*C] = chunk i, inside the slot's plan.slot_bytes
+    std::vector<CopySeg> segs;
+    for (int i = 0; i < g.n; ++i) segs.push_back(CopySeg{g.chunks[i], g.dst + (int64_t)i * lp.chunk, lp.chunk});
+    std::vector<Extent> srcs;
+    for (int i = 0; i < g.n; ++i) srcs.push_back({g.chunks[i], g.chunks[i] + lp.chunk});
+    const int rc = check_segments(segs, srcs, {Extent{g.dst, g.dst + p->slot_bytes}}, "gather");
+    if (rc != SWS_OK) return rc;
+  }
   if (g_gather_engine == SWS_GATHER_COPY_ENGINE) {  // slot[i*C : (i+1)*C] = chunk i, by the copy engines
     for (int i = 0; i < g.n; ++i) {
       cudaError_t e = cudaMemcpyAsync(g.dst + (int64_t)i * lp.chunk, g.chunks[i], (size_t)lp.chunk,
@@ -238,6 +246,11 @@ int stage_scales(sws_ctx* c, int32_t layer, cudaStream_t s) {
     if (e.scale_offset < 0 || e.scale_bytes == 0) continue;
     chunk_segments(e.scale_offset, e.scale_offset + e.scale_bytes, lp.chunk, chunks, nullptr,
                    c->ws + c->ws_scales + e.scale_stage, &segs);
+  }
+  if (check_bounds()) {  // chunks -> the workspace's staging area (its last bytes)
+    const int rc = check_segments(segs, chunk_extents(chunks, p->n_shards, lp.chunk),
+                                  {Extent{c->ws + c->ws_scales, c->ws + c->ws_bytes}}, "linear: scale staging");
+    if (rc != SWS_OK) return rc;
   }
   const cudaError_t ce = launch_relayout(segs, s);
   return ce == cudaSuccess ? SWS_OK : cuda_fail(ce, "linear: scale staging kernel");
@@ -912,6 +925,10 @@ int sws_set_option(int32_t option, int64_t value) {
     case SWS_OPT_HOST_WAIT_MS:
       if (value < 1 || value > 3600000) return fail(SWS_E_INVALID, "set_option: host wait %lld ms", (long long)value);
       g_host_wait_ms = (int)value;
+      return SWS_OK;
+    case SWS_OPT_CHECK_BOUNDS:
+      if (value != 0 && value != 1) return fail(SWS_E_INVALID, "set_option: check bounds %lld", (long long)value);
+      set_check_bounds(value != 0);
       return SWS_OK;
     case SWS_OPT_GATHER_ENGINE:
       if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE && value != SWS_GATHER_TMA_SHARED_SM)

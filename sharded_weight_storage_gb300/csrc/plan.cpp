@@ -67,6 +67,76 @@ void chunk_segments(int64_t g0, int64_t g1, int64_t c, void* const* chunks, cons
     g0 += len;
   }
 }
+
+namespace {
+bool g_check_bounds = false;
+}  // namespace
+bool check_bounds() { return g_check_bounds; }
+void set_check_bounds(bool on) { g_check_bounds = on; }
+
+std::vector<Extent> chunk_extents(void* const* chunks, int32_t n, int64_t c) {
+  std::vector<Extent> x;
+  for (int32_t i = 0; i < n; ++i) {
+    const uint8_t* b = static_cast<const uint8_t*>(chunks[i]);
+    x.push_back({b, b + c});
+  }
+  return x;
+}
+
+int check_segments(const std::vector<CopySeg>& segs, std::vector<Extent> srcs, std::vector<Extent> dsts,
+                   const char* what) {
+  auto by_lo = [](const Extent& a, const Extent& b) { return a.lo < b.lo; };
+  std::sort(srcs.begin(), srcs.end(), by_lo);
+  std::sort(dsts.begin(), dsts.end(), by_lo);
+  // [a, a + len) inside some extent: the last extent starting at or before a must reach a + len
+  auto inside = [&](const std::vector<Extent>& xs, const uint8_t* a, int64_t len) {
+    auto it = std::upper_bound(xs.begin(), xs.end(), Extent{a, a}, by_lo);
+    if (it == xs.begin()) return false;
+    --it;
+    return a >= it->lo && a + len <= it->hi;
+  };
+  for (size_t i = 0; i < segs.size(); ++i) {
+    const CopySeg& g = segs[i];
+    if (g.len <= 0) continue;
+    if (!inside(dsts, g.dst, g.len))
+      return fail(SWS_E_INVALID, "%s: copy segment %zu writes [%p, +%lld) outside its buffer", what, i,
+                  static_cast<void*>(g.dst), (long long)g.len);
+    if (g.src && !inside(srcs, g.src, g.len))
+      return fail(SWS_E_INVALID, "%s: copy segment %zu reads [%p, +%lld) outside its buffer", what, i,
+                  static_cast<const void*>(g.src), (long long)g.len);
+  }
+  return SWS_OK;
+}
+
+namespace {
+// The copy segments of sws_relayout for one layer, with the extents of the
+// row shards they read.
+void relayout_segments(const sws_plan* p, int32_t layer, const void* const* row_shards, void* const* chunks,
+                       std::vector<CopySeg>* segs, std::vector<Extent>* shard_extents) {
+  const LayerPlan& lp = p->layers[layer];
+  const int32_t n = p->n_shards;
+  const int64_t c = lp.chunk;
+  // Walk T once, cutting it into maximal runs that stay inside one chunk and
+  // one source (a row shard, or padding; with SWS_SCALES_IN_T the scale
+  // regions are written as zeros here and filled by sws_relayout_scales).
+  auto emit = [&](int64_t g0, int64_t g1, const uint8_t* src) {  // T bytes [g0, g1)
+    chunk_segments(g0, g1, c, chunks, src, nullptr, segs);
+  };
+  for (size_t k = 0; k < lp.sharded.size(); ++k) {
+    const EntryPlan& e = p->entries[lp.sharded[k]];
+    const int64_t per = e.bytes / n;  // bytes of one row shard
+    for (int32_t r = 0; r < n && per > 0; ++r) {
+      const uint8_t* sh = static_cast<const uint8_t*>(row_shards[k * n + r]);
+      emit(e.offset + r * per, e.offset + (r + 1) * per, sh);
+      shard_extents->push_back({sh, sh + per});
+    }
+    const int64_t end = e.offset + e.bytes;
+    const int64_t next = (k + 1 < lp.sharded.size()) ? p->entries[lp.sharded[k + 1]].offset : lp.total;
+    if (next > end) emit(end, next, nullptr);  // padding after the entry
+  }
+  if (lp.sharded.empty()) emit(0, lp.total, nullptr);
+}
+}  // namespace
 }  // namespace sws
 
 extern "C" {
@@ -201,27 +271,13 @@ int sws_relayout(const sws_plan* p, int32_t layer, const void* const* row_shards
     for (int32_t r = 0; r < n; ++r)
       if (p->entries[lp.sharded[k]].bytes > 0 && !row_shards[k * n + r])
         return fail(SWS_E_INVALID, "relayout: row shard %d of sharded entry %zu is NULL", r, k);
-  // Walk T once, cutting it into maximal runs that stay inside one chunk and
-  // one source (a row shard, or padding; with SWS_SCALES_IN_T the scale
-  // regions are written as zeros here and filled by sws_relayout_scales).
   std::vector<CopySeg> segs;
-  const int64_t c = lp.chunk;
-  auto emit = [&](int64_t g0, int64_t g1, const uint8_t* src) {  // T bytes [g0, g1)
-    chunk_segments(g0, g1, c, chunks, src, nullptr, &segs);
-  };
-  int64_t g = 0;
-  for (size_t k = 0; k < lp.sharded.size(); ++k) {
-    const EntryPlan& e = p->entries[lp.sharded[k]];
-    const int64_t per = e.bytes / n;  // bytes of one row shard
-    for (int32_t r = 0; r < n && per > 0; ++r)
-      emit(e.offset + r * per, e.offset + (r + 1) * per, static_cast<const uint8_t*>(row_shards[k * n + r]));
-    int64_t end = e.offset + e.bytes;
-    int64_t next = (k + 1 < lp.sharded.size()) ? p->entries[lp.sharded[k + 1]].offset : lp.total;
-    if (next > end) emit(end, next, nullptr);  // padding after the entry
-    g = next;
+  std::vector<Extent> shards;
+  relayout_segments(p, layer, row_shards, chunks, &segs, &shards);
+  if (check_bounds()) {
+    const int rc = check_segments(segs, shards, chunk_extents(chunks, n, lp.chunk), "relayout");
+    if (rc != SWS_OK) return rc;
   }
-  if (lp.sharded.empty()) emit(0, lp.total, nullptr);
-  (void)g;
   cudaError_t e = launch_relayout(segs, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "relayout kernel launch");
   return SWS_OK;
@@ -242,16 +298,43 @@ int sws_relayout_scales(const sws_plan* p, int32_t layer, const float* const* sc
   // Each rank holds the full (replicated) scale tensor and copies out the
   // bytes that fall into its window [i*C, (i+1)*C) of T.
   std::vector<CopySeg> segs;
+  std::vector<Extent> srcs;
   for (size_t k = 0; k < lp.all.size(); ++k) {
     const EntryPlan& e = p->entries[lp.all[k]];
     if (e.scale_offset < 0 || e.scale_bytes == 0) continue;
     if (!scales[k]) return fail(SWS_E_INVALID, "relayout_scales: entry %zu of layer %d has no scales", k, layer);
-    chunk_segments(e.scale_offset, e.scale_offset + e.scale_bytes, lp.chunk, chunks,
-                   reinterpret_cast<const uint8_t*>(scales[k]), nullptr, &segs);
+    const uint8_t* sc = reinterpret_cast<const uint8_t*>(scales[k]);
+    chunk_segments(e.scale_offset, e.scale_offset + e.scale_bytes, lp.chunk, chunks, sc, nullptr, &segs);
+    srcs.push_back({sc, sc + e.scale_bytes});
   }
   if (segs.empty()) return SWS_OK;
+  if (check_bounds()) {
+    const int rc = check_segments(segs, srcs, chunk_extents(chunks, p->n_shards, lp.chunk), "relayout_scales");
+    if (rc != SWS_OK) return rc;
+  }
   cudaError_t e = launch_relayout(segs, (cudaStream_t)stream);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "relayout_scales kernel launch");
+}
+
+int sws_test_check_relayout(const sws_plan* p, int32_t layer, int64_t chunk_bytes) {
+  if (!p) return fail(SWS_E_INVALID, "test_check_relayout: plan is NULL");
+  if (layer < 0 || layer >= (int32_t)p->layers.size())
+    return fail(SWS_E_INVALID, "test_check_relayout: layer %d", layer);
+  const LayerPlan& lp = p->layers[layer];
+  const int32_t n = p->n_shards;
+  // Stand-in addresses, never dereferenced: row shards and chunks 2^36 bytes
+  // apart (more than any of them holds), from 2^52 up.
+  auto at = [](uint64_t i) { return reinterpret_cast<uint8_t*>(((uint64_t)1 << 52) + (i << 36)); };
+  if ((lp.sharded.size() + 1) * (size_t)n >= ((size_t)1 << 14))
+    return fail(SWS_E_INVALID, "test_check_relayout: too many row shards for the stand-in addresses");
+  std::vector<const void*> shards(lp.sharded.size() * (size_t)n);
+  for (size_t i = 0; i < shards.size(); ++i) shards[i] = at(i);
+  std::vector<void*> chunks(n);
+  for (int32_t i = 0; i < n; ++i) chunks[i] = at(shards.size() + i);
+  std::vector<CopySeg> segs;
+  std::vector<Extent> srcs;
+  relayout_segments(p, layer, shards.data(), chunks.data(), &segs, &srcs);
+  return check_segments(segs, srcs, chunk_extents(chunks.data(), n, chunk_bytes), "relayout");
 }
 
 }  // extern "C"

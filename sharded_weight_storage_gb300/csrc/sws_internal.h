@@ -158,6 +158,20 @@ cudaError_t launch_relayout(const std::vector<CopySeg>& segs, cudaStream_t s);
 // nullptr with to_chunks fills the chunk bytes with zeros.
 void chunk_segments(int64_t g0, int64_t g1, int64_t c, void* const* chunks, const uint8_t* lin_src, uint8_t* lin_dst,
                     std::vector<CopySeg>* segs);
+// SWS_OPT_CHECK_BOUNDS: a buffer [lo, hi) that copy segments may read or write.
+struct Extent {
+  const uint8_t* lo;
+  const uint8_t* hi;
+};
+bool check_bounds();
+void set_check_bounds(bool on);
+// SWS_E_INVALID (naming `what` and the segment) if a segment reads outside
+// every extent of `srcs` (zero fills read nothing) or writes outside every
+// extent of `dsts`; SWS_OK otherwise.
+int check_segments(const std::vector<CopySeg>& segs, std::vector<Extent> srcs, std::vector<Extent> dsts,
+                   const char* what);
+// The extents of a layer's N chunks of c bytes.
+std::vector<Extent> chunk_extents(void* const* chunks, int32_t n, int64_t c);
 
 // Decode linears (m <= 64): a group of up to kMaxDecodeGroup linears that
 // share m runs as one launch. Slot path: each item's weight is a view `w`

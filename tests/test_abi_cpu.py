@@ -308,3 +308,45 @@ def test_host_wait_option_range(swslib):
         assert ei.value.code == S.E_INVALID
     S.set_option(S.OPT_HOST_WAIT_MS, 10000)
     assert S.lib().sws_noalloc_status(0, None) == S.E_INVALID
+
+
+def test_bounds_self_check_of_relayout_segments(swslib):
+    # SWS_OPT_CHECK_BOUNDS, host only: every copy segment of the relayout lies
+    # inside its row shard and its chunk of C bytes; checked against chunks
+    # 16 bytes too short (a planted mistake in the chunk size) it is refused,
+    # and against longer ones it passes.
+    from test_oracle_pins import read_padding_golden
+    import warnings
+    S = swslib
+    dt = {1: S.E4M3, 2: S.BF16, 4: S.F32}
+    plans = []
+    for n, ents, total, chunk in read_padding_golden().values():
+        plans.append(([(0, dt[e], r, c) for (_, r, c, e, _) in ents], n))
+    rng = np.random.default_rng(77)
+    for n in (1, 2, 3, 7, 16):
+        for _ in range(6):
+            ents = []
+            for _ in range(int(rng.integers(1, 7))):
+                rows = int(rng.integers(1, 5)) * n if rng.random() < 0.8 else int(rng.integers(1, 40))
+                ents.append((int(rng.integers(0, 3)), dt[int(rng.choice([1, 2, 4]))], rows, int(rng.integers(1, 90))))
+            plans.append((ents, n))
+    checked = 0
+    for ents, n in plans:
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            plan = S.Plan(ents, n)
+        for l in range(plan.info()[0]):
+            total, chunk, _ = plan.layer(l)
+            assert S.test_check_relayout(plan, l, chunk) == S.OK
+            assert S.test_check_relayout(plan, l, chunk + 16) == S.OK
+            if total > 0:
+                assert S.test_check_relayout(plan, l, chunk - 16) == S.E_INVALID
+                assert "outside its buffer" in S.last_error()
+                checked += 1
+    assert checked >= 20
+    for bad in (2, -1):
+        with pytest.raises(S.SwsError) as ei:
+            S.set_option(S.OPT_CHECK_BOUNDS, bad)
+        assert ei.value.code == S.E_INVALID
+    S.set_option(S.OPT_CHECK_BOUNDS, 1)
+    S.set_option(S.OPT_CHECK_BOUNDS, 0)

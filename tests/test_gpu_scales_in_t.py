@@ -202,3 +202,35 @@ def test_shared_expert_layer_full_size_with_scales_in_t(S):
             torch.cuda.synchronize()
             assert_close(bf16_tensor_to_f64(y)[:, sel], ref, f"{w.entries[j].name} src {src}")
     assert st.ctx.status() == 0
+
+
+@pytest.mark.parametrize("case", [STRADDLE, MIXED], ids=["straddle", "mixed"])
+def test_bounds_self_check_passes_every_copy_of_the_path(S, case):
+    # SWS_OPT_CHECK_BOUNDS on for the relayout, the scale relayout, the
+    # gathers and the chunk-map scale staging: every segment the library
+    # builds stays inside its buffers, so all calls go through, and the
+    # results are the oracle's.
+    shapes, n = case
+    rng = np.random.default_rng(91)
+    codes, scales = _weights(rng, shapes)
+    S.set_option(S.OPT_CHECK_BOUNDS, 1)
+    try:
+        st = _build(S, shapes, n, codes, scales)
+        for slot in (0, 1):
+            st.ctx.gather_to_slot(0, slot, 0)
+        torch.cuda.synchronize()
+        plan = _oracle(shapes, n, codes, scales)
+        t = O.pack(plan, 0, {j: codes[j] for j in range(len(shapes))}, scales=scales)
+        for slot in (0, 1):
+            assert np.array_equal(st.slots[slot][:t.size].cpu().numpy(), t)
+        m = 8
+        for j in range(len(shapes)):
+            x = WL.draw_x(92, j, m, shapes[j][3]).cuda()
+            for src in (S.SRC_SLOT0, S.SRC_FUSED):
+                y = torch.empty((m, shapes[j][2]), dtype=torch.bfloat16, device="cuda")
+                st.ctx.linear(j, src, x.data_ptr(), m, y.data_ptr(), 0)
+                torch.cuda.synchronize()
+                assert_close(bf16_tensor_to_f64(y), _ref(shapes, j, x, codes, scales), f"entry {j} src {src}")
+        assert st.ctx.status() == 0
+    finally:
+        S.set_option(S.OPT_CHECK_BOUNDS, 0)
