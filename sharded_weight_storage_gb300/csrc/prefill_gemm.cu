@@ -79,13 +79,13 @@ constexpr int kPairABytes = (kPairM / 2) * kBK;         // 16 KB
 constexpr int kPairBBytes = (kPairN / 2) * kBK;         // 16 KB
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairEpiWarps = 16;
-constexpr int kPairThreads = (2 + kPairEpiWarps) * 32;
+constexpr int kPairThreads = (3 + kPairEpiWarps) * 32;  // with a scale warp
 
 constexpr int kTmemCols = 512;
 
-// Scale-factor ring: each promotion thread fetches ex[m, kb] (and lane 0 of
-// each warp s_w[nb, kb]) kScaleDepth slabs ahead with cp.async into shared
-// memory, so no register waits on a global load.
+// Slabs of scale factors kept in flight ahead of the promotion warps, and the
+// shared memory the one-CTA kernel sets aside for them (its output staging
+// follows this space).
 constexpr int kScaleDepth = 8;
 __host__ __device__ constexpr int scale_ring_bytes(int epi_warps) { return kScaleDepth * (epi_warps * 32 + epi_warps) * 4; }
 // Factor ring of the one-CTA FP8 kernel, filled by its scale warp: per slab
@@ -99,7 +99,7 @@ static_assert(kFactorRingBytes <= scale_ring_bytes(kEpiWarps), "factor ring fits
 constexpr int kOutChunk = 32;
 constexpr int kOutWarpBytes = 32 * kOutChunk * 2;
 constexpr int kSmemBytes = kStages * kStageBytes + scale_ring_bytes(kEpiWarps) + kEpiWarps * kOutWarpBytes + 1024;
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + scale_ring_bytes(kPairEpiWarps) + 1024;
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + kScaleDepth * (kBM + 2) * 4 + 1024;
 
 struct PrefillParams {
   CUtensorMap tmap_x;  // xq [M, K] u8
@@ -260,85 +260,6 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, uint64_t ff, uint32_t
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
 }
 
-// 4-byte asynchronous global -> shared copy (completion per thread through
-// cp.async groups).
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dev::smem_addr(dst)), "l"(src) : "memory");
-}
-
-// One promotion thread's share of a tile: output row m, columns
-// n0 .. n0+kCols-1 (TMEM lane and column `lane_base` within each slab buffer,
-// buffers kBufCols columns apart, kNBuf of them used in turn). For each slab
-// it waits for the slab buffer, adds it into acc with the factor
-// ex[m, kb] * s_w[n0/128, kb], and releases the buffer (once per warp) on
-// `release[buf]` (this CTA's barrier, or the first CTA's for a pair).
-// TMEM is read kLd (16 or 32) columns per load. Returns false if a wait ran out.
-template <bool kPair, int kEpiW, int kCols, int kNBuf, int kBufCols, int kLd>
-__device__ __forceinline__ bool promote_tile(const PrefillParams& p, float (&acc)[kCols], int64_t m, int64_t n0,
-                                             uint32_t lane_base, uint64_t* tfull, const uint32_t (&release)[kNBuf],
-                                             float* ring_ex, float* ring_sw, int64_t& it, int lane,
-                                             volatile int* s_abort) {
-  const int G = p.kslabs;
-  const int64_t sw_rows = (p.N + 127) / 128, nb = n0 / 128;
-  const float* exr = p.ex + (m < p.M ? m : 0) * G;
-  const float* swr = p.sw + (nb < sw_rows ? nb : 0) * G;
-  const bool nb_live = nb < sw_rows, live = m < p.M && nb_live;
-  // ring_ex[d * stride] / ring_sw[d] hold slab kb's factors for d = kb % kScaleDepth
-  // (ring_sw is the warp's: all its lanes share nb, lane 0 fetches it).
-  constexpr int kStride = kEpiW * 32;
-  auto fetch = [&](int kb) {
-    if (kb < G) {
-      const int d = kb % kScaleDepth;
-      if (live) cp_async4(ring_ex + d * kStride, exr + kb);
-      if (lane == 0 && nb_live) cp_async4(ring_sw + d, swr + kb);
-    }
-    dev::cp_async_commit();
-  };
-#pragma unroll
-  for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
-  for (int d = 0; d < kScaleDepth; ++d) fetch(d);
-  bool ok = true;
-  for (int kb = 0; kb < G && ok; ++kb) {
-    const int buf = (int)(it % kNBuf);
-    ok = dev::mbar_wait(&tfull[buf], (uint32_t)((it / kNBuf) & 1), kWaitLimitNs);
-    if (!ok) {
-      set_abort(p, s_abort);
-      break;
-    }
-    tc_fence_after();
-    dev::cp_async_wait<kScaleDepth - 1>();  // slab kb's factors have landed
-    __syncwarp();
-    const int d = kb % kScaleDepth;
-    const float fk = live ? ring_ex[d * kStride] * ring_sw[d] : 0.f;
-    uint64_t ff;  // (fk, fk) for the packed FMAs
-    asm("mov.b64 %0, {%1, %1};" : "=l"(ff) : "f"(fk));
-    __syncwarp();  // every lane has read slot d before lane 0 refills it
-    fetch(kb + kScaleDepth);
-#pragma unroll
-    for (int c = 0; c < kCols / kLd; ++c) {
-      uint32_t v[kLd];
-      if constexpr (kLd == 32)
-        tmem_ld32(lane_base + buf * kBufCols + c * kLd, v);
-      else
-        tmem_ld16(lane_base + buf * kBufCols + c * kLd, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < kLd; i += 2) fma2(acc[c * kLd + i], acc[c * kLd + i + 1], ff, v[i], v[i + 1]);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      if (kPair)  // the first CTA's barrier, through its cluster address
-        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(release[buf]) : "memory");
-      else
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(release[buf]) : "memory");
-    }
-    ++it;
-  }
-  dev::cp_async_wait<0>();  // no copy into the ring outlives the tile
-  return ok;
-}
-
 // Row m, columns n0 .. n0+kCols-1 of Y as bf16 (round to nearest even).
 template <int kCols>
 __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&acc)[kCols], int64_t m, int64_t n0) {
@@ -367,17 +288,24 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const float (&
   }
 }
 
-// One promotion thread's share of a tile in the one-CTA kernel: as
-// promote_tile, with each slab's two factors taken from the factor ring that
-// the scale warp fills (slot it % kScaleDepth: fslot_full says it is filled,
-// fslot_empty takes one arrival per promotion warp once read). `g` selects the
-// tile's 128-column block (its weight-scale row).
-template <int kCols>
+// One promotion thread's share of a tile: TMEM lane `row` of the tile, kCols
+// columns from `lane_base` within each slab buffer (two buffers, kBN columns
+// apart, used in turn). For each K slab kb it waits for the slab buffer and
+// for the slab's factors in the ring the scale warp fills (slot
+// it % kScaleDepth: fslot_full says it is filled, fslot_empty takes one
+// arrival per promotion warp once read), adds the buffer into acc scaled by
+// ex[m, kb] * s_w[nb, kb], and releases the buffer once per warp. `g` is the
+// warp's kCols-column group of the tile; release0 is the address of the first
+// slab buffer's empty barrier (the second's follows it), this CTA's or, for a
+// pair, the first CTA's through its cluster address. Returns false if a wait
+// ran out.
+template <int kCols, bool kPair = false>
 __device__ __forceinline__ bool promote_tile_ring(const PrefillParams& p, float (&acc)[kCols], int row, int g,
-                                                  uint32_t lane_base, uint64_t* tfull, uint64_t* tempty,
+                                                  uint32_t lane_base, uint64_t* tfull, uint32_t release0,
                                                   const float* ring, uint64_t* fslot_full, uint64_t* fslot_empty,
                                                   int64_t& it, int lane, volatile int* s_abort) {
   const int G = p.kslabs;
+  const int nbi = g * kCols / 128;  // the tile's 128-column block of these columns
 #pragma unroll
   for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
   for (int kb = 0; kb < G; ++kb) {
@@ -389,7 +317,7 @@ __device__ __forceinline__ bool promote_tile_ring(const PrefillParams& p, float 
     }
     tc_fence_after();
     const float* slot = ring + d * kFactorSlot;
-    const float fk = slot[row] * slot[kBM + g];
+    const float fk = slot[row] * slot[kBM + nbi];
     __syncwarp();
     if (lane == 0) dev::mbar_arrive(&fslot_empty[d]);
     uint64_t ff;  // (fk, fk) for the packed FMAs
@@ -404,7 +332,13 @@ __device__ __forceinline__ bool promote_tile_ring(const PrefillParams& p, float 
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) dev::mbar_arrive(&tempty[buf]);
+    if (lane == 0) {
+      const uint32_t rel = release0 + 8u * (uint32_t)buf;  // the two slab buffers' barriers are adjacent
+      if (kPair)  // the first CTA's barrier, through its cluster address
+        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(rel) : "memory");
+      else
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(rel) : "memory");
+    }
     ++it;
   }
   return true;
@@ -596,8 +530,8 @@ __global__ void __launch_bounds__(kFp8Threads, 1) prefill_kernel(const __grid_co
       const int64_t m = (int64_t)mt * kBM + row;
       const int64_t n0 = (int64_t)nt * kBN + g * kCols;
       float acc[kCols];
-      if (!promote_tile_ring<kCols>(p, acc, row, g, lane_base, tfull, tempty, ring, ffull, fempty, it, lane,
-                                    &s_abort))
+      if (!promote_tile_ring<kCols>(p, acc, row, g, lane_base, tfull, dev::smem_addr(&tempty[0]), ring, ffull,
+                                    fempty, it, lane, &s_abort))
         break;
       store_rows_staged<kCols>(p, acc, m - lane, n0, lane, stage);
     }
@@ -625,6 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   constexpr int kNBuf = kTmemCols / kPairN;  // 2 slab buffers
   extern __shared__ uint8_t dsm[];
   __shared__ __align__(8) uint64_t full[kPairStages], empty[kPairStages], tfull[kNBuf], tempty[kNBuf], mdone;
+  __shared__ __align__(8) uint64_t ffull[kScaleDepth], fempty[kScaleDepth];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
@@ -643,6 +578,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     for (int b = 0; b < kNBuf; ++b) {
       dev::mbar_init(&tfull[b], 1);
       dev::mbar_init(&tempty[b], 2 * kPairEpiWarps);
+    }
+    for (int d = 0; d < kScaleDepth; ++d) {
+      dev::mbar_init(&ffull[d], 32);  // every lane of this CTA's scale warp
+      dev::mbar_init(&fempty[d], kPairEpiWarps);
     }
     dev::mbar_init(&mdone, 1);
     dev::fence_mbar_init();
@@ -722,6 +661,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         dev::mbar_wait(&mdone, 0, kWaitLimitNs);
       }
     }
+  } else if (warp == 2 + kPairEpiWarps) {
+    // ---- scale warp (both CTAs): this CTA's factors into its ring ------------
+    float* ring = reinterpret_cast<float*>(smem + kPairStages * kPairStageBytes);
+    const int64_t sw_rows = (p.N + 127) / 128;
+    int64_t it = 0;
+    for (int64_t tile = first; tile < tiles && !s_abort; tile += stride) {
+      const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
+      const int64_t m0 = (int64_t)mt * kPairM + (int64_t)rank * (kPairM / 2) + lane * 4;
+      const int64_t nb0 = (int64_t)nt * (kPairN / 128);
+      bool ok = true;
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const int d = (int)(it % kScaleDepth);
+        if (!dev::mbar_wait(&fempty[d], (uint32_t)(((it / kScaleDepth) & 1) ^ 1), kWaitLimitNs)) {
+          set_abort(p, &s_abort);
+          ok = false;
+          break;
+        }
+        float* slot = ring + d * kFactorSlot;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) slot[lane * 4 + r] = m0 + r < p.M ? __ldg(p.ex + (m0 + r) * G + kb) : 0.f;
+        if (lane < 2) slot[kBM + lane] = nb0 + lane < sw_rows ? __ldg(p.sw + (nb0 + lane) * G + kb) : 0.f;
+        dev::mbar_arrive(&ffull[d]);  // each lane, after its own stores
+      }
+      if (!ok) break;
+    }
   } else {
     // ---- promotion and output (both CTAs): 16 warps, 64 columns each ------------
     constexpr int kCols = kPairN / (kPairEpiWarps / 4);
@@ -729,20 +693,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int g = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + g * kCols;
-    uint32_t release[kNBuf];
-#pragma unroll
-    for (int b = 0; b < kNBuf; ++b) release[b] = cluster_addr(&tempty[b], 0);
-    float* ring = reinterpret_cast<float*>(smem + kPairStages * kPairStageBytes);
-    float* ring_ex = ring + (threadIdx.x - 64);
-    float* ring_sw = ring + kScaleDepth * kPairEpiWarps * 32 + (warp - 2) * kScaleDepth;
+    const float* ring = reinterpret_cast<const float*>(smem + kPairStages * kPairStageBytes);
     int64_t it = 0;
     for (int64_t tile = first; tile < tiles && !s_abort; tile += stride) {
       const int32_t mt = (int32_t)(tile % p.m_tiles), nt = (int32_t)(tile / p.m_tiles);
       const int64_t m = (int64_t)mt * kPairM + (int64_t)rank * (kPairM / 2) + row;
       const int64_t n0 = (int64_t)nt * kPairN + g * kCols;
       float acc[kCols];
-      if (!promote_tile<true, kPairEpiWarps, kCols, kNBuf, kPairN, 16>(p, acc, m, n0, lane_base, tfull, release,
-                                                                       ring_ex, ring_sw, it, lane, &s_abort))
+      if (!promote_tile_ring<kCols, true>(p, acc, row, g, lane_base, tfull, cluster_addr(&tempty[0], 0), ring,
+                                          ffull, fempty, it, lane, &s_abort))
         break;
       store_row<kCols>(p, acc, m, n0);
     }
