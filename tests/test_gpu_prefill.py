@@ -179,3 +179,36 @@ def test_prefill_full_size_sampled_rows(S, kernel, m):
         ref, _ = _ref_quantised(x, layers[0].codes[j], layers[0].scales[j], rows=sel)
         assert_close(bf16_tensor_to_f64(y)[sel], ref, f"entry {j} (sampled rows)")
     assert st.ctx.status() == 0
+
+
+@pytest.mark.parametrize("m", [1000, 2048])
+def test_layer_equals_linears_alone_bit_for_bit(S, m):
+    # A prefill layer of the workload's full-size linears (layer_linears: the
+    # next linear's activations quantised on the side stream while the
+    # previous GEMM runs, two buffers used in turn) against each linear run
+    # alone: the quantiser is exact and the GEMM deterministic, so every
+    # output must be equal; m = 1000 ends rows in a partial tile. Sampled rows
+    # must meet the oracle.
+    w = WL.PREFILL
+    ents = workload_entries(w, 1)
+    layers = draw_layers(WL.scaled_workload(w, n_layers=1), 1)
+    st = build_stack(S, ents, w.n_shards, layers, max_m=m)
+    st.ctx.gather_to_slot(0, 0, 0)
+    xs = [WL.draw_x(w.key, j, m, c) for j, (_, r, c) in enumerate(ents)]
+    xd = [x.cuda() for x in xs]
+    ys = [torch.full((m, r), float("nan"), dtype=torch.bfloat16, device="cuda") for (_, r, c) in ents]
+    rng = np.random.default_rng(77 + m)
+    sel = np.unique(np.concatenate([[0, m - 1], rng.choice(m, size=24, replace=False)]))
+    for rep in range(2):  # twice: the second call reuses buffers the first one wrote
+        st.ctx.layer_linears(0, S.SRC_SLOT0, [x.data_ptr() for x in xd], [y.data_ptr() for y in ys], m, 0)
+        torch.cuda.synchronize()
+        assert st.ctx.status() == 0
+        for j, (_, r, c) in enumerate(ents):
+            alone = torch.empty((m, r), dtype=torch.bfloat16, device="cuda")
+            st.ctx.linear(j, S.SRC_SLOT0, xd[j].data_ptr(), m, alone.data_ptr(), 0)
+            torch.cuda.synchronize()
+            assert torch.equal(ys[j].view(torch.int16), alone.view(torch.int16)), f"rep {rep} entry {j}"
+    for j, (_, r, c) in enumerate(ents):
+        ref, _ = _ref_quantised(xs[j], layers[0].codes[j], layers[0].scales[j], rows=sel)
+        assert_close(bf16_tensor_to_f64(ys[j])[sel], ref, f"entry {j} (sampled rows)")
+    assert st.ctx.status() == 0
