@@ -434,6 +434,8 @@ int32_t sws_trace_count(const sws_ctx* ctx);
  * mma.sync launch is one.
  * Both prefill kernels compute the same sums in the same slab order per output
  * element and give bit-identical results.
+ * An option may be set from any thread; a call running at the same time on
+ * another thread sees its old value or its new one.
  * SWS_E_INVALID for an unknown option or value. */
 int sws_set_option(int32_t option, int64_t value);
 

@@ -23,22 +23,25 @@ using namespace sws;
 
 namespace sws {
 
+// Process-wide options are atomics: a thread may set one while another is
+// inside a call, which then sees the old value or the new one.
 namespace {
-int g_host_wait_ms = 10000;  // SWS_OPT_HOST_WAIT_MS
+std::atomic<int> g_host_wait_ms{10000};  // SWS_OPT_HOST_WAIT_MS
 }
 
-int host_wait_ms() { return g_host_wait_ms; }
+int host_wait_ms() { return g_host_wait_ms.load(std::memory_order_relaxed); }
 
 int wait_event_deadline(cudaEvent_t ev, const char* what) {
   const auto t0 = std::chrono::steady_clock::now();
-  const auto limit = std::chrono::milliseconds(g_host_wait_ms);
+  const int wait_ms = host_wait_ms();
+  const auto limit = std::chrono::milliseconds(wait_ms);
   for (int spin = 0;; ++spin) {
     const cudaError_t e = cudaEventQuery(ev);
     if (e == cudaSuccess) return SWS_OK;
     if (e != cudaErrorNotReady) return cuda_fail(e, what);
     if (std::chrono::steady_clock::now() - t0 > limit)
       return fail(SWS_E_TIMEOUT, "%s: the device had not reached the event after %d ms (host wait limit)", what,
-                  g_host_wait_ms);
+                  wait_ms);
     if (spin > 64) std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
 }
@@ -67,9 +70,10 @@ int device_sync_deadline(int device, const char* what) {
     return fail(SWS_E_INVALID, "%s: could not start the wait thread", what);
   }
   std::unique_lock<std::mutex> lock(st->mu);
-  if (!st->cv.wait_for(lock, std::chrono::milliseconds(g_host_wait_ms), [&] { return st->done; }))
+  const int wait_ms = host_wait_ms();
+  if (!st->cv.wait_for(lock, std::chrono::milliseconds(wait_ms), [&] { return st->done; }))
     return fail(SWS_E_TIMEOUT, "%s: the device had not finished its queued work after %d ms (host wait limit)", what,
-                g_host_wait_ms);
+                wait_ms);
   return st->err == cudaSuccess ? SWS_OK : cuda_fail(st->err, what);
 }
 
@@ -139,7 +143,7 @@ int ensure_events(sws_ctx* c, size_t n) {
   return SWS_OK;
 }
 
-int g_gather_engine = SWS_GATHER_TMA;
+std::atomic<int> g_gather_engine{SWS_GATHER_TMA};
 
 // overlap_prev: launch the kernel with programmatic stream serialisation (see
 // launch_gather); only the stand-alone gather call asks for it. Inside
@@ -167,7 +171,8 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s, bool ov
     const int rc = check_segments(segs, srcs, {Extent{g.dst, g.dst + p->slot_bytes}}, "gather");
     if (rc != SWS_OK) return rc;
   }
-  if (g_gather_engine == SWS_GATHER_COPY_ENGINE) {  // slot[i*C : (i+1)*C] = chunk i, by the copy engines
+  const int engine = g_gather_engine.load(std::memory_order_relaxed);
+  if (engine == SWS_GATHER_COPY_ENGINE) {  // slot[i*C : (i+1)*C] = chunk i, by the copy engines
     for (int i = 0; i < g.n; ++i) {
       cudaError_t e = cudaMemcpyAsync(g.dst + (int64_t)i * lp.chunk, g.chunks[i], (size_t)lp.chunk,
                                       cudaMemcpyDeviceToDevice, s);
@@ -178,7 +183,7 @@ int gather_impl(sws_ctx* c, int32_t layer, int32_t slot, cudaStream_t s, bool ov
   g.status = status_word(c);
   g.trace = next_trace(c);
   g.tag = (kTraceGather << 56) | ((uint64_t)layer << 32) | (uint64_t)(uint32_t)slot;
-  g.shared_sm = g_gather_engine == SWS_GATHER_TMA_SHARED_SM;
+  g.shared_sm = engine == SWS_GATHER_TMA_SHARED_SM;
   g.overlap_prev = overlap_prev;
   cudaError_t e = launch_gather(g, s);
   return e == cudaSuccess ? SWS_OK : cuda_fail(e, "gather kernel launch");
@@ -924,7 +929,7 @@ int sws_set_option(int32_t option, int64_t value) {
       return SWS_OK;
     case SWS_OPT_HOST_WAIT_MS:
       if (value < 1 || value > 3600000) return fail(SWS_E_INVALID, "set_option: host wait %lld ms", (long long)value);
-      g_host_wait_ms = (int)value;
+      g_host_wait_ms.store((int)value, std::memory_order_relaxed);
       return SWS_OK;
     case SWS_OPT_CHECK_BOUNDS:
       if (value != 0 && value != 1) return fail(SWS_E_INVALID, "set_option: check bounds %lld", (long long)value);
@@ -933,7 +938,7 @@ int sws_set_option(int32_t option, int64_t value) {
     case SWS_OPT_GATHER_ENGINE:
       if (value != SWS_GATHER_TMA && value != SWS_GATHER_COPY_ENGINE && value != SWS_GATHER_TMA_SHARED_SM)
         return fail(SWS_E_INVALID, "set_option: gather engine %lld", (long long)value);
-      g_gather_engine = (int)value;
+      g_gather_engine.store((int)value, std::memory_order_relaxed);
       return SWS_OK;
     default:
       return fail(SWS_E_INVALID, "set_option: unknown option %d", option);

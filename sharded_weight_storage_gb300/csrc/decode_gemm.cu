@@ -634,17 +634,18 @@ int build_params(DecodeParams& p, const DecodeGroup& g, int64_t* row_blocks, boo
 }  // namespace
 
 namespace {
-int g_decode_kernel = kDecodeAuto;
+std::atomic<int> g_decode_kernel{kDecodeAuto};  // SWS_OPT_DECODE_KERNEL
 }
 
-void set_decode_kernel(int k) { g_decode_kernel = k; }
+void set_decode_kernel(int k) { g_decode_kernel.store(k, std::memory_order_relaxed); }
 
 // The tcgen05 kernel streams the weights at the HBM rate for every m <= 64
 // (its MMAs and activation split are small next to the weight bytes); the
 // mma.sync kernel serves chunk-map launches beyond the tcgen05 segment tables
 // and can be selected for comparison.
 int decode_kernel_for(int64_t m) {
-  if (g_decode_kernel != kDecodeAuto) return g_decode_kernel;
+  const int k = g_decode_kernel.load(std::memory_order_relaxed);
+  if (k != kDecodeAuto) return k;
   (void)m;
   return kDecodeTc;
 }

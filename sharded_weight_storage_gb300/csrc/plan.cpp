@@ -69,10 +69,10 @@ void chunk_segments(int64_t g0, int64_t g1, int64_t c, void* const* chunks, cons
 }
 
 namespace {
-bool g_check_bounds = false;
+std::atomic<bool> g_check_bounds{false};  // SWS_OPT_CHECK_BOUNDS
 }  // namespace
-bool check_bounds() { return g_check_bounds; }
-void set_check_bounds(bool on) { g_check_bounds = on; }
+bool check_bounds() { return g_check_bounds.load(std::memory_order_relaxed); }
+void set_check_bounds(bool on) { g_check_bounds.store(on, std::memory_order_relaxed); }
 
 std::vector<Extent> chunk_extents(void* const* chunks, int32_t n, int64_t c) {
   std::vector<Extent> x;

@@ -919,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_16_kernel(const __grid_co
   }
 }
 
-int g_prefill_kernel = kPrefillAuto;
+std::atomic<int> g_prefill_kernel{kPrefillAuto};  // SWS_OPT_PREFILL_KERNEL
 
 // Clusters of two prefill_pair_kernel CTAs that fit on the current device at
 // once (0 if none; cached per device).
@@ -949,7 +949,7 @@ int pair_cluster_capacity() {
 
 }  // namespace
 
-void set_prefill_kernel(int k) { g_prefill_kernel = k; }
+void set_prefill_kernel(int k) { g_prefill_kernel.store(k, std::memory_order_relaxed); }
 
 int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   if (a.m <= 0 || a.rows <= 0) return SWS_OK;
@@ -957,7 +957,7 @@ int launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     return fail(SWS_E_UNSUPPORTED, "prefill: cols=%lld is not a positive multiple of 128", (long long)a.cols);
   if (!aligned16(a.w) || !aligned16(a.xq) || !aligned16(a.y) || !aligned16(a.ex) || !aligned16(a.scales))
     return fail(SWS_E_ALIGN, "prefill: pointer not 16-byte aligned");
-  const int choice = g_prefill_kernel;
+  const int choice = g_prefill_kernel.load(std::memory_order_relaxed);
   const int clusters = choice == kPrefillPair ? pair_cluster_capacity() : 0;
   if (choice == kPrefillPair && clusters <= 0)
     return fail(SWS_E_UNSUPPORTED, "prefill: no cluster of two CTAs fits on this device");
