@@ -446,6 +446,20 @@ int sws_set_option(int32_t option, int64_t value);
  * its buffers (chunk_bytes >= the plan's C), SWS_E_INVALID otherwise. */
 int sws_test_check_relayout(const sws_plan* plan, int32_t layer, int64_t chunk_bytes);
 
+/* Test hook of the decode launch's split-K bookkeeping (host only, no device
+ * memory): lays out the units of `n_linears` linears (rows[i] x cols[i],
+ * elem_bytes 1 for E4M3 or 2 for BF16/F16 weights) as a tcgen05 decode launch
+ * from slot views does - each linear's 256-row blocks in turn, each block
+ * ceil(cols * elem_bytes / 128) K slabs, CTA c of `grid` taking units
+ * [c*U/grid, (c+1)*U/grid) - and writes the settle tasks that launch would
+ * run: one per row block that more than one CTA works on, 6 int32 each
+ * (linear, row block, rows, first CTA, last CTA, partial slot of the first
+ * CTA: 2c for its first run, 2c+1 for its last). Returns the number of tasks
+ * (at most `capacity`), or SWS_E_INVALID for 1 <= n_linears <= 8,
+ * cols % 16 == 0 or 1 <= grid <= min(U, 256) not holding. */
+int sws_test_settle_plan(int32_t n_linears, const int64_t* rows, const int64_t* cols, int32_t elem_bytes,
+                         int64_t grid, int32_t* out, int32_t capacity);
+
 /* Failure-detection check: one kernel waits, with the bounded wait every
  * kernel of the library uses, on a barrier that nothing arrives at; after
  * limit_ns (0..1e8) it records SWS_E_TIMEOUT in the context's status word (as

@@ -11,7 +11,8 @@ from ._lib import (BF16, E4M3, F16, E_ALIGN, E_CUDA, E_INVALID, E_STATE, E_TIMEO
                    OPT_DECODE_KERNEL, DECODE_AUTO, DECODE_MMA, DECODE_TCGEN05, OPT_PREFILL_KERNEL,
                    PREFILL_AUTO, PREFILL_SINGLE, PREFILL_PAIR, OPT_GATHER_ENGINE, GATHER_TMA, GATHER_COPY_ENGINE,
                    GATHER_TMA_SHARED_SM, OPT_HOST_WAIT_MS, OPT_CHECK_BOUNDS, SCALES_IN_T, relayout_scales, linear_noalloc,
-                   noalloc_status, test_bounded_wait_noalloc, test_check_relayout)
+                   noalloc_status, test_bounded_wait_noalloc, test_check_relayout,
+                   test_settle_plan)
 
 lib()  # load now: no silent fallback when the extension is missing
 
@@ -22,4 +23,4 @@ __all__ = ["Plan", "Ctx", "Graph", "SwsError", "plan_create", "relayout", "works
            "DECODE_MMA", "DECODE_TCGEN05", "OPT_PREFILL_KERNEL", "PREFILL_AUTO", "PREFILL_SINGLE",
            "PREFILL_PAIR", "OPT_GATHER_ENGINE", "GATHER_TMA", "GATHER_COPY_ENGINE", "GATHER_TMA_SHARED_SM",
            "OPT_HOST_WAIT_MS", "OPT_CHECK_BOUNDS", "SCALES_IN_T", "relayout_scales", "linear_noalloc", "noalloc_status",
-           "test_bounded_wait_noalloc", "test_check_relayout"]
+           "test_bounded_wait_noalloc", "test_check_relayout", "test_settle_plan"]

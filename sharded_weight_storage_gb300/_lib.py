@@ -82,6 +82,8 @@ _PROTOS = [
     ("sws_prefetch_layer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_test_bounded_wait", C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
     ("sws_test_check_relayout", C.c_int, [C.c_void_p, C.c_int32, C.c_int64]),
+    ("sws_test_settle_plan", C.c_int, [C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64), C.c_int32,
+                                       C.c_int64, C.POINTER(C.c_int32), C.c_int32]),
     ("sws_wait_prefetch", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p]),
     ("sws_ctx_status", C.c_int, [C.c_void_p, C.c_int32]),
     ("sws_trace_begin", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
@@ -209,6 +211,20 @@ def test_check_relayout(plan: "Plan", layer: int, chunk_bytes: int) -> int:
     """sws_test_check_relayout: the SWS_OPT_CHECK_BOUNDS check of the relayout's
     copy segments against chunks of `chunk_bytes` (host only). Returns the code."""
     return lib().sws_test_check_relayout(plan.handle, layer, chunk_bytes)
+
+
+def test_settle_plan(rows: Sequence[int], cols: Sequence[int], elem_bytes: int, grid: int) -> list:
+    """sws_test_settle_plan: the settle tasks of a tcgen05 decode launch over
+    these linears on `grid` CTAs (host only), as tuples (linear, row block,
+    rows, first CTA, last CTA, first CTA's partial slot)."""
+    n = len(rows)
+    cap = 256
+    out = (C.c_int32 * (6 * cap))()
+    r = (C.c_int64 * n)(*rows)
+    c = (C.c_int64 * n)(*cols)
+    k = lib().sws_test_settle_plan(n, r, c, elem_bytes, grid, out, cap)
+    check(k if k < 0 else 0, "test_settle_plan")
+    return [tuple(out[6 * t:6 * t + 6]) for t in range(k)]
 
 
 def noalloc_status(clear: bool = False) -> int:

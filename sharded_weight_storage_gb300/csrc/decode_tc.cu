@@ -54,7 +54,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 #include "decode_common.cuh"
 #include "ptx.cuh"
@@ -1000,3 +1002,71 @@ int64_t tc_slot_bytes(int64_t m) { return (int64_t)kTcRows * tc_n_pad(m) * 4; }
 }  // namespace dec
 
 }  // namespace sws
+
+// Test hook (host only): the settle tasks of a tcgen05 decode launch from
+// slot views of the given linears on `grid` CTAs. The unit space is laid out
+// as a slot-view launch lays it out (each linear's 256-row blocks in turn,
+// ceil(cols * elem_bytes / 128) K slabs each) and settle_plan runs on it;
+// the outputs are stand-ins in a host array, so each task's Y pointer tells
+// its linear and row block. Writes 6 values per task (linear, row block,
+// rows, first CTA, last CTA, partial slot of the first CTA) and returns the
+// number of tasks, or a negative status.
+extern "C" int sws_test_settle_plan(int32_t n_linears, const int64_t* rows, const int64_t* cols, int32_t elem_bytes,
+                                    int64_t grid, int32_t* out, int32_t capacity) {
+  using namespace sws;
+  using namespace sws::dec;
+  if (n_linears < 1 || n_linears > kMaxDecodeGroup || !rows || !cols || !out || capacity < 0)
+    return fail(SWS_E_INVALID, "test_settle_plan: %d linears", n_linears);
+  if (elem_bytes != 1 && elem_bytes != 2) return fail(SWS_E_INVALID, "test_settle_plan: elem_bytes %d", elem_bytes);
+  int64_t total_rows = 0;
+  for (int i = 0; i < n_linears; ++i) {
+    if (rows[i] < 1 || rows[i] > ((int64_t)1 << 24) || cols[i] < 16 || cols[i] % 16 != 0 || cols[i] > ((int64_t)1 << 24))
+      return fail(SWS_E_INVALID, "test_settle_plan: linear %d is [%lld, %lld]", i, (long long)rows[i],
+                  (long long)cols[i]);
+    total_rows += rows[i];
+  }
+  std::unique_ptr<DecodeParams> p(new DecodeParams());
+  std::vector<uint16_t> ybuf((size_t)total_rows);
+  std::vector<int64_t> first_row(n_linears);
+  p->n_entries = n_linears;
+  p->m = 1;
+  p->units = 0;
+  int64_t rb = 0, off = 0;
+  for (int i = 0; i < n_linears; ++i) {
+    DecodeEntry& e = p->e[i];
+    e.y = ybuf.data() + off;
+    first_row[i] = off;
+    e.rows = rows[i];
+    e.row_base = 0;
+    e.y_rows = rows[i];
+    e.linear = i;
+    e.split_owner = 1;
+    e.cols = cols[i];
+    e.slabs = (int32_t)cdiv(cols[i] * elem_bytes, kSlabK);
+    e.unit_begin = p->units;
+    e.rb_begin = rb;
+    const int64_t nrb = cdiv(rows[i], kTcUnitRows);
+    rb += nrb;
+    p->units += nrb * e.slabs;
+    off += rows[i];
+  }
+  if (grid < 1 || grid > std::min<int64_t>(p->units, kMaxGrid))
+    return fail(SWS_E_INVALID, "test_settle_plan: grid %lld for %lld units", (long long)grid, (long long)p->units);
+  std::unique_ptr<SettlePlan> sp(new SettlePlan());
+  settle_plan(*p, grid, sp.get());
+  if (sp->n > capacity) return fail(SWS_E_INVALID, "test_settle_plan: %d tasks, room for %d", sp->n, capacity);
+  for (int t = 0; t < sp->n; ++t) {
+    const SettleTask& k = sp->task[t];
+    const int64_t d = k.y - ybuf.data();
+    int i = n_linears - 1;
+    while (i > 0 && d < first_row[i]) --i;
+    int32_t* o = out + 6 * t;
+    o[0] = i;
+    o[1] = (int32_t)((d - first_row[i]) / kTcRows);
+    o[2] = k.rows;
+    o[3] = k.cf;
+    o[4] = k.cl;
+    o[5] = k.cf_slot;
+  }
+  return sp->n;
+}

@@ -350,3 +350,74 @@ def test_bounds_self_check_of_relayout_segments(swslib):
         assert ei.value.code == S.E_INVALID
     S.set_option(S.OPT_CHECK_BOUNDS, 1)
     S.set_option(S.OPT_CHECK_BOUNDS, 0)
+
+
+def _settle_tasks_by_definition(rows, cols, elem, G):
+    """The split-K bookkeeping of a decode launch, from its definition: units
+    are (linear, 256-row block, K slab) in order, CTA c takes units
+    [c*U//G, (c+1)*U//G), and every row block that more than one CTA works on
+    needs one settle task: its first and last CTA, its rows, and where the
+    first CTA left its partial sums (its first run's slot 2c when its range
+    starts inside that row block, else its last run's, 2c+1)."""
+    units = []
+    for i, (r, c) in enumerate(zip(rows, cols)):
+        slabs = -(-c * elem // 128)
+        for rbl in range(-(-r // 256)):
+            units += [(i, rbl)] * slabs
+    U = len(units)
+    start = [c * U // G for c in range(G + 1)]
+    owner = [c for c in range(G) for _ in range(start[c], start[c + 1])]
+    ctas = {}
+    for u, key in enumerate(units):
+        ctas.setdefault(key, set()).add(owner[u])
+    tasks = []
+    for key in dict.fromkeys(units):  # row blocks in unit order
+        cs = sorted(ctas[key])
+        if len(cs) > 1:
+            i, rbl = key
+            cf, cl = cs[0], cs[-1]
+            tasks.append((i, rbl, min(256, rows[i] - 256 * rbl), cf, cl, 2 * cf + (0 if units[start[cf]] == key else 1)))
+    return tasks, U
+
+
+def test_decode_settle_tasks_match_the_partition(swslib):
+    # Host logic of the tcgen05 decode launch: the settle tasks its planner
+    # derives with closed-form unit arithmetic, against the tasks read off the
+    # partition unit by unit - the decode workloads' layers on one CTA per SM,
+    # and random groups (ragged row blocks, 1 to 8 linears, E4M3 and 16-bit
+    # weights) on every grid from 1 CTA to one per unit.
+    S = swslib
+    cases = []
+    for w in (WL.SHARED_EXPERT, WL.ATTN_KDA):
+        rows = [e.rows for e in w.entries]
+        cols = [e.cols for e in w.entries]
+        for elem in (1, 2):
+            for G in (1, 2, 151, 152, 256):
+                cases.append((rows, cols, elem, G))
+    rng = np.random.default_rng(2024)
+    for _ in range(60):
+        n = int(rng.integers(1, 9))
+        rows = [int(rng.integers(1, 1400)) for _ in range(n)]
+        cols = [16 * int(rng.integers(1, 80)) for _ in range(n)]
+        elem = int(rng.choice([1, 2]))
+        U = sum(-(-r // 256) * -(-c * elem // 128) for r, c in zip(rows, cols))
+        for G in sorted({1, min(U, 256), int(rng.integers(1, min(U, 256) + 1))}):
+            cases.append((rows, cols, elem, G))
+    n_tasks = 0
+    for rows, cols, elem, G in cases:
+        want, U = _settle_tasks_by_definition(rows, cols, elem, G)
+        got = S.test_settle_plan(rows, cols, elem, G)
+        assert got == want, (rows, cols, elem, G)
+        n_tasks += len(got)
+    assert n_tasks > 500
+    # refusals: no linear, more than 8, cols not a multiple of 16, grid outside [1, min(U, 256)]
+    with pytest.raises(S.SwsError):
+        S.test_settle_plan([], [], 1, 1)
+    with pytest.raises(S.SwsError):
+        S.test_settle_plan([256] * 9, [128] * 9, 1, 1)
+    with pytest.raises(S.SwsError):
+        S.test_settle_plan([256], [120], 1, 1)
+    with pytest.raises(S.SwsError):
+        S.test_settle_plan([256], [256], 1, 3)  # 2 units
+    with pytest.raises(S.SwsError):
+        S.test_settle_plan([256], [256], 1, 0)
